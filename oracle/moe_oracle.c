@@ -1,0 +1,354 @@
+/*
+ * CPU oracle for the single-GPU MoE layer hot path.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path may link, load or call
+ * this file: only the tests, the smoke check and the benchmark's CPU-baseline leg
+ * use it.  It shares no code, header, table or constant with the CUDA library.
+ *
+ * Every function is the plain definition of one step, written out in fp64 with
+ * no blocking, fusion or reordering beyond what the definition states.  Sources:
+ *
+ *  [BLOG]  "Lower latency and higher throughput with multi-node DeepSeek
+ *          deployment" (Perplexity blog).
+ *            §Expert Parallelism: a MoE layer has 256 routed experts and one
+ *              shared expert; each token goes to 8 distinct routed experts whose
+ *              outputs are summed with weights, and the shared expert's output
+ *              is added.
+ *            §Roofline / GEMM: a Linear layer is the product [m,k]x[k,n].
+ *            §MoE Router: top-k of the router scores, keeping the indices of the
+ *              selected elements; dense dispatch needs the routing aggregated per
+ *              expert instead of per token.
+ *            §Quantization: the activation is SiLU (DeepSeek-V3/R1).
+ *  [CANN]  "DeepSeek-R1 prefill inference optimisation on Atlas A3"
+ *          (cann-recipes-infer), §MoE deployment strategy (Double-Routing):
+ *            step 1, init-routing expands each token and sorts the copies,
+ *              returning expanded_x, expanded_row_idx (used to restore the
+ *              original order) and tokens_per_expert;
+ *            step 6, the inverse permutation is the argsort of the permutation;
+ *            step 8, finalize-routing restores the original order through
+ *              expanded_src_to_dst_row, applies scales=topk_weight and adds the
+ *              shared expert output passed as skip1.
+ *
+ * Readings where the pages are silent (each is listed with its reason in the
+ * design notes): selection is on fp32 scores s_e = fl32(logit_e + bias_e) with
+ * ties going to the lower expert id; slots are in descending score order;
+ * source rows are token-major (src = t*k + j); the sort is stable (ascending
+ * src inside an expert); no token is dropped or padded; the SwiGLU expert is
+ * W2 (silu(Wgate v) * (Wup v)); the shared experts' outputs are summed and form
+ * one skip tensor.
+ *
+ * Rounding points (dt = storage dtype, RNE): logits are stored as fp32; the
+ * expert hidden h, the expert output y and the shared output are stored in dt;
+ * the layer output is rounded once to dt.  All sums are fp64.
+ *
+ * dtype codes: 0 = fp32 (float), 1 = bf16 (uint16 bit pattern).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+enum { OR_F32 = 0, OR_BF16 = 1 };
+
+/* ---- storage conversions ------------------------------------------------ */
+
+/* bf16 bit pattern -> value: the bf16 bits are the top half of an fp32. */
+static double bf16_bits_to_double(uint16_t b) {
+    uint32_t u = (uint32_t)b << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+/* fp32 -> bf16 bits, round to nearest, ties to even (finite inputs). */
+static uint16_t float_to_bf16_bits(float f) {
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    uint32_t lsb = (u >> 16) & 1u;
+    u += 0x7FFFu + lsb;
+    return (uint16_t)(u >> 16);
+}
+
+/* Value of element i of an array stored in dtype dt. */
+static double load(const void* p, int dt, size_t i) {
+    if (dt == OR_BF16) return bf16_bits_to_double(((const uint16_t*)p)[i]);
+    return (double)((const float*)p)[i];
+}
+
+/* Round a double to the storage dtype and return the stored value.  bf16 goes
+ * through fp32 first (fp64 -> fp32 -> bf16, each RNE). */
+static double round_to(double v, int dt) {
+    float f = (float)v;
+    if (dt == OR_BF16) return bf16_bits_to_double(float_to_bf16_bits(f));
+    return (double)f;
+}
+
+static void store(void* p, int dt, size_t i, double v) {
+    if (dt == OR_BF16) ((uint16_t*)p)[i] = float_to_bf16_bits((float)v);
+    else ((float*)p)[i] = (float)v;
+}
+
+int oracle_num_threads(void) {
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+void oracle_set_num_threads(int n) {
+#ifdef _OPENMP
+    if (n > 0) omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+}
+
+/* Exposed so that tests can pin the rounding helper against a library cast. */
+void oracle_round_array(const double* in, int dt, int64_t n, double* out) {
+    for (int64_t i = 0; i < n; ++i) out[i] = round_to(in[i], dt);
+}
+
+/* ---- gate GEMM ------------------------------------------------------------
+ * [BLOG §Roofline / GEMM]: logits = x [T,H] times the router weight; the
+ * router weight is stored like a Linear weight, wg [E,H] (H contiguous), so
+ *   logits[t,e] = sum_h x[t,h] * wg[e,h].                                    */
+void oracle_gate_logits(const void* x, const void* wg, int dt, int T, int H, int E,
+                        double* logits) {
+    #pragma omp parallel for schedule(static)
+    for (int t = 0; t < T; ++t) {
+        for (int e = 0; e < E; ++e) {
+            double acc = 0.0;
+            for (int h = 0; h < H; ++h)
+                acc += load(x, dt, (size_t)t * H + h) * load(wg, dt, (size_t)e * H + h);
+            logits[(size_t)t * E + e] = acc;
+        }
+    }
+}
+
+/* ---- top-k routing --------------------------------------------------------
+ * [BLOG §MoE Router]: per token, the k experts with the highest scores, with
+ * their indices.  Score s_e = fl32(logits[t,e] + bias[e]) (bias may be NULL).
+ * Selection order: descending s, ties to the lower expert id; this is a full
+ * stable sort of the experts by (-s, e) truncated to k, written as k passes of
+ * "pick the best remaining".
+ * Weights: softmax over all E scores, then the k selected probabilities; with
+ * renorm != 0 they are divided by their sum (the full softmax denominator
+ * cancels, leaving a softmax over the selected scores).                      */
+void oracle_route_topk(const float* logits, const float* bias, int T, int E, int k,
+                       int renorm, int32_t* ids, double* w) {
+    #pragma omp parallel for schedule(static)
+    for (int t = 0; t < T; ++t) {
+        float* s = (float*)malloc(sizeof(float) * (size_t)E);
+        char* taken = (char*)calloc((size_t)E, 1);
+        for (int e = 0; e < E; ++e) {
+            float b = bias ? bias[e] : 0.0f;
+            s[e] = logits[(size_t)t * E + e] + b; /* one fp32 add */
+        }
+        for (int j = 0; j < k; ++j) {
+            int best = -1;
+            for (int e = 0; e < E; ++e) {
+                if (taken[e]) continue;
+                if (best < 0 || s[e] > s[best]) best = e; /* strict: ties keep lower id */
+            }
+            taken[best] = 1;
+            ids[(size_t)t * k + j] = best;
+        }
+        /* softmax over all E scores (shifted by the max for range only). */
+        double smax = -INFINITY;
+        for (int e = 0; e < E; ++e) if ((double)s[e] > smax) smax = (double)s[e];
+        double denom_all = 0.0;
+        for (int e = 0; e < E; ++e) denom_all += exp((double)s[e] - smax);
+        double sel_sum = 0.0;
+        for (int j = 0; j < k; ++j) {
+            double p = exp((double)s[ids[(size_t)t * k + j]] - smax) / denom_all;
+            w[(size_t)t * k + j] = p;
+            sel_sum += p;
+        }
+        if (renorm)
+            for (int j = 0; j < k; ++j) w[(size_t)t * k + j] /= sel_sum;
+        free(s);
+        free(taken);
+    }
+}
+
+/* ---- init-routing -----------------------------------------------------------
+ * [CANN §MoE deployment, Double-Routing step 1] + [BLOG §MoE Router]
+ * (aggregation per expert).  Source row src = t*k + j (token-major).
+ *   tokens_per_expert[e] = #{src : ids[src] == e}
+ *   expert_offsets       = exclusive prefix sum of tokens_per_expert ([E+1])
+ *   expanded_row_idx[src] = expert_offsets[ids[src]]
+ *                           + #{src' < src : ids[src'] == ids[src]}
+ *   expanded_x[expanded_row_idx[src], :] = x[src / k, :]
+ * i.e. a stable sort of the source rows by expert id.  Ids outside [0,E) get
+ * expanded_row_idx = -1, are not counted and the function returns the number
+ * of such ids.                                                               */
+int oracle_init_routing(const int32_t* ids, int T, int k, int E, const void* x, int dt,
+                        int H, void* expanded_x, int32_t* expanded_row_idx,
+                        int32_t* tokens_per_expert, int32_t* expert_offsets) {
+    int64_t R = (int64_t)T * k;
+    int bad = 0;
+    for (int e = 0; e < E; ++e) tokens_per_expert[e] = 0;
+    for (int64_t src = 0; src < R; ++src) {
+        int e = ids[src];
+        if (e < 0 || e >= E) { ++bad; continue; }
+        tokens_per_expert[e] += 1;
+    }
+    expert_offsets[0] = 0;
+    for (int e = 0; e < E; ++e) expert_offsets[e + 1] = expert_offsets[e] + tokens_per_expert[e];
+    int32_t* seen = (int32_t*)calloc((size_t)E, sizeof(int32_t));
+    for (int64_t src = 0; src < R; ++src) {
+        int e = ids[src];
+        if (e < 0 || e >= E) { expanded_row_idx[src] = -1; continue; }
+        expanded_row_idx[src] = expert_offsets[e] + seen[e];
+        seen[e] += 1;
+    }
+    free(seen);
+    if (expanded_x) {
+        size_t esz = dt == OR_BF16 ? 2 : 4;
+        for (int64_t src = 0; src < R; ++src) {
+            int32_t dst = expanded_row_idx[src];
+            if (dst < 0) continue;
+            memcpy((char*)expanded_x + (size_t)dst * H * esz,
+                   (const char*)x + (size_t)(src / k) * H * esz, (size_t)H * esz);
+        }
+    }
+    return bad;
+}
+
+/* ---- one SwiGLU expert on one row ------------------------------------------
+ * [BLOG §Expert Parallelism] (expert FFN) and [BLOG §Quantization] (SiLU):
+ *   g = wgate v,  u = wup v          (wgate, wup: [I,H], H contiguous)
+ *   h_i = silu(g_i) * u_i,  silu(z) = z / (1 + exp(-z))
+ *   y = w2 h                          (w2: [H,I], I contiguous)
+ * h is rounded to dt when round_h != 0 (the stored intermediate); y is
+ * returned unrounded.                                                        */
+static void expert_ffn_row(const void* v, size_t v_off, int dt, const void* wgate,
+                           const void* wup, const void* w2, size_t wgu_off, size_t w2_off,
+                           int H, int I, int round_h, double* hbuf, double* y) {
+    for (int i = 0; i < I; ++i) {
+        double g = 0.0, u = 0.0;
+        for (int h = 0; h < H; ++h) {
+            double vh = load(v, dt, v_off + h);
+            g += load(wgate, dt, wgu_off + (size_t)i * H + h) * vh;
+            u += load(wup, dt, wgu_off + (size_t)i * H + h) * vh;
+        }
+        double hi = g / (1.0 + exp(-g)) * u;
+        hbuf[i] = round_h ? round_to(hi, dt) : hi;
+    }
+    for (int o = 0; o < H; ++o) {
+        double acc = 0.0;
+        for (int i = 0; i < I; ++i) acc += load(w2, dt, w2_off + (size_t)o * I + i) * hbuf[i];
+        y[o] = acc;
+    }
+}
+
+/* Expert FFN applied to n rows of a [*,H] matrix: rows[r] = FFN_{expert[r]}(a[r]).
+ * Weights: wgate/wup [E,I,H], w2 [E,H,I].  The output of each row is rounded to
+ * dt (the stored expert output).  Rows with expert < 0 are left untouched.   */
+void oracle_expert_ffn_rows(const void* a, int dt, int64_t n, const int32_t* expert,
+                            const void* wgate, const void* wup, const void* w2, int H, int I,
+                            double* y) {
+    #pragma omp parallel
+    {
+        double* hbuf = (double*)malloc(sizeof(double) * (size_t)I);
+        double* yr = (double*)malloc(sizeof(double) * (size_t)H);
+        #pragma omp for schedule(dynamic, 1)
+        for (int64_t r = 0; r < n; ++r) {
+            int e = expert[r];
+            if (e < 0) continue;
+            expert_ffn_row(a, (size_t)r * H, dt, wgate, wup, w2, (size_t)e * I * H,
+                           (size_t)e * H * I, H, I, dt == OR_BF16, hbuf, yr);
+            for (int o = 0; o < H; ++o) y[(size_t)r * H + o] = round_to(yr[o], dt);
+        }
+        free(hbuf);
+        free(yr);
+    }
+}
+
+/* ---- finalize-routing --------------------------------------------------------
+ * [CANN §MoE deployment, Double-Routing step 8]:
+ *   out[t,:] = skip[t,:] + sum_j scales[t,j] * y[expanded_src_to_dst_row[t*k+j], :]
+ * skip may be NULL; rows whose index is outside [0, n_rows) are skipped.  The
+ * result is returned unrounded (fp64).                                       */
+void oracle_finalize_routing(const void* y, int dt, int64_t n_rows, const void* skip,
+                             const double* scales, const int32_t* expanded_row_idx, int T,
+                             int H, int k, double* out) {
+    #pragma omp parallel for schedule(static)
+    for (int t = 0; t < T; ++t) {
+        for (int o = 0; o < H; ++o) {
+            double acc = skip ? load(skip, dt, (size_t)t * H + o) : 0.0;
+            for (int j = 0; j < k; ++j) {
+                int32_t r = expanded_row_idx[(size_t)t * k + j];
+                if (r < 0 || r >= n_rows) continue;
+                acc += scales[(size_t)t * k + j] * load(y, dt, (size_t)r * H + o);
+            }
+            out[(size_t)t * H + o] = acc;
+        }
+    }
+}
+
+/* ---- the whole layer, brute force per token ---------------------------------
+ * [BLOG §Expert Parallelism]: out[t] = shared(x_t) + sum_j w_j * FFN_{e_j}(x_t)
+ * with e_j, w_j from the router on the gate logits.  S shared experts (weights
+ * sgate/sup [S,I,H], s2 [S,H,I]) are summed into one shared output, stored in
+ * dt; each routed expert output is stored in dt; the final sum is rounded to dt.
+ * Only the tokens listed in tokens[0..n_tok) are evaluated (all when tokens is
+ * NULL, n_tok = T).  Returns for those tokens: logits64 [n_tok,E] (fp64, before
+ * the fp32 store; may be NULL), ids [n_tok,k], w [n_tok,k], out [n_tok,H]
+ * (already rounded to dt, returned as double).                               */
+void oracle_layer(const void* x, int dt, int T, int H, int E, int k, int I, int S, int renorm,
+                  const void* wg, const float* bias, const void* wgate, const void* wup,
+                  const void* w2, const void* sgate, const void* sup, const void* s2,
+                  const int32_t* tokens, int n_tok, double* logits64, int32_t* ids, double* w,
+                  double* out) {
+    if (!tokens) n_tok = T;
+    #pragma omp parallel
+    {
+        double* l64 = (double*)malloc(sizeof(double) * (size_t)E);
+        float* l32 = (float*)malloc(sizeof(float) * (size_t)E);
+        double* hbuf = (double*)malloc(sizeof(double) * (size_t)I);
+        double* yr = (double*)malloc(sizeof(double) * (size_t)H);
+        double* ysh = (double*)malloc(sizeof(double) * (size_t)H);
+        #pragma omp for schedule(dynamic, 1)
+        for (int n = 0; n < n_tok; ++n) {
+            int t = tokens ? tokens[n] : n;
+            size_t xo = (size_t)t * H;
+            /* gate logits for this token, stored as fp32 */
+            for (int e = 0; e < E; ++e) {
+                double acc = 0.0;
+                for (int h = 0; h < H; ++h) acc += load(x, dt, xo + h) * load(wg, dt, (size_t)e * H + h);
+                l64[e] = acc;
+                l32[e] = (float)acc;
+                if (logits64) logits64[(size_t)n * E + e] = acc;
+            }
+            oracle_route_topk(l32, bias, 1, E, k, renorm, ids + (size_t)n * k, w + (size_t)n * k);
+            /* shared experts: one summed output, stored in dt */
+            for (int o = 0; o < H; ++o) ysh[o] = 0.0;
+            for (int s = 0; s < S; ++s) {
+                expert_ffn_row(x, xo, dt, sgate, sup, s2, (size_t)s * I * H, (size_t)s * H * I, H, I,
+                               dt == OR_BF16, hbuf, yr);
+                for (int o = 0; o < H; ++o) ysh[o] += yr[o];
+            }
+            double* orow = out + (size_t)n * H;
+            for (int o = 0; o < H; ++o) orow[o] = round_to(ysh[o], dt);
+            /* routed experts, each output stored in dt, weighted sum */
+            for (int j = 0; j < k; ++j) {
+                int e = ids[(size_t)n * k + j];
+                expert_ffn_row(x, xo, dt, wgate, wup, w2, (size_t)e * I * H, (size_t)e * H * I, H, I,
+                               dt == OR_BF16, hbuf, yr);
+                double wj = w[(size_t)n * k + j];
+                for (int o = 0; o < H; ++o) orow[o] += wj * round_to(yr[o], dt);
+            }
+            for (int o = 0; o < H; ++o) orow[o] = round_to(orow[o], dt);
+        }
+        free(l64);
+        free(l32);
+        free(hbuf);
+        free(yr);
+        free(ysh);
+    }
+}

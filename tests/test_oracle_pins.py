@@ -1,0 +1,310 @@
+"""Pins of the CPU oracle against things other than itself (CPU only).
+
+Each test checks one oracle function against a closed form, an invariant, a
+library routine on a special case, or brute force on tiny inputs, chosen so that
+a plausible slip (a dropped term, a wrong sign or index, a transposed operand,
+gate and up swapped, an unstable sort) fails at least one of them.
+"""
+import math
+
+import numpy as np
+import pytest
+import scipy.special
+import torch
+import torch.nn.functional as F
+
+from moe_expert_routing_route_gb300 import inputs
+
+F32, BF16 = 0, 1
+
+
+def _bf16_bits(a: np.ndarray) -> np.ndarray:
+    return inputs.to_numpy(torch.from_numpy(np.asarray(a, np.float32)).to(torch.bfloat16))
+
+
+def _bits_to_f64(b: np.ndarray) -> np.ndarray:
+    return torch.from_numpy(b.view(np.int16)).view(torch.bfloat16).to(torch.float64).numpy()
+
+
+# ---- storage rounding --------------------------------------------------------
+
+def test_round_to_bf16_matches_torch_cast(oracle):
+    rng = np.random.default_rng(0)
+    v = np.concatenate([rng.standard_normal(4000).astype(np.float32),
+                        # exact ties between two bf16 neighbours: 1 + 2^-8 and 1 + 3*2^-8
+                        np.array([1 + 2**-8, 1 + 3 * 2**-8, -(1 + 2**-8), 0.0, -0.0], np.float32)])
+    got = oracle.round_to(v.astype(np.float64), BF16)
+    want = torch.from_numpy(v).to(torch.bfloat16).to(torch.float64).numpy()
+    assert np.array_equal(got, want)
+    # ties go to even: 1 + 2^-8 -> 1.0, 1 + 3*2^-8 -> 1 + 2^-6 (upper neighbour is even)
+    assert got[-5] == 1.0 and got[-4] == 1 + 2**-6
+
+
+def test_round_to_f32_matches_numpy(oracle):
+    v = np.random.default_rng(1).standard_normal(1000)
+    assert np.array_equal(oracle.round_to(v, F32), v.astype(np.float32).astype(np.float64))
+
+
+# ---- gate GEMM ---------------------------------------------------------------
+
+@pytest.mark.parametrize("dt", ["f32", "bf16"])
+def test_gate_logits_equals_library_matmul(oracle, dt):
+    cfg = inputs.LayerConfig("t", T=37, H=96, E=24, k=2, I=8, S=0, dtype=dt, seed=5)
+    d = inputs.make_layer(cfg, with_weights=False)
+    x, wg = inputs.to_numpy(d["x"]), inputs.to_numpy(d["wg"])
+    got = oracle.gate_logits(x, wg)
+    want = d["x"].to(torch.float64).numpy() @ d["wg"].to(torch.float64).numpy().T  # [T,H]x[H,E]
+    np.testing.assert_allclose(got, want, rtol=1e-12, atol=1e-12)
+
+
+# ---- top-k routing -------------------------------------------------------------
+
+def _brute_topk(s: np.ndarray, k: int):
+    """Full sort of the experts by (-score, id), truncated to k."""
+    return [sorted(range(s.size), key=lambda e: (-float(s[e]), e))[:k] for _ in [0]][0]
+
+
+@pytest.mark.parametrize("ties", [None, "quantised"])
+@pytest.mark.parametrize("use_bias", [False, True])
+def test_topk_ids_equal_brute_force_sort(oracle, ties, use_bias):
+    T, E, k = 60, 16, 4
+    logits = inputs.random_logits(T, E, seed=3, ties=ties).numpy()
+    bias = (np.round(np.random.default_rng(2).standard_normal(E) * 4) / 4).astype(np.float32) \
+        if use_bias else None
+    ids, w = oracle.route_topk(logits, k, renorm=True, bias=bias)
+    for t in range(T):
+        s = logits[t] + (bias if bias is not None else 0)  # fp32 + fp32 -> fp32
+        assert s.dtype == np.float32
+        assert list(ids[t]) == _brute_topk(s, k)
+
+
+def test_topk_weights_are_library_softmax(oracle):
+    T, E, k = 40, 32, 6
+    logits = inputs.random_logits(T, E, seed=4).numpy()
+    ids, w = oracle.route_topk(logits, k, renorm=True)
+    _, w_raw = oracle.route_topk(logits, k, renorm=False)
+    for t in range(T):
+        sel = logits[t][ids[t]].astype(np.float64)
+        np.testing.assert_allclose(w[t], scipy.special.softmax(sel), rtol=1e-13)
+        full = scipy.special.softmax(logits[t].astype(np.float64))
+        np.testing.assert_allclose(w_raw[t], full[ids[t]], rtol=1e-13)
+    np.testing.assert_allclose(w.sum(1), 1.0, rtol=0, atol=1e-14)
+    # descending slots: weights are non-increasing along j
+    assert np.all(np.diff(w, axis=1) <= 0)
+
+
+def test_topk_all_equal_scores(oracle):
+    T, E, k = 5, 12, 3
+    logits = inputs.random_logits(T, E, seed=0, ties="all_equal").numpy()
+    ids, w = oracle.route_topk(logits, k, renorm=True)
+    assert np.array_equal(ids, np.tile(np.arange(k, dtype=np.int32), (T, 1)))
+    assert np.all(w == 1.0 / k)
+    _, w_raw = oracle.route_topk(logits, k, renorm=False)
+    np.testing.assert_allclose(w_raw, 1.0 / E, rtol=1e-15)
+
+
+def test_topk_k_equals_E_is_full_softmax(oracle):
+    T, E = 7, 8
+    logits = inputs.random_logits(T, E, seed=9).numpy()
+    ids, w = oracle.route_topk(logits, E, renorm=True)
+    for t in range(T):
+        assert sorted(ids[t]) == list(range(E))
+        np.testing.assert_allclose(w[t], scipy.special.softmax(logits[t].astype(np.float64))[ids[t]],
+                                   rtol=1e-13)
+
+
+def test_topk_bias_moves_selection(oracle):
+    logits = np.zeros((1, 8), np.float32)
+    logits[0, 3] = 1.0
+    bias = np.zeros(8, np.float32)
+    bias[6] = 5.0
+    ids, w = oracle.route_topk(logits, 2, renorm=True, bias=bias)
+    assert list(ids[0]) == [6, 3]
+    # the bias feeds the weights too: softmax over (5, 1)
+    np.testing.assert_allclose(w[0], scipy.special.softmax(np.array([5.0, 1.0])), rtol=1e-14)
+
+
+# ---- init-routing --------------------------------------------------------------
+
+@pytest.mark.parametrize("T,k,E,distinct", [(50, 4, 16, True), (33, 3, 5, False), (1, 1, 1, True),
+                                            (64, 2, 16, True)])
+def test_init_routing_invariants(oracle, T, k, E, distinct):
+    ids = inputs.random_ids(T, k, E, seed=T + k, distinct=distinct).numpy()
+    x = inputs.to_numpy(inputs.random_rows(T, 24, torch.bfloat16, seed=1))
+    r = oracle.init_routing(ids, x, E)
+    cnt, off, idx, ex = r["tokens_per_expert"], r["expert_offsets"], r["expanded_row_idx"], r["expanded_x"]
+    R = T * k
+    assert r["bad"] == 0
+    assert cnt.sum() == R
+    assert np.array_equal(cnt, np.bincount(ids.ravel(), minlength=E))
+    assert off[0] == 0 and np.array_equal(np.diff(off), cnt)
+    assert np.array_equal(np.sort(idx), np.arange(R))  # a permutation
+    # stable sort by expert: numpy's stable argsort gives dst -> src
+    order = np.argsort(ids.ravel(), kind="stable")
+    assert np.array_equal(idx[order], np.arange(R))
+    # the inverse permutation is the argsort of the permutation (Double-Routing step 6)
+    inv = np.argsort(idx)
+    assert np.array_equal(idx[inv], np.arange(R))
+    # rows: expanded_x[dst] is the source token's row, bit for bit
+    assert np.array_equal(ex[idx], x[np.arange(R) // k])
+    # stability: ascending src inside each expert's segment
+    for e in range(E):
+        seg = inv[off[e]:off[e + 1]]
+        assert np.all(np.diff(seg) > 0)
+        assert np.all(ids.ravel()[seg] == e)
+
+
+def test_init_routing_flags_bad_ids(oracle):
+    ids = np.array([[0, 5], [2, -1], [1, 1]], np.int32)
+    r = oracle.init_routing(ids, None, 3, H=0)
+    assert r["bad"] == 2
+    assert r["expanded_row_idx"][1] == -1 and r["expanded_row_idx"][3] == -1
+    assert r["tokens_per_expert"].tolist() == [1, 2, 1]
+
+
+# ---- finalize-routing ----------------------------------------------------------
+
+@pytest.mark.parametrize("dt", [torch.float32, torch.bfloat16])
+def test_finalize_identity_experts_k1_reproduces_x(oracle, dt):
+    """k=1, unit weight, identity experts (y = expanded_x), no shared: out == x exactly."""
+    T, E, k, H = 40, 8, 1, 32
+    ids = inputs.random_ids(T, k, E, seed=7).numpy()
+    x = inputs.to_numpy(inputs.random_rows(T, H, dt, seed=3))
+    r = oracle.init_routing(ids, x, E)
+    out = oracle.finalize_routing(r["expanded_x"], np.ones((T, k)), r["expanded_row_idx"])
+    xd = x.astype(np.float64) if x.dtype == np.float32 else _bits_to_f64(x)
+    assert np.array_equal(out, xd)
+
+
+def test_finalize_identity_experts_renormalised_weights(oracle):
+    T, E, k, H = 30, 16, 4, 20
+    logits = inputs.random_logits(T, E, seed=11).numpy()
+    ids, w = oracle.route_topk(logits, k, renorm=True)
+    x = inputs.random_rows(T, H, torch.float32, seed=5).numpy()
+    r = oracle.init_routing(ids, x, E)
+    out = oracle.finalize_routing(r["expanded_x"], w, r["expanded_row_idx"])
+    np.testing.assert_allclose(out, x.astype(np.float64), rtol=1e-13, atol=1e-13)
+
+
+def test_finalize_skip_and_one_hot_scales(oracle):
+    T, k, H = 6, 3, 10
+    R = T * k
+    y = inputs.random_rows(R, H, torch.float32, seed=2).numpy()
+    skip = inputs.random_rows(T, H, torch.float32, seed=3, tag="misc").numpy()
+    idx = np.random.default_rng(0).permutation(R).astype(np.int32)
+    zero = np.zeros((T, k))
+    assert np.array_equal(oracle.finalize_routing(y, zero, idx, skip), skip.astype(np.float64))
+    onehot = np.zeros((T, k))
+    onehot[:, 2] = 1.0
+    out = oracle.finalize_routing(y, onehot, idx)
+    assert np.array_equal(out, y[idx.reshape(T, k)[:, 2]].astype(np.float64))
+
+
+# ---- expert FFN ------------------------------------------------------------------
+
+def test_ffn_closed_form_detects_gate_up_swap(oracle):
+    """H=I=1: y = c * silu(a v) * (b v); silu from torch (a library routine)."""
+    a, b, c, v = 2.0, 3.0, 0.5, 1.0
+    wg = np.array([[[a]]], np.float32)
+    wu = np.array([[[b]]], np.float32)
+    w2 = np.array([[[c]]], np.float32)
+    y = oracle.expert_ffn_rows(np.array([[v]], np.float32), np.array([0], np.int32), wg, wu, w2)
+    want = c * F.silu(torch.tensor(a * v, dtype=torch.float64)).item() * (b * v)
+    swapped = c * F.silu(torch.tensor(b * v, dtype=torch.float64)).item() * (a * v)
+    assert abs(y[0, 0] - want) < 1e-6 and abs(y[0, 0] - swapped) > 0.1
+
+
+def test_ffn_zero_up_or_zero_gate_gives_zero(oracle):
+    cfg = inputs.LayerConfig("t", T=4, H=16, E=2, k=1, I=8, S=0, dtype="f32", seed=1)
+    d = inputs.make_layer(cfg)
+    x = d["x"].numpy()
+    ex = np.array([0, 1, 0, 1], np.int32)
+    zero = np.zeros_like(d["w_up"].numpy())
+    assert np.all(oracle.expert_ffn_rows(x, ex, d["w_gate"].numpy(), zero, d["w2"].numpy()) == 0)
+    assert np.all(oracle.expert_ffn_rows(x, ex, zero, d["w_up"].numpy(), d["w2"].numpy()) == 0)
+
+
+def _dense_swiglu(x, wg, wu, w2):
+    """Textbook SwiGLU MLP (Shazeer 2020) with torch library ops in fp64."""
+    x = x.to(torch.float64)
+    return (F.silu(x @ wg.to(torch.float64).T) * (x @ wu.to(torch.float64).T)) @ w2.to(torch.float64).T
+
+
+def test_layer_E1_k1_is_dense_swiglu_mlp(oracle):
+    """One routed expert, top-1 (weight 1) + one shared expert = two dense SwiGLU MLPs."""
+    cfg = inputs.LayerConfig("t", T=12, H=48, E=1, k=1, I=40, S=1, dtype="f32", seed=8)
+    d = inputs.make_layer(cfg)
+    r = oracle.layer(*(inputs.to_numpy(d[n]) for n in
+                       ("x", "wg", "w_gate", "w_up", "w2", "s_gate", "s_up", "s2")), k=1)
+    assert np.all(r["ids"] == 0) and np.all(r["w"] == 1.0)
+    want = (_dense_swiglu(d["x"], d["w_gate"][0], d["w_up"][0], d["w2"][0])
+            + _dense_swiglu(d["x"], d["s_gate"][0], d["s_up"][0], d["s2"][0])).numpy()
+    np.testing.assert_allclose(r["out"], want, rtol=2e-6, atol=2e-6)
+
+
+def test_ffn_rows_match_dense_mlp_per_expert(oracle):
+    cfg = inputs.LayerConfig("t", T=10, H=40, E=3, k=1, I=24, S=0, dtype="f32", seed=12)
+    d = inputs.make_layer(cfg)
+    ex = np.array([2, 0, 1, 1, 0, 2, 2, 0, 1, 0], np.int32)
+    y = oracle.expert_ffn_rows(d["x"].numpy(), ex, d["w_gate"].numpy(), d["w_up"].numpy(), d["w2"].numpy())
+    for e in range(3):
+        rows = np.nonzero(ex == e)[0]
+        want = _dense_swiglu(d["x"][rows], d["w_gate"][e], d["w_up"][e], d["w2"][e]).numpy()
+        np.testing.assert_allclose(y[rows], want, rtol=2e-6, atol=2e-6)
+
+
+# ---- whole layer: brute force vs the permutation pipeline --------------------------
+
+@pytest.mark.parametrize("dt", ["f32", "bf16"])
+def test_layer_brute_force_equals_permutation_pipeline(oracle, dt):
+    """Per-token loop == route -> init-routing -> expert FFN on expanded rows ->
+    finalize with the shared output as skip (same rounding points: exact)."""
+    cfg = inputs.LayerConfig("t", T=48, H=64, E=8, k=3, I=32, S=1, dtype=dt, seed=21)
+    d = inputs.make_layer(cfg)
+    n = {k_: inputs.to_numpy(v) for k_, v in d.items() if isinstance(v, torch.Tensor)}
+    r = oracle.layer(n["x"], n["wg"], n["w_gate"], n["w_up"], n["w2"], n["s_gate"], n["s_up"], n["s2"],
+                     k=cfg.k)
+    logits32 = r["logits64"].astype(np.float32)
+    ids, w = oracle.route_topk(logits32, cfg.k, renorm=True)
+    assert np.array_equal(ids, r["ids"]) and np.array_equal(w, r["w"])
+    ir = oracle.init_routing(ids, n["x"], cfg.E)
+    expert_of_row = np.repeat(np.arange(cfg.E, dtype=np.int32), ir["tokens_per_expert"])
+    y = oracle.expert_ffn_rows(ir["expanded_x"], expert_of_row, n["w_gate"], n["w_up"], n["w2"])
+    ysh = oracle.expert_ffn_rows(n["x"], np.zeros(cfg.T, np.int32), n["s_gate"], n["s_up"], n["s2"])
+    code = F32 if dt == "f32" else BF16
+    store = (lambda a: a.astype(np.float32)) if dt == "f32" else _bf16_bits
+    out = oracle.finalize_routing(store(y), w, ir["expanded_row_idx"], skip=store(ysh))
+    assert np.array_equal(oracle.round_to(out, code), r["out"])
+
+
+def test_layer_token_subset_matches_full(oracle):
+    cfg = inputs.LayerConfig("t", T=20, H=32, E=6, k=2, I=16, S=2, dtype="bf16", seed=4)
+    d = inputs.make_layer(cfg)
+    args = [inputs.to_numpy(d[n]) for n in ("x", "wg", "w_gate", "w_up", "w2", "s_gate", "s_up", "s2")]
+    full = oracle.layer(*args, k=2)
+    toks = np.array([19, 3, 3, 0], np.int32)
+    sub = oracle.layer(*args, k=2, tokens=toks)
+    for name in ("ids", "w", "out", "logits64"):
+        assert np.array_equal(sub[name], full[name][toks])
+
+
+def test_layer_two_shared_experts_sum(oracle):
+    """S=2 shared experts contribute the sum of two dense SwiGLU MLPs (fp32, E=1, k=1)."""
+    cfg = inputs.LayerConfig("t", T=6, H=16, E=1, k=1, I=8, S=2, dtype="f32", seed=13)
+    d = inputs.make_layer(cfg)
+    r = oracle.layer(*(inputs.to_numpy(d[n]) for n in
+                       ("x", "wg", "w_gate", "w_up", "w2", "s_gate", "s_up", "s2")), k=1)
+    want = _dense_swiglu(d["x"], d["w_gate"][0], d["w_up"][0], d["w2"][0]).numpy()
+    for s in range(2):
+        want = want + _dense_swiglu(d["x"], d["s_gate"][s], d["s_up"][s], d["s2"][s]).numpy()
+    np.testing.assert_allclose(r["out"], want, rtol=2e-6, atol=2e-6)
+
+
+def test_layer_zipf_bias_feeds_selection(oracle):
+    cfg = inputs.CONFIGS["tiny_fp32"].replace(zipf_s=1.2, T=16)
+    d = inputs.make_layer(cfg)
+    args = [inputs.to_numpy(d[n]) for n in ("x", "wg", "w_gate", "w_up", "w2", "s_gate", "s_up", "s2")]
+    r = oracle.layer(*args, k=cfg.k, bias=d["bias"].numpy())
+    s = (r["logits64"].astype(np.float32) + d["bias"].numpy())
+    for t in range(cfg.T):
+        assert list(r["ids"][t]) == _brute_topk(s[t], cfg.k)
