@@ -1,0 +1,355 @@
+"""Benchmark of the MoE layer forward on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload dsv3_prefill] [--no-cpu-baseline]
+
+One step = one full layer forward (gate GEMM, top-k routing, init-routing,
+row permutation, grouped SwiGLU up GEMM, grouped down GEMM, shared expert,
+finalize) over one batch of T tokens with inputs resident in HBM.  The default
+workload is the DeepSeek-V3-shaped prefill layer: T=4096, H=7168, 256 routed
+experts, top-8, I=2048, one shared expert, bf16 (synthetic, seeded).  Weights
+(22.6 GB) are far larger than L2, so every step streams them from HBM.
+
+Multi-GPU: the layer does not shard here (one process per GPU runs an
+independent replica on its own batch), so N GPUs process N batches per step
+("scaling": "weak"); value = tokens of all ranks / max step time over ranks.
+
+--impl reference times the CPU oracle (test infrastructure) on the host cores
+on a bounded sample of tokens of the same workload, and prints the same line
+with "impl": "reference".
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from moe_expert_routing_route_gb300 import inputs, roofline  # noqa: E402
+
+METRIC = "MoE-layer tokens/sec at 1 GB300; grouped-GEMM % tensor peak; routing GB/s vs HBM"
+UNIT = "tokens/s"
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+KERNEL_SOURCES = {
+    "up_routed": "gemm_tc.cu", "down_routed": "gemm_tc.cu", "up_shared": "gemm_tc.cu",
+    "down_shared": "gemm_tc.cu", "gate": "gemm_tc.cu", "permute_rows": "permute.cu",
+    "init_routing": "permute.cu", "route": "route.cu", "finalize": "finalize.cu",
+}
+
+
+# ---- distributed plumbing (replicas only; used for barrier and max-over-ranks) ----
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(value: float, world: int) -> float:
+    if world == 1:
+        return value
+    import torch.distributed as dist
+    dev = torch.device("cuda", torch.cuda.current_device()) if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---- clocks during the timed region ----
+
+class ClockSampler:
+    FIELDS = ["clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.active",
+              "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
+              "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
+
+    def __init__(self, device_index: int):
+        self.samples = []  # (host time, fields)
+        self.proc = None
+        uuid = None
+        try:
+            uuid = "GPU-" + str(torch.cuda.get_device_properties(device_index).uuid)
+        except Exception:
+            pass
+        cmd = ["nvidia-smi", "--query-gpu=" + ",".join(self.FIELDS), "--format=csv,noheader,nounits",
+               "-lms", "20"]
+        if uuid:
+            cmd += ["-i", uuid]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), [s.strip() for s in line.split(",")]))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0: float, t1: float) -> dict:
+        rows = [f for (t, f) in self.samples if t0 <= t <= t1 + 0.05]
+        if not rows and self.samples:  # window shorter than the sampling period: nearest sample
+            rows = [min(self.samples, key=lambda s: abs(s[0] - (t0 + t1) / 2))[1]]
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for f in rows:
+            try:
+                sm.append(float(f[0]))
+                smax.append(float(f[1]))
+            except (ValueError, IndexError):
+                continue
+            for name, v in zip(names, f[4:8]):
+                if v.strip().lower() == "active":
+                    reasons.add(name)
+        return dict(sm_mhz=statistics.median(sm) if sm else None, sm_max_mhz=max(smax) if smax else None,
+                    reasons=sorted(reasons), samples=len(sm))
+
+
+# ---- roofline inputs ----
+
+def source_hash(name: str) -> str:
+    p = os.path.join(ROOT, "moe_expert_routing_route_gb300", "csrc", name)
+    with open(p, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def measured_traffic(stage: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the kernel source as it is now (else None)."""
+    if not os.path.exists(TRAFFIC_FILE):
+        return None
+    for line in open(TRAFFIC_FILE):
+        parts = line.split()
+        if len(parts) >= 4 and not line.startswith("#") and parts[0] == stage and parts[1] == workload:
+            if parts[3] == source_hash(KERNEL_SOURCES[stage]):
+                return float(parts[2])
+    return None
+
+
+# ---- the CPU oracle on a bounded sample ----
+
+def sample_tokens(cfg, n: int, offset: int = 0) -> np.ndarray:
+    g = inputs.generator("cpu", cfg.seed + offset, "misc")
+    return torch.randperm(cfg.T, generator=g)[:n].sort().values.numpy().astype(np.int32)
+
+
+def oracle_layer_time(cfg, host: dict, toks: np.ndarray) -> float:
+    import oracle
+    t0 = time.perf_counter()
+    oracle.layer(host["x"], host["wg"], host["w_gate"], host["w_up"], host["w2"], host.get("s_gate"),
+                 host.get("s_up"), host.get("s2"), k=cfg.k, renorm=cfg.renormalize, bias=host.get("bias"),
+                 tokens=toks)
+    return time.perf_counter() - t0
+
+
+def host_layer(d: dict) -> dict:
+    return {k: inputs.to_numpy(v) for k, v in d.items() if isinstance(v, torch.Tensor)}
+
+
+def cpu_baseline(cfg, host: dict, budget_s: float = 12.0) -> dict:
+    import oracle
+    n = 4
+    t = oracle_layer_time(cfg, host, sample_tokens(cfg, n))
+    n = int(max(4, min(cfg.T, n * budget_s / max(t, 1e-3))))
+    t = oracle_layer_time(cfg, host, sample_tokens(cfg, n, offset=1))
+    return dict(value=n / t, unit=UNIT, cores=min(oracle.num_threads(), n), kind="oracle",
+                sample=f"{n} of {cfg.T} tokens of {cfg.name}, whole layer per token in fp64 "
+                       f"(gate, routing, shared + {cfg.k} routed SwiGLU experts), {t:.1f} s")
+
+
+# ---- arms ----
+
+def run_reference(args, world, rank):
+    cfg = inputs.CONFIGS[args.workload]
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    # the same seeded workload as the GPU arm (drawn on the GPU when there is one)
+    d = inputs.make_layer(cfg, "cuda" if torch.cuda.is_available() else "cpu")
+    host = host_layer(d)
+    del d
+    toks = sample_tokens(cfg, args.ref_tokens)
+    for _ in range(args.warmup):
+        oracle_layer_time(cfg, host, toks)
+    times = [oracle_layer_time(cfg, host, toks) for _ in range(args.steps)]
+    per_step = sum(times) / len(times)
+    value = args.ref_tokens / per_step
+    cores = min(oracle.num_threads(), args.ref_tokens)
+    line = dict(metric=METRIC, value=value, unit=UNIT, n_gpus=args.gpus, steps=args.steps, warmup=args.warmup,
+                ms_per_step=per_step * 1e3, higher_is_better=True, scaling="weak", vs_baseline=None,
+                dtype="f64", data="synthetic", impl="reference",
+                config=dict(workload=cfg.name, T=cfg.T, H=cfg.H, E=cfg.E, k=cfg.k, I=cfg.I, S=cfg.S,
+                            tokens_per_step=args.ref_tokens),
+                cpu_baseline=dict(value=value, unit=UNIT, cores=cores, kind="oracle",
+                                  sample=f"{args.ref_tokens} of {cfg.T} tokens of {cfg.name} per step"),
+                e2e=dict(value=value, unit=UNIT, h2d_bytes_per_step=0, d2h_bytes_per_step=0))
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, world, rank, local):
+    from moe_expert_routing_route_gb300 import binding
+
+    cfg = inputs.CONFIGS[args.workload]
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    import __graft_entry__
+    __graft_entry__.build_library()
+
+    d = inputs.make_layer(cfg, dev)
+    layer = binding.MoELayer(T=cfg.T, k=cfg.k, w_router=d["wg"], w_gate=d["w_gate"], w_up=d["w_up"], w2=d["w2"],
+                             s_gate=d["s_gate"] if cfg.S else None, s_up=d["s_up"] if cfg.S else None,
+                             s2=d["s2"] if cfg.S else None, expert_bias=d["bias"], renormalize=cfg.renormalize)
+    x = d["x"]
+    out = torch.empty_like(x)
+    stream = torch.cuda.current_stream()
+    nst = binding.MOE_NUM_STAGES
+    for _ in range(args.warmup):
+        layer.forward(x, out)
+    torch.cuda.synchronize()
+    if layer.device_status() != 0:
+        raise RuntimeError("device status word set during warm-up")
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nst + 1)] for _ in range(args.steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local)
+    time.sleep(0.1)
+    launches0 = binding.launch_count()
+    barrier(world)
+    torch.cuda.synchronize()
+    wall0 = time.time()
+    start.record(stream)
+    for i in range(args.steps):
+        layer.forward(x, out, events=evs[i])
+    end.record(stream)
+    torch.cuda.synchronize()
+    wall1 = time.time()
+    barrier(world)
+    launches = binding.launch_count() - launches0
+    clk = clocks.summary(wall0, wall1)
+    clocks.stop()
+    ms = start.elapsed_time(end) / args.steps
+    ms_max = max_over_ranks(ms, world)
+    stage_ms = {name: sum(evs[i][s].elapsed_time(evs[i][s + 1]) for i in range(args.steps)) / args.steps
+                for s, name in enumerate(binding.stage_names())}
+    if layer.device_status() != 0:
+        raise RuntimeError("device status word set during the timed region")
+
+    # roofline of the dominant kernel
+    counts = layer.field("tokens_per_expert").cpu().numpy()
+    touched = int((counts > 0).sum())
+    costs = roofline.stage_costs(cfg.T, cfg.H, cfg.E, cfg.k, cfg.I, cfg.S, cfg.esize, touched)
+    peaks = roofline.load_peaks()
+    top = max(stage_ms, key=stage_ms.get)
+    fl, by = costs[top]
+    rl = roofline.roofline_entry(fl, by, stage_ms[top] / 1e3, peaks, sustained=True)
+    rl["traffic"] = measured_traffic(top, cfg.name)
+    rl["kernel"] = top
+    rl["algorithmic_bytes"] = by
+    rl["algorithmic_flops"] = fl
+    rl["peak_source"] = peaks["source"]
+    stages = {}
+    for name, t in stage_ms.items():
+        f_, b_ = costs[name]
+        stages[name] = dict(us=round(t * 1e3, 2), tflops=round(f_ / (t / 1e3) / 1e12, 2) if t > 0 else None,
+                            gbs=round(b_ / (t / 1e3) / 1e9, 1) if t > 0 else None)
+    layer_fl = sum(f for f, _ in costs.values())
+    gemm_fl = sum(costs[s][0] for s in ("up_routed", "down_routed", "up_shared", "down_shared"))
+    gemm_ms = sum(stage_ms[s] for s in ("up_routed", "down_routed", "up_shared", "down_shared"))
+
+    # end to end from pinned host memory through the C ABI
+    x_host = x.cpu().pin_memory()
+    out_host = torch.empty_like(x_host).pin_memory()
+    layer.forward_host(x_host, out_host)
+    barrier(world)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        layer.forward_host(x_host, out_host)
+    e2e_s = (time.perf_counter() - t0) / args.steps
+    e2e_s = max_over_ranks(e2e_s, world)
+    nbytes_io = x.numel() * x.element_size()
+
+    cpu = None
+    if world == 1 and rank == 0 and not args.no_cpu_baseline:
+        import oracle
+        oracle.build()
+        cpu = cpu_baseline(cfg, host_layer(d), budget_s=args.cpu_budget)
+
+    if rank == 0:
+        tokens = cfg.T * world
+        line = dict(metric=METRIC, value=tokens / (ms_max / 1e3), unit=UNIT, n_gpus=world, steps=args.steps,
+                    warmup=args.warmup, ms_per_step=ms_max, higher_is_better=True, scaling="weak",
+                    vs_baseline=None, dtype=cfg.dtype, data="synthetic (seeded N(0,1) x, N(0,1/sqrt(fan_in)) "
+                    "weights, random-init DeepSeek-V3-shaped MoE layer)",
+                    config=dict(workload=cfg.name, T=cfg.T, H=cfg.H, E=cfg.E, k=cfg.k, I=cfg.I, S=cfg.S,
+                                global_batch=tokens, parallelism=f"replicas{world}",
+                                l2="inputs larger than L2: 22.6 GB of expert weights streamed every step"
+                                if cfg.H == 7168 else "small workload"),
+                    roofline=rl, cpu_baseline=cpu,
+                    e2e=dict(value=tokens / e2e_s, unit=UNIT, h2d_bytes_per_step=nbytes_io,
+                             d2h_bytes_per_step=nbytes_io),
+                    gpu_launches=int(launches), clocks=clk, stages=stages,
+                    grouped_gemm=dict(tflops=round(gemm_fl / (gemm_ms / 1e3) / 1e12, 1),
+                                      frac_of_bf16_peak=round(gemm_fl / (gemm_ms / 1e3) / 1e12 /
+                                                              peaks["bf16_tflops_sustained"], 3)),
+                    layer_tflops=round(layer_fl / (ms_max / 1e3) / 1e12, 1))
+        print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="dsv3_prefill", choices=sorted(inputs.CONFIGS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
+    ap.add_argument("--ref-tokens", type=int, default=16, help="tokens per step for --impl reference")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        args.warmup = 3
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+    else:
+        run_ours(args, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,251 @@
+/*
+ * moe.h -- C ABI of libmoe, the single-GPU MoE layer hot path for GB300 (sm_103a).
+ *
+ *   logits = x Wr^T                     (gate GEMM)
+ *   top-k routing                       (moe_route_topk)
+ *   init-routing permutation            (moe_init_routing)
+ *   per-expert SwiGLU FFN, grouped GEMM (moe_grouped_ffn)
+ *   finalize-routing + shared expert    (moe_finalize_routing)
+ *   all of the above on one stream      (moe_layer_forward)
+ *
+ * Sources for the operations (cited per entry point below):
+ *   [BLOG] "Lower latency and higher throughput with multi-node DeepSeek
+ *          deployment" (Perplexity blog): §Expert Parallelism, §Roofline /
+ *          GroupGEMM, §Roofline / GEMM, §Quantization, §CUDA Graph, §MoE Router.
+ *   [CANN] "DeepSeek-R1 prefill inference optimisation on Atlas A3"
+ *          (cann-recipes-infer): §MoE deployment strategy, Double-Routing
+ *          steps 1 (init-routing), 6 (argsort inverse) and 8 (finalize-routing).
+ *
+ * Conventions shared by every entry point:
+ *   - Every pointer argument is a DEVICE pointer unless its name ends in _host.
+ *     The caller allocates and owns all memory, including workspaces; the
+ *     library never allocates, frees or synchronises (except
+ *     moe_check_device_status and moe_layer_forward_host, which say so).
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default
+ *     stream).  Apart from moe_layer_forward_host and moe_check_device_status
+ *     they issue no host synchronisation, so a sequence of calls can be
+ *     captured into a CUDA graph.
+ *   - Device pointers must be 16-byte aligned.  Matrices are row-major and
+ *     contiguous; weights are stored like Linear weights, [out, in] with the
+ *     reduction dimension contiguous.
+ *   - dtype: MOE_F32 (float) or MOE_BF16 (bfloat16).  Accumulation is fp32.
+ *   - Argument errors are returned synchronously (MOE_ERR_INVALID_ARG,
+ *     MOE_ERR_UNSUPPORTED) before anything is enqueued.  A failed launch returns
+ *     MOE_ERR_CUDA.  Data errors found on the device (an expert id outside
+ *     [0,E), a row index outside its buffer, inconsistent offsets, a bounded
+ *     wait that ran out) never trap: the kernel skips the offending row, sets a
+ *     bit in the status word at the start of the workspace and carries on.
+ *     Every entry point that takes a workspace clears that word first;
+ *     moe_check_device_status reads it.  After a data error the outputs are
+ *     unspecified.
+ *   - Sizes: 0 <= T, 1 <= k <= min(E, 32), E <= 1024, H % 8 == 0, I % 8 == 0,
+ *     T*k < 2^31.  T == 0 is a no-op.
+ */
+#ifndef MOE_H
+#define MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* moe_stream_t; /* identical to cudaStream_t */
+
+typedef enum moe_status {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = 1, /* null pointer, size out of range, workspace too small */
+    MOE_ERR_UNSUPPORTED = 2, /* valid request outside what the kernels handle (alignment, dtype, shape) */
+    MOE_ERR_CUDA = 3,        /* a CUDA runtime call or a launch failed */
+    MOE_ERR_DEVICE = 4       /* moe_check_device_status: the device status word is non-zero */
+} moe_status_t;
+
+typedef enum moe_dtype { MOE_F32 = 0, MOE_BF16 = 1 } moe_dtype_t;
+
+/* Bits of the device status word (first 4 bytes of a workspace). */
+#define MOE_DEVERR_BAD_EXPERT_ID 0x1u /* init-routing met an id outside [0,E) */
+#define MOE_DEVERR_BAD_ROW_INDEX 0x2u /* finalize met an expanded_row_idx outside [0,rows) */
+#define MOE_DEVERR_BAD_OFFSETS 0x4u   /* grouped FFN got decreasing or out-of-range offsets */
+#define MOE_DEVERR_TIMEOUT 0x8u       /* a bounded on-chip wait gave up (about one second) */
+
+/* Every workspace starts with this many bytes of header (the status word). */
+#define MOE_WS_HEADER_BYTES 256
+
+/* Version of this ABI; bumped on any incompatible change. */
+int moe_abi_version(void);
+
+/* Human-readable name of a status code (static storage). */
+const char* moe_status_string(moe_status_t status);
+
+/* Number of kernels this library has launched in this process (all devices). */
+uint64_t moe_kernel_launch_count(void);
+
+/* Synchronises `stream`, then reads and returns the status word of `ws` in
+ * *word (may be NULL).  Returns MOE_OK if the word is zero, MOE_ERR_DEVICE if
+ * not, MOE_ERR_CUDA if the synchronisation failed.  This call blocks. */
+moe_status_t moe_check_device_status(const void* ws, moe_stream_t stream, uint32_t* word);
+
+/* ---------------------------------------------------------------------------
+ * Gate GEMM.  [BLOG §Roofline / GEMM]: a Linear projection is [m,k]x[k,n].
+ *   logits[t,e] = sum_h x[t,h] * w_router[e,h]        (fp32 accumulate and out)
+ * x [T,H], w_router [E,H] in dt; logits [T,E] fp32.
+ * bf16 runs on tcgen05 tensor cores; fp32 runs on the FFMA pipes. */
+moe_status_t moe_gate_logits(const void* x, const void* w_router, moe_dtype_t dt, int T, int H,
+                             int E, float* logits, moe_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * Top-k routing.  [BLOG §MoE Router]: top-k of the router scores, keeping
+ * the indices of the selected experts; [BLOG §Expert Parallelism]: each token
+ * goes to k distinct routed experts whose outputs are summed with weights.
+ *   s_e        = logits[t,e] + expert_bias[e]   (one fp32 add; bias may be NULL)
+ *   topk_ids   = the k experts with the largest s, in descending order of s;
+ *                equal scores go to the lower expert id (ids are distinct)
+ *   topk_w     = softmax over all E scores, taken at the selected experts;
+ *                with renormalize != 0 divided by their sum (so they sum to 1)
+ * logits [T,E] fp32, finite; expert_bias [E] fp32 or NULL;
+ * topk_ids [T,k] int32, topk_w [T,k] fp32 (outputs, row-major). */
+moe_status_t moe_route_topk(const float* logits, const float* expert_bias, int T, int E, int k,
+                            int renormalize, int32_t* topk_ids, float* topk_w, moe_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * Init-routing.  [CANN §MoE deployment, Double-Routing step 1]: expand every
+ * token k times and sort the copies by expert, returning expanded_x,
+ * expanded_row_idx (which restores the original order) and tokens_per_expert.
+ * With source row src = t*k + j (token-major):
+ *   tokens_per_expert[e] = #{src : topk_ids[src] == e}
+ *   expert_offsets[e]    = sum_{e' < e} tokens_per_expert[e'],  expert_offsets[E] = T*k
+ *   expanded_row_idx[src] = expert_offsets[id] + #{src' < src : topk_ids[src'] == id}
+ *   expanded_x[expanded_row_idx[src], :] = x[src / k, :]
+ * i.e. a stable sort by expert id; no token is dropped or padded.
+ * x [T,H] dt; topk_ids [T,k] int32 (ids need not be distinct);
+ * outputs expanded_x [T*k,H] dt, expanded_row_idx [T*k] int32,
+ * tokens_per_expert [E] int32, expert_offsets [E+1] int32.
+ * ws: at least moe_init_routing_workspace_bytes(T,E,k) bytes (scratch +
+ * status word).  An id outside [0,E) is not counted, its expanded_row_idx is
+ * -1 and MOE_DEVERR_BAD_EXPERT_ID is set. */
+size_t moe_init_routing_workspace_bytes(int T, int E, int k);
+moe_status_t moe_init_routing(const void* x, moe_dtype_t dt, const int32_t* topk_ids, int T, int H,
+                              int E, int k, void* expanded_x, int32_t* expanded_row_idx,
+                              int32_t* tokens_per_expert, int32_t* expert_offsets, void* ws,
+                              size_t ws_bytes, moe_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * Expert weight packing for the grouped FFN.  Interleaves each expert's gate
+ * and up projections in blocks of 128 output rows so that one GEMM tile holds
+ * matching gate and up columns (the SwiGLU epilogue needs both):
+ *   Ip = I rounded up to a multiple of 128
+ *   packed[e, 256*b + r,       :] = w_gate[e, 128*b + r, :]   (0 <= r < 128)
+ *   packed[e, 256*b + 128 + r, :] = w_up  [e, 128*b + r, :]
+ * rows past I are zero.  w_gate, w_up [E,I,H] dt; packed [E, 2*Ip, H] dt,
+ * moe_w13_packed_bytes(dt,E,H,I) bytes.  Shared experts are packed the same
+ * way with E = 1 and I = S*I (their gate/up rows stacked). */
+size_t moe_w13_packed_bytes(moe_dtype_t dt, int E, int H, int I);
+moe_status_t moe_pack_w13(const void* w_gate, const void* w_up, moe_dtype_t dt, int E, int H, int I,
+                          void* w13_packed, moe_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * Grouped SwiGLU expert FFN.  [BLOG §Roofline / GroupGEMM]: g groups, group i
+ * multiplies [m_i,k]x[k,n]; here group e is expert e's segment of rows
+ * [expert_offsets[e], expert_offsets[e+1]) of `a`.  [BLOG §Expert Parallelism]
+ * and [BLOG §Quantization] (SiLU):
+ *   h[r,:] = silu(a[r,:] Wgate_e^T) * (a[r,:] Wup_e^T),  silu(z) = z/(1+exp(-z))
+ *   y[r,:] = h[r,:] W2_e^T
+ * h is stored in dt (fp32 accumulate, one rounding), y likewise.  Group sizes
+ * are read on the device (no host round trip), so expert_offsets can be the
+ * output of moe_init_routing on the same stream.
+ * a [rows,H] dt; expert_offsets [E+1] int32 (device), or NULL for one group of
+ * all `rows` rows (E must then be 1); w13_packed from moe_pack_w13; w2 [E,H,I];
+ * y [rows,H] dt (rows outside every segment are left untouched).
+ * ws: at least moe_grouped_ffn_workspace_bytes(dt,rows,I) bytes (h + status).
+ * bf16 runs on tcgen05 tensor cores (TMA-fed, persistent, device-side tile
+ * scheduler); fp32 runs on the FFMA pipes. */
+size_t moe_grouped_ffn_workspace_bytes(moe_dtype_t dt, int rows, int I);
+moe_status_t moe_grouped_ffn(const void* a, moe_dtype_t dt, const int32_t* expert_offsets, int E,
+                             int rows, int H, int I, const void* w13_packed, const void* w2, void* y,
+                             void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * Finalize-routing.  [CANN §MoE deployment, Double-Routing step 8]: restore
+ * the token order through expanded_src_to_dst_row, weight by scales=topk_weight
+ * and add the shared expert output (skip1):
+ *   out[t,:] = skip[t,:] + sum_j topk_w[t,j] * y[expanded_row_idx[t*k+j], :]
+ * summed in fp32 and rounded once to dt.  y [y_rows,H] dt; skip [T,H] dt or
+ * NULL; topk_w [T,k] fp32; expanded_row_idx [T*k] int32; out [T,H] dt.
+ * ws: NULL, or a workspace of at least MOE_WS_HEADER_BYTES whose status word
+ * receives MOE_DEVERR_BAD_ROW_INDEX for an index outside [0,y_rows) (that
+ * term is skipped either way). */
+moe_status_t moe_finalize_routing(const void* y, int64_t y_rows, const void* skip, const float* topk_w,
+                                  const int32_t* expanded_row_idx, moe_dtype_t dt, int T, int H, int k,
+                                  void* out, void* ws, moe_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * The whole layer.  [BLOG §Expert Parallelism]: out[t] = shared(x_t) +
+ * sum_j w_j FFN_{e_j}(x_t) with 8-of-256 style top-k routing; the steps above
+ * run back to back on one stream with fixed grids and no host synchronisation
+ * ([BLOG §Quantization]: persistent kernels read the routing counts on the
+ * device; [BLOG §CUDA Graph]: the call can be captured in a CUDA graph). */
+typedef struct moe_layer_desc {
+    int T;  /* tokens */
+    int H;  /* hidden size */
+    int E;  /* routed experts */
+    int k;  /* experts per token */
+    int I;  /* intermediate size of one expert */
+    int S;  /* shared experts (each of intermediate size I); 0 = none */
+    moe_dtype_t dtype;
+    int renormalize;           /* top-k weights renormalised to sum 1 */
+    const void* w_router;      /* [E,H] */
+    const float* expert_bias;  /* [E] fp32 added to the logits, or NULL */
+    const void* w13;           /* moe_pack_w13(w_gate [E,I,H], w_up [E,I,H]) */
+    const void* w2;            /* [E,H,I] */
+    const void* w13_shared;    /* moe_pack_w13 with E=1, I=S*I of the stacked shared gate/up [S*I,H]; NULL iff S == 0 */
+    const void* w2_shared;     /* [H, S*I]: the shared down projections side by side; NULL iff S == 0 */
+} moe_layer_desc;
+
+/* Layer steps timed by moe_layer_forward_timed, in launch order. */
+#define MOE_NUM_STAGES 9
+const char* moe_stage_name(int stage); /* "gate", "route", "init_routing", "permute_rows",
+                                          "up_routed", "up_shared", "down_routed",
+                                          "down_shared", "finalize" */
+
+/* Workspace fields of the layer (intermediates a caller may inspect). */
+typedef enum moe_ws_field {
+    MOE_WS_LOGITS = 0,            /* [T,E] fp32 */
+    MOE_WS_TOPK_IDS = 1,          /* [T,k] int32 */
+    MOE_WS_TOPK_W = 2,            /* [T,k] fp32 */
+    MOE_WS_TOKENS_PER_EXPERT = 3, /* [E] int32 */
+    MOE_WS_EXPERT_OFFSETS = 4,    /* [E+1] int32 */
+    MOE_WS_EXPANDED_ROW_IDX = 5,  /* [T*k] int32 */
+    MOE_WS_EXPANDED_X = 6,        /* [T*k,H] dt */
+    MOE_WS_H_ROUTED = 7,          /* [T*k,I] dt */
+    MOE_WS_H_SHARED = 8,          /* [T,S*I] dt */
+    MOE_WS_Y_ROUTED = 9,          /* [T*k,H] dt */
+    MOE_WS_Y_SHARED = 10,         /* [T,H] dt */
+    MOE_WS_X_IN = 11,             /* [T,H] dt: staging for moe_layer_forward_host */
+    MOE_WS_OUT = 12,              /* [T,H] dt: staging for moe_layer_forward_host */
+    MOE_WS_NUM_FIELDS = 13
+} moe_ws_field;
+
+size_t moe_layer_workspace_bytes(const moe_layer_desc* desc);
+moe_status_t moe_layer_workspace_field(const moe_layer_desc* desc, moe_ws_field field, size_t* offset,
+                                       size_t* bytes);
+
+/* x [T,H] dt, out [T,H] dt, ws of moe_layer_workspace_bytes(desc) bytes. */
+moe_status_t moe_layer_forward(const moe_layer_desc* desc, const void* x, void* out, void* ws,
+                               size_t ws_bytes, moe_stream_t stream);
+
+/* As moe_layer_forward, also recording stage_events[i] (cudaEvent_t) before
+ * step i and stage_events[MOE_NUM_STAGES] after the last one. */
+moe_status_t moe_layer_forward_timed(const moe_layer_desc* desc, const void* x, void* out, void* ws,
+                                     size_t ws_bytes, moe_stream_t stream, void* const* stage_events);
+
+/* End to end from HOST memory: copies x_host [T,H] into the workspace, runs
+ * the layer, copies the result to out_host [T,H] and synchronises `stream`
+ * (this call blocks).  Pinned host buffers give asynchronous copies. */
+moe_status_t moe_layer_forward_host(const moe_layer_desc* desc, const void* x_host, void* out_host,
+                                    void* ws, size_t ws_bytes, moe_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_H */

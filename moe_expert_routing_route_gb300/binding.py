@@ -1,0 +1,280 @@
+"""Thin ctypes binding of libmoe (include/moe.h).
+
+Argument marshalling only: every step of the layer runs in the CUDA kernels of
+libmoe.so.  PyTorch supplies device memory, streams and events.  There is no
+fallback: if libmoe.so is missing or a call fails, an exception is raised.
+Function names follow the C ABI.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libmoe.so")
+
+MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA, MOE_ERR_DEVICE = range(5)
+MOE_F32, MOE_BF16 = 0, 1
+MOE_DEVERR_BAD_EXPERT_ID, MOE_DEVERR_BAD_ROW_INDEX, MOE_DEVERR_BAD_OFFSETS, MOE_DEVERR_TIMEOUT = 1, 2, 4, 8
+MOE_WS_HEADER_BYTES = 256
+MOE_NUM_STAGES = 9
+WS_FIELDS = ["logits", "topk_ids", "topk_w", "tokens_per_expert", "expert_offsets", "expanded_row_idx",
+             "expanded_x", "h_routed", "h_shared", "y_routed", "y_shared", "x_in", "out"]
+
+# The exported entry points (name -> (restype, argtypes)).
+P, I32, I64, SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t
+
+
+class LayerDesc(ctypes.Structure):
+    _fields_ = [("T", I32), ("H", I32), ("E", I32), ("k", I32), ("I", I32), ("S", I32), ("dtype", I32),
+                ("renormalize", I32), ("w_router", P), ("expert_bias", P), ("w13", P), ("w2", P),
+                ("w13_shared", P), ("w2_shared", P)]
+
+
+_DP = ctypes.POINTER(LayerDesc)
+SIGNATURES = {
+    "moe_abi_version": (I32, []),
+    "moe_status_string": (ctypes.c_char_p, [I32]),
+    "moe_kernel_launch_count": (ctypes.c_uint64, []),
+    "moe_check_device_status": (I32, [P, P, ctypes.POINTER(ctypes.c_uint32)]),
+    "moe_gate_logits": (I32, [P, P, I32, I32, I32, I32, P, P]),
+    "moe_route_topk": (I32, [P, P, I32, I32, I32, I32, P, P, P]),
+    "moe_init_routing_workspace_bytes": (SZ, [I32, I32, I32]),
+    "moe_init_routing": (I32, [P, I32, P, I32, I32, I32, I32, P, P, P, P, P, SZ, P]),
+    "moe_w13_packed_bytes": (SZ, [I32, I32, I32, I32]),
+    "moe_pack_w13": (I32, [P, P, I32, I32, I32, I32, P, P]),
+    "moe_grouped_ffn_workspace_bytes": (SZ, [I32, I32, I32]),
+    "moe_grouped_ffn": (I32, [P, I32, P, I32, I32, I32, I32, P, P, P, P, SZ, P]),
+    "moe_finalize_routing": (I32, [P, I64, P, P, P, I32, I32, I32, I32, P, P, P]),
+    "moe_stage_name": (ctypes.c_char_p, [I32]),
+    "moe_layer_workspace_bytes": (SZ, [_DP]),
+    "moe_layer_workspace_field": (I32, [_DP, I32, ctypes.POINTER(SZ), ctypes.POINTER(SZ)]),
+    "moe_layer_forward": (I32, [_DP, P, P, P, SZ, P]),
+    "moe_layer_forward_timed": (I32, [_DP, P, P, P, SZ, P, ctypes.POINTER(P)]),
+    "moe_layer_forward_host": (I32, [_DP, P, P, P, SZ, P]),
+}
+
+_lock = threading.Lock()
+_lib = None
+
+
+class MoEError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        name = lib().moe_status_string(status).decode() if _lib is not None else str(status)
+        super().__init__(f"{what} failed: {name}")
+
+
+def lib():
+    """Load libmoe.so (built by __graft_entry__.build() or python -m ...build)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(f"libmoe.so not found at {LIB_PATH}: build it first "
+                                   "(python -c 'import __graft_entry__ as g; g.build()')")
+            L = ctypes.CDLL(LIB_PATH)
+            for name, (res, args) in SIGNATURES.items():
+                fn = getattr(L, name)
+                fn.restype = res
+                fn.argtypes = args
+            _lib = L
+        return _lib
+
+
+def _check(st: int, what: str):
+    if st != MOE_OK:
+        raise MoEError(st, what)
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("device tensors expected")
+    if not t.is_contiguous():
+        raise ValueError("contiguous tensors expected")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _dt(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return MOE_F32
+    if t.dtype == torch.bfloat16:
+        return MOE_BF16
+    raise TypeError(f"float32 or bfloat16 expected, got {t.dtype}")
+
+
+def launch_count() -> int:
+    return int(lib().moe_kernel_launch_count())
+
+
+def moe_check_device_status(ws: torch.Tensor, stream=None) -> int:
+    """Synchronise and return the status word of a workspace (0 = no device error)."""
+    word = ctypes.c_uint32(0)
+    st = lib().moe_check_device_status(_ptr(ws), _stream(stream), ctypes.byref(word))
+    if st not in (MOE_OK, MOE_ERR_DEVICE):
+        _check(st, "moe_check_device_status")
+    return int(word.value)
+
+
+def moe_gate_logits(x: torch.Tensor, w_router: torch.Tensor, stream=None) -> torch.Tensor:
+    T, H = x.shape
+    E = w_router.shape[0]
+    logits = torch.empty((T, E), dtype=torch.float32, device=x.device)
+    _check(lib().moe_gate_logits(_ptr(x), _ptr(w_router), _dt(x), T, H, E, _ptr(logits), _stream(stream)),
+           "moe_gate_logits")
+    return logits
+
+
+def moe_route_topk(logits: torch.Tensor, k: int, renormalize: bool = True, expert_bias=None, stream=None):
+    T, E = logits.shape
+    ids = torch.empty((T, k), dtype=torch.int32, device=logits.device)
+    w = torch.empty((T, k), dtype=torch.float32, device=logits.device)
+    _check(lib().moe_route_topk(_ptr(logits), _ptr(expert_bias), T, E, k, int(bool(renormalize)), _ptr(ids),
+                                _ptr(w), _stream(stream)), "moe_route_topk")
+    return ids, w
+
+
+def moe_init_routing(x: torch.Tensor, topk_ids: torch.Tensor, E: int, stream=None, ws=None) -> dict:
+    T, H = x.shape
+    k = topk_ids.shape[1]
+    dev = x.device
+    need = lib().moe_init_routing_workspace_bytes(T, E, k)
+    if ws is None:
+        ws = torch.empty(need, dtype=torch.uint8, device=dev)
+    out = dict(expanded_x=torch.empty((T * k, H), dtype=x.dtype, device=dev),
+               expanded_row_idx=torch.empty(T * k, dtype=torch.int32, device=dev),
+               tokens_per_expert=torch.empty(E, dtype=torch.int32, device=dev),
+               expert_offsets=torch.empty(E + 1, dtype=torch.int32, device=dev), ws=ws)
+    _check(lib().moe_init_routing(_ptr(x), _dt(x), _ptr(topk_ids), T, H, E, k, _ptr(out["expanded_x"]),
+                                  _ptr(out["expanded_row_idx"]), _ptr(out["tokens_per_expert"]),
+                                  _ptr(out["expert_offsets"]), _ptr(ws), ws.numel(), _stream(stream)),
+           "moe_init_routing")
+    return out
+
+
+def moe_pack_w13(w_gate: torch.Tensor, w_up: torch.Tensor, stream=None) -> torch.Tensor:
+    """w_gate, w_up [E,I,H] (or [I,H] for one expert) -> packed [E, 2*Ip, H]."""
+    if w_gate.dim() == 2:
+        w_gate, w_up = w_gate.unsqueeze(0), w_up.unsqueeze(0)
+    E, I, H = w_gate.shape
+    dt = _dt(w_gate)
+    nbytes = lib().moe_w13_packed_bytes(dt, E, H, I)
+    packed = torch.empty(nbytes // w_gate.element_size(), dtype=w_gate.dtype, device=w_gate.device)
+    _check(lib().moe_pack_w13(_ptr(w_gate), _ptr(w_up), dt, E, H, I, _ptr(packed), _stream(stream)),
+           "moe_pack_w13")
+    return packed.view(E, -1, H)
+
+
+def moe_grouped_ffn(a: torch.Tensor, expert_offsets, E: int, I: int, w13_packed: torch.Tensor,
+                    w2: torch.Tensor, y: torch.Tensor | None = None, ws=None, stream=None):
+    rows, H = a.shape
+    dt = _dt(a)
+    need = lib().moe_grouped_ffn_workspace_bytes(dt, rows, I)
+    if ws is None:
+        ws = torch.empty(need, dtype=torch.uint8, device=a.device)
+    if y is None:
+        y = torch.zeros((rows, H), dtype=a.dtype, device=a.device)
+    _check(lib().moe_grouped_ffn(_ptr(a), dt, _ptr(expert_offsets), E, rows, H, I, _ptr(w13_packed), _ptr(w2),
+                                 _ptr(y), _ptr(ws), ws.numel(), _stream(stream)), "moe_grouped_ffn")
+    return y, ws
+
+
+def moe_finalize_routing(y: torch.Tensor, topk_w: torch.Tensor, expanded_row_idx: torch.Tensor,
+                         skip: torch.Tensor | None = None, ws=None, stream=None) -> torch.Tensor:
+    T, k = topk_w.shape
+    H = y.shape[1]
+    out = torch.empty((T, H), dtype=y.dtype, device=y.device)
+    _check(lib().moe_finalize_routing(_ptr(y), y.shape[0], _ptr(skip), _ptr(topk_w), _ptr(expanded_row_idx),
+                                      _dt(y), T, H, k, _ptr(out), _ptr(ws), _stream(stream)),
+           "moe_finalize_routing")
+    return out
+
+
+def stage_names() -> list[str]:
+    return [lib().moe_stage_name(i).decode() for i in range(MOE_NUM_STAGES)]
+
+
+class MoELayer:
+    """A MoE layer whose weights live on the device, with its workspace.
+
+    Weights: w_router [E,H]; w_gate, w_up [E,I,H]; w2 [E,H,I]; shared experts
+    s_gate, s_up [S,I,H], s2 [S,H,I] (S may be 0); expert_bias [E] fp32 or None.
+    The gate/up weights are packed once (moe_pack_w13)."""
+
+    def __init__(self, *, T: int, k: int, w_router, w_gate, w_up, w2, s_gate=None, s_up=None, s2=None,
+                 expert_bias=None, renormalize: bool = True, stream=None):
+        E, I, H = w_gate.shape
+        S = 0 if s_gate is None else s_gate.shape[0]
+        self.T, self.H, self.E, self.k, self.I, self.S = T, H, E, k, I, S
+        self.dtype = w_gate.dtype
+        self.w_router = w_router.contiguous()
+        self.w13 = moe_pack_w13(w_gate.contiguous(), w_up.contiguous(), stream)
+        self.w2 = w2.contiguous()
+        if S:
+            self.w13_shared = moe_pack_w13(s_gate.reshape(S * I, H).contiguous(),
+                                           s_up.reshape(S * I, H).contiguous(), stream)
+            # [S,H,I] -> [H, S*I]: the shared down projections side by side
+            self.w2_shared = s2.permute(1, 0, 2).reshape(H, S * I).contiguous()
+        else:
+            self.w13_shared = self.w2_shared = None
+        self.expert_bias = None if expert_bias is None else expert_bias.to(torch.float32).contiguous()
+        self.desc = LayerDesc(T, H, E, k, I, S, _dt(w_gate), int(bool(renormalize)), self.w_router.data_ptr(),
+                              0 if self.expert_bias is None else self.expert_bias.data_ptr(), self.w13.data_ptr(),
+                              self.w2.data_ptr(), 0 if S == 0 else self.w13_shared.data_ptr(),
+                              0 if S == 0 else self.w2_shared.data_ptr())
+        nbytes = lib().moe_layer_workspace_bytes(ctypes.byref(self.desc))
+        if nbytes == 0:
+            raise MoEError(MOE_ERR_INVALID_ARG, "moe_layer_workspace_bytes")
+        self.ws = torch.empty(nbytes, dtype=torch.uint8, device=w_gate.device)
+
+    def field(self, name: str) -> torch.Tensor:
+        """A view of one intermediate in the workspace (see moe_ws_field)."""
+        off, nb = SZ(0), SZ(0)
+        _check(lib().moe_layer_workspace_field(ctypes.byref(self.desc), WS_FIELDS.index(name), ctypes.byref(off),
+                                               ctypes.byref(nb)), "moe_layer_workspace_field")
+        raw = self.ws[off.value:off.value + nb.value]
+        T, H, E, k, I, S = self.T, self.H, self.E, self.k, self.I, self.S
+        shapes = dict(logits=((T, E), torch.float32), topk_ids=((T, k), torch.int32),
+                      topk_w=((T, k), torch.float32), tokens_per_expert=((E,), torch.int32),
+                      expert_offsets=((E + 1,), torch.int32), expanded_row_idx=((T * k,), torch.int32),
+                      expanded_x=((T * k, H), self.dtype), h_routed=((T * k, I), self.dtype),
+                      h_shared=((T, S * I), self.dtype), y_routed=((T * k, H), self.dtype),
+                      y_shared=((T, H), self.dtype), x_in=((T, H), self.dtype), out=((T, H), self.dtype))
+        shape, dtype = shapes[name]
+        return raw.view(dtype).view(shape)
+
+    def forward(self, x: torch.Tensor, out: torch.Tensor | None = None, stream=None, events=None):
+        if out is None:
+            out = torch.empty_like(x)
+        if events is None:
+            st = lib().moe_layer_forward(ctypes.byref(self.desc), _ptr(x), _ptr(out), _ptr(self.ws),
+                                         self.ws.numel(), _stream(stream))
+        else:
+            arr = (P * (MOE_NUM_STAGES + 1))(*[ctypes.c_void_p(e.cuda_event) for e in events])
+            st = lib().moe_layer_forward_timed(ctypes.byref(self.desc), _ptr(x), _ptr(out), _ptr(self.ws),
+                                               self.ws.numel(), _stream(stream), arr)
+        _check(st, "moe_layer_forward")
+        return out
+
+    def forward_host(self, x_host: torch.Tensor, out_host: torch.Tensor, stream=None):
+        """End to end from host memory (blocks until out_host is written)."""
+        if x_host.is_cuda or out_host.is_cuda:
+            raise ValueError("host tensors expected")
+        st = lib().moe_layer_forward_host(ctypes.byref(self.desc), ctypes.c_void_p(x_host.data_ptr()),
+                                          ctypes.c_void_p(out_host.data_ptr()), _ptr(self.ws), self.ws.numel(),
+                                          _stream(stream))
+        _check(st, "moe_layer_forward_host")
+        return out_host
+
+    def device_status(self, stream=None) -> int:
+        return moe_check_device_status(self.ws, stream)

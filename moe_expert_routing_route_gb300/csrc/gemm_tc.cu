@@ -1,0 +1,553 @@
+// Grouped GEMM on the 5th-generation tensor cores (tcgen05 + TMEM), fed by TMA.
+//
+// "Lower latency and higher throughput with multi-node DeepSeek deployment"
+// (Perplexity blog):
+//   §Roofline / GroupGEMM: g groups, group i computes [m_i,k]x[k,n]; FLOPs
+//     2*g*m*k*n, I/O bytes g*(m*k + n*k + m*n) -- here group e is expert e's
+//     segment of the expert-sorted rows.
+//   §Quantization: a fixed number of persistent kernels read the routing
+//     information on the device to find how many tokens each expert got and
+//     split the work dynamically, instead of sizing work by buffer upper
+//     bounds (which breaks under CUDA graphs).  The grid here is one CTA per
+//     SM; every CTA rebuilds the tile table from the expert offsets in device
+//     memory and walks the tiles blockIdx.x, blockIdx.x + gridDim.x, ...
+//   §Quantization: SiLU is applied to the up-projection output; here it is
+//     fused into the GEMM epilogue (SwiGLU: h = silu(gate) * up).
+//
+// Per CTA (192 threads):
+//   warp 0, one lane   TMA producer: A tile [128 x 64] and B tile [BN x 64]
+//                      per k-block into a ring of shared-memory stages
+//   warp 1, one lane   MMA issuer: 4 x tcgen05.mma (M=128, N=BN, K=16) per
+//                      stage into one of two TMEM accumulators; tcgen05.commit
+//                      frees the stage / publishes the accumulator
+//   warps 2..5         epilogue: tcgen05.ld of the accumulator (one row per
+//                      thread), SwiGLU / bf16 / fp32 conversion, masked stores
+// The two TMEM accumulators let the epilogue of tile i overlap the MMAs of
+// tile i+1.  Tiles are ordered (expert, n-tile, m-tile) with m fastest, so the
+// CTAs working on the m-tiles of one weight panel run side by side and share
+// it through L2.  Rows of a tile past the expert's segment belong to the next
+// expert (or are zero-filled past the buffer by TMA); they cost MMA work but
+// are never stored.
+//
+// Every wait on an mbarrier is bounded (about one second): on timeout the
+// waiting role raises an abort flag in shared memory and MOE_DEVERR_TIMEOUT in
+// the status word, every role leaves its loop, the producer waits (bounded) for
+// the copies it issued, the MMA thread waits (bounded) for its MMAs, and TMEM
+// is freed before the CTA exits.  No trap, no unbounded spin.
+#include "moe_internal.cuh"
+
+#include <cuda.h>
+#include <mutex>
+
+namespace moe {
+namespace {
+
+constexpr int BM = 128;      // MMA M (rows of A per tile), cta_group::1
+constexpr int BK = 64;       // k-block: one 128-byte swizzle row of bf16
+constexpr int UMMA_K = 16;   // K of one tcgen05.mma kind::f16
+constexpr int kThreads = 192;
+constexpr int kMaxGroups = 1024;
+constexpr int kPackBlock = 128;  // gate rows (and up rows) per packed block
+constexpr uint64_t kWaitLimitNs = 1000000000ull;
+
+template <int BN>
+struct Cfg {
+    static constexpr int A_BYTES = BM * BK * 2;
+    static constexpr int B_BYTES = BN * BK * 2;
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr int STAGES = BN == 256 ? 4 : (BN == 128 ? 6 : 8);
+    static constexpr int TMEM_COLS = 2 * BN;  // two fp32 accumulators
+    static constexpr int NUM_BARS = 2 * STAGES + 5;
+    static constexpr size_t SMEM = 1024 + (size_t)STAGES * STAGE_BYTES + NUM_BARS * 8 + 16 +
+                                   (size_t)(3 * kMaxGroups + 1) * 4;
+};
+
+struct Params {
+    const int32_t* offsets;
+    int G, M, K, Nb, N, NT;
+    void* C;
+    int64_t ldc;
+    uint32_t* status;
+};
+
+// ---- PTX wrappers -----------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+__device__ __forceinline__ uint64_t globaltimer() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x, int y) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];" ::"r"(
+            dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y)
+        : "memory");
+}
+__device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tmem_alloc(uint32_t slot, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot), "r"(ncols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void mma_bf16(uint32_t d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                         uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                 : "memory");
+}
+// 32 TMEM lanes x 32 consecutive 32-bit columns; the wait sits in the same
+// statement so the registers are only defined once the data has arrived.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
+          "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]),
+          "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]),
+          "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr)
+        : "memory");
+}
+
+// Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, rows of
+// 128 bytes, 8-row core-matrix groups 1024 bytes apart (stride byte offset),
+// leading byte offset unused for this layout (encoded 1), descriptor version 1.
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
+    return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
+           ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+// Instruction descriptor, kind::f16: D fp32, A and B bf16, both K-major, M x N.
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+// Bounded wait on an mbarrier phase.  Returns false when the wait ran out (and
+// then raises the abort flag) or when another role already aborted.
+__device__ __noinline__ bool wait_phase(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                        uint32_t* status) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer();
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((it & 31u) == 0) {
+            if (*abort_flag) return false;
+            if (globaltimer() - t0 > kWaitLimitNs) {
+                *abort_flag = 1;
+                set_status(status, MOE_DEVERR_TIMEOUT);
+                return false;
+            }
+        }
+    }
+}
+// Bounded wait used while shutting down: ignores the abort flag.
+__device__ __noinline__ void wait_drain(uint32_t bar, uint32_t parity, uint32_t* status) {
+    const uint64_t t0 = globaltimer();
+    while (!mbar_try_wait(bar, parity)) {
+        if (globaltimer() - t0 > kWaitLimitNs) {
+            set_status(status, MOE_DEVERR_TIMEOUT);
+            return;
+        }
+    }
+}
+
+// tile -> (group, m-tile, n-tile).  prefix[g] = first tile of group g,
+// prefix[G] = total; tiles of a group are n-major, m fastest.
+__device__ __forceinline__ void decode_tile(int tile, const int* prefix, int G, int NT, int& g, int& m, int& n) {
+    int lo = 0, hi = G - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (prefix[mid] <= tile) lo = mid;
+        else hi = mid - 1;
+    }
+    g = lo;
+    const int local = tile - prefix[g];
+    const int mt = (prefix[g + 1] - prefix[g]) / NT;
+    n = local / mt;
+    m = local - n * mt;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// Store 32 consecutive outputs of one row (columns col0..col0+31, valid below N).
+template <int EPI>
+__device__ __forceinline__ void store_row32(void* C, int64_t ldc, int64_t row, int col0, int N,
+                                            const float (&v)[32]) {
+    if (EPI == TC_EPI_F32) {
+        float* dst = static_cast<float*>(C) + row * ldc + col0;
+        if (col0 + 32 <= N && (ldc & 3) == 0) {
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+                reinterpret_cast<float4*>(dst)[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+        } else {
+#pragma unroll
+            for (int c = 0; c < 32; ++c)
+                if (col0 + c < N) dst[c] = v[c];
+        }
+    } else {
+        __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(C) + row * ldc + col0;
+        if (col0 + 32 <= N) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                uint4 u;
+                u.x = pack_bf16x2(v[8 * q + 0], v[8 * q + 1]);
+                u.y = pack_bf16x2(v[8 * q + 2], v[8 * q + 3]);
+                u.z = pack_bf16x2(v[8 * q + 4], v[8 * q + 5]);
+                u.w = pack_bf16x2(v[8 * q + 6], v[8 * q + 7]);
+                reinterpret_cast<uint4*>(dst)[q] = u;
+            }
+        } else {
+#pragma unroll
+            for (int c = 0; c < 32; ++c)
+                if (col0 + c < N) dst[c] = __float2bfloat16_rn(v[c]);
+        }
+    }
+}
+
+template <int BN, int EPI>
+__global__ void __launch_bounds__(kThreads, 1)
+tc_grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
+                       const Params p) {
+    using Cf = Cfg<BN>;
+    constexpr int STAGES = Cf::STAGES;
+    constexpr uint32_t IDESC = idesc_bf16(BM, BN);
+    static_assert(EPI != TC_EPI_SWIGLU || BN == 2 * kPackBlock, "SwiGLU tiles hold one packed block");
+
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_addr = smem_u32(smem_raw);
+    uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
+    uint8_t* sA = smem;
+    uint8_t* sB = smem + STAGES * Cf::A_BYTES;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sB + STAGES * Cf::B_BYTES);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + Cf::NUM_BARS);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    int* prefix = reinterpret_cast<int*>(tmem_slot + 4);  // [G+1]
+    int* gstart = prefix + kMaxGroups + 1;               // [G]
+    int* gend = gstart + kMaxGroups;                     // [G]
+
+    auto full_bar = [&](int s) { return smem_u32(bars + s); };
+    auto empty_bar = [&](int s) { return smem_u32(bars + STAGES + s); };
+    auto tfull_bar = [&](int a) { return smem_u32(bars + 2 * STAGES + a); };
+    auto tempty_bar = [&](int a) { return smem_u32(bars + 2 * STAGES + 2 + a); };
+    const uint32_t drain_bar = smem_u32(bars + 2 * STAGES + 4);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int G = p.G, NT = p.NT;
+
+    // ---- group table from the device-side offsets ----
+    for (int g = threadIdx.x; g < G; g += kThreads) {
+        int a = 0, b = p.M;
+        if (p.offsets) {
+            a = p.offsets[g];
+            b = p.offsets[g + 1];
+        }
+        if (a < 0 || b < a || b > p.M) {
+            set_status(p.status, MOE_DEVERR_BAD_OFFSETS);
+            a = b = 0;
+        }
+        gstart[g] = a;
+        gend[g] = b;
+    }
+    if (threadIdx.x == 0) *abort_flag = 0;
+    __syncthreads();
+    if (warp == 0) {
+        int run = 0;
+        for (int g0 = 0; g0 < G; g0 += 32) {
+            const int g = g0 + lane;
+            const int v = g < G ? (gend[g] - gstart[g] + BM - 1) / BM * NT : 0;
+            int incl = v;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const int nb = __shfl_up_sync(0xffffffffu, incl, off);
+                if (lane >= off) incl += nb;
+            }
+            if (g < G) prefix[g] = run + incl - v;
+            run += __shfl_sync(0xffffffffu, incl, 31);
+        }
+        if (lane == 0) {
+            prefix[G] = run;
+            for (int s = 0; s < STAGES; ++s) {
+                mbar_init(full_bar(s), 1);
+                mbar_init(empty_bar(s), 1);
+            }
+            for (int a = 0; a < 2; ++a) {
+                mbar_init(tfull_bar(a), 1);
+                mbar_init(tempty_bar(a), 4);
+            }
+            mbar_init(drain_bar, 1);
+            asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            prefetch_tensormap(&mapA);
+            prefetch_tensormap(&mapB);
+        }
+    } else if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), Cf::TMEM_COLS);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    const int total = prefix[G];
+    const int KB = (p.K + BK - 1) / BK;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ---------------- TMA producer ----------------
+            int s = 0;
+            uint32_t ph = 0, issued = 0, issued_par = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
+                int g, m, n;
+                decode_tile(tile, prefix, G, NT, g, m, n);
+                const int row0 = gstart[g] + m * BM;
+                const int brow = g * p.Nb + n * BN;
+                for (int kb = 0; kb < KB; ++kb) {
+                    if (!wait_phase(empty_bar(s), ph ^ 1u, abort_flag, p.status)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(full_bar(s), Cf::STAGE_BYTES);
+                    tma_load_2d(smem_u32(sA + s * Cf::A_BYTES), &mapA, full_bar(s), kb * BK, row0);
+                    tma_load_2d(smem_u32(sB + s * Cf::B_BYTES), &mapB, full_bar(s), kb * BK, brow);
+                    issued |= 1u << s;
+                    issued_par = (issued_par & ~(1u << s)) | (ph << s);
+                    if (++s == STAGES) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                }
+            }
+            // every copy this thread started has landed before the CTA exits
+            for (int q = 0; q < STAGES; ++q)
+                if ((issued >> q) & 1u) wait_drain(full_bar(q), (issued_par >> q) & 1u, p.status);
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // ---------------- MMA issuer ----------------
+            int s = 0, acc = 0;
+            uint32_t ph = 0, aph = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
+                if (!wait_phase(tempty_bar(acc), aph ^ 1u, abort_flag, p.status)) break;
+                tc_fence_after();
+                const uint32_t d = tmem_base + (uint32_t)(acc * BN);
+                for (int kb = 0; kb < KB; ++kb) {
+                    if (!wait_phase(full_bar(s), ph, abort_flag, p.status)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint64_t adesc = smem_desc_sw128(smem_u32(sA + s * Cf::A_BYTES));
+                    const uint64_t bdesc = smem_desc_sw128(smem_u32(sB + s * Cf::B_BYTES));
+#pragma unroll
+                    for (int kk = 0; kk < BK / UMMA_K; ++kk)  // +32 bytes per K=16 slice
+                        mma_bf16(d, adesc + 2u * kk, bdesc + 2u * kk, IDESC, (kb | kk) != 0);
+                    mma_commit(empty_bar(s));
+                    if (++s == STAGES) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                mma_commit(tfull_bar(acc));
+                if (++acc == 2) {
+                    acc = 0;
+                    aph ^= 1u;
+                }
+            }
+            // all MMAs issued by this thread are complete before TMEM is freed
+            mma_commit(drain_bar);
+            wait_drain(drain_bar, 0, p.status);
+        }
+    } else {
+        // ---------------- epilogue: warps 2..5 ----------------
+        const int eg = warp & 3;  // TMEM lane group this warp may access
+        const int r = eg * 32 + lane;
+        int acc = 0;
+        uint32_t aph = 0;
+        for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+            int g, m, n;
+            decode_tile(tile, prefix, G, NT, g, m, n);
+            const int64_t row = (int64_t)gstart[g] + (int64_t)m * BM + r;
+            const bool valid = row < gend[g];
+            // warp-uniform decision: the TMEM loads below are .sync.aligned
+            if (!__all_sync(0xffffffffu, wait_phase(tfull_bar(acc), aph, abort_flag, p.status))) break;
+            tc_fence_after();
+            const uint32_t taddr = tmem_base + ((uint32_t)(eg * 32) << 16) + (uint32_t)(acc * BN);
+            if (EPI == TC_EPI_SWIGLU) {
+#pragma unroll 1
+                for (int c = 0; c < kPackBlock; c += 32) {
+                    uint32_t gr[32], ur[32];
+                    tmem_ld32(taddr + c, gr);
+                    tmem_ld32(taddr + kPackBlock + c, ur);
+                    float h[32];
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        const float gv = __uint_as_float(gr[i]);
+                        h[i] = gv / (1.0f + __expf(-gv)) * __uint_as_float(ur[i]);
+                    }
+                    if (valid) store_row32<EPI>(p.C, p.ldc, row, n * kPackBlock + c, p.N, h);
+                }
+            } else {
+#pragma unroll 1
+                for (int c = 0; c < BN; c += 32) {
+                    uint32_t vr[32];
+                    tmem_ld32(taddr + c, vr);
+                    float v[32];
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(vr[i]);
+                    if (valid) store_row32<EPI>(p.C, p.ldc, row, n * BN + c, p.N, v);
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(tempty_bar(acc));
+            if (++acc == 2) {
+                acc = 0;
+                aph ^= 1u;
+            }
+        }
+    }
+
+    __syncwarp();
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, Cf::TMEM_COLS);
+    }
+}
+
+// ---- host side --------------------------------------------------------------------
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(ptr);
+    });
+    return fn;
+}
+
+// 2-D bf16 map over a row-major [outer, inner] matrix; box = 64 x box_outer,
+// 128-byte swizzle, out-of-range elements read as zero.
+bool make_map(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer, uint32_t box_outer) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {inner, outer};
+    const cuuint64_t strides[1] = {inner * 2};
+    const cuuint32_t box[2] = {(cuuint32_t)BK, box_outer};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int BN, int EPI>
+moe_status_t launch_impl(const TcGroupedGemm& g, cudaStream_t s) {
+    using Cf = Cfg<BN>;
+    static std::once_flag attr_once[64];
+    int dev = 0;
+    MOE_CUDA_TRY(cudaGetDevice(&dev));
+    cudaError_t attr_err = cudaSuccess;
+    std::call_once(attr_once[dev & 63], [&] {
+        attr_err = cudaFuncSetAttribute(tc_grouped_gemm_kernel<BN, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        (int)Cf::SMEM);
+    });
+    MOE_CUDA_TRY(attr_err);
+
+    CUtensorMap ma, mb;
+    if (!make_map(&ma, g.A, (uint64_t)g.K, (uint64_t)g.M, BM)) return MOE_ERR_CUDA;
+    if (!make_map(&mb, g.B, (uint64_t)g.K, (uint64_t)g.G * g.Nb, BN)) return MOE_ERR_CUDA;
+
+    Params p;
+    p.offsets = g.offsets;
+    p.G = g.G;
+    p.M = g.M;
+    p.K = g.K;
+    p.Nb = g.Nb;
+    p.N = g.N;
+    p.NT = EPI == TC_EPI_SWIGLU ? g.Nb / BN : (int)ceil_div(g.N, BN);
+    p.C = g.C;
+    p.ldc = g.ldc;
+    p.status = g.status;
+
+    const int64_t max_tiles = (int64_t)p.NT * (ceil_div(g.M, BM) + (g.offsets ? g.G : 0));
+    const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(sm_count(), max_tiles));
+    tc_grouped_gemm_kernel<BN, EPI><<<grid, kThreads, Cf::SMEM, s>>>(ma, mb, p);
+    note_launch();
+    return last_launch_status();
+}
+
+}  // namespace
+
+int tc_packed_block() { return kPackBlock; }
+
+moe_status_t launch_tc_grouped_gemm(const TcGroupedGemm& g, cudaStream_t s) {
+    if (g.M == 0 || g.G == 0) return MOE_OK;
+    if (g.G > kMaxGroups) return MOE_ERR_UNSUPPORTED;
+    switch (g.epi) {
+        case TC_EPI_SWIGLU:
+            if (g.Nb % (2 * kPackBlock) != 0) return MOE_ERR_INVALID_ARG;
+            return launch_impl<256, TC_EPI_SWIGLU>(g, s);
+        case TC_EPI_BF16:
+            return launch_impl<256, TC_EPI_BF16>(g, s);
+        case TC_EPI_F32:
+            if (g.N <= 64) return launch_impl<64, TC_EPI_F32>(g, s);
+            if (g.N <= 128) return launch_impl<128, TC_EPI_F32>(g, s);
+            return launch_impl<256, TC_EPI_F32>(g, s);
+    }
+    return MOE_ERR_INVALID_ARG;
+}
+
+}  // namespace moe

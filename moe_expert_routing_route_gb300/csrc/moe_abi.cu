@@ -1,0 +1,410 @@
+// C ABI of libmoe (declared in include/moe.h): argument checks, workspace
+// layout and the stream-ordered composition of the layer.
+//
+// "Lower latency and higher throughput with multi-node DeepSeek deployment"
+// (Perplexity blog), §Expert Parallelism (the layer: routed experts summed with
+// weights plus the shared expert), §Quantization (kernels read the routing
+// counts on the device; fixed grids), §CUDA Graph (no host synchronisation so
+// the whole forward can be captured).  "DeepSeek-R1 prefill inference
+// optimisation on Atlas A3" (cann-recipes-infer), §MoE deployment strategy
+// (init-routing / expert compute / finalize-routing split of the layer).
+#include "moe_internal.cuh"
+
+#include <atomic>
+#include <climits>
+
+namespace moe {
+
+namespace {
+std::atomic<uint64_t> g_launches{0};
+int g_sm_count[64] = {0};
+
+constexpr size_t kAlign = 256;
+
+bool bad_dtype(moe_dtype_t dt) { return dt != MOE_F32 && dt != MOE_BF16; }
+
+moe_status_t check_sizes(int T, int H, int E, int k) {
+    if (T < 0 || H <= 0 || E <= 0 || k <= 0) return MOE_ERR_INVALID_ARG;
+    if (E > 1024 || k > 32 || k > E) return MOE_ERR_INVALID_ARG;
+    if ((int64_t)T * k >= INT_MAX) return MOE_ERR_INVALID_ARG;
+    if (H % 8 != 0) return MOE_ERR_UNSUPPORTED;
+    return MOE_OK;
+}
+
+uint32_t* status_word(void* ws) { return static_cast<uint32_t*>(ws); }
+
+moe_status_t clear_status(void* ws, cudaStream_t s) {
+    if (!ws) return MOE_OK;
+    MOE_CUDA_TRY(cudaMemsetAsync(ws, 0, sizeof(uint32_t), s));
+    return MOE_OK;
+}
+
+int packed_rows(int I) { return 2 * (int)round_up((size_t)I, (size_t)tc_packed_block()); }
+
+// Routed grouped FFN: up (SwiGLU) then down, for bf16 on tcgen05, fp32 on FFMA.
+moe_status_t grouped_ffn(const void* a, moe_dtype_t dt, const int32_t* offsets, int G, int rows, int H, int I,
+                         const void* w13p, const void* w2, void* h, void* y, uint32_t* status, cudaStream_t s,
+                         cudaEvent_t ev_mid) {
+    if (rows == 0) {
+        if (ev_mid) MOE_CUDA_TRY(cudaEventRecord(ev_mid, s));
+        return MOE_OK;
+    }
+    if (dt == MOE_BF16) {
+        TcGroupedGemm up{a, rows, H, offsets, G, w13p, packed_rows(I), I, h, I, TC_EPI_SWIGLU, status};
+        MOE_TRY(launch_tc_grouped_gemm(up, s));
+        if (ev_mid) MOE_CUDA_TRY(cudaEventRecord(ev_mid, s));
+        TcGroupedGemm down{h, rows, I, offsets, G, w2, H, H, y, H, TC_EPI_BF16, status};
+        return launch_tc_grouped_gemm(down, s);
+    }
+    MOE_TRY(launch_simt_grouped_ffn_up(static_cast<const float*>(a), rows, H, offsets, G,
+                                       static_cast<const float*>(w13p), packed_rows(I) / 2, I,
+                                       static_cast<float*>(h), status, s));
+    if (ev_mid) MOE_CUDA_TRY(cudaEventRecord(ev_mid, s));
+    return launch_simt_grouped_down(static_cast<const float*>(h), rows, I, offsets, G,
+                                    static_cast<const float*>(w2), H, static_cast<float*>(y), status, s);
+}
+
+moe_status_t gate(const void* x, const void* wr, moe_dtype_t dt, int T, int H, int E, float* logits,
+                  cudaStream_t s) {
+    if (T == 0) return MOE_OK;
+    if (dt == MOE_BF16) {
+        TcGroupedGemm g{x, T, H, nullptr, 1, wr, E, E, logits, E, TC_EPI_F32, nullptr};
+        return launch_tc_grouped_gemm(g, s);
+    }
+    return launch_simt_gate(static_cast<const float*>(x), static_cast<const float*>(wr), T, H, E, logits, s);
+}
+
+// ---- layer workspace layout ----
+struct Layout {
+    size_t off[MOE_WS_NUM_FIELDS];
+    size_t bytes[MOE_WS_NUM_FIELDS];
+    size_t scratch_off, scratch_bytes, total;
+};
+
+Layout layout(const moe_layer_desc& d) {
+    Layout L{};
+    const size_t b = dt_size(d.dtype);
+    const size_t T = (size_t)d.T, H = (size_t)d.H, E = (size_t)d.E, R = (size_t)d.T * d.k, I = (size_t)d.I,
+                 S = (size_t)d.S;
+    L.bytes[MOE_WS_LOGITS] = T * E * 4;
+    L.bytes[MOE_WS_TOPK_IDS] = R * 4;
+    L.bytes[MOE_WS_TOPK_W] = R * 4;
+    L.bytes[MOE_WS_TOKENS_PER_EXPERT] = E * 4;
+    L.bytes[MOE_WS_EXPERT_OFFSETS] = (E + 1) * 4;
+    L.bytes[MOE_WS_EXPANDED_ROW_IDX] = R * 4;
+    L.bytes[MOE_WS_EXPANDED_X] = R * H * b;
+    L.bytes[MOE_WS_H_ROUTED] = R * I * b;
+    L.bytes[MOE_WS_H_SHARED] = T * S * I * b;
+    L.bytes[MOE_WS_Y_ROUTED] = R * H * b;
+    L.bytes[MOE_WS_Y_SHARED] = T * H * b;
+    L.bytes[MOE_WS_X_IN] = T * H * b;
+    L.bytes[MOE_WS_OUT] = T * H * b;
+    size_t cur = MOE_WS_HEADER_BYTES;
+    for (int f = 0; f < MOE_WS_NUM_FIELDS; ++f) {
+        L.off[f] = cur;
+        cur += round_up(L.bytes[f], kAlign);
+    }
+    L.scratch_off = cur;
+    L.scratch_bytes = init_routing_scratch_bytes(d.T, d.E, d.k);
+    L.total = cur + round_up(L.scratch_bytes, kAlign);
+    return L;
+}
+
+moe_status_t check_desc(const moe_layer_desc* d) {
+    if (!d) return MOE_ERR_INVALID_ARG;
+    MOE_TRY(check_sizes(d->T, d->H, d->E, d->k));
+    if (bad_dtype(d->dtype) || d->I <= 0 || d->S < 0) return MOE_ERR_INVALID_ARG;
+    if (d->I % 8 != 0) return MOE_ERR_UNSUPPORTED;
+    if (!d->w_router || !d->w13 || !d->w2) return MOE_ERR_INVALID_ARG;
+    if (d->S > 0 && (!d->w13_shared || !d->w2_shared)) return MOE_ERR_INVALID_ARG;
+    if ((int64_t)d->S * d->I >= INT_MAX / 2) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(d->w_router) || !aligned16(d->w13) || !aligned16(d->w2) || !aligned16(d->expert_bias) ||
+        !aligned16(d->w13_shared) || !aligned16(d->w2_shared))
+        return MOE_ERR_UNSUPPORTED;
+    return MOE_OK;
+}
+
+template <typename T>
+T* at(void* ws, size_t off) {
+    return reinterpret_cast<T*>(static_cast<char*>(ws) + off);
+}
+
+moe_status_t record(void* const* ev, int i, cudaStream_t s) {
+    if (ev && ev[i]) MOE_CUDA_TRY(cudaEventRecord(static_cast<cudaEvent_t>(ev[i]), s));
+    return MOE_OK;
+}
+
+moe_status_t layer_forward(const moe_layer_desc* d, const void* x, void* out, void* ws, size_t ws_bytes,
+                           cudaStream_t s, void* const* ev) {
+    MOE_TRY(check_desc(d));
+    if (!x || !out || !ws) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(out) || !aligned16(ws)) return MOE_ERR_UNSUPPORTED;
+    const Layout L = layout(*d);
+    if (ws_bytes < L.total) return MOE_ERR_INVALID_ARG;
+    if (d->T == 0) {
+        for (int i = 0; i <= MOE_NUM_STAGES; ++i) MOE_TRY(record(ev, i, s));
+        return MOE_OK;
+    }
+    const int T = d->T, H = d->H, E = d->E, k = d->k, I = d->I, R = T * k;
+    const int SI = d->S * d->I;
+    const moe_dtype_t dt = d->dtype;
+    uint32_t* status = status_word(ws);
+    float* logits = at<float>(ws, L.off[MOE_WS_LOGITS]);
+    int32_t* ids = at<int32_t>(ws, L.off[MOE_WS_TOPK_IDS]);
+    float* w = at<float>(ws, L.off[MOE_WS_TOPK_W]);
+    int32_t* counts = at<int32_t>(ws, L.off[MOE_WS_TOKENS_PER_EXPERT]);
+    int32_t* offsets = at<int32_t>(ws, L.off[MOE_WS_EXPERT_OFFSETS]);
+    int32_t* row_idx = at<int32_t>(ws, L.off[MOE_WS_EXPANDED_ROW_IDX]);
+    void* ex = at<void>(ws, L.off[MOE_WS_EXPANDED_X]);
+    void* h = at<void>(ws, L.off[MOE_WS_H_ROUTED]);
+    void* hs = at<void>(ws, L.off[MOE_WS_H_SHARED]);
+    void* y = at<void>(ws, L.off[MOE_WS_Y_ROUTED]);
+    void* ys = at<void>(ws, L.off[MOE_WS_Y_SHARED]);
+    int32_t* scratch = at<int32_t>(ws, L.scratch_off);
+
+    MOE_TRY(clear_status(ws, s));
+    MOE_TRY(record(ev, 0, s));
+    MOE_TRY(gate(x, d->w_router, dt, T, H, E, logits, s));
+    MOE_TRY(record(ev, 1, s));
+    MOE_TRY(launch_route_topk(logits, d->expert_bias, T, E, k, d->renormalize, ids, w, s));
+    MOE_TRY(record(ev, 2, s));
+    MOE_TRY(launch_init_routing_index(ids, R, E, counts, offsets, row_idx, scratch, status, s));
+    MOE_TRY(record(ev, 3, s));
+    MOE_TRY(launch_permute_rows(x, (size_t)H * dt_size(dt), row_idx, T, k, ex, s));
+    MOE_TRY(record(ev, 4, s));
+    // routed up (stage 4) ... routed down (stage 6); the shared up (stage 5) runs
+    // between them so each stage boundary is one kernel.
+    if (dt == MOE_BF16) {
+        TcGroupedGemm up{ex, R, H, offsets, E, d->w13, packed_rows(I), I, h, I, TC_EPI_SWIGLU, status};
+        MOE_TRY(launch_tc_grouped_gemm(up, s));
+        MOE_TRY(record(ev, 5, s));
+        if (SI > 0) {
+            TcGroupedGemm sup{x, T, H, nullptr, 1, d->w13_shared, packed_rows(SI), SI, hs, SI, TC_EPI_SWIGLU,
+                              status};
+            MOE_TRY(launch_tc_grouped_gemm(sup, s));
+        }
+        MOE_TRY(record(ev, 6, s));
+        TcGroupedGemm down{h, R, I, offsets, E, d->w2, H, H, y, H, TC_EPI_BF16, status};
+        MOE_TRY(launch_tc_grouped_gemm(down, s));
+        MOE_TRY(record(ev, 7, s));
+        if (SI > 0) {
+            TcGroupedGemm sdown{hs, T, SI, nullptr, 1, d->w2_shared, H, H, ys, H, TC_EPI_BF16, status};
+            MOE_TRY(launch_tc_grouped_gemm(sdown, s));
+        }
+    } else {
+        const float* w13 = static_cast<const float*>(d->w13);
+        MOE_TRY(launch_simt_grouped_ffn_up(static_cast<const float*>(ex), R, H, offsets, E, w13,
+                                           packed_rows(I) / 2, I, static_cast<float*>(h), status, s));
+        MOE_TRY(record(ev, 5, s));
+        if (SI > 0)
+            MOE_TRY(launch_simt_grouped_ffn_up(static_cast<const float*>(x), T, H, nullptr, 1,
+                                               static_cast<const float*>(d->w13_shared), packed_rows(SI) / 2, SI,
+                                               static_cast<float*>(hs), status, s));
+        MOE_TRY(record(ev, 6, s));
+        MOE_TRY(launch_simt_grouped_down(static_cast<const float*>(h), R, I, offsets, E,
+                                         static_cast<const float*>(d->w2), H, static_cast<float*>(y), status, s));
+        MOE_TRY(record(ev, 7, s));
+        if (SI > 0)
+            MOE_TRY(launch_simt_grouped_down(static_cast<const float*>(hs), T, SI, nullptr, 1,
+                                             static_cast<const float*>(d->w2_shared), H, static_cast<float*>(ys),
+                                             status, s));
+    }
+    MOE_TRY(record(ev, 8, s));
+    MOE_TRY(launch_finalize(y, R, SI > 0 ? ys : nullptr, w, row_idx, dt, T, H, k, out, status, s));
+    MOE_TRY(record(ev, 9, s));
+    return MOE_OK;
+}
+
+}  // namespace
+
+void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+
+moe_status_t last_launch_status() { return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+int sm_count() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+    int& c = g_sm_count[dev & 63];
+    if (c == 0) {
+        int v = 0;
+        cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
+        c = v > 0 ? v : 1;
+    }
+    return c;
+}
+
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+int moe_abi_version(void) { return 1; }
+
+const char* moe_status_string(moe_status_t st) {
+    switch (st) {
+        case MOE_OK: return "MOE_OK";
+        case MOE_ERR_INVALID_ARG: return "MOE_ERR_INVALID_ARG";
+        case MOE_ERR_UNSUPPORTED: return "MOE_ERR_UNSUPPORTED";
+        case MOE_ERR_CUDA: return "MOE_ERR_CUDA";
+        case MOE_ERR_DEVICE: return "MOE_ERR_DEVICE";
+    }
+    return "MOE_ERR_UNKNOWN";
+}
+
+uint64_t moe_kernel_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+moe_status_t moe_check_device_status(const void* ws, moe_stream_t stream, uint32_t* word) {
+    if (!ws) return MOE_ERR_INVALID_ARG;
+    uint32_t v = 0;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    MOE_CUDA_TRY(cudaStreamSynchronize(s));
+    MOE_CUDA_TRY(cudaMemcpyAsync(&v, ws, sizeof v, cudaMemcpyDeviceToHost, s));
+    MOE_CUDA_TRY(cudaStreamSynchronize(s));
+    if (word) *word = v;
+    return v ? MOE_ERR_DEVICE : MOE_OK;
+}
+
+moe_status_t moe_gate_logits(const void* x, const void* w_router, moe_dtype_t dt, int T, int H, int E,
+                             float* logits, moe_stream_t stream) {
+    MOE_TRY(check_sizes(T, H, E, 1));
+    if (bad_dtype(dt)) return MOE_ERR_INVALID_ARG;
+    if (T == 0) return MOE_OK;
+    if (!x || !w_router || !logits) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(w_router) || !aligned16(logits)) return MOE_ERR_UNSUPPORTED;
+    return gate(x, w_router, dt, T, H, E, logits, reinterpret_cast<cudaStream_t>(stream));
+}
+
+moe_status_t moe_route_topk(const float* logits, const float* expert_bias, int T, int E, int k, int renormalize,
+                            int32_t* topk_ids, float* topk_w, moe_stream_t stream) {
+    MOE_TRY(check_sizes(T, 8, E, k));
+    if (T == 0) return MOE_OK;
+    if (!logits || !topk_ids || !topk_w) return MOE_ERR_INVALID_ARG;
+    return launch_route_topk(logits, expert_bias, T, E, k, renormalize ? 1 : 0, topk_ids, topk_w,
+                             reinterpret_cast<cudaStream_t>(stream));
+}
+
+size_t moe_init_routing_workspace_bytes(int T, int E, int k) {
+    if (T < 0 || E <= 0 || k <= 0) return 0;
+    return MOE_WS_HEADER_BYTES + round_up(init_routing_scratch_bytes(T, E, k), kAlign);
+}
+
+moe_status_t moe_init_routing(const void* x, moe_dtype_t dt, const int32_t* topk_ids, int T, int H, int E, int k,
+                              void* expanded_x, int32_t* expanded_row_idx, int32_t* tokens_per_expert,
+                              int32_t* expert_offsets, void* ws, size_t ws_bytes, moe_stream_t stream) {
+    MOE_TRY(check_sizes(T, H, E, k));
+    if (bad_dtype(dt)) return MOE_ERR_INVALID_ARG;
+    if (!ws || ws_bytes < moe_init_routing_workspace_bytes(T, E, k)) return MOE_ERR_INVALID_ARG;
+    if (!tokens_per_expert || !expert_offsets) return MOE_ERR_INVALID_ARG;
+    if (T > 0 && (!x || !topk_ids || !expanded_x || !expanded_row_idx)) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(expanded_x) || !aligned16(ws)) return MOE_ERR_UNSUPPORTED;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    MOE_TRY(clear_status(ws, s));
+    const int R = T * k;
+    MOE_TRY(launch_init_routing_index(topk_ids, R, E, tokens_per_expert, expert_offsets, expanded_row_idx,
+                                      at<int32_t>(ws, MOE_WS_HEADER_BYTES), status_word(ws), s));
+    return launch_permute_rows(x, (size_t)H * dt_size(dt), expanded_row_idx, T, k, expanded_x, s);
+}
+
+size_t moe_w13_packed_bytes(moe_dtype_t dt, int E, int H, int I) {
+    if (bad_dtype(dt) || E <= 0 || H <= 0 || I <= 0) return 0;
+    return (size_t)E * packed_rows(I) * (size_t)H * dt_size(dt);
+}
+
+moe_status_t moe_pack_w13(const void* w_gate, const void* w_up, moe_dtype_t dt, int E, int H, int I,
+                          void* w13_packed, moe_stream_t stream) {
+    if (bad_dtype(dt) || E <= 0 || H <= 0 || I <= 0) return MOE_ERR_INVALID_ARG;
+    if (H % 8 != 0) return MOE_ERR_UNSUPPORTED;
+    if (!w_gate || !w_up || !w13_packed) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(w_gate) || !aligned16(w_up) || !aligned16(w13_packed)) return MOE_ERR_UNSUPPORTED;
+    return launch_pack_w13(w_gate, w_up, dt_size(dt), E, H, I, w13_packed, reinterpret_cast<cudaStream_t>(stream));
+}
+
+size_t moe_grouped_ffn_workspace_bytes(moe_dtype_t dt, int rows, int I) {
+    if (bad_dtype(dt) || rows < 0 || I <= 0) return 0;
+    return MOE_WS_HEADER_BYTES + round_up((size_t)rows * I * dt_size(dt), kAlign);
+}
+
+moe_status_t moe_grouped_ffn(const void* a, moe_dtype_t dt, const int32_t* expert_offsets, int E, int rows, int H,
+                             int I, const void* w13_packed, const void* w2, void* y, void* ws, size_t ws_bytes,
+                             moe_stream_t stream) {
+    if (bad_dtype(dt) || rows < 0 || H <= 0 || I <= 0 || E <= 0 || E > 1024) return MOE_ERR_INVALID_ARG;
+    if (!expert_offsets && E != 1) return MOE_ERR_INVALID_ARG;
+    if (H % 8 != 0 || I % 8 != 0) return MOE_ERR_UNSUPPORTED;
+    if (!ws || ws_bytes < moe_grouped_ffn_workspace_bytes(dt, rows, I)) return MOE_ERR_INVALID_ARG;
+    if (rows > 0 && (!a || !w13_packed || !w2 || !y)) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(a) || !aligned16(w13_packed) || !aligned16(w2) || !aligned16(y) || !aligned16(ws))
+        return MOE_ERR_UNSUPPORTED;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    MOE_TRY(clear_status(ws, s));
+    return grouped_ffn(a, dt, expert_offsets, E, rows, H, I, w13_packed, w2, at<void>(ws, MOE_WS_HEADER_BYTES), y,
+                       status_word(ws), s, nullptr);
+}
+
+moe_status_t moe_finalize_routing(const void* y, int64_t y_rows, const void* skip, const float* topk_w,
+                                  const int32_t* expanded_row_idx, moe_dtype_t dt, int T, int H, int k, void* out,
+                                  void* ws, moe_stream_t stream) {
+    MOE_TRY(check_sizes(T, H, 32, k));
+    if (bad_dtype(dt) || y_rows < 0) return MOE_ERR_INVALID_ARG;
+    if (T == 0) return MOE_OK;
+    if (!y || !topk_w || !expanded_row_idx || !out) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(y) || !aligned16(skip) || !aligned16(out) || !aligned16(ws)) return MOE_ERR_UNSUPPORTED;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    MOE_TRY(clear_status(ws, s));
+    return launch_finalize(y, y_rows, skip, topk_w, expanded_row_idx, dt, T, H, k, out,
+                           ws ? status_word(ws) : nullptr, s);
+}
+
+const char* moe_stage_name(int stage) {
+    static const char* names[MOE_NUM_STAGES] = {"gate",      "route",     "init_routing", "permute_rows", "up_routed",
+                                                "up_shared", "down_routed", "down_shared", "finalize"};
+    return (stage >= 0 && stage < MOE_NUM_STAGES) ? names[stage] : "";
+}
+
+size_t moe_layer_workspace_bytes(const moe_layer_desc* desc) {
+    if (!desc || check_sizes(desc->T, desc->H, desc->E, desc->k) != MOE_OK || desc->I <= 0 || desc->S < 0 ||
+        bad_dtype(desc->dtype))
+        return 0;
+    return layout(*desc).total;
+}
+
+moe_status_t moe_layer_workspace_field(const moe_layer_desc* desc, moe_ws_field field, size_t* offset,
+                                       size_t* bytes) {
+    if (!desc || field < 0 || field >= MOE_WS_NUM_FIELDS) return MOE_ERR_INVALID_ARG;
+    if (check_sizes(desc->T, desc->H, desc->E, desc->k) != MOE_OK || desc->I <= 0 || desc->S < 0 ||
+        bad_dtype(desc->dtype))
+        return MOE_ERR_INVALID_ARG;
+    const Layout L = layout(*desc);
+    if (offset) *offset = L.off[field];
+    if (bytes) *bytes = L.bytes[field];
+    return MOE_OK;
+}
+
+moe_status_t moe_layer_forward(const moe_layer_desc* desc, const void* x, void* out, void* ws, size_t ws_bytes,
+                               moe_stream_t stream) {
+    return layer_forward(desc, x, out, ws, ws_bytes, reinterpret_cast<cudaStream_t>(stream), nullptr);
+}
+
+moe_status_t moe_layer_forward_timed(const moe_layer_desc* desc, const void* x, void* out, void* ws, size_t ws_bytes,
+                                     moe_stream_t stream, void* const* stage_events) {
+    return layer_forward(desc, x, out, ws, ws_bytes, reinterpret_cast<cudaStream_t>(stream), stage_events);
+}
+
+moe_status_t moe_layer_forward_host(const moe_layer_desc* desc, const void* x_host, void* out_host, void* ws,
+                                    size_t ws_bytes, moe_stream_t stream) {
+    MOE_TRY(check_desc(desc));
+    if (!x_host || !out_host || !ws) return MOE_ERR_INVALID_ARG;
+    if (ws_bytes < layout(*desc).total) return MOE_ERR_INVALID_ARG;
+    const Layout L = layout(*desc);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    void* xin = at<void>(ws, L.off[MOE_WS_X_IN]);
+    void* xout = at<void>(ws, L.off[MOE_WS_OUT]);
+    const size_t bytes = L.bytes[MOE_WS_X_IN];
+    if (bytes) MOE_CUDA_TRY(cudaMemcpyAsync(xin, x_host, bytes, cudaMemcpyHostToDevice, s));
+    MOE_TRY(layer_forward(desc, xin, xout, ws, ws_bytes, s, nullptr));
+    if (bytes) MOE_CUDA_TRY(cudaMemcpyAsync(out_host, xout, bytes, cudaMemcpyDeviceToHost, s));
+    MOE_CUDA_TRY(cudaStreamSynchronize(s));
+    return MOE_OK;
+}
+
+}  // extern "C"

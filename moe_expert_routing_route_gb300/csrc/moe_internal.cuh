@@ -1,0 +1,90 @@
+// Internal declarations of libmoe: launchers each .cu file provides, and the
+// small helpers they share.  Not part of the public ABI (that is include/moe.h).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <cstdint>
+#include <cstddef>
+#include <algorithm>
+
+#include "moe.h"
+
+namespace moe {
+
+// ---- launch bookkeeping ------------------------------------------------------
+void note_launch();                    // counts one kernel launch
+moe_status_t last_launch_status();     // MOE_ERR_CUDA if the last launch failed
+int sm_count();                        // SMs of the current device (cached per device)
+
+#define MOE_TRY(expr)                           \
+    do {                                        \
+        moe_status_t _st = (expr);              \
+        if (_st != MOE_OK) return _st;          \
+    } while (0)
+
+#define MOE_CUDA_TRY(expr)                      \
+    do {                                        \
+        if ((expr) != cudaSuccess) return MOE_ERR_CUDA; \
+    } while (0)
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+inline size_t round_up(size_t a, size_t b) { return (a + b - 1) / b * b; }
+inline size_t dt_size(moe_dtype_t dt) { return dt == MOE_BF16 ? 2 : 4; }
+
+// ---- device helpers -------------------------------------------------------------
+__device__ __forceinline__ void set_status(uint32_t* status, uint32_t bit) {
+    if (status) atomicOr(status, bit);
+}
+
+// ---- launchers (stream-ordered, no host sync) ------------------------------------
+// route.cu
+moe_status_t launch_route_topk(const float* logits, const float* bias, int T, int E, int k, int renorm,
+                               int32_t* ids, float* w, cudaStream_t s);
+
+// permute.cu
+size_t init_routing_scratch_bytes(int T, int E, int k);
+moe_status_t launch_init_routing_index(const int32_t* ids, int R, int E, int32_t* counts,
+                                       int32_t* offsets, int32_t* row_idx, int32_t* scratch,
+                                       uint32_t* status, cudaStream_t s);
+moe_status_t launch_permute_rows(const void* x, size_t row_bytes, const int32_t* row_idx, int T, int k,
+                                 void* expanded_x, cudaStream_t s);
+moe_status_t launch_pack_w13(const void* w_gate, const void* w_up, size_t esize, int E, int H, int I,
+                             void* packed, cudaStream_t s);
+
+// finalize.cu
+moe_status_t launch_finalize(const void* y, int64_t y_rows, const void* skip, const float* w,
+                             const int32_t* row_idx, moe_dtype_t dt, int T, int H, int k, void* out,
+                             uint32_t* status, cudaStream_t s);
+
+// gemm_tc.cu: bf16 tcgen05 grouped GEMM, C = A B^T per group.
+enum TcEpilogue { TC_EPI_SWIGLU = 0, TC_EPI_BF16 = 1, TC_EPI_F32 = 2 };
+struct TcGroupedGemm {
+    const void* A;            // [M, K] bf16, row stride K
+    int M;                    // rows of A
+    int K;
+    const int32_t* offsets;   // [G+1] device, or nullptr for one group [0, M)
+    int G;
+    const void* B;            // [G * Nb, K] bf16
+    int Nb;                   // B rows per group
+    int N;                    // valid output columns per group
+    void* C;                  // output base (row r of A -> row r of C)
+    int64_t ldc;              // elements
+    TcEpilogue epi;
+    uint32_t* status;
+};
+moe_status_t launch_tc_grouped_gemm(const TcGroupedGemm& g, cudaStream_t s);
+int tc_packed_block();        // rows of gate (and of up) per packed block: 128
+
+// gemm_simt.cu: fp32 (FFMA) GEMMs of the same shapes.
+moe_status_t launch_simt_gate(const float* x, const float* wr, int T, int H, int E, float* logits,
+                              cudaStream_t s);
+moe_status_t launch_simt_grouped_ffn_up(const float* a, int M, int H, const int32_t* offsets, int G,
+                                        const float* w13_packed, int Ip, int I, float* h,
+                                        uint32_t* status, cudaStream_t s);
+moe_status_t launch_simt_grouped_down(const float* h, int M, int I, const int32_t* offsets, int G,
+                                      const float* w2, int H, float* y, uint32_t* status,
+                                      cudaStream_t s);
+
+}  // namespace moe

@@ -1,0 +1,257 @@
+// Init-routing: the expand-and-sort permutation of the token rows.
+//
+// "DeepSeek-R1 prefill inference optimisation on Atlas A3" (cann-recipes-infer),
+// §MoE deployment strategy, Double-Routing step 1: expand every token k times,
+// sort the copies by expert, and return expanded_x, expanded_row_idx (which
+// restores the original order) and tokens_per_expert.  "Lower latency and
+// higher throughput with multi-node DeepSeek deployment" (Perplexity blog),
+// §MoE Router: dense dispatch needs the routing aggregated per expert.
+//
+// The sort is a stable counting sort in three small kernels plus one copy:
+//   hist    one warp per chunk of kChunk source rows -> per-chunk histogram
+//           hist[c][e] (chunk-major: coalesced writes)
+//   scan    one block: tokens_per_expert, expert_offsets and, for every
+//           (chunk, expert), the first destination row of that chunk's copies
+//   scatter one warp per chunk, chunks in source order, 32 rows per step;
+//           __match_any_sync groups the lanes with the same expert and the
+//           rank inside the group keeps source order (stable)
+//   copy    x is read once (16-byte vectors) and each row is written to its
+//           k destinations (HBM-bound: T*H*b read + T*k*H*b written)
+#include "moe_internal.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kChunk = 1024;   // source rows per warp-chunk
+constexpr int kHistWarps = 8;  // warps per block in hist/scatter
+
+__global__ void __launch_bounds__(kHistWarps * 32)
+hist_kernel(const int32_t* __restrict__ ids, int R, int E, int NW, int32_t* __restrict__ hist,
+            uint32_t* status) {
+    extern __shared__ int32_t sh[];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int c = blockIdx.x * kHistWarps + warp;
+    if (c >= NW) return;
+    int32_t* my = sh + warp * E;
+    for (int e = lane; e < E; e += 32) my[e] = 0;
+    __syncwarp();
+    const int beg = c * kChunk, end = min(R, beg + kChunk);
+    bool bad = false;
+    for (int src = beg + lane; src < end; src += 32) {
+        const int id = __ldg(ids + src);
+        if ((unsigned)id < (unsigned)E) atomicAdd(&my[id], 1);
+        else bad = true;
+    }
+    if (bad) set_status(status, MOE_DEVERR_BAD_EXPERT_ID);
+    __syncwarp();
+    for (int e = lane; e < E; e += 32) hist[(size_t)c * E + e] = my[e];
+}
+
+// Exclusive scan of up to 1024 values held one per thread; returns the
+// exclusive prefix of thread tid and writes the total to *total.
+__device__ int block_exclusive_scan_1024(int v, int* warp_tot, int* total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int incl = v;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int n = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += n;
+    }
+    if (lane == 31) warp_tot[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        const int wv = lane < (int)(blockDim.x >> 5) ? warp_tot[lane] : 0;
+        int wincl = wv;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int n = __shfl_up_sync(0xffffffffu, wincl, off);
+            if (lane >= off) wincl += n;
+        }
+        warp_tot[lane] = wincl - wv;  // exclusive prefix of warp totals
+        if (lane == 31) *total = wincl;
+    }
+    __syncthreads();
+    return warp_tot[warp] + incl - v;
+}
+
+__global__ void __launch_bounds__(1024)
+scan_kernel(int32_t* __restrict__ hist, int NW, int E, int32_t* __restrict__ counts,
+            int32_t* __restrict__ offsets) {
+    __shared__ int part[1024];
+    __shared__ int warp_tot[32];
+    __shared__ int total;
+    const int tid = threadIdx.x;
+    const int P = max(1, 1024 / E);  // parts per expert along the chunk axis
+    const bool active = tid < P * E;
+    const int e = tid % E, p = tid / E;
+    const int per = (NW + P - 1) / P;
+    const int c0 = min(NW, p * per), c1 = min(NW, c0 + per);
+
+    int sum = 0;
+    if (active)
+        for (int c = c0; c < c1; ++c) sum += hist[(size_t)c * E + e];
+    part[tid] = active ? sum : 0;
+    __syncthreads();
+    int cnt = 0;
+    if (tid < E) {
+        int run = 0;
+        for (int q = 0; q < P; ++q) {
+            const int v = part[q * E + tid];
+            part[q * E + tid] = run;
+            run += v;
+        }
+        cnt = run;
+        counts[tid] = run;
+    }
+    __syncthreads();
+    const int excl = block_exclusive_scan_1024(tid < E ? cnt : 0, warp_tot, &total);
+    __shared__ int base_sh[1024];
+    if (tid < E) {
+        base_sh[tid] = excl;
+        offsets[tid] = excl;
+    }
+    if (tid == 0) offsets[E] = total;
+    __syncthreads();
+    if (active) {
+        int run = base_sh[e] + part[tid];
+        for (int c = c0; c < c1; ++c) {
+            const size_t i = (size_t)c * E + e;
+            const int v = hist[i];
+            hist[i] = run;
+            run += v;
+        }
+    }
+}
+
+__global__ void __launch_bounds__(kHistWarps * 32)
+scatter_kernel(const int32_t* __restrict__ ids, int R, int E, int NW, const int32_t* __restrict__ base,
+               int32_t* __restrict__ row_idx) {
+    extern __shared__ int32_t sh[];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int c = blockIdx.x * kHistWarps + warp;
+    if (c >= NW) return;
+    int32_t* next = sh + warp * E;  // next destination row of each expert in this chunk
+    for (int e = lane; e < E; e += 32) next[e] = base[(size_t)c * E + e];
+    __syncwarp();
+    const unsigned lt_mask = (1u << lane) - 1u;
+    const int beg = c * kChunk, end = min(R, beg + kChunk);
+    for (int s0 = beg; s0 < end; s0 += 32) {
+        const int src = s0 + lane;
+        const bool in = src < end;
+        const int id = in ? __ldg(ids + src) : -1;
+        const bool ok = in && (unsigned)id < (unsigned)E;
+        const unsigned group = __match_any_sync(0xffffffffu, ok ? (unsigned)id : 0xffffffffu);
+        const int rank = __popc(group & lt_mask);
+        const int first = ok ? next[id] : 0;
+        __syncwarp();
+        if (ok && rank == 0) next[id] = first + __popc(group);
+        __syncwarp();
+        if (in) row_idx[src] = ok ? first + rank : -1;
+    }
+}
+
+constexpr int kCopyThreads = 128;
+constexpr int kCopyUnroll = 4;
+
+__global__ void __launch_bounds__(kCopyThreads)
+permute_rows_kernel(const uint4* __restrict__ x, int nvec, const int32_t* __restrict__ row_idx, int T,
+                    int k, int R, uint4* __restrict__ out) {
+    __shared__ int dst[32];
+    for (int t = blockIdx.x; t < T; t += gridDim.x) {
+        if (threadIdx.x < k) {
+            const int d = row_idx[(size_t)t * k + threadIdx.x];
+            dst[threadIdx.x] = (d >= 0 && d < R) ? d : -1;
+        }
+        __syncthreads();
+        const uint4* xr = x + (size_t)t * nvec;
+        for (int v0 = threadIdx.x; v0 < nvec; v0 += kCopyUnroll * kCopyThreads) {
+            uint4 val[kCopyUnroll];
+#pragma unroll
+            for (int u = 0; u < kCopyUnroll; ++u) {
+                const int v = v0 + u * kCopyThreads;
+                if (v < nvec) val[u] = __ldcs(xr + v);  // read once: streaming
+            }
+            for (int j = 0; j < k; ++j) {
+                const int d = dst[j];
+                if (d < 0) continue;
+                uint4* orow = out + (size_t)d * nvec;
+#pragma unroll
+                for (int u = 0; u < kCopyUnroll; ++u) {
+                    const int v = v0 + u * kCopyThreads;
+                    if (v < nvec) orow[v] = val[u];
+                }
+            }
+        }
+        __syncthreads();
+    }
+}
+
+__global__ void pack_w13_kernel(const uint4* __restrict__ wg, const uint4* __restrict__ wu, int E, int I,
+                                int Ip, int nvec, uint4* __restrict__ packed) {
+    const int64_t rows = (int64_t)E * 2 * Ip;
+    for (int64_t row = blockIdx.x; row < rows; row += gridDim.x) {
+        const int e = (int)(row / (2 * Ip));
+        const int r = (int)(row % (2 * Ip));
+        const int q = r % 256;
+        const int i = (r / 256) * 128 + (q & 127);
+        const uint4* src = i < I ? ((q < 128 ? wg : wu) + ((size_t)e * I + i) * nvec) : nullptr;
+        uint4* dst = packed + (size_t)row * nvec;
+        for (int v = threadIdx.x; v < nvec; v += blockDim.x)
+            dst[v] = src ? src[v] : make_uint4(0, 0, 0, 0);
+    }
+}
+
+}  // namespace
+
+size_t init_routing_scratch_bytes(int T, int E, int k) {
+    const int64_t R = (int64_t)T * k;
+    const int64_t NW = ceil_div(R, kChunk);
+    return (size_t)(NW > 0 ? NW : 1) * (size_t)E * sizeof(int32_t);
+}
+
+moe_status_t launch_init_routing_index(const int32_t* ids, int R, int E, int32_t* counts, int32_t* offsets,
+                                       int32_t* row_idx, int32_t* scratch, uint32_t* status,
+                                       cudaStream_t s) {
+    const int NW = (int)ceil_div(R, kChunk);
+    const int blocks = (int)ceil_div(NW > 0 ? NW : 1, kHistWarps);
+    const size_t sm = (size_t)kHistWarps * E * sizeof(int32_t);
+    if (NW > 0) {
+        hist_kernel<<<blocks, kHistWarps * 32, sm, s>>>(ids, R, E, NW, scratch, status);
+        note_launch();
+        MOE_TRY(last_launch_status());
+    }
+    scan_kernel<<<1, 1024, 0, s>>>(scratch, NW, E, counts, offsets);
+    note_launch();
+    MOE_TRY(last_launch_status());
+    if (NW > 0) {
+        scatter_kernel<<<blocks, kHistWarps * 32, sm, s>>>(ids, R, E, NW, scratch, row_idx);
+        note_launch();
+        MOE_TRY(last_launch_status());
+    }
+    return MOE_OK;
+}
+
+moe_status_t launch_permute_rows(const void* x, size_t row_bytes, const int32_t* row_idx, int T, int k,
+                                 void* expanded_x, cudaStream_t s) {
+    if (T == 0) return MOE_OK;
+    const int nvec = (int)(row_bytes / 16);
+    const int grid = (int)std::min<int64_t>(T, (int64_t)sm_count() * 16);
+    permute_rows_kernel<<<grid, kCopyThreads, 0, s>>>(static_cast<const uint4*>(x), nvec, row_idx, T, k,
+                                                      T * k, static_cast<uint4*>(expanded_x));
+    note_launch();
+    return last_launch_status();
+}
+
+moe_status_t launch_pack_w13(const void* w_gate, const void* w_up, size_t esize, int E, int H, int I,
+                             void* packed, cudaStream_t s) {
+    const int Ip = (int)round_up((size_t)I, 128);
+    const int nvec = (int)((size_t)H * esize / 16);
+    const int64_t rows = (int64_t)E * 2 * Ip;
+    const int grid = (int)std::min<int64_t>(rows, (int64_t)sm_count() * 32);
+    pack_w13_kernel<<<grid, 128, 0, s>>>(static_cast<const uint4*>(w_gate), static_cast<const uint4*>(w_up),
+                                         E, I, Ip, nvec, static_cast<uint4*>(packed));
+    note_launch();
+    return last_launch_status();
+}
+
+}  // namespace moe

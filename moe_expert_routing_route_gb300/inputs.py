@@ -67,6 +67,10 @@ CONFIGS = {
                                dtype="bf16", seed=3),
     "dsv3_zipf_prefill": LayerConfig("dsv3_zipf_prefill", T=16384, H=7168, E=256, k=8, I=2048,
                                      S=1, dtype="bf16", seed=4, zipf_s=1.2),
+    # Profiling slice: the DeepSeek-V3 prefill layer's per-expert shape (about 128 rows
+    # per expert) on 32 experts, small enough for ncu captures (~5 GB on the device).
+    "dsv3_prefill_slice": LayerConfig("dsv3_prefill_slice", T=512, H=7168, E=32, k=8, I=2048, S=1,
+                                      dtype="bf16", seed=2),
 }
 CONFIG_ORDER = ["tiny_fp32", "mid_bf16", "dsv3_prefill", "dsv3_decode", "dsv3_zipf_prefill"]
 

@@ -1,0 +1,83 @@
+"""Algorithmic FLOPs and bytes of each layer step, for roofline fractions.
+
+"Lower latency and higher throughput with multi-node DeepSeek deployment"
+(Perplexity blog), §Roofline: the horizontal axis is arithmetic intensity, FLOPs
+over memory I/O bytes computed from the kernel's semantics; the ceilings are the
+peak tensor throughput and the memory bandwidth.  §Roofline / GroupGEMM: g
+groups of [m,k]x[k,n] cost 2*g*m*k*n FLOPs and g*(m*k + n*k + m*n) elements of
+I/O; §Roofline / GEMM: one [m,k]x[k,n] costs 2*m*k*n FLOPs and m*k + n*k + m*n
+elements.
+
+Bytes here are the compulsory traffic of each step: every input read once,
+every output written once, weights of the experts that received at least one
+row.  The fused SwiGLU up-projection writes h [rows, I] instead of the [rows, 2I]
+GEMM output, so its output term is half the plain GroupGEMM one.
+"""
+from __future__ import annotations
+
+import json
+import os
+
+
+def gemm_cost(m: int, k: int, n: int):
+    """(FLOPs, I/O elements) of one [m,k]x[k,n] GEMM."""
+    return 2 * m * k * n, m * k + n * k + m * n
+
+
+def group_gemm_cost(g: int, m: int, k: int, n: int):
+    """(FLOPs, I/O elements) of g equal groups of [m,k]x[k,n]."""
+    return 2 * g * m * k * n, g * (m * k + n * k + m * n)
+
+
+def balanced_tokens_per_expert(batch: int, q_len: int, top_k: int, ranks: int, experts: int) -> float:
+    """Average rows per expert when `ranks` data-parallel ranks each route
+    batch*q_len tokens to top_k of `experts` experts."""
+    return batch * q_len * top_k * ranks / experts
+
+
+def stage_costs(T: int, H: int, E: int, k: int, I: int, S: int, esize: int, touched: int) -> dict:
+    """{stage: (flops, bytes)} for the nine layer steps.  touched = experts with >= 1 row."""
+    R = T * k
+    b = esize
+    SI = S * I
+    c = {}
+    c["gate"] = (2 * T * H * E, T * H * b + E * H * b + T * E * 4)
+    c["route"] = (0, T * E * 4 + R * 8)
+    c["init_routing"] = (0, 2 * R * 4 + R * 4 + (E + 1) * 4 + E * 4)
+    c["permute_rows"] = (0, T * H * b + R * H * b + R * 4)
+    c["up_routed"] = (2 * R * H * 2 * I, touched * 2 * I * H * b + R * H * b + R * I * b)
+    c["up_shared"] = (2 * T * H * 2 * SI, (2 * SI * H + T * H + T * SI) * b if S else 0)
+    c["down_routed"] = (2 * R * I * H, touched * H * I * b + R * I * b + R * H * b)
+    c["down_shared"] = (2 * T * SI * H, (H * SI + T * SI + T * H) * b if S else 0)
+    c["finalize"] = (0, R * H * b + (T * H * b if S else 0) + T * H * b + R * 8)
+    return c
+
+
+def layer_flops(T: int, H: int, E: int, k: int, I: int, S: int) -> int:
+    return sum(f for f, _ in stage_costs(T, H, E, k, I, S, 2, E).values())
+
+
+def load_peaks(path: str | None = None) -> dict:
+    """Measured peaks of this machine's GPUs if present, else the stated fallback."""
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    path = path or os.path.join(root, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return dict(hbm_gbs=float(p["hbm_gbs"]), bf16_tflops=float(p["bf16_tflops"]),
+                    bf16_tflops_sustained=float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                    source="measured")
+    return dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0, source="fallback")
+
+
+def roofline_entry(flops: float, nbytes: float, seconds: float, peaks: dict, sustained: bool = True) -> dict:
+    """The binding roofline of one kernel: whichever of compute time at the
+    tensor peak and byte time at HBM bandwidth is larger."""
+    tf = peaks["bf16_tflops_sustained"] if sustained else peaks["bf16_tflops"]
+    t_compute = flops / (tf * 1e12) if flops else 0.0
+    t_bytes = nbytes / (peaks["hbm_gbs"] * 1e9)
+    if t_compute > t_bytes:
+        achieved = flops / seconds / 1e12
+        return dict(bound="tensor", achieved=achieved, peak=tf, unit="TFLOP/s", frac=achieved / tf)
+    achieved = nbytes / seconds / 1e9
+    return dict(bound="hbm", achieved=achieved, peak=peaks["hbm_gbs"], unit="GB/s", frac=achieved / peaks["hbm_gbs"])

@@ -1,0 +1,66 @@
+"""Comparison helpers shared by the tests (no arithmetic of the method here)."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from moe_expert_routing_route_gb300 import inputs
+
+
+def f64(a) -> np.ndarray:
+    """Values of a torch tensor or a numpy array (bf16 bit patterns included) as fp64."""
+    if isinstance(a, torch.Tensor):
+        return a.detach().cpu().to(torch.float64).numpy()
+    a = np.asarray(a)
+    if a.dtype == np.uint16:
+        return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(torch.float64).numpy()
+    return a.astype(np.float64)
+
+
+def rel_l2(got, want) -> float:
+    got, want = f64(got), f64(want)
+    den = np.linalg.norm(want)
+    return float(np.linalg.norm(got - want) / (den if den > 0 else 1.0))
+
+
+def np_(t):
+    return inputs.to_numpy(t)
+
+
+def routing_ambiguity(scores: np.ndarray, k: int, err: float) -> np.ndarray:
+    """True for tokens whose top-k (with slot order) could flip under a score
+    perturbation of at most `err` per element: some adjacent gap among the k+1
+    best scores is <= 2*err."""
+    T, E = scores.shape
+    srt = -np.sort(-scores, axis=1)[:, :min(k + 1, E)]
+    gaps = srt[:, :-1] - srt[:, 1:]
+    return np.any(gaps <= 2 * err, axis=1)
+
+
+def check_topk_valid(ids: np.ndarray, scores: np.ndarray, err: float):
+    """ids [k] must be distinct and a top-k of `scores` (descending) up to 2*err."""
+    k = ids.size
+    assert len(set(ids.tolist())) == k, "duplicate expert ids"
+    s = scores[ids]
+    assert np.all(s[:-1] >= s[1:] - 2 * err), "slots not in descending order"
+    rest = np.setdiff1d(np.arange(scores.size), ids)
+    if rest.size:
+        assert s.min() >= scores[rest].max() - 2 * err, "a better expert was left out"
+
+
+def check_permutation_properties(ids: np.ndarray, E: int, counts, offsets, row_idx, x=None, ex=None):
+    """Init-routing outputs that hold for any ids: counts = histogram, offsets =
+    exclusive scan, row_idx a stable expert-major permutation, rows copied."""
+    R = ids.size
+    counts, offsets, row_idx = np.asarray(counts), np.asarray(offsets), np.asarray(row_idx)
+    assert np.array_equal(counts, np.bincount(ids.ravel(), minlength=E))
+    assert offsets[0] == 0 and np.array_equal(np.diff(offsets), counts) and offsets[-1] == R
+    assert np.array_equal(np.sort(row_idx), np.arange(R))
+    inv = np.argsort(row_idx)
+    flat = ids.ravel()
+    for e in np.nonzero(counts)[0]:
+        seg = inv[offsets[e]:offsets[e + 1]]
+        assert np.all(flat[seg] == e) and np.all(np.diff(seg) > 0)
+    if x is not None:
+        k = ids.shape[1]
+        assert np.array_equal(ex[row_idx], x[np.arange(R) // k])
