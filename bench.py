@@ -243,6 +243,9 @@ def run_ours(args, world, rank, local):
         raise RuntimeError("device status word set during warm-up")
 
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nst + 1)] for _ in range(args.steps)]
+    for step_evs in evs:  # create the CUDA events before the timed region
+        for e in step_evs:
+            e.record(stream)
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(local)
     time.sleep(0.1)

@@ -260,6 +260,11 @@ class MoELayer:
             st = lib().moe_layer_forward(ctypes.byref(self.desc), _ptr(x), _ptr(out), _ptr(self.ws),
                                          self.ws.numel(), _stream(stream))
         else:
+            if len(events) != MOE_NUM_STAGES + 1:
+                raise ValueError(f"{MOE_NUM_STAGES + 1} events expected")
+            for e in events:  # torch creates the CUDA event on its first record
+                if e.cuda_event == 0:
+                    e.record()
             arr = (P * (MOE_NUM_STAGES + 1))(*[ctypes.c_void_p(e.cuda_event) for e in events])
             st = lib().moe_layer_forward_timed(ctypes.byref(self.desc), _ptr(x), _ptr(out), _ptr(self.ws),
                                                self.ws.numel(), _stream(stream), arr)
