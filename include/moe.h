@@ -22,9 +22,9 @@
  *     library never allocates, frees or synchronises (except
  *     moe_check_device_status and moe_layer_forward_host, which say so).
  *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default
- *     stream).  Apart from moe_layer_forward_host and moe_check_device_status
- *     they issue no host synchronisation, so a sequence of calls can be
- *     captured into a CUDA graph.
+ *     stream).  The entry points other than moe_layer_forward_host,
+ *     moe_check_device_status and moe_init_routing_noalloc issue no host
+ *     synchronisation, so a sequence of them can be captured into a CUDA graph.
  *   - Device pointers must be 16-byte aligned.  Matrices are row-major and
  *     contiguous; weights are stored like Linear weights, [out, in] with the
  *     reduction dimension contiguous.
@@ -129,6 +129,29 @@ moe_status_t moe_init_routing(const void* x, moe_dtype_t dt, const int32_t* topk
                               int E, int k, void* expanded_x, int32_t* expanded_row_idx,
                               int32_t* tokens_per_expert, int32_t* expert_offsets, void* ws,
                               size_t ws_bytes, moe_stream_t stream);
+
+/* Init-routing without a workspace, for callers that cannot allocate device
+ * memory: for example a serving engine that gives all device memory to its own
+ * pool at start-up and permits no further cudaMalloc, a latency-critical loop
+ * that must not pay cudaMalloc's implicit synchronisation, or a C program with
+ * no device allocator.  The pages have no counterpart to this entry point.
+ * Outputs and argument meanings are those of moe_init_routing; the caller still
+ * passes every input and output buffer.
+ * Scratch: a fixed 1 MiB array in this library's device memory (262144 int32),
+ * held on every GPU that loads the library until the process exits.  A call
+ * needs ceil(T*k/1024)*E of those ints (E=256: up to 1,048,576 expanded rows);
+ * a larger call returns MOE_ERR_UNSUPPORTED.  No allocation of any kind is made.
+ * The first call on a device looks up the array's device address (with that
+ * device current) and keeps it; make that first call before any stream
+ * capture.  All calls share the array and it keeps the last call's contents
+ * (every entry a call reads is rewritten by that call, so nothing needs
+ * clearing), but calls whose kernels overlap on the GPU race on it.  There is
+ * no status word: an id outside [0,E) shows as expanded_row_idx = -1 and is not
+ * counted in tokens_per_expert. */
+moe_status_t moe_init_routing_noalloc(const void* x, moe_dtype_t dt, const int32_t* topk_ids, int T, int H,
+                                      int E, int k, void* expanded_x, int32_t* expanded_row_idx,
+                                      int32_t* tokens_per_expert, int32_t* expert_offsets,
+                                      moe_stream_t stream);
 
 /* ---------------------------------------------------------------------------
  * Expert weight packing for the grouped FFN.  Interleaves each expert's gate

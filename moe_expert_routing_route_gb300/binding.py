@@ -44,6 +44,7 @@ SIGNATURES = {
     "moe_route_topk": (I32, [P, P, I32, I32, I32, I32, P, P, P]),
     "moe_init_routing_workspace_bytes": (SZ, [I32, I32, I32]),
     "moe_init_routing": (I32, [P, I32, P, I32, I32, I32, I32, P, P, P, P, P, SZ, P]),
+    "moe_init_routing_noalloc": (I32, [P, I32, P, I32, I32, I32, I32, P, P, P, P, P]),
     "moe_w13_packed_bytes": (SZ, [I32, I32, I32, I32]),
     "moe_pack_w13": (I32, [P, P, I32, I32, I32, I32, P, P]),
     "moe_grouped_ffn_workspace_bytes": (SZ, [I32, I32, I32]),
@@ -159,6 +160,23 @@ def moe_init_routing(x: torch.Tensor, topk_ids: torch.Tensor, E: int, stream=Non
                                   _ptr(out["expanded_row_idx"]), _ptr(out["tokens_per_expert"]),
                                   _ptr(out["expert_offsets"]), _ptr(ws), ws.numel(), _stream(stream)),
            "moe_init_routing")
+    return out
+
+
+def moe_init_routing_noalloc(x: torch.Tensor, topk_ids: torch.Tensor, E: int, stream=None) -> dict:
+    """moe_init_routing without a workspace: the library's fixed device array is the
+    scratch (for callers that cannot allocate; calls must not overlap on the GPU)."""
+    T, H = x.shape
+    k = topk_ids.shape[1]
+    dev = x.device
+    out = dict(expanded_x=torch.empty((T * k, H), dtype=x.dtype, device=dev),
+               expanded_row_idx=torch.empty(T * k, dtype=torch.int32, device=dev),
+               tokens_per_expert=torch.empty(E, dtype=torch.int32, device=dev),
+               expert_offsets=torch.empty(E + 1, dtype=torch.int32, device=dev))
+    _check(lib().moe_init_routing_noalloc(_ptr(x), _dt(x), _ptr(topk_ids), T, H, E, k, _ptr(out["expanded_x"]),
+                                          _ptr(out["expanded_row_idx"]), _ptr(out["tokens_per_expert"]),
+                                          _ptr(out["expert_offsets"]), _stream(stream)),
+           "moe_init_routing_noalloc")
     return out
 
 
