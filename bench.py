@@ -42,8 +42,8 @@ METRIC = "MoE-layer tokens/sec at 1 GB300; grouped-GEMM % tensor peak; routing G
 UNIT = "tokens/s"
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.txt")
 KERNEL_SOURCES = {
-    "up_routed": "gemm_tc.cu", "down_routed": "gemm_tc.cu", "up_shared": "gemm_tc.cu",
-    "down_shared": "gemm_tc.cu", "gate": "gemm_tc.cu", "permute_rows": "permute.cu",
+    "up": "gemm_tc.cu", "down": "gemm_tc.cu", "shared": "gemm_tc.cu", "gate": "gemm_tc.cu",
+    "permute_rows": "permute.cu",
     "init_routing": "permute.cu", "route": "route.cu", "finalize": "finalize.cu",
 }
 
@@ -242,7 +242,7 @@ def run_ours(args, world, rank, local):
     if layer.device_status() != 0:
         raise RuntimeError("device status word set during warm-up")
 
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nst + 1)] for _ in range(args.steps)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2 * nst)] for _ in range(args.steps)]
     for step_evs in evs:  # create the CUDA events before the timed region
         for e in step_evs:
             e.record(stream)
@@ -265,7 +265,7 @@ def run_ours(args, world, rank, local):
     clocks.stop()
     ms = start.elapsed_time(end) / args.steps
     ms_max = max_over_ranks(ms, world)
-    stage_ms = {name: sum(evs[i][s].elapsed_time(evs[i][s + 1]) for i in range(args.steps)) / args.steps
+    stage_ms = {name: sum(evs[i][2 * s].elapsed_time(evs[i][2 * s + 1]) for i in range(args.steps)) / args.steps
                 for s, name in enumerate(binding.stage_names())}
     if layer.device_status() != 0:
         raise RuntimeError("device status word set during the timed region")
@@ -289,8 +289,8 @@ def run_ours(args, world, rank, local):
         stages[name] = dict(us=round(t * 1e3, 2), tflops=round(f_ / (t / 1e3) / 1e12, 2) if t > 0 else None,
                             gbs=round(b_ / (t / 1e3) / 1e9, 1) if t > 0 else None)
     layer_fl = sum(f for f, _ in costs.values())
-    gemm_fl = sum(costs[s][0] for s in ("up_routed", "down_routed", "up_shared", "down_shared"))
-    gemm_ms = sum(stage_ms[s] for s in ("up_routed", "down_routed", "up_shared", "down_shared"))
+    gemm_fl = sum(costs[s][0] for s in ("up", "down", "shared"))
+    gemm_ms = sum(stage_ms[s] for s in ("up", "down", "shared"))
 
     # end to end from pinned host memory through the C ABI
     x_host = x.cpu().pin_memory()

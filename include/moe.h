@@ -225,11 +225,13 @@ typedef struct moe_layer_desc {
     const void* w2_shared;     /* [H, S*I]: the shared down projections side by side; NULL iff S == 0 */
 } moe_layer_desc;
 
-/* Layer steps timed by moe_layer_forward_timed, in launch order. */
-#define MOE_NUM_STAGES 9
+/* Layer steps timed by moe_layer_forward_timed.  "shared" (both projections of
+ * the shared experts) runs on a second stream of the library's, forked after
+ * the gate and joined before "up", concurrently with route, init_routing and
+ * permute_rows; "up" and "down" are the routed experts. */
+#define MOE_NUM_STAGES 8
 const char* moe_stage_name(int stage); /* "gate", "route", "init_routing", "permute_rows",
-                                          "up_routed", "up_shared", "down_routed",
-                                          "down_shared", "finalize" */
+                                          "shared", "up", "down", "finalize" */
 
 /* Workspace fields of the layer (intermediates a caller may inspect). */
 typedef enum moe_ws_field {
@@ -253,12 +255,18 @@ size_t moe_layer_workspace_bytes(const moe_layer_desc* desc);
 moe_status_t moe_layer_workspace_field(const moe_layer_desc* desc, moe_ws_field field, size_t* offset,
                                        size_t* bytes);
 
-/* x [T,H] dt, out [T,H] dt, ws of moe_layer_workspace_bytes(desc) bytes. */
+/* x [T,H] dt, out [T,H] dt, ws of moe_layer_workspace_bytes(desc) bytes.
+ * With S > 0 the first call on a device creates the library's second stream
+ * and two events for that device (no device memory is allocated); make that
+ * first call outside stream capture.  The call's work forks onto that stream
+ * and joins back into `stream`. */
 moe_status_t moe_layer_forward(const moe_layer_desc* desc, const void* x, void* out, void* ws,
                                size_t ws_bytes, moe_stream_t stream);
 
-/* As moe_layer_forward, also recording stage_events[i] (cudaEvent_t) before
- * step i and stage_events[MOE_NUM_STAGES] after the last one. */
+/* As moe_layer_forward, also recording stage_events[2*i] (cudaEvent_t) when
+ * stage i starts and stage_events[2*i+1] when it ends (2*MOE_NUM_STAGES events;
+ * NULL entries are skipped).  The "shared" stage's events are recorded on the
+ * library's second stream. */
 moe_status_t moe_layer_forward_timed(const moe_layer_desc* desc, const void* x, void* out, void* ws,
                                      size_t ws_bytes, moe_stream_t stream, void* const* stage_events);
 

@@ -20,7 +20,7 @@ MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA, MOE_ERR_DEVICE =
 MOE_F32, MOE_BF16 = 0, 1
 MOE_DEVERR_BAD_EXPERT_ID, MOE_DEVERR_BAD_ROW_INDEX, MOE_DEVERR_BAD_OFFSETS, MOE_DEVERR_TIMEOUT = 1, 2, 4, 8
 MOE_WS_HEADER_BYTES = 256
-MOE_NUM_STAGES = 9
+MOE_NUM_STAGES = 8
 WS_FIELDS = ["logits", "topk_ids", "topk_w", "tokens_per_expert", "expert_offsets", "expanded_row_idx",
              "expanded_x", "h_routed", "h_shared", "y_routed", "y_shared", "x_in", "out"]
 
@@ -278,12 +278,12 @@ class MoELayer:
             st = lib().moe_layer_forward(ctypes.byref(self.desc), _ptr(x), _ptr(out), _ptr(self.ws),
                                          self.ws.numel(), _stream(stream))
         else:
-            if len(events) != MOE_NUM_STAGES + 1:
-                raise ValueError(f"{MOE_NUM_STAGES + 1} events expected")
+            if len(events) != 2 * MOE_NUM_STAGES:
+                raise ValueError(f"{2 * MOE_NUM_STAGES} events expected (start, end per stage)")
             for e in events:  # torch creates the CUDA event on its first record
                 if e.cuda_event == 0:
                     e.record()
-            arr = (P * (MOE_NUM_STAGES + 1))(*[ctypes.c_void_p(e.cuda_event) for e in events])
+            arr = (P * (2 * MOE_NUM_STAGES))(*[ctypes.c_void_p(e.cuda_event) for e in events])
             st = lib().moe_layer_forward_timed(ctypes.byref(self.desc), _ptr(x), _ptr(out), _ptr(self.ws),
                                                self.ws.numel(), _stream(stream), arr)
         _check(st, "moe_layer_forward")

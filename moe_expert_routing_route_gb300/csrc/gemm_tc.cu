@@ -37,6 +37,7 @@
 #include "moe_internal.cuh"
 
 #include <cuda.h>
+#include <climits>
 #include <mutex>
 
 namespace moe {
@@ -249,7 +250,7 @@ __device__ __forceinline__ void store_row32(void* C, int64_t ldc, int64_t row, i
 template <int BN, int EPI>
 __global__ void __launch_bounds__(kThreads, 1)
 tc_grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
-                       const Params p) {
+                       const __grid_constant__ Params p) {
     using Cf = Cfg<BN>;
     constexpr int STAGES = Cf::STAGES;
     constexpr uint32_t IDESC = idesc_bf16(BM, BN);
@@ -529,6 +530,27 @@ moe_status_t launch_impl(const TcGroupedGemm& g, cudaStream_t s) {
     return last_launch_status();
 }
 
+// Gate-style launches (one dense problem, fp32 out): pick the n-tile width
+// that minimises waves x per-k-block time, where a k-block costs the larger of
+// its MMA time (M=128, N=BN, K=64: 2*BN cycles) and its operand fill
+// ((16 KB + BN*128 B) at ~128 B per cycle per SM).  Ties go to the wider tile.
+int pick_bn_f32(int M, int N) {
+    const int sms = sm_count();
+    int best = 256;
+    int64_t best_cost = INT64_MAX;
+    for (int bn : {256, 128, 64}) {
+        const int64_t tiles = ceil_div(M, BM) * ceil_div(N, bn);
+        const int64_t waves = ceil_div(tiles, sms);
+        const int64_t per_kb = std::max<int64_t>(2 * bn, (16384 + (int64_t)bn * 128) / 128);
+        const int64_t cost = waves * per_kb;
+        if (cost < best_cost) {
+            best_cost = cost;
+            best = bn;
+        }
+    }
+    return best;
+}
+
 }  // namespace
 
 int tc_packed_block() { return kPackBlock; }
@@ -543,9 +565,11 @@ moe_status_t launch_tc_grouped_gemm(const TcGroupedGemm& g, cudaStream_t s) {
         case TC_EPI_BF16:
             return launch_impl<256, TC_EPI_BF16>(g, s);
         case TC_EPI_F32:
-            if (g.N <= 64) return launch_impl<64, TC_EPI_F32>(g, s);
-            if (g.N <= 128) return launch_impl<128, TC_EPI_F32>(g, s);
-            return launch_impl<256, TC_EPI_F32>(g, s);
+            switch (pick_bn_f32(g.M, g.N)) {
+                case 64: return launch_impl<64, TC_EPI_F32>(g, s);
+                case 128: return launch_impl<128, TC_EPI_F32>(g, s);
+                default: return launch_impl<256, TC_EPI_F32>(g, s);
+            }
     }
     return MOE_ERR_INVALID_ARG;
 }

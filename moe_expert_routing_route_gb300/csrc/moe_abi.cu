@@ -12,6 +12,7 @@
 
 #include <atomic>
 #include <climits>
+#include <mutex>
 
 namespace moe {
 
@@ -41,27 +42,29 @@ moe_status_t clear_status(void* ws, cudaStream_t s) {
 
 int packed_rows(int I) { return 2 * (int)round_up((size_t)I, (size_t)tc_packed_block()); }
 
-// Routed grouped FFN: up (SwiGLU) then down, for bf16 on tcgen05, fp32 on FFMA.
-moe_status_t grouped_ffn(const void* a, moe_dtype_t dt, const int32_t* offsets, int G, int rows, int H, int I,
-                         const void* w13p, const void* w2, void* h, void* y, uint32_t* status, cudaStream_t s,
-                         cudaEvent_t ev_mid) {
-    if (rows == 0) {
-        if (ev_mid) MOE_CUDA_TRY(cudaEventRecord(ev_mid, s));
-        return MOE_OK;
-    }
+// Grouped FFN halves: up (SwiGLU into h) and down (h into y); bf16 on tcgen05,
+// fp32 on the FFMA pipes.  offsets == nullptr means one dense group of `rows`.
+moe_status_t ffn_up(const void* a, moe_dtype_t dt, const int32_t* offsets, int G, int rows, int H, int I,
+                    const void* w13p, void* h, uint32_t* status, cudaStream_t s) {
+    if (rows == 0) return MOE_OK;
     if (dt == MOE_BF16) {
         TcGroupedGemm up{a, rows, H, offsets, G, w13p, packed_rows(I), I, h, I, TC_EPI_SWIGLU, status};
-        MOE_TRY(launch_tc_grouped_gemm(up, s));
-        if (ev_mid) MOE_CUDA_TRY(cudaEventRecord(ev_mid, s));
+        return launch_tc_grouped_gemm(up, s);
+    }
+    return launch_simt_grouped_ffn_up(static_cast<const float*>(a), rows, H, offsets, G,
+                                      static_cast<const float*>(w13p), packed_rows(I) / 2, I, static_cast<float*>(h),
+                                      status, s);
+}
+
+moe_status_t ffn_down(const void* h, moe_dtype_t dt, const int32_t* offsets, int G, int rows, int H, int I,
+                      const void* w2, void* y, uint32_t* status, cudaStream_t s) {
+    if (rows == 0) return MOE_OK;
+    if (dt == MOE_BF16) {
         TcGroupedGemm down{h, rows, I, offsets, G, w2, H, H, y, H, TC_EPI_BF16, status};
         return launch_tc_grouped_gemm(down, s);
     }
-    MOE_TRY(launch_simt_grouped_ffn_up(static_cast<const float*>(a), rows, H, offsets, G,
-                                       static_cast<const float*>(w13p), packed_rows(I) / 2, I,
-                                       static_cast<float*>(h), status, s));
-    if (ev_mid) MOE_CUDA_TRY(cudaEventRecord(ev_mid, s));
-    return launch_simt_grouped_down(static_cast<const float*>(h), rows, I, offsets, G,
-                                    static_cast<const float*>(w2), H, static_cast<float*>(y), status, s);
+    return launch_simt_grouped_down(static_cast<const float*>(h), rows, I, offsets, G, static_cast<const float*>(w2),
+                                    H, static_cast<float*>(y), status, s);
 }
 
 moe_status_t gate(const void* x, const void* wr, moe_dtype_t dt, int T, int H, int E, float* logits,
@@ -129,8 +132,43 @@ T* at(void* ws, size_t off) {
     return reinterpret_cast<T*>(static_cast<char*>(ws) + off);
 }
 
-moe_status_t record(void* const* ev, int i, cudaStream_t s) {
-    if (ev && ev[i]) MOE_CUDA_TRY(cudaEventRecord(static_cast<cudaEvent_t>(ev[i]), s));
+// Stage timing: ev[2*i] before stage i, ev[2*i+1] after it (caller's events).
+enum Stage { ST_GATE = 0, ST_ROUTE, ST_INIT, ST_PERMUTE, ST_SHARED, ST_UP, ST_DOWN, ST_FINALIZE };
+moe_status_t mark(void* const* ev, int stage, int end, cudaStream_t s) {
+    void* e = ev ? ev[2 * stage + end] : nullptr;
+    if (e) MOE_CUDA_TRY(cudaEventRecord(static_cast<cudaEvent_t>(e), s));
+    return MOE_OK;
+}
+
+// Per-device side stream for the shared experts, with the fork/join events.
+// The shared experts depend only on x, so they run on the side stream while
+// the main stream routes and permutes the tokens -- kernels that leave most of
+// the SMs idle ("Lower latency and higher throughput with multi-node DeepSeek
+// deployment", §Dispatch Overlap: the shared expert is computed while the
+// tokens are being dispatched).  The mutex keeps each call's record/wait pairs
+// together when several host threads use one device.
+struct SideStream {
+    cudaStream_t stream = nullptr;
+    cudaEvent_t fork = nullptr, join = nullptr;
+    std::mutex mu;
+};
+SideStream g_side[64];
+std::mutex g_side_init;
+
+moe_status_t side_stream(SideStream** out) {
+    int dev = 0;
+    MOE_CUDA_TRY(cudaGetDevice(&dev));
+    if (dev < 0 || dev >= 64) return MOE_ERR_UNSUPPORTED;
+    SideStream& ss = g_side[dev];
+    std::lock_guard<std::mutex> lock(g_side_init);
+    if (!ss.stream) {
+        int lo = 0, hi = 0;
+        MOE_CUDA_TRY(cudaDeviceGetStreamPriorityRange(&lo, &hi));
+        MOE_CUDA_TRY(cudaStreamCreateWithPriority(&ss.stream, cudaStreamNonBlocking, lo));
+        MOE_CUDA_TRY(cudaEventCreateWithFlags(&ss.fork, cudaEventDisableTiming));
+        MOE_CUDA_TRY(cudaEventCreateWithFlags(&ss.join, cudaEventDisableTiming));
+    }
+    *out = &ss;
     return MOE_OK;
 }
 
@@ -142,7 +180,10 @@ moe_status_t layer_forward(const moe_layer_desc* d, const void* x, void* out, vo
     const Layout L = layout(*d);
     if (ws_bytes < L.total) return MOE_ERR_INVALID_ARG;
     if (d->T == 0) {
-        for (int i = 0; i <= MOE_NUM_STAGES; ++i) MOE_TRY(record(ev, i, s));
+        for (int i = 0; i < MOE_NUM_STAGES; ++i) {
+            MOE_TRY(mark(ev, i, 0, s));
+            MOE_TRY(mark(ev, i, 1, s));
+        }
         return MOE_OK;
     }
     const int T = d->T, H = d->H, E = d->E, k = d->k, I = d->I, R = T * k;
@@ -162,56 +203,49 @@ moe_status_t layer_forward(const moe_layer_desc* d, const void* x, void* out, vo
     void* ys = at<void>(ws, L.off[MOE_WS_Y_SHARED]);
     int32_t* scratch = at<int32_t>(ws, L.scratch_off);
 
+    SideStream* side = nullptr;
+    if (SI > 0) MOE_TRY(side_stream(&side));
+    std::unique_lock<std::mutex> side_lock;
+    if (side) side_lock = std::unique_lock<std::mutex>(side->mu);
+
     MOE_TRY(clear_status(ws, s));
-    MOE_TRY(record(ev, 0, s));
+    MOE_TRY(mark(ev, ST_GATE, 0, s));
     MOE_TRY(gate(x, d->w_router, dt, T, H, E, logits, s));
-    MOE_TRY(record(ev, 1, s));
-    MOE_TRY(launch_route_topk(logits, d->expert_bias, T, E, k, d->renormalize, ids, w, s));
-    MOE_TRY(record(ev, 2, s));
-    MOE_TRY(launch_init_routing_index(ids, R, E, counts, offsets, row_idx, scratch, status, s));
-    MOE_TRY(record(ev, 3, s));
-    MOE_TRY(launch_permute_rows(x, (size_t)H * dt_size(dt), row_idx, T, k, ex, s));
-    MOE_TRY(record(ev, 4, s));
-    // routed up (stage 4) ... routed down (stage 6); the shared up (stage 5) runs
-    // between them so each stage boundary is one kernel.
-    if (dt == MOE_BF16) {
-        TcGroupedGemm up{ex, R, H, offsets, E, d->w13, packed_rows(I), I, h, I, TC_EPI_SWIGLU, status};
-        MOE_TRY(launch_tc_grouped_gemm(up, s));
-        MOE_TRY(record(ev, 5, s));
-        if (SI > 0) {
-            TcGroupedGemm sup{x, T, H, nullptr, 1, d->w13_shared, packed_rows(SI), SI, hs, SI, TC_EPI_SWIGLU,
-                              status};
-            MOE_TRY(launch_tc_grouped_gemm(sup, s));
-        }
-        MOE_TRY(record(ev, 6, s));
-        TcGroupedGemm down{h, R, I, offsets, E, d->w2, H, H, y, H, TC_EPI_BF16, status};
-        MOE_TRY(launch_tc_grouped_gemm(down, s));
-        MOE_TRY(record(ev, 7, s));
-        if (SI > 0) {
-            TcGroupedGemm sdown{hs, T, SI, nullptr, 1, d->w2_shared, H, H, ys, H, TC_EPI_BF16, status};
-            MOE_TRY(launch_tc_grouped_gemm(sdown, s));
-        }
+    MOE_TRY(mark(ev, ST_GATE, 1, s));
+    if (side) {
+        // fork: shared experts on the side stream, after the gate
+        MOE_CUDA_TRY(cudaEventRecord(side->fork, s));
+        MOE_CUDA_TRY(cudaStreamWaitEvent(side->stream, side->fork, 0));
+        cudaStream_t ss = side->stream;
+        MOE_TRY(mark(ev, ST_SHARED, 0, ss));
+        MOE_TRY(ffn_up(x, dt, nullptr, 1, T, H, SI, d->w13_shared, hs, status, ss));
+        MOE_TRY(ffn_down(hs, dt, nullptr, 1, T, H, SI, d->w2_shared, ys, status, ss));
+        MOE_TRY(mark(ev, ST_SHARED, 1, ss));
+        MOE_CUDA_TRY(cudaEventRecord(side->join, ss));
     } else {
-        const float* w13 = static_cast<const float*>(d->w13);
-        MOE_TRY(launch_simt_grouped_ffn_up(static_cast<const float*>(ex), R, H, offsets, E, w13,
-                                           packed_rows(I) / 2, I, static_cast<float*>(h), status, s));
-        MOE_TRY(record(ev, 5, s));
-        if (SI > 0)
-            MOE_TRY(launch_simt_grouped_ffn_up(static_cast<const float*>(x), T, H, nullptr, 1,
-                                               static_cast<const float*>(d->w13_shared), packed_rows(SI) / 2, SI,
-                                               static_cast<float*>(hs), status, s));
-        MOE_TRY(record(ev, 6, s));
-        MOE_TRY(launch_simt_grouped_down(static_cast<const float*>(h), R, I, offsets, E,
-                                         static_cast<const float*>(d->w2), H, static_cast<float*>(y), status, s));
-        MOE_TRY(record(ev, 7, s));
-        if (SI > 0)
-            MOE_TRY(launch_simt_grouped_down(static_cast<const float*>(hs), T, SI, nullptr, 1,
-                                             static_cast<const float*>(d->w2_shared), H, static_cast<float*>(ys),
-                                             status, s));
+        MOE_TRY(mark(ev, ST_SHARED, 0, s));
+        MOE_TRY(mark(ev, ST_SHARED, 1, s));
     }
-    MOE_TRY(record(ev, 8, s));
+    MOE_TRY(mark(ev, ST_ROUTE, 0, s));
+    MOE_TRY(launch_route_topk(logits, d->expert_bias, T, E, k, d->renormalize, ids, w, s));
+    MOE_TRY(mark(ev, ST_ROUTE, 1, s));
+    MOE_TRY(mark(ev, ST_INIT, 0, s));
+    MOE_TRY(launch_init_routing_index(ids, R, E, counts, offsets, row_idx, scratch, status, s));
+    MOE_TRY(mark(ev, ST_INIT, 1, s));
+    MOE_TRY(mark(ev, ST_PERMUTE, 0, s));
+    MOE_TRY(launch_permute_rows(x, (size_t)H * dt_size(dt), row_idx, T, k, ex, s));
+    MOE_TRY(mark(ev, ST_PERMUTE, 1, s));
+    // join: the routed GEMMs need every SM, so they start after the shared experts
+    if (side) MOE_CUDA_TRY(cudaStreamWaitEvent(s, side->join, 0));
+    MOE_TRY(mark(ev, ST_UP, 0, s));
+    MOE_TRY(ffn_up(ex, dt, offsets, E, R, H, I, d->w13, h, status, s));
+    MOE_TRY(mark(ev, ST_UP, 1, s));
+    MOE_TRY(mark(ev, ST_DOWN, 0, s));
+    MOE_TRY(ffn_down(h, dt, offsets, E, R, H, I, d->w2, y, status, s));
+    MOE_TRY(mark(ev, ST_DOWN, 1, s));
+    MOE_TRY(mark(ev, ST_FINALIZE, 0, s));
     MOE_TRY(launch_finalize(y, R, SI > 0 ? ys : nullptr, w, row_idx, dt, T, H, k, out, status, s));
-    MOE_TRY(record(ev, 9, s));
+    MOE_TRY(mark(ev, ST_FINALIZE, 1, s));
     return MOE_OK;
 }
 
@@ -337,8 +371,9 @@ moe_status_t moe_grouped_ffn(const void* a, moe_dtype_t dt, const int32_t* exper
         return MOE_ERR_UNSUPPORTED;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     MOE_TRY(clear_status(ws, s));
-    return grouped_ffn(a, dt, expert_offsets, E, rows, H, I, w13_packed, w2, at<void>(ws, MOE_WS_HEADER_BYTES), y,
-                       status_word(ws), s, nullptr);
+    void* h = at<void>(ws, MOE_WS_HEADER_BYTES);
+    MOE_TRY(ffn_up(a, dt, expert_offsets, E, rows, H, I, w13_packed, h, status_word(ws), s));
+    return ffn_down(h, dt, expert_offsets, E, rows, H, I, w2, y, status_word(ws), s);
 }
 
 moe_status_t moe_finalize_routing(const void* y, int64_t y_rows, const void* skip, const float* topk_w,
@@ -356,8 +391,8 @@ moe_status_t moe_finalize_routing(const void* y, int64_t y_rows, const void* ski
 }
 
 const char* moe_stage_name(int stage) {
-    static const char* names[MOE_NUM_STAGES] = {"gate",      "route",     "init_routing", "permute_rows", "up_routed",
-                                                "up_shared", "down_routed", "down_shared", "finalize"};
+    static const char* names[MOE_NUM_STAGES] = {"gate",   "route", "init_routing", "permute_rows",
+                                                "shared", "up",    "down",         "finalize"};
     return (stage >= 0 && stage < MOE_NUM_STAGES) ? names[stage] : "";
 }
 

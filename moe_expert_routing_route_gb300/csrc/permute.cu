@@ -8,13 +8,14 @@
 // §MoE Router: dense dispatch needs the routing aggregated per expert.
 //
 // The sort is a stable counting sort in three small kernels plus one copy:
-//   hist    one warp per chunk of kChunk source rows -> per-chunk histogram
+//   hist    one block per chunk of kChunk source rows -> per-chunk histogram
 //           hist[c][e] (chunk-major: coalesced writes)
 //   scan    one block: tokens_per_expert, expert_offsets and, for every
 //           (chunk, expert), the first destination row of that chunk's copies
-//   scatter one warp per chunk, chunks in source order, 32 rows per step;
-//           __match_any_sync groups the lanes with the same expert and the
-//           rank inside the group keeps source order (stable)
+//   scatter one block per chunk; each warp ranks its 128 rows in source order
+//           (__match_any_sync groups the lanes with the same expert, the rank
+//           inside the group keeps source order), then the warps' per-expert
+//           counts are prefix-summed in warp order: stable overall
 //   copy    x is read once (16-byte vectors) and each row is written to its
 //           k destinations (HBM-bound: T*H*b read + T*k*H*b written)
 #include "moe_internal.cuh"
@@ -22,29 +23,29 @@
 namespace moe {
 namespace {
 
-constexpr int kChunk = 1024;   // source rows per warp-chunk
-constexpr int kHistWarps = 8;  // warps per block in hist/scatter
+constexpr int kChunk = 1024;      // source rows per chunk (one block)
+constexpr int kChunkThreads = 256;
+constexpr int kChunkWarps = kChunkThreads / 32;
+constexpr int kRowsPerWarp = kChunk / kChunkWarps;  // 128 = 4 steps of 32
+constexpr int kSteps = kRowsPerWarp / 32;
 
-__global__ void __launch_bounds__(kHistWarps * 32)
+__global__ void __launch_bounds__(kChunkThreads)
 hist_kernel(const int32_t* __restrict__ ids, int R, int E, int NW, int32_t* __restrict__ hist,
             uint32_t* status) {
-    extern __shared__ int32_t sh[];
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int c = blockIdx.x * kHistWarps + warp;
-    if (c >= NW) return;
-    int32_t* my = sh + warp * E;
-    for (int e = lane; e < E; e += 32) my[e] = 0;
-    __syncwarp();
+    extern __shared__ int32_t sh[];  // [E]
+    const int c = blockIdx.x;
+    for (int e = threadIdx.x; e < E; e += kChunkThreads) sh[e] = 0;
+    __syncthreads();
     const int beg = c * kChunk, end = min(R, beg + kChunk);
     bool bad = false;
-    for (int src = beg + lane; src < end; src += 32) {
+    for (int src = beg + threadIdx.x; src < end; src += kChunkThreads) {
         const int id = __ldg(ids + src);
-        if ((unsigned)id < (unsigned)E) atomicAdd(&my[id], 1);
+        if ((unsigned)id < (unsigned)E) atomicAdd(&sh[id], 1);
         else bad = true;
     }
     if (bad) set_status(status, MOE_DEVERR_BAD_EXPERT_ID);
-    __syncwarp();
-    for (int e = lane; e < E; e += 32) hist[(size_t)c * E + e] = my[e];
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += kChunkThreads) hist[(size_t)c * E + e] = sh[e];
 }
 
 // Exclusive scan of up to 1024 values held one per thread; returns the
@@ -123,30 +124,50 @@ scan_kernel(int32_t* __restrict__ hist, int NW, int E, int32_t* __restrict__ cou
     }
 }
 
-__global__ void __launch_bounds__(kHistWarps * 32)
+__global__ void __launch_bounds__(kChunkThreads)
 scatter_kernel(const int32_t* __restrict__ ids, int R, int E, int NW, const int32_t* __restrict__ base,
                int32_t* __restrict__ row_idx) {
-    extern __shared__ int32_t sh[];
+    extern __shared__ int32_t sh[];  // [kChunkWarps][E]: per-warp counts, then per-warp first rows
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int c = blockIdx.x * kHistWarps + warp;
-    if (c >= NW) return;
-    int32_t* next = sh + warp * E;  // next destination row of each expert in this chunk
-    for (int e = lane; e < E; e += 32) next[e] = base[(size_t)c * E + e];
-    __syncwarp();
+    const int c = blockIdx.x;
+    for (int i = threadIdx.x; i < kChunkWarps * E; i += kChunkThreads) sh[i] = 0;
+    const int beg = c * kChunk + warp * kRowsPerWarp, end = min(R, c * kChunk + kChunk);
+    int id[kSteps], rank[kSteps];
+#pragma unroll
+    for (int q = 0; q < kSteps; ++q) {  // all loads first
+        const int src = beg + q * 32 + lane;
+        id[q] = src < end ? __ldg(ids + src) : -1;
+    }
+    __syncthreads();
+    int32_t* cnt = sh + warp * E;
     const unsigned lt_mask = (1u << lane) - 1u;
-    const int beg = c * kChunk, end = min(R, beg + kChunk);
-    for (int s0 = beg; s0 < end; s0 += 32) {
-        const int src = s0 + lane;
-        const bool in = src < end;
-        const int id = in ? __ldg(ids + src) : -1;
-        const bool ok = in && (unsigned)id < (unsigned)E;
-        const unsigned group = __match_any_sync(0xffffffffu, ok ? (unsigned)id : 0xffffffffu);
-        const int rank = __popc(group & lt_mask);
-        const int first = ok ? next[id] : 0;
+#pragma unroll
+    for (int q = 0; q < kSteps; ++q) {
+        const bool ok = (unsigned)id[q] < (unsigned)E;
+        const unsigned group = __match_any_sync(0xffffffffu, ok ? (unsigned)id[q] : 0xffffffffu);
+        const int r = __popc(group & lt_mask);
+        const int first = ok ? cnt[id[q]] : 0;
         __syncwarp();
-        if (ok && rank == 0) next[id] = first + __popc(group);
+        if (ok && r == 0) cnt[id[q]] = first + __popc(group);
         __syncwarp();
-        if (in) row_idx[src] = ok ? first + rank : -1;
+        rank[q] = first + r;
+        if (!ok) id[q] = -1;
+    }
+    __syncthreads();
+    // per expert: the chunk's first row plus the counts of the earlier warps
+    for (int e = threadIdx.x; e < E; e += kChunkThreads) {
+        int run = base[(size_t)c * E + e];
+        for (int w = 0; w < kChunkWarps; ++w) {
+            const int v = sh[w * E + e];
+            sh[w * E + e] = run;
+            run += v;
+        }
+    }
+    __syncthreads();
+#pragma unroll
+    for (int q = 0; q < kSteps; ++q) {
+        const int src = beg + q * 32 + lane;
+        if (src < end) row_idx[src] = id[q] >= 0 ? cnt[id[q]] + rank[q] : -1;
     }
 }
 
@@ -213,10 +234,8 @@ moe_status_t launch_init_routing_index(const int32_t* ids, int R, int E, int32_t
                                        int32_t* row_idx, int32_t* scratch, uint32_t* status,
                                        cudaStream_t s) {
     const int NW = (int)ceil_div(R, kChunk);
-    const int blocks = (int)ceil_div(NW > 0 ? NW : 1, kHistWarps);
-    const size_t sm = (size_t)kHistWarps * E * sizeof(int32_t);
     if (NW > 0) {
-        hist_kernel<<<blocks, kHistWarps * 32, sm, s>>>(ids, R, E, NW, scratch, status);
+        hist_kernel<<<NW, kChunkThreads, (size_t)E * sizeof(int32_t), s>>>(ids, R, E, NW, scratch, status);
         note_launch();
         MOE_TRY(last_launch_status());
     }
@@ -224,7 +243,8 @@ moe_status_t launch_init_routing_index(const int32_t* ids, int R, int E, int32_t
     note_launch();
     MOE_TRY(last_launch_status());
     if (NW > 0) {
-        scatter_kernel<<<blocks, kHistWarps * 32, sm, s>>>(ids, R, E, NW, scratch, row_idx);
+        scatter_kernel<<<NW, kChunkThreads, (size_t)kChunkWarps * E * sizeof(int32_t), s>>>(ids, R, E, NW, scratch,
+                                                                                              row_idx);
         note_launch();
         MOE_TRY(last_launch_status());
     }

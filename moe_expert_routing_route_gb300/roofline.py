@@ -35,22 +35,36 @@ def balanced_tokens_per_expert(batch: int, q_len: int, top_k: int, ranks: int, e
     return batch * q_len * top_k * ranks / experts
 
 
-def stage_costs(T: int, H: int, E: int, k: int, I: int, S: int, esize: int, touched: int) -> dict:
-    """{stage: (flops, bytes)} for the nine layer steps.  touched = experts with >= 1 row."""
+def gemm_part_costs(T: int, H: int, E: int, k: int, I: int, S: int, esize: int, touched: int) -> dict:
+    """{part: (flops, bytes)} of the four expert GEMMs: up/down x routed/shared."""
     R = T * k
     b = esize
     SI = S * I
-    c = {}
-    c["gate"] = (2 * T * H * E, T * H * b + E * H * b + T * E * 4)
-    c["route"] = (0, T * E * 4 + R * 8)
-    c["init_routing"] = (0, 2 * R * 4 + R * 4 + (E + 1) * 4 + E * 4)
-    c["permute_rows"] = (0, T * H * b + R * H * b + R * 4)
-    c["up_routed"] = (2 * R * H * 2 * I, touched * 2 * I * H * b + R * H * b + R * I * b)
-    c["up_shared"] = (2 * T * H * 2 * SI, (2 * SI * H + T * H + T * SI) * b if S else 0)
-    c["down_routed"] = (2 * R * I * H, touched * H * I * b + R * I * b + R * H * b)
-    c["down_shared"] = (2 * T * SI * H, (H * SI + T * SI + T * H) * b if S else 0)
-    c["finalize"] = (0, R * H * b + (T * H * b if S else 0) + T * H * b + R * 8)
-    return c
+    return {
+        "up_routed": (2 * R * H * 2 * I, touched * 2 * I * H * b + R * H * b + R * I * b),
+        "up_shared": (2 * T * H * 2 * SI, (2 * SI * H + T * H + T * SI) * b if S else 0),
+        "down_routed": (2 * R * I * H, touched * H * I * b + R * I * b + R * H * b),
+        "down_shared": (2 * T * SI * H, (H * SI + T * SI + T * H) * b if S else 0),
+    }
+
+
+def stage_costs(T: int, H: int, E: int, k: int, I: int, S: int, esize: int, touched: int) -> dict:
+    """{stage: (flops, bytes)} for the eight layer stages.  touched = experts with >= 1 row.
+    "shared" is both projections of the shared experts; "up"/"down" the routed ones."""
+    R = T * k
+    b = esize
+    g = gemm_part_costs(T, H, E, k, I, S, esize, touched)
+    add = lambda a, c: (a[0] + c[0], a[1] + c[1])  # noqa: E731
+    return {
+        "gate": (2 * T * H * E, T * H * b + E * H * b + T * E * 4),
+        "route": (0, T * E * 4 + R * 8),
+        "init_routing": (0, 2 * R * 4 + R * 4 + (E + 1) * 4 + E * 4),
+        "permute_rows": (0, T * H * b + R * H * b + R * 4),
+        "shared": add(g["up_shared"], g["down_shared"]),
+        "up": g["up_routed"],
+        "down": g["down_routed"],
+        "finalize": (0, R * H * b + (T * H * b if S else 0) + T * H * b + R * 8),
+    }
 
 
 def layer_flops(T: int, H: int, E: int, k: int, I: int, S: int) -> int:

@@ -28,7 +28,7 @@ def test_routed_up_projection_is_a_group_gemm_with_half_output():
     T, H, E, k, I = 4096, 7168, 256, 8, 2048
     m = T * k // E
     fl, el = roofline.group_gemm_cost(E, m, H, 2 * I)
-    c = roofline.stage_costs(T, H, E, k, I, 1, 2, touched=E)
+    c = roofline.gemm_part_costs(T, H, E, k, I, 1, 2, touched=E)
     assert c["up_routed"][0] == fl
     assert c["up_routed"][1] == 2 * (el - E * m * I)
     fl2, el2 = roofline.group_gemm_cost(E, m, I, H)
@@ -39,7 +39,7 @@ def test_dsv3_prefill_is_weight_bound_on_measured_peaks():
     """At ~128 rows per expert the grouped GEMM sits left of the ridge point (the
     page: GroupGEMM is memory-bound in most configurations)."""
     T, H, E, k, I = 4096, 7168, 256, 8, 2048
-    c = roofline.stage_costs(T, H, E, k, I, 1, 2, touched=E)
+    c = roofline.gemm_part_costs(T, H, E, k, I, 1, 2, touched=E)
     f, b = c["up_routed"]
     peaks = dict(hbm_gbs=6787.2, bf16_tflops=1927.2, bf16_tflops_sustained=1721.0)
     assert f / b < peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
@@ -60,3 +60,12 @@ def test_prefill_table_split_is_consistent():
         total = tokens / (r["latency_ms"] / 1e3)
         assert abs(total - r["total_tokens_s"]) < 1.0
         assert int(total / p["cards"]) == r["per_card_tokens_s"]
+
+
+def test_stage_costs_sum_the_parts():
+    T, H, E, k, I, S = 4096, 2048, 64, 6, 1408, 2
+    parts = roofline.gemm_part_costs(T, H, E, k, I, S, 2, touched=E)
+    st = roofline.stage_costs(T, H, E, k, I, S, 2, touched=E)
+    assert st["shared"] == tuple(a + b for a, b in zip(parts["up_shared"], parts["down_shared"]))
+    assert st["up"] == parts["up_routed"] and st["down"] == parts["down_routed"]
+    assert list(st) == ["gate", "route", "init_routing", "permute_rows", "shared", "up", "down", "finalize"]

@@ -156,9 +156,14 @@ def test_layer_forward_host_matches_device():
 def test_layer_stage_events():
     cfg = inputs.LayerConfig("ev_bf16", T=256, H=256, E=32, k=4, I=128, S=1, dtype="bf16", seed=23)
     d, layer = make(cfg)
-    evs = [torch.cuda.Event(enable_timing=True) for _ in range(binding.MOE_NUM_STAGES + 1)]
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(2 * binding.MOE_NUM_STAGES)]
     out = layer.forward(d["x"], events=evs)
     torch.cuda.synchronize()
-    times = [evs[i].elapsed_time(evs[i + 1]) for i in range(binding.MOE_NUM_STAGES)]
+    times = [evs[2 * i].elapsed_time(evs[2 * i + 1]) for i in range(binding.MOE_NUM_STAGES)]
     assert all(t >= 0 for t in times)
+    names = binding.stage_names()
+    # the shared experts overlap routing: they start after the gate and end before "up"
+    sh, up, gate = names.index("shared"), names.index("up"), names.index("gate")
+    assert evs[2 * gate + 1].elapsed_time(evs[2 * sh]) >= 0
+    assert evs[2 * sh + 1].elapsed_time(evs[2 * up]) >= 0
     assert torch.equal(out, layer.forward(d["x"]))
