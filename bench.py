@@ -170,7 +170,7 @@ def oracle_layer_time(cfg, host: dict, toks: np.ndarray) -> float:
     t0 = time.perf_counter()
     oracle.layer(host["x"], host["wg"], host["w_gate"], host["w_up"], host["w2"], host.get("s_gate"),
                  host.get("s_up"), host.get("s2"), k=cfg.k, renorm=cfg.renormalize, bias=host.get("bias"),
-                 tokens=toks)
+                 tokens=toks, n_group=cfg.n_group, topk_group=cfg.topk_group, group_rule=cfg.group_rule)
     return time.perf_counter() - t0
 
 
@@ -231,7 +231,8 @@ def run_ours(args, world, rank, local):
     d = inputs.make_layer(cfg, dev)
     layer = binding.MoELayer(T=cfg.T, k=cfg.k, w_router=d["wg"], w_gate=d["w_gate"], w_up=d["w_up"], w2=d["w2"],
                              s_gate=d["s_gate"] if cfg.S else None, s_up=d["s_up"] if cfg.S else None,
-                             s2=d["s2"] if cfg.S else None, expert_bias=d["bias"], renormalize=cfg.renormalize)
+                             s2=d["s2"] if cfg.S else None, expert_bias=d["bias"], renormalize=cfg.renormalize,
+                             n_group=cfg.n_group, topk_group=cfg.topk_group, group_rule=cfg.group_rule)
     x = d["x"]
     out = torch.empty_like(x)
     stream = torch.cuda.current_stream()

@@ -108,6 +108,23 @@ moe_status_t moe_gate_logits(const void* x, const void* w_router, moe_dtype_t dt
 moe_status_t moe_route_topk(const float* logits, const float* expert_bias, int T, int E, int k,
                             int renormalize, int32_t* topk_ids, float* topk_w, moe_stream_t stream);
 
+/* Group-limited top-k.  [BLOG §MoE Router]: flat routing is the special case
+ * of DeepSeek routing in which the selected group is all experts.  The E
+ * experts form n_group contiguous groups of E/n_group; a group's score is the
+ * largest s_e in it (group_rule 0) or the sum of its two largest s_e as one
+ * fp32 add (group_rule 1); the topk_group best groups are kept (ties to the
+ * lower group index); topk_ids are the k best experts of the kept groups
+ * (descending s, ties to the lower id).  Weights as in moe_route_topk (softmax
+ * over all E scores at the selected experts, renormalised when asked).
+ * 1 <= n_group <= 32, E % n_group == 0, 1 <= topk_group <= n_group,
+ * k <= topk_group * E/n_group; group_rule 1 needs E/n_group >= 2.
+ * n_group == 1 is exactly moe_route_topk. */
+#define MOE_GROUP_SCORE_MAX 0
+#define MOE_GROUP_SCORE_TOP2_SUM 1
+moe_status_t moe_route_topk_grouped(const float* logits, const float* expert_bias, int T, int E, int k,
+                                    int n_group, int topk_group, int group_rule, int renormalize,
+                                    int32_t* topk_ids, float* topk_w, moe_stream_t stream);
+
 /* ---------------------------------------------------------------------------
  * Init-routing.  [CANN §MoE deployment, Double-Routing step 1]: expand every
  * token k times and sort the copies by expert, returning expanded_x,
@@ -223,6 +240,9 @@ typedef struct moe_layer_desc {
     const void* w2;            /* [E,H,I] */
     const void* w13_shared;    /* moe_pack_w13 with E=1, I=S*I of the stacked shared gate/up [S*I,H]; NULL iff S == 0 */
     const void* w2_shared;     /* [H, S*I]: the shared down projections side by side; NULL iff S == 0 */
+    int n_group;               /* 0 or 1: flat top-k; > 1: group-limited (moe_route_topk_grouped) */
+    int topk_group;            /* groups kept when n_group > 1 */
+    int group_rule;            /* MOE_GROUP_SCORE_MAX or MOE_GROUP_SCORE_TOP2_SUM */
 } moe_layer_desc;
 
 /* Layer steps timed by moe_layer_forward_timed.  "shared" (both projections of

@@ -31,7 +31,7 @@ P, I32, I64, SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t
 class LayerDesc(ctypes.Structure):
     _fields_ = [("T", I32), ("H", I32), ("E", I32), ("k", I32), ("I", I32), ("S", I32), ("dtype", I32),
                 ("renormalize", I32), ("w_router", P), ("expert_bias", P), ("w13", P), ("w2", P),
-                ("w13_shared", P), ("w2_shared", P)]
+                ("w13_shared", P), ("w2_shared", P), ("n_group", I32), ("topk_group", I32), ("group_rule", I32)]
 
 
 _DP = ctypes.POINTER(LayerDesc)
@@ -42,6 +42,7 @@ SIGNATURES = {
     "moe_check_device_status": (I32, [P, P, ctypes.POINTER(ctypes.c_uint32)]),
     "moe_gate_logits": (I32, [P, P, I32, I32, I32, I32, P, P]),
     "moe_route_topk": (I32, [P, P, I32, I32, I32, I32, P, P, P]),
+    "moe_route_topk_grouped": (I32, [P, P, I32, I32, I32, I32, I32, I32, I32, P, P, P]),
     "moe_init_routing_workspace_bytes": (SZ, [I32, I32, I32]),
     "moe_init_routing": (I32, [P, I32, P, I32, I32, I32, I32, P, P, P, P, P, SZ, P]),
     "moe_init_routing_noalloc": (I32, [P, I32, P, I32, I32, I32, I32, P, P, P, P, P]),
@@ -145,6 +146,20 @@ def moe_route_topk(logits: torch.Tensor, k: int, renormalize: bool = True, exper
     return ids, w
 
 
+GROUP_RULES = {"max": 0, "top2_sum": 1}
+
+
+def moe_route_topk_grouped(logits: torch.Tensor, k: int, n_group: int, topk_group: int, rule: str = "max",
+                           renormalize: bool = True, expert_bias=None, stream=None):
+    T, E = logits.shape
+    ids = torch.empty((T, k), dtype=torch.int32, device=logits.device)
+    w = torch.empty((T, k), dtype=torch.float32, device=logits.device)
+    _check(lib().moe_route_topk_grouped(_ptr(logits), _ptr(expert_bias), T, E, k, n_group, topk_group,
+                                        GROUP_RULES[rule], int(bool(renormalize)), _ptr(ids), _ptr(w),
+                                        _stream(stream)), "moe_route_topk_grouped")
+    return ids, w
+
+
 def moe_init_routing(x: torch.Tensor, topk_ids: torch.Tensor, E: int, stream=None, ws=None) -> dict:
     T, H = x.shape
     k = topk_ids.shape[1]
@@ -230,7 +245,8 @@ class MoELayer:
     The gate/up weights are packed once (moe_pack_w13)."""
 
     def __init__(self, *, T: int, k: int, w_router, w_gate, w_up, w2, s_gate=None, s_up=None, s2=None,
-                 expert_bias=None, renormalize: bool = True, stream=None):
+                 expert_bias=None, renormalize: bool = True, n_group: int = 1, topk_group: int = 1,
+                 group_rule: str = "max", stream=None):
         E, I, H = w_gate.shape
         S = 0 if s_gate is None else s_gate.shape[0]
         self.T, self.H, self.E, self.k, self.I, self.S = T, H, E, k, I, S
@@ -249,7 +265,8 @@ class MoELayer:
         self.desc = LayerDesc(T, H, E, k, I, S, _dt(w_gate), int(bool(renormalize)), self.w_router.data_ptr(),
                               0 if self.expert_bias is None else self.expert_bias.data_ptr(), self.w13.data_ptr(),
                               self.w2.data_ptr(), 0 if S == 0 else self.w13_shared.data_ptr(),
-                              0 if S == 0 else self.w2_shared.data_ptr())
+                              0 if S == 0 else self.w2_shared.data_ptr(), n_group, topk_group,
+                              GROUP_RULES[group_rule])
         nbytes = lib().moe_layer_workspace_bytes(ctypes.byref(self.desc))
         if nbytes == 0:
             raise MoEError(MOE_ERR_INVALID_ARG, "moe_layer_workspace_bytes")

@@ -113,9 +113,20 @@ Layout layout(const moe_layer_desc& d) {
     return L;
 }
 
+moe_status_t check_grouping(int E, int k, int n_group, int topk_group, int rule) {
+    if (n_group <= 1) return MOE_OK;
+    if (n_group > 32 || E % n_group != 0) return MOE_ERR_INVALID_ARG;
+    if (topk_group < 1 || topk_group > n_group) return MOE_ERR_INVALID_ARG;
+    if ((int64_t)k > (int64_t)topk_group * (E / n_group)) return MOE_ERR_INVALID_ARG;
+    if (rule != MOE_GROUP_SCORE_MAX && rule != MOE_GROUP_SCORE_TOP2_SUM) return MOE_ERR_INVALID_ARG;
+    if (rule == MOE_GROUP_SCORE_TOP2_SUM && E / n_group < 2) return MOE_ERR_INVALID_ARG;
+    return MOE_OK;
+}
+
 moe_status_t check_desc(const moe_layer_desc* d) {
     if (!d) return MOE_ERR_INVALID_ARG;
     MOE_TRY(check_sizes(d->T, d->H, d->E, d->k));
+    MOE_TRY(check_grouping(d->E, d->k, d->n_group, d->topk_group, d->group_rule));
     if (bad_dtype(d->dtype) || d->I <= 0 || d->S < 0) return MOE_ERR_INVALID_ARG;
     if (d->I % 8 != 0) return MOE_ERR_UNSUPPORTED;
     if (!d->w_router || !d->w13 || !d->w2) return MOE_ERR_INVALID_ARG;
@@ -227,7 +238,8 @@ moe_status_t layer_forward(const moe_layer_desc* d, const void* x, void* out, vo
         MOE_TRY(mark(ev, ST_SHARED, 1, s));
     }
     MOE_TRY(mark(ev, ST_ROUTE, 0, s));
-    MOE_TRY(launch_route_topk(logits, d->expert_bias, T, E, k, d->renormalize, ids, w, s));
+    MOE_TRY(launch_route_topk(logits, d->expert_bias, T, E, k, d->renormalize, ids, w, s, d->n_group,
+                              d->topk_group, d->group_rule));
     MOE_TRY(mark(ev, ST_ROUTE, 1, s));
     MOE_TRY(mark(ev, ST_INIT, 0, s));
     MOE_TRY(launch_init_routing_index(ids, R, E, counts, offsets, row_idx, scratch, status, s));
@@ -316,6 +328,18 @@ moe_status_t moe_route_topk(const float* logits, const float* expert_bias, int T
     if (!logits || !topk_ids || !topk_w) return MOE_ERR_INVALID_ARG;
     return launch_route_topk(logits, expert_bias, T, E, k, renormalize ? 1 : 0, topk_ids, topk_w,
                              reinterpret_cast<cudaStream_t>(stream));
+}
+
+moe_status_t moe_route_topk_grouped(const float* logits, const float* expert_bias, int T, int E, int k, int n_group,
+                                    int topk_group, int group_rule, int renormalize, int32_t* topk_ids, float* topk_w,
+                                    moe_stream_t stream) {
+    MOE_TRY(check_sizes(T, 8, E, k));
+    if (n_group < 1) return MOE_ERR_INVALID_ARG;
+    MOE_TRY(check_grouping(E, k, n_group, topk_group, group_rule));
+    if (T == 0) return MOE_OK;
+    if (!logits || !topk_ids || !topk_w) return MOE_ERR_INVALID_ARG;
+    return launch_route_topk(logits, expert_bias, T, E, k, renormalize ? 1 : 0, topk_ids, topk_w,
+                             reinterpret_cast<cudaStream_t>(stream), n_group, topk_group, group_rule);
 }
 
 size_t moe_init_routing_workspace_bytes(int T, int E, int k) {

@@ -40,8 +40,11 @@ __device__ __forceinline__ void set_status(uint32_t* status, uint32_t bit) {
 
 // ---- launchers (stream-ordered, no host sync) ------------------------------------
 // route.cu
+// n_group <= 1: flat top-k; otherwise group-limited (topk_group groups kept,
+// rule 0 = group max, rule 1 = sum of the group's two largest scores).
 moe_status_t launch_route_topk(const float* logits, const float* bias, int T, int E, int k, int renorm,
-                               int32_t* ids, float* w, cudaStream_t s);
+                               int32_t* ids, float* w, cudaStream_t s, int n_group = 1, int topk_group = 1,
+                               int rule = 0);
 
 // permute.cu
 size_t init_routing_scratch_bytes(int T, int E, int k);

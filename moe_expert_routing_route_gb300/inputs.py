@@ -39,6 +39,9 @@ class LayerConfig:
     seed: int
     zipf_s: float | None = None
     renormalize: bool = True
+    n_group: int = 1          # > 1: group-limited routing
+    topk_group: int = 1
+    group_rule: str = "max"   # "max" | "top2_sum"
 
     @property
     def R(self) -> int:
@@ -67,6 +70,10 @@ CONFIGS = {
                                dtype="bf16", seed=3),
     "dsv3_zipf_prefill": LayerConfig("dsv3_zipf_prefill", T=16384, H=7168, E=256, k=8, I=2048,
                                      S=1, dtype="bf16", seed=4, zipf_s=1.2),
+    # The prefill layer with DeepSeek-V3's group-limited routing (8 groups of 32
+    # experts, 4 groups kept, group score = sum of its two best scores).
+    "dsv3_prefill_grouped": LayerConfig("dsv3_prefill_grouped", T=4096, H=7168, E=256, k=8, I=2048, S=1,
+                                        dtype="bf16", seed=2, n_group=8, topk_group=4, group_rule="top2_sum"),
     # Profiling slice: the DeepSeek-V3 prefill layer's per-expert shape (about 128 rows
     # per expert) on 32 experts, small enough for ncu captures (~5 GB on the device).
     "dsv3_prefill_slice": LayerConfig("dsv3_prefill_slice", T=512, H=7168, E=32, k=8, I=2048, S=1,

@@ -54,12 +54,13 @@ def _load():
         lib.oracle_round_array.argtypes = [P, I, L, P]
         lib.oracle_gate_logits.argtypes = [P, P, I, I, I, I, P]
         lib.oracle_route_topk.argtypes = [P, P, I, I, I, I, P, P]
+        lib.oracle_route_topk_grouped.argtypes = [P, P, I, I, I, I, I, I, I, P, P]
         lib.oracle_init_routing.argtypes = [P, I, I, I, P, I, I, P, P, P, P]
         lib.oracle_init_routing.restype = I
         lib.oracle_expert_ffn_rows.argtypes = [P, I, L, P, P, P, P, I, I, P]
         lib.oracle_finalize_routing.argtypes = [P, I, L, P, P, P, I, I, I, P]
         lib.oracle_layer.argtypes = [P, I, I, I, I, I, I, I, I, P, P, P, P, P, P, P, P, P, I,
-                                     P, P, P, P]
+                                     P, P, P, P, I, I, I]
         _lib = lib
         return lib
 
@@ -124,6 +125,19 @@ def route_topk(logits: np.ndarray, k: int, renorm: bool = True, bias: np.ndarray
     return ids, w
 
 
+def route_topk_grouped(logits: np.ndarray, k: int, n_group: int, topk_group: int, rule: str = "max",
+                       renorm: bool = True, bias: np.ndarray | None = None):
+    """Group-limited top-k (rule "max" or "top2_sum").  Returns (ids [T,k], w [T,k])."""
+    logits = _c(logits, np.float32)
+    bias = _c(bias, np.float32)
+    T, E = logits.shape
+    ids = np.empty((T, k), np.int32)
+    w = np.empty((T, k), np.float64)
+    _load().oracle_route_topk_grouped(_ptr(logits), _ptr(bias), T, E, k, n_group, topk_group,
+                                      {"max": 0, "top2_sum": 1}[rule], int(bool(renorm)), _ptr(ids), _ptr(w))
+    return ids, w
+
+
 def init_routing(ids: np.ndarray, x: np.ndarray | None, E: int, H: int | None = None):
     """Init-routing.  ids [T,k] int32, x [T,H] (float32 or bf16 bits) or None.
 
@@ -179,7 +193,7 @@ def finalize_routing(y: np.ndarray, scales: np.ndarray, expanded_row_idx: np.nda
 
 
 def layer(x, wg, wgate, wup, w2, sgate=None, sup=None, s2=None, *, k: int, renorm: bool = True,
-          bias=None, tokens=None):
+          bias=None, tokens=None, n_group: int = 1, topk_group: int = 1, group_rule: str = "max"):
     """Brute-force per-token MoE layer.
 
     x [T,H]; wg [E,H]; wgate/wup [E,I,H]; w2 [E,H,I]; sgate/sup [S,I,H]; s2 [S,H,I].
@@ -201,5 +215,6 @@ def layer(x, wg, wgate, wup, w2, sgate=None, sup=None, s2=None, *, k: int, renor
     out = np.empty((n, H), np.float64)
     _load().oracle_layer(_ptr(x), dt, T, H, E, k, I, S, int(bool(renorm)), _ptr(wg), _ptr(bias),
                          _ptr(wgate), _ptr(wup), _ptr(w2), _ptr(sgate), _ptr(sup), _ptr(s2),
-                         _ptr(toks), n, _ptr(logits), _ptr(ids), _ptr(w), _ptr(out))
+                         _ptr(toks), n, _ptr(logits), _ptr(ids), _ptr(w), _ptr(out), n_group, topk_group,
+                         {"max": 0, "top2_sum": 1}[group_rule])
     return dict(logits64=logits, ids=ids, w=w, out=out)

@@ -175,6 +175,74 @@ void oracle_route_topk(const float* logits, const float* bias, int T, int E, int
     }
 }
 
+/* ---- group-limited top-k ------------------------------------------------------
+ * [BLOG §MoE Router]: flat top-k is the special case of DeepSeek routing in
+ * which the selected group is all experts.  Steps, per token:
+ *   1. s_e = fl32(logits[t,e] + bias[e])                        (as above)
+ *   2. the E experts form n_group contiguous groups of E/n_group;
+ *      group score = the largest s in the group (rule 0), or the sum of the
+ *      two largest s in the group as one fp32 add (rule 1);
+ *   3. the topk_group groups with the highest group score are kept (ties to
+ *      the lower group index);
+ *   4. top-k over the experts of the kept groups, descending s, ties to the
+ *      lower expert id;
+ *   5. weights: softmax over all E scores at the selected experts, divided
+ *      by their sum when renorm != 0 (as in the flat router).
+ * Every decision (2-4) is taken on fp32 values with fp32 arithmetic.       */
+void oracle_route_topk_grouped(const float* logits, const float* bias, int T, int E, int k, int n_group,
+                               int topk_group, int rule, int renorm, int32_t* ids, double* w) {
+    const int gs = E / n_group;
+    #pragma omp parallel for schedule(static)
+    for (int t = 0; t < T; ++t) {
+        float* s = (float*)malloc(sizeof(float) * (size_t)E);
+        float* gscore = (float*)malloc(sizeof(float) * (size_t)n_group);
+        char* gkept = (char*)calloc((size_t)n_group, 1);
+        char* taken = (char*)calloc((size_t)E, 1);
+        for (int e = 0; e < E; ++e) s[e] = logits[(size_t)t * E + e] + (bias ? bias[e] : 0.0f);
+        for (int g = 0; g < n_group; ++g) {
+            float m1 = -INFINITY, m2 = -INFINITY;  /* largest, second largest */
+            for (int e = g * gs; e < (g + 1) * gs; ++e) {
+                if (s[e] > m1) { m2 = m1; m1 = s[e]; }
+                else if (s[e] > m2) { m2 = s[e]; }
+            }
+            gscore[g] = rule == 1 ? m1 + m2 : m1;
+        }
+        for (int r = 0; r < topk_group; ++r) {
+            int best = -1;
+            for (int g = 0; g < n_group; ++g) {
+                if (gkept[g]) continue;
+                if (best < 0 || gscore[g] > gscore[best]) best = g;
+            }
+            gkept[best] = 1;
+        }
+        for (int j = 0; j < k; ++j) {
+            int best = -1;
+            for (int e = 0; e < E; ++e) {
+                if (taken[e] || !gkept[e / gs]) continue;
+                if (best < 0 || s[e] > s[best]) best = e;
+            }
+            taken[best] = 1;
+            ids[(size_t)t * k + j] = best;
+        }
+        double smax = -INFINITY;
+        for (int e = 0; e < E; ++e) if ((double)s[e] > smax) smax = (double)s[e];
+        double denom_all = 0.0;
+        for (int e = 0; e < E; ++e) denom_all += exp((double)s[e] - smax);
+        double sel_sum = 0.0;
+        for (int j = 0; j < k; ++j) {
+            double p = exp((double)s[ids[(size_t)t * k + j]] - smax) / denom_all;
+            w[(size_t)t * k + j] = p;
+            sel_sum += p;
+        }
+        if (renorm)
+            for (int j = 0; j < k; ++j) w[(size_t)t * k + j] /= sel_sum;
+        free(s);
+        free(gscore);
+        free(gkept);
+        free(taken);
+    }
+}
+
 /* ---- init-routing -----------------------------------------------------------
  * [CANN §MoE deployment, Double-Routing step 1] + [BLOG §MoE Router]
  * (aggregation per expert).  Source row src = t*k + j (token-major).
@@ -293,7 +361,8 @@ void oracle_finalize_routing(const void* y, int dt, int64_t n_rows, const void* 
 
 /* ---- the whole layer, brute force per token ---------------------------------
  * [BLOG §Expert Parallelism]: out[t] = shared(x_t) + sum_j w_j * FFN_{e_j}(x_t)
- * with e_j, w_j from the router on the gate logits.  S shared experts (weights
+ * with e_j, w_j from the router on the gate logits (flat, or group-limited when
+ * n_group > 1).  S shared experts (weights
  * sgate/sup [S,I,H], s2 [S,H,I]) are summed into one shared output, stored in
  * dt; each routed expert output is stored in dt; the final sum is rounded to dt.
  * Only the tokens listed in tokens[0..n_tok) are evaluated (all when tokens is
@@ -304,7 +373,7 @@ void oracle_layer(const void* x, int dt, int T, int H, int E, int k, int I, int 
                   const void* wg, const float* bias, const void* wgate, const void* wup,
                   const void* w2, const void* sgate, const void* sup, const void* s2,
                   const int32_t* tokens, int n_tok, double* logits64, int32_t* ids, double* w,
-                  double* out) {
+                  double* out, int n_group, int topk_group, int group_rule) {
     if (!tokens) n_tok = T;
     #pragma omp parallel
     {
@@ -325,7 +394,11 @@ void oracle_layer(const void* x, int dt, int T, int H, int E, int k, int I, int 
                 l32[e] = (float)acc;
                 if (logits64) logits64[(size_t)n * E + e] = acc;
             }
-            oracle_route_topk(l32, bias, 1, E, k, renorm, ids + (size_t)n * k, w + (size_t)n * k);
+            if (n_group > 1)
+                oracle_route_topk_grouped(l32, bias, 1, E, k, n_group, topk_group, group_rule, renorm,
+                                          ids + (size_t)n * k, w + (size_t)n * k);
+            else
+                oracle_route_topk(l32, bias, 1, E, k, renorm, ids + (size_t)n * k, w + (size_t)n * k);
             /* shared experts: one summed output, stored in dt */
             for (int o = 0; o < H; ++o) ysh[o] = 0.0;
             for (int s = 0; s < S; ++s) {

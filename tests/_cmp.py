@@ -33,8 +33,9 @@ def routing_ambiguity(scores: np.ndarray, k: int, err: float) -> np.ndarray:
     best scores is <= 2*err."""
     T, E = scores.shape
     srt = -np.sort(-scores, axis=1)[:, :min(k + 1, E)]
-    gaps = srt[:, :-1] - srt[:, 1:]
-    return np.any(gaps <= 2 * err, axis=1)
+    with np.errstate(invalid="ignore"):
+        gaps = srt[:, :-1] - srt[:, 1:]  # -inf entries (masked experts) never count as ties
+    return np.any(np.nan_to_num(gaps, nan=np.inf) <= 2 * err, axis=1)
 
 
 def check_topk_valid(ids: np.ndarray, scores: np.ndarray, err: float):

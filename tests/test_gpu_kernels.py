@@ -47,6 +47,30 @@ def test_route_all_equal_scores():
     assert torch.all(w == 0.25)
 
 
+@pytest.mark.parametrize("T,E,k,n_group,topk_group", [(1000, 256, 8, 8, 4), (300, 64, 6, 8, 3), (50, 32, 4, 4, 1),
+                                                  (77, 1024, 32, 32, 8), (200, 160, 7, 5, 5), (9, 256, 8, 1, 1)])
+@pytest.mark.parametrize("rule", ["max", "top2_sum"])
+@pytest.mark.parametrize("ties", [None, "quantised"])
+@pytest.mark.parametrize("renorm", [True, False])
+def test_route_topk_grouped(oracle, T, E, k, n_group, topk_group, rule, ties, renorm):
+    logits = inputs.random_logits(T, E, seed=T + E + n_group, ties=ties)
+    bias = inputs.zipf_bias(inputs.CONFIGS["dsv3_zipf_prefill"]) if E == 256 else None
+    ids, w = binding.moe_route_topk_grouped(logits.to(DEV), k, n_group, topk_group, rule, renorm,
+                                            None if bias is None else bias.to(DEV))
+    r_ids, r_w = oracle.route_topk_grouped(logits.numpy(), k, n_group, topk_group, rule, renorm=renorm,
+                                           bias=None if bias is None else bias.numpy())
+    assert np.array_equal(ids.cpu().numpy(), r_ids)
+    np.testing.assert_allclose(w.cpu().numpy(), r_w, rtol=1e-5, atol=1e-7)
+
+
+def test_route_topk_grouped_rejects_bad_grouping():
+    logits = torch.zeros((4, 24), device=DEV)
+    for args in [(3, 5, 2), (3, 4, 5), (20, 4, 1), (3, 48, 1)]:  # E % n_group, topk_group > n_group, k too big, n_group > 32
+        k, n_group, topk_group = args
+        with pytest.raises(binding.MoEError):
+            binding.moe_route_topk_grouped(logits, k, n_group, topk_group)
+
+
 # ---- init-routing ------------------------------------------------------------------
 
 @pytest.mark.parametrize("T,k,E,H,distinct", [

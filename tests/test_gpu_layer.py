@@ -30,7 +30,8 @@ def make(cfg):
     d = inputs.make_layer(cfg, DEV)
     layer = binding.MoELayer(T=cfg.T, k=cfg.k, w_router=d["wg"], w_gate=d["w_gate"], w_up=d["w_up"], w2=d["w2"],
                              s_gate=d["s_gate"] if cfg.S else None, s_up=d["s_up"] if cfg.S else None,
-                             s2=d["s2"] if cfg.S else None, expert_bias=d["bias"], renormalize=cfg.renormalize)
+                             s2=d["s2"] if cfg.S else None, expert_bias=d["bias"], renormalize=cfg.renormalize,
+                             n_group=cfg.n_group, topk_group=cfg.topk_group, group_rule=cfg.group_rule)
     return d, layer
 
 
@@ -49,10 +50,32 @@ def check_layer(oracle, cfg, d, layer, out, tokens=None):
     amb = routing_ambiguity(s_ref, k, maxerr)
     ids = layer.field("topk_ids").cpu().numpy()
     w = layer.field("topk_w").cpu().numpy()
-    r_ids, r_w = oracle.route_topk(l32, k, renorm=cfg.renormalize, bias=bias)
+    if cfg.n_group > 1:
+        r_ids, r_w = oracle.route_topk_grouped(l32, k, cfg.n_group, cfg.topk_group, cfg.group_rule,
+                                               renorm=cfg.renormalize, bias=bias)
+        # ambiguous: a near-tie among the best k+1 experts of the kept groups, or
+        # between the last kept group and the next one (a top-2 sum carries the
+        # error of two scores)
+        gs = E // cfg.n_group
+        srt = -np.sort(-s_ref.reshape(len(s_ref), cfg.n_group, gs), axis=2)
+        gscore = srt[:, :, 0] + (srt[:, :, 1] if cfg.group_rule == "top2_sum" else 0)
+        masked = s_ref.copy()
+        for t in range(len(s_ref)):
+            keep = np.zeros(cfg.n_group, bool)
+            keep[np.unique(r_ids[t] // gs)] = True
+            order = np.argsort(-gscore[t], kind="stable")[:cfg.topk_group]
+            keep[order] = True
+            masked[t][~np.repeat(keep, gs)] = -np.inf
+        amb = routing_ambiguity(masked, k, maxerr)
+        if cfg.topk_group < cfg.n_group:
+            gsorted = -np.sort(-gscore, axis=1)
+            amb |= gsorted[:, cfg.topk_group - 1] - gsorted[:, cfg.topk_group] <= 4 * maxerr
+    else:
+        r_ids, r_w = oracle.route_topk(l32, k, renorm=cfg.renormalize, bias=bias)
     assert np.array_equal(ids[~amb], r_ids[~amb])
-    for t in np.nonzero(amb)[0]:
-        check_topk_valid(ids[t], s_ref[t], maxerr)
+    if cfg.n_group == 1:
+        for t in np.nonzero(amb)[0]:
+            check_topk_valid(ids[t], s_ref[t], maxerr)
     np.testing.assert_allclose(w[~amb], r_w[~amb], rtol=1e-4, atol=1e-6)
     # permutation: properties on the GPU's ids; bit-exact against the oracle when routing agrees
     counts = layer.field("tokens_per_expert").cpu().numpy()
@@ -68,7 +91,8 @@ def check_layer(oracle, cfg, d, layer, out, tokens=None):
     toks = np.arange(cfg.T, dtype=np.int32) if tokens is None else np.asarray(tokens, np.int32)
     ref = oracle.layer(n["x"], n["wg"], n["w_gate"], n["w_up"], n["w2"], n.get("s_gate") if cfg.S else None,
                        n.get("s_up") if cfg.S else None, n.get("s2") if cfg.S else None, k=k,
-                       renorm=cfg.renormalize, bias=bias, tokens=None if tokens is None else toks)
+                       renorm=cfg.renormalize, bias=bias, tokens=None if tokens is None else toks,
+                       n_group=cfg.n_group, topk_group=cfg.topk_group, group_rule=cfg.group_rule)
     same = np.array([set(ids[t]) == set(ref["ids"][i]) for i, t in enumerate(toks)])
     assert (~same).sum() <= max(1, len(toks) // 100)
     got = f64(out)[toks][same]
@@ -88,6 +112,10 @@ SMALL = [
     inputs.LayerConfig("one_token_bf16", T=1, H=128, E=8, k=8, I=128, S=1, dtype="bf16", seed=14),
     inputs.LayerConfig("zipf_bf16", T=512, H=256, E=64, k=8, I=128, S=1, dtype="bf16", seed=15, zipf_s=1.2),
     inputs.LayerConfig("dense_E1_bf16", T=200, H=256, E=1, k=1, I=256, S=1, dtype="bf16", seed=16),
+    inputs.LayerConfig("grouped_bf16", T=300, H=256, E=64, k=6, I=128, S=1, dtype="bf16", seed=17, n_group=8,
+                       topk_group=3, group_rule="top2_sum"),
+    inputs.LayerConfig("grouped_fp32", T=64, H=128, E=16, k=2, I=64, S=1, dtype="f32", seed=18, n_group=4,
+                       topk_group=2, group_rule="max"),
 ]
 
 
@@ -98,7 +126,8 @@ def test_layer_small(oracle, cfg):
     check_layer(oracle, cfg, d, layer, out)
 
 
-FULL = [("mid_bf16", 96), ("dsv3_prefill", 48), ("dsv3_decode", 32), ("dsv3_zipf_prefill", 32)]
+FULL = [("mid_bf16", 96), ("dsv3_prefill", 48), ("dsv3_decode", 32), ("dsv3_zipf_prefill", 32),
+        ("dsv3_prefill_grouped", 32)]
 
 
 @pytest.mark.parametrize("name,n_sample", FULL, ids=[f[0] for f in FULL])

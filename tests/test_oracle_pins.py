@@ -308,3 +308,59 @@ def test_layer_zipf_bias_feeds_selection(oracle):
     s = (r["logits64"].astype(np.float32) + d["bias"].numpy())
     for t in range(cfg.T):
         assert list(r["ids"][t]) == _brute_topk(s[t], cfg.k)
+
+
+# ---- group-limited top-k -----------------------------------------------------------
+
+@pytest.mark.parametrize("rule", ["max", "top2_sum"])
+def test_grouped_topk_single_group_is_flat(oracle, rule):
+    """The page's special case: one group holding all experts is flat top-k."""
+    logits = inputs.random_logits(50, 32, seed=5, ties="quantised").numpy()
+    flat_ids, flat_w = oracle.route_topk(logits, 6)
+    for n_group, topk_group in [(1, 1), (4, 4), (8, 8)]:
+        ids, w = oracle.route_topk_grouped(logits, 6, n_group, topk_group, rule)
+        assert np.array_equal(ids, flat_ids) and np.array_equal(w, flat_w)
+
+
+def _brute_grouped(s, k, n_group, topk_group, rule):
+    gs = s.size // n_group
+    gscore = []
+    for g in range(n_group):
+        top = sorted(s[g * gs:(g + 1) * gs].tolist(), reverse=True)
+        gscore.append(np.float32(top[0]) if rule == "max" else np.float32(top[0]) + np.float32(top[1]))
+    kept = sorted(range(n_group), key=lambda g: (-float(gscore[g]), g))[:topk_group]
+    cand = [e for e in range(s.size) if e // gs in kept]
+    return sorted(cand, key=lambda e: (-float(s[e]), e))[:k]
+
+
+@pytest.mark.parametrize("rule", ["max", "top2_sum"])
+@pytest.mark.parametrize("E,n_group,topk_group,k", [(16, 4, 2, 3), (32, 8, 3, 8), (12, 3, 1, 4)])
+def test_grouped_topk_brute_force(oracle, rule, E, n_group, topk_group, k):
+    T = 60
+    logits = inputs.random_logits(T, E, seed=E + k, ties="quantised").numpy()
+    bias = (np.round(np.random.default_rng(E).standard_normal(E) * 2) / 4).astype(np.float32)
+    ids, w = oracle.route_topk_grouped(logits, k, n_group, topk_group, rule, bias=bias)
+    for t in range(T):
+        s = logits[t] + bias
+        assert list(ids[t]) == _brute_grouped(s, k, n_group, topk_group, rule)
+        np.testing.assert_allclose(w[t], scipy.special.softmax(s[ids[t]].astype(np.float64)), rtol=1e-13)
+
+
+def test_grouped_topk_rules_differ():
+    """A group with one large score and weak others: "max" keeps it, "top2_sum" may not."""
+    import oracle as o
+    s = np.array([[5.0, -9.0, 3.0, 2.9]], np.float32)  # groups {0,1}, {2,3}
+    ids_max, _ = o.route_topk_grouped(s, 1, 2, 1, "max")
+    ids_sum, _ = o.route_topk_grouped(s, 1, 2, 1, "top2_sum")
+    assert ids_max[0, 0] == 0 and ids_sum[0, 0] == 2
+
+
+def test_layer_grouped_routing_uses_grouped_router(oracle):
+    cfg = inputs.LayerConfig("t", T=24, H=32, E=16, k=3, I=16, S=1, dtype="f32", seed=31)
+    d = inputs.make_layer(cfg)
+    args = [inputs.to_numpy(d[n]) for n in ("x", "wg", "w_gate", "w_up", "w2", "s_gate", "s_up", "s2")]
+    r = oracle.layer(*args, k=3, n_group=4, topk_group=2, group_rule="top2_sum")
+    ids, w = oracle.route_topk_grouped(r["logits64"].astype(np.float32), 3, 4, 2, "top2_sum")
+    assert np.array_equal(r["ids"], ids) and np.array_equal(r["w"], w)
+    # the selected experts come from at most two groups
+    assert all(len({e // 4 for e in row}) <= 2 for row in r["ids"])
