@@ -237,6 +237,8 @@ def run_ours(args, world, rank, local):
     out = torch.empty_like(x)
     stream = torch.cuda.current_stream()
     nst = binding.MOE_NUM_STAGES
+    if args.ep > 1:
+        return run_ours_ep(args, world, rank, local, cfg, layer, x, out)
     for _ in range(args.warmup):
         layer.forward(x, out)
     torch.cuda.synchronize()
@@ -332,6 +334,49 @@ def run_ours(args, world, rank, local):
         print(json.dumps(line), flush=True)
 
 
+def run_ours_ep(args, world, rank, local, cfg, layer, x, out):
+    """The layer through expert-parallel Double-Routing with --ep virtual ranks on one GPU."""
+    from moe_expert_routing_route_gb300 import binding
+    stream = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        layer.forward_ep(x, args.ep, out)
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local)
+    time.sleep(0.1)
+    launches0 = binding.launch_count()
+    barrier(world)
+    torch.cuda.synchronize()
+    wall0 = time.time()
+    start.record(stream)
+    for _ in range(args.steps):
+        layer.forward_ep(x, args.ep, out)
+    end.record(stream)
+    torch.cuda.synchronize()
+    wall1 = time.time()
+    barrier(world)
+    launches = binding.launch_count() - launches0
+    clk = clocks.summary(wall0, wall1)
+    clocks.stop()
+    if binding.moe_check_device_status(layer.ws_ep) != 0:
+        raise RuntimeError("device status word set during the timed region")
+    ms_max = max_over_ranks(start.elapsed_time(end) / args.steps, world)
+    layer.forward(x, out)  # the single-routing pass fills the routing fields read below
+    counts = layer.field("tokens_per_expert").cpu().numpy()
+    costs = roofline.stage_costs(cfg.T, cfg.H, cfg.E, cfg.k, cfg.I, cfg.S, cfg.esize, int((counts > 0).sum()))
+    fl, by = sum(c[0] for c in costs.values()), sum(c[1] for c in costs.values())
+    rl = roofline.roofline_entry(fl, by, ms_max / 1e3, roofline.load_peaks(), sustained=True)
+    rl.update(kernel="whole layer (double routing)", traffic=None, algorithmic_bytes=by, algorithmic_flops=fl)
+    if rank == 0:
+        tokens = cfg.T * world
+        print(json.dumps(dict(metric=METRIC, value=tokens / (ms_max / 1e3), unit=UNIT, n_gpus=world,
+                              steps=args.steps, warmup=args.warmup, ms_per_step=ms_max, higher_is_better=True,
+                              scaling="weak", vs_baseline=None, dtype=cfg.dtype, data="synthetic",
+                              config=dict(workload=cfg.name, ep_virtual_ranks=args.ep, T=cfg.T, H=cfg.H, E=cfg.E,
+                                          k=cfg.k, I=cfg.I, S=cfg.S, parallelism=f"replicas{world}"),
+                              roofline=rl, cpu_baseline=None, gpu_launches=int(launches), clocks=clk)), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -342,6 +387,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--ref-tokens", type=int, default=16, help="tokens per step for --impl reference")
+    ap.add_argument("--ep", type=int, default=1,
+                    help="run the layer through expert-parallel Double-Routing with this many virtual ranks")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3

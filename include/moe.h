@@ -220,6 +220,31 @@ moe_status_t moe_finalize_routing(const void* y, int64_t y_rows, const void* ski
                                   void* out, void* ws, moe_stream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * Re-routing.  [CANN §MoE deployment, Double-Routing step 4]: after the
+ * token AlltoAll a rank holds, from each of W source ranks in rank order, that
+ * source's rows for the rank's E_local experts, grouped by local expert in
+ * expert order (the layout init-routing gives a contiguous expert range).
+ * Re-routing sorts them by local expert, stable (source order, then arrival):
+ *   x_sorted[i, :] = x_recv[gathered_ids_unsort[i], :]
+ *   tokens_per_local_expert[e] = sum_p counts[p, e];  local_offsets = exclusive scan [E_local+1]
+ * counts [W, E_local] int32 (device); x_recv, x_sorted [N, H] dt with N the
+ * sum of counts (checked on the device: a mismatch moves no rows and sets
+ * MOE_DEVERR_BAD_OFFSETS); gathered_ids_unsort [N] int32.
+ * ws: moe_re_routing_workspace_bytes(W, E_local) bytes. */
+size_t moe_re_routing_workspace_bytes(int W, int E_local);
+moe_status_t moe_re_routing(const void* x_recv, moe_dtype_t dt, const int32_t* counts, int W, int E_local, int N,
+                            int H, void* x_sorted, int32_t* gathered_ids_unsort, int32_t* tokens_per_local_expert,
+                            int32_t* local_offsets, void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* [CANN §MoE deployment, Double-Routing step 6]: the rows back in received
+ * order, the page's index_select with the argsort of gathered_ids_unsort:
+ *   out[gathered_ids_unsort[i], :] = y_sorted[i, :]
+ * y_sorted, out [N, H] dt; ws NULL or a workspace whose status word receives
+ * MOE_DEVERR_BAD_ROW_INDEX for an index outside [0, N). */
+moe_status_t moe_unsort_rows(const void* y_sorted, moe_dtype_t dt, const int32_t* gathered_ids_unsort, int N, int H,
+                             void* out, void* ws, moe_stream_t stream);
+
+/* ---------------------------------------------------------------------------
  * The whole layer.  [BLOG §Expert Parallelism]: out[t] = shared(x_t) +
  * sum_j w_j FFN_{e_j}(x_t) with 8-of-256 style top-k routing; the steps above
  * run back to back on one stream with fixed grids and no host synchronisation
@@ -289,6 +314,18 @@ moe_status_t moe_layer_forward(const moe_layer_desc* desc, const void* x, void* 
  * library's second stream. */
 moe_status_t moe_layer_forward_timed(const moe_layer_desc* desc, const void* x, void* out, void* ws,
                                      size_t ws_bytes, moe_stream_t stream, void* const* stage_events);
+
+/* The layer through expert-parallel Double-Routing with W virtual ranks on
+ * one GPU ([CANN §MoE deployment], steps 1-8): rank p owns tokens
+ * [p*T/W, (p+1)*T/W) and experts [p*E/W, (p+1)*E/W); init-routing runs per
+ * rank, the token AlltoAll and its reverse are device-side copies of row
+ * blocks sized from the per-rank counts on the device, each rank re-routes,
+ * runs its experts, un-sorts and returns the rows, and finalize runs per rank.
+ * The output equals moe_layer_forward's bit for bit.  1 <= W <= 32,
+ * T % W == 0, E % W == 0; ws of moe_layer_workspace_bytes_ep(desc, W) bytes. */
+size_t moe_layer_workspace_bytes_ep(const moe_layer_desc* desc, int W);
+moe_status_t moe_layer_forward_ep(const moe_layer_desc* desc, int W, const void* x, void* out, void* ws,
+                                  size_t ws_bytes, moe_stream_t stream);
 
 /* End to end from HOST memory: copies x_host [T,H] into the workspace, runs
  * the layer, copies the result to out_host [T,H] and synchronises `stream`

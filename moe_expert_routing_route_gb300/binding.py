@@ -51,6 +51,11 @@ SIGNATURES = {
     "moe_grouped_ffn_workspace_bytes": (SZ, [I32, I32, I32]),
     "moe_grouped_ffn": (I32, [P, I32, P, I32, I32, I32, I32, P, P, P, P, SZ, P]),
     "moe_finalize_routing": (I32, [P, I64, P, P, P, I32, I32, I32, I32, P, P, P]),
+    "moe_re_routing_workspace_bytes": (SZ, [I32, I32]),
+    "moe_re_routing": (I32, [P, I32, P, I32, I32, I32, I32, P, P, P, P, P, SZ, P]),
+    "moe_unsort_rows": (I32, [P, I32, P, I32, I32, P, P, P]),
+    "moe_layer_workspace_bytes_ep": (SZ, [_DP, I32]),
+    "moe_layer_forward_ep": (I32, [_DP, I32, P, P, P, SZ, P]),
     "moe_stage_name": (ctypes.c_char_p, [I32]),
     "moe_layer_workspace_bytes": (SZ, [_DP]),
     "moe_layer_workspace_field": (I32, [_DP, I32, ctypes.POINTER(SZ), ctypes.POINTER(SZ)]),
@@ -233,6 +238,30 @@ def moe_finalize_routing(y: torch.Tensor, topk_w: torch.Tensor, expanded_row_idx
     return out
 
 
+def moe_re_routing(x_recv: torch.Tensor, counts: torch.Tensor, stream=None) -> dict:
+    """Second routing of Double-Routing; counts [W, E_local] int32 on the device."""
+    N, H = x_recv.shape
+    W, El = counts.shape
+    dev = x_recv.device
+    ws = torch.empty(lib().moe_re_routing_workspace_bytes(W, El), dtype=torch.uint8, device=dev)
+    out = dict(x_sorted=torch.empty_like(x_recv), gathered_ids_unsort=torch.empty(N, dtype=torch.int32, device=dev),
+               tokens_per_local_expert=torch.empty(El, dtype=torch.int32, device=dev),
+               local_offsets=torch.empty(El + 1, dtype=torch.int32, device=dev), ws=ws)
+    _check(lib().moe_re_routing(_ptr(x_recv), _dt(x_recv), _ptr(counts.contiguous()), W, El, N, H,
+                                _ptr(out["x_sorted"]), _ptr(out["gathered_ids_unsort"]),
+                                _ptr(out["tokens_per_local_expert"]), _ptr(out["local_offsets"]), _ptr(ws),
+                                ws.numel(), _stream(stream)), "moe_re_routing")
+    return out
+
+
+def moe_unsort_rows(y_sorted: torch.Tensor, gathered_ids_unsort: torch.Tensor, ws=None, stream=None):
+    N, H = y_sorted.shape
+    out = torch.empty_like(y_sorted)
+    _check(lib().moe_unsort_rows(_ptr(y_sorted), _dt(y_sorted), _ptr(gathered_ids_unsort), N, H, _ptr(out),
+                                 _ptr(ws), _stream(stream)), "moe_unsort_rows")
+    return out
+
+
 def stage_names() -> list[str]:
     return [lib().moe_stage_name(i).decode() for i in range(MOE_NUM_STAGES)]
 
@@ -315,6 +344,19 @@ class MoELayer:
                                           _stream(stream))
         _check(st, "moe_layer_forward_host")
         return out_host
+
+    def forward_ep(self, x: torch.Tensor, W: int, out: torch.Tensor | None = None, stream=None):
+        """The layer through Double-Routing with W virtual expert-parallel ranks."""
+        if out is None:
+            out = torch.empty_like(x)
+        need = lib().moe_layer_workspace_bytes_ep(ctypes.byref(self.desc), W)
+        if need == 0:
+            raise MoEError(MOE_ERR_INVALID_ARG, "moe_layer_workspace_bytes_ep")
+        if getattr(self, "ws_ep", None) is None or self.ws_ep.numel() < need:
+            self.ws_ep = torch.empty(need, dtype=torch.uint8, device=x.device)
+        _check(lib().moe_layer_forward_ep(ctypes.byref(self.desc), W, _ptr(x), _ptr(out), _ptr(self.ws_ep),
+                                          self.ws_ep.numel(), _stream(stream)), "moe_layer_forward_ep")
+        return out
 
     def device_status(self, stream=None) -> int:
         return moe_check_device_status(self.ws, stream)

@@ -261,6 +261,95 @@ moe_status_t layer_forward(const moe_layer_desc* d, const void* x, void* out, vo
     return MOE_OK;
 }
 
+// ---- expert-parallel Double-Routing on one GPU ----
+struct EpLayout {
+    size_t recv_off, sorted_off, gidx_off, scratch_off, total;
+};
+
+EpLayout ep_layout(const moe_layer_desc& d, int W, const Layout& L) {
+    EpLayout e{};
+    const size_t R = (size_t)d.T * d.k, rb = (size_t)d.H * dt_size(d.dtype);
+    size_t cur = L.total;
+    e.recv_off = cur;
+    cur += round_up(R * rb, kAlign);
+    e.sorted_off = cur;
+    cur += round_up(R * rb, kAlign);
+    e.gidx_off = cur;
+    cur += round_up(R * 4, kAlign);
+    e.scratch_off = cur;
+    cur += round_up(ep_scratch_ints(W, d.E) * 4, kAlign);
+    e.total = cur;
+    return e;
+}
+
+moe_status_t check_ep(const moe_layer_desc* d, int W) {
+    MOE_TRY(check_desc(d));
+    if (W < 1 || W > 32 || d->T % W != 0 || d->E % W != 0) return MOE_ERR_INVALID_ARG;
+    return MOE_OK;
+}
+
+moe_status_t layer_forward_ep(const moe_layer_desc* d, int W, const void* x, void* out, void* ws, size_t ws_bytes,
+                              cudaStream_t s) {
+    MOE_TRY(check_ep(d, W));
+    if (!x || !out || !ws) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(out) || !aligned16(ws)) return MOE_ERR_UNSUPPORTED;
+    const Layout L = layout(*d);
+    const EpLayout EL = ep_layout(*d, W, L);
+    if (ws_bytes < EL.total) return MOE_ERR_INVALID_ARG;
+    if (d->T == 0) return MOE_OK;
+    const int T = d->T, H = d->H, E = d->E, k = d->k, I = d->I, R = T * k, SI = d->S * d->I;
+    const int El = E / W, Tp = T / W, Rp = Tp * k;
+    const moe_dtype_t dt = d->dtype;
+    const size_t rb = (size_t)H * dt_size(dt), eb = dt_size(dt);
+    uint32_t* status = status_word(ws);
+    float* logits = at<float>(ws, L.off[MOE_WS_LOGITS]);
+    int32_t* ids = at<int32_t>(ws, L.off[MOE_WS_TOPK_IDS]);
+    float* w = at<float>(ws, L.off[MOE_WS_TOPK_W]);
+    void* h = at<void>(ws, L.off[MOE_WS_H_ROUTED]);
+    void* hs = at<void>(ws, L.off[MOE_WS_H_SHARED]);
+    void* y = at<void>(ws, L.off[MOE_WS_Y_ROUTED]);
+    void* ys = at<void>(ws, L.off[MOE_WS_Y_SHARED]);
+    EpBuffers b{W, T, E, k, rb, x, ids, at<int32_t>(ws, L.off[MOE_WS_EXPANDED_ROW_IDX]),
+                at<void>(ws, L.off[MOE_WS_EXPANDED_X]), at<void>(ws, EL.recv_off), at<void>(ws, EL.sorted_off),
+                at<int32_t>(ws, EL.gidx_off), at<int32_t>(ws, EL.scratch_off), at<int32_t>(ws, L.scratch_off), status};
+
+    SideStream* side = nullptr;
+    if (SI > 0) MOE_TRY(side_stream(&side));
+    std::unique_lock<std::mutex> side_lock;
+    if (side) side_lock = std::unique_lock<std::mutex>(side->mu);
+
+    MOE_TRY(clear_status(ws, s));
+    MOE_TRY(gate(x, d->w_router, dt, T, H, E, logits, s));
+    if (side) {
+        MOE_CUDA_TRY(cudaEventRecord(side->fork, s));
+        MOE_CUDA_TRY(cudaStreamWaitEvent(side->stream, side->fork, 0));
+        MOE_TRY(ffn_up(x, dt, nullptr, 1, T, H, SI, d->w13_shared, hs, status, side->stream));
+        MOE_TRY(ffn_down(hs, dt, nullptr, 1, T, H, SI, d->w2_shared, ys, status, side->stream));
+        MOE_CUDA_TRY(cudaEventRecord(side->join, side->stream));
+    }
+    MOE_TRY(launch_route_topk(logits, d->expert_bias, T, E, k, d->renormalize, ids, w, s, d->n_group, d->topk_group,
+                              d->group_rule));
+    MOE_TRY(ep_route_and_dispatch(b, s));  // steps 1-4
+    if (side) MOE_CUDA_TRY(cudaStreamWaitEvent(s, side->join, 0));
+    // step 5: each rank's experts on its sorted rows
+    const size_t w13_expert = (size_t)packed_rows(I) * H * eb, w2_expert = (size_t)H * I * eb;
+    for (int q = 0; q < W; ++q)
+        MOE_TRY(ffn_up(b.sorted, dt, ep_rank_offsets(b, q), El, R, H, I,
+                       static_cast<const char*>(d->w13) + (size_t)q * El * w13_expert, h, status, s));
+    for (int q = 0; q < W; ++q)
+        MOE_TRY(ffn_down(h, dt, ep_rank_offsets(b, q), El, R, H, I,
+                         static_cast<const char*>(d->w2) + (size_t)q * El * w2_expert, y, status, s));
+    // steps 6-7: back to received order, back to the source ranks (into the free buffers)
+    MOE_TRY(ep_combine(b, y, b.recv, b.expanded, s));
+    // step 8: finalize on each source rank
+    for (int p = 0; p < W; ++p)
+        MOE_TRY(launch_finalize(static_cast<const char*>(b.expanded) + (size_t)p * Rp * rb, Rp,
+                                SI > 0 ? static_cast<const char*>(ys) + (size_t)p * Tp * rb : nullptr,
+                                w + (size_t)p * Tp * k, b.row_idx + (size_t)p * Rp, dt, Tp, H, k,
+                                static_cast<char*>(out) + (size_t)p * Tp * rb, status, s));
+    return MOE_OK;
+}
+
 }  // namespace
 
 void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
@@ -340,6 +429,41 @@ moe_status_t moe_route_topk_grouped(const float* logits, const float* expert_bia
     if (!logits || !topk_ids || !topk_w) return MOE_ERR_INVALID_ARG;
     return launch_route_topk(logits, expert_bias, T, E, k, renormalize ? 1 : 0, topk_ids, topk_w,
                              reinterpret_cast<cudaStream_t>(stream), n_group, topk_group, group_rule);
+}
+
+size_t moe_re_routing_workspace_bytes(int W, int E_local) {
+    if (W <= 0 || E_local <= 0) return 0;
+    return MOE_WS_HEADER_BYTES + round_up(re_routing_plan_ints(W, E_local) * 4, kAlign);
+}
+
+moe_status_t moe_re_routing(const void* x_recv, moe_dtype_t dt, const int32_t* counts, int W, int E_local, int N, int H,
+                            void* x_sorted, int32_t* gathered_ids_unsort, int32_t* tokens_per_local_expert,
+                            int32_t* local_offsets, void* ws, size_t ws_bytes, moe_stream_t stream) {
+    if (bad_dtype(dt) || W < 1 || W > 4096 || E_local < 1 || E_local > 1024 || N < 0 || H <= 0)
+        return MOE_ERR_INVALID_ARG;
+    if (H % 8 != 0) return MOE_ERR_UNSUPPORTED;
+    if (!counts || !tokens_per_local_expert || !local_offsets || !ws) return MOE_ERR_INVALID_ARG;
+    if (ws_bytes < moe_re_routing_workspace_bytes(W, E_local)) return MOE_ERR_INVALID_ARG;
+    if (N > 0 && (!x_recv || !x_sorted || !gathered_ids_unsort)) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(x_recv) || !aligned16(x_sorted) || !aligned16(ws)) return MOE_ERR_UNSUPPORTED;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    MOE_TRY(clear_status(ws, s));
+    return launch_re_routing(x_recv, (size_t)H * dt_size(dt), counts, W, E_local, N, x_sorted, gathered_ids_unsort,
+                             tokens_per_local_expert, local_offsets, at<int32_t>(ws, MOE_WS_HEADER_BYTES),
+                             status_word(ws), s);
+}
+
+moe_status_t moe_unsort_rows(const void* y_sorted, moe_dtype_t dt, const int32_t* gathered_ids_unsort, int N, int H,
+                             void* out, void* ws, moe_stream_t stream) {
+    if (bad_dtype(dt) || N < 0 || H <= 0) return MOE_ERR_INVALID_ARG;
+    if (H % 8 != 0) return MOE_ERR_UNSUPPORTED;
+    if (N == 0) return MOE_OK;
+    if (!y_sorted || !gathered_ids_unsort || !out) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(y_sorted) || !aligned16(out) || !aligned16(ws)) return MOE_ERR_UNSUPPORTED;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    MOE_TRY(clear_status(ws, s));
+    return launch_unsort_rows(y_sorted, (size_t)H * dt_size(dt), gathered_ids_unsort, N, out,
+                              ws ? status_word(ws) : nullptr, s);
 }
 
 size_t moe_init_routing_workspace_bytes(int T, int E, int k) {
@@ -447,6 +571,16 @@ moe_status_t moe_layer_forward(const moe_layer_desc* desc, const void* x, void* 
 moe_status_t moe_layer_forward_timed(const moe_layer_desc* desc, const void* x, void* out, void* ws, size_t ws_bytes,
                                      moe_stream_t stream, void* const* stage_events) {
     return layer_forward(desc, x, out, ws, ws_bytes, reinterpret_cast<cudaStream_t>(stream), stage_events);
+}
+
+size_t moe_layer_workspace_bytes_ep(const moe_layer_desc* desc, int W) {
+    if (check_ep(desc, W) != MOE_OK) return 0;
+    return ep_layout(*desc, W, layout(*desc)).total;
+}
+
+moe_status_t moe_layer_forward_ep(const moe_layer_desc* desc, int W, const void* x, void* out, void* ws,
+                                  size_t ws_bytes, moe_stream_t stream) {
+    return layer_forward_ep(desc, W, x, out, ws, ws_bytes, reinterpret_cast<cudaStream_t>(stream));
 }
 
 moe_status_t moe_layer_forward_host(const moe_layer_desc* desc, const void* x_host, void* out_host, void* ws,

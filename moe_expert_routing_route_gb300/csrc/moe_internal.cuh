@@ -56,6 +56,32 @@ moe_status_t launch_permute_rows(const void* x, size_t row_bytes, const int32_t*
 moe_status_t launch_pack_w13(const void* w_gate, const void* w_up, size_t esize, int E, int H, int I,
                              void* packed, cudaStream_t s);
 
+// ep.cu: Double-Routing pieces (re-routing, unsort, the virtual-rank exchange).
+size_t re_routing_plan_ints(int W, int El);
+moe_status_t launch_re_routing(const void* x_recv, size_t row_bytes, const int32_t* counts, int W, int El, int N,
+                               void* x_sorted, int32_t* gidx, int32_t* tpl, int32_t* local_off, int32_t* plan,
+                               uint32_t* status, cudaStream_t s);
+moe_status_t launch_unsort_rows(const void* y_sorted, size_t row_bytes, const int32_t* gidx, int N, void* out,
+                                uint32_t* status, cudaStream_t s);
+struct EpBuffers {
+    int W, T, E, k;
+    size_t row_bytes;
+    const void* x;          // [T,H]
+    const int32_t* ids;     // [T,k]
+    int32_t* row_idx;       // [T*k]: per source rank, rows local to the rank
+    void* expanded;         // [T*k,H]: the source ranks' expanded rows, rank after rank
+    void* recv;             // [T*k,H]: rows as received, receiving rank after rank
+    void* sorted;           // [T*k,H]: received rows sorted by local expert
+    int32_t* gidx;          // [T*k]: sorted row -> received row
+    int32_t* scratch;       // ep_scratch_ints(W, E)
+    int32_t* hist_scratch;  // init-routing histogram scratch for T/W tokens
+    uint32_t* status;
+};
+size_t ep_scratch_ints(int W, int E);
+moe_status_t ep_route_and_dispatch(const EpBuffers& b, cudaStream_t s);
+const int32_t* ep_rank_offsets(const EpBuffers& b, int q);  // [E/W + 1] rows of rank q's experts in `sorted`
+moe_status_t ep_combine(const EpBuffers& b, const void* y_sorted, void* y_recv, void* y_expanded, cudaStream_t s);
+
 // finalize.cu
 moe_status_t launch_finalize(const void* y, int64_t y_rows, const void* skip, const float* w,
                              const int32_t* row_idx, moe_dtype_t dt, int T, int H, int k, void* out,

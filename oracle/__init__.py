@@ -58,6 +58,8 @@ def _load():
         lib.oracle_init_routing.argtypes = [P, I, I, I, P, I, I, P, P, P, P]
         lib.oracle_init_routing.restype = I
         lib.oracle_expert_ffn_rows.argtypes = [P, I, L, P, P, P, P, I, I, P]
+        lib.oracle_re_routing.argtypes = [P, I, P, I, I, I, P, P, P, P]
+        lib.oracle_unsort_rows.argtypes = [P, I, P, L, I, P]
         lib.oracle_finalize_routing.argtypes = [P, I, L, P, P, P, I, I, I, P]
         lib.oracle_layer.argtypes = [P, I, I, I, I, I, I, I, I, P, P, P, P, P, P, P, P, P, I,
                                      P, P, P, P, I, I, I]
@@ -157,6 +159,32 @@ def init_routing(ids: np.ndarray, x: np.ndarray | None, E: int, H: int | None = 
                                       _ptr(cnt), _ptr(off))
     return dict(expanded_x=ex, expanded_row_idx=idx, tokens_per_expert=cnt, expert_offsets=off,
                 bad=bad)
+
+
+def re_routing(x_recv: np.ndarray, counts: np.ndarray):
+    """Second routing of Double-Routing.  counts [W, E_local] (rows from source p for
+    local expert e, arrival order p-major).  Returns dict(x_sorted, gathered_ids_unsort,
+    tokens_per_local_expert, local_offsets)."""
+    x_recv = _c(x_recv)
+    counts = _c(counts, np.int32)
+    W, El = counts.shape
+    N, H = x_recv.shape
+    assert counts.sum() == N
+    xs = np.zeros_like(x_recv)
+    gidx = np.empty(N, np.int32)
+    tpl = np.empty(El, np.int32)
+    off = np.empty(El + 1, np.int32)
+    _load().oracle_re_routing(_ptr(x_recv), _dt(x_recv), _ptr(counts), W, El, H, _ptr(xs), _ptr(gidx), _ptr(tpl),
+                              _ptr(off))
+    return dict(x_sorted=xs, gathered_ids_unsort=gidx, tokens_per_local_expert=tpl, local_offsets=off)
+
+
+def unsort_rows(y_sorted: np.ndarray, gathered_ids_unsort: np.ndarray) -> np.ndarray:
+    y_sorted = _c(y_sorted)
+    gidx = _c(gathered_ids_unsort, np.int32)
+    out = np.zeros_like(y_sorted)
+    _load().oracle_unsort_rows(_ptr(y_sorted), _dt(y_sorted), _ptr(gidx), gidx.size, y_sorted.shape[1], _ptr(out))
+    return out
 
 
 def expert_ffn_rows(a: np.ndarray, expert: np.ndarray, wgate, wup, w2) -> np.ndarray:

@@ -287,6 +287,54 @@ int oracle_init_routing(const int32_t* ids, int T, int k, int E, const void* x, 
     return bad;
 }
 
+/* ---- re-routing (second routing of Double-Routing) ---------------------------
+ * [CANN §MoE deployment, Double-Routing steps 3-4]: a rank receives, from each
+ * of W source ranks in rank order, that source's rows for the rank's E_local
+ * experts, grouped by expert in expert order (counts[p*E_local + e] rows from
+ * source p for local expert e).  Re-routing sorts the received rows by local
+ * expert, stable (source order, then arrival order, inside an expert):
+ *   x_sorted[i, :] = x_recv[gathered_ids_unsort[i], :]
+ *   tokens_per_local_expert[e] = sum_p counts[p, e]; local_offsets = exclusive scan.
+ * Written as: enumerate the received rows in arrival order with their local
+ * expert, then a counting sort by expert.                                      */
+void oracle_re_routing(const void* x_recv, int dt, const int32_t* counts, int W, int E_local, int H,
+                       void* x_sorted, int32_t* gathered_ids_unsort, int32_t* tokens_per_local_expert,
+                       int32_t* local_offsets) {
+    int64_t N = 0;
+    for (int i = 0; i < W * E_local; ++i) N += counts[i];
+    int32_t* expert_of = (int32_t*)malloc(sizeof(int32_t) * (size_t)(N > 0 ? N : 1));
+    int64_t r = 0;
+    for (int p = 0; p < W; ++p)
+        for (int e = 0; e < E_local; ++e)
+            for (int i = 0; i < counts[p * E_local + e]; ++i) expert_of[r++] = e;
+    for (int e = 0; e < E_local; ++e) tokens_per_local_expert[e] = 0;
+    for (int64_t i = 0; i < N; ++i) tokens_per_local_expert[expert_of[i]] += 1;
+    local_offsets[0] = 0;
+    for (int e = 0; e < E_local; ++e) local_offsets[e + 1] = local_offsets[e] + tokens_per_local_expert[e];
+    int32_t* next = (int32_t*)malloc(sizeof(int32_t) * (size_t)E_local);
+    for (int e = 0; e < E_local; ++e) next[e] = local_offsets[e];
+    size_t esz = dt == OR_BF16 ? 2 : 4;
+    for (int64_t i = 0; i < N; ++i) {
+        int32_t dst = next[expert_of[i]]++;
+        gathered_ids_unsort[dst] = (int32_t)i;
+        if (x_sorted)
+            memcpy((char*)x_sorted + (size_t)dst * H * esz, (const char*)x_recv + (size_t)i * H * esz,
+                   (size_t)H * esz);
+    }
+    free(next);
+    free(expert_of);
+}
+
+/* [CANN step 6]: rows back in received order, out[gathered_ids_unsort[i]] =
+ * y_sorted[i] (the page's index_select with the argsort of gathered_ids_unsort). */
+void oracle_unsort_rows(const void* y_sorted, int dt, const int32_t* gathered_ids_unsort, int64_t N, int H,
+                        void* out) {
+    size_t esz = dt == OR_BF16 ? 2 : 4;
+    for (int64_t i = 0; i < N; ++i)
+        memcpy((char*)out + (size_t)gathered_ids_unsort[i] * H * esz, (const char*)y_sorted + (size_t)i * H * esz,
+               (size_t)H * esz);
+}
+
 /* ---- one SwiGLU expert on one row ------------------------------------------
  * [BLOG §Expert Parallelism] (expert FFN) and [BLOG §Quantization] (SiLU):
  *   g = wgate v,  u = wup v          (wgate, wup: [I,H], H contiguous)

@@ -364,3 +364,47 @@ def test_layer_grouped_routing_uses_grouped_router(oracle):
     assert np.array_equal(r["ids"], ids) and np.array_equal(r["w"], w)
     # the selected experts come from at most two groups
     assert all(len({e // 4 for e in row}) <= 2 for row in r["ids"])
+
+
+# ---- re-routing (Double-Routing, second permutation) -------------------------------
+
+def test_re_routing_is_a_stable_sort_by_local_expert(oracle):
+    rng = np.random.default_rng(3)
+    W, El, H = 4, 5, 12
+    counts = rng.integers(0, 6, size=(W, El)).astype(np.int32)
+    counts[2, :] = 0  # a source that sends nothing
+    counts[:, 3] = 0  # an expert that receives nothing
+    N = int(counts.sum())
+    x = inputs.random_rows(N, H, torch.float32, seed=4).numpy()
+    r = oracle.re_routing(x, counts)
+    keys = np.concatenate([np.repeat(np.arange(El), counts[p]) for p in range(W)])
+    order = np.argsort(keys, kind="stable")  # library stable sort
+    assert np.array_equal(r["gathered_ids_unsort"], order)
+    assert np.array_equal(r["x_sorted"], x[order])
+    assert np.array_equal(r["tokens_per_local_expert"], counts.sum(0))
+    assert np.array_equal(np.diff(r["local_offsets"]), counts.sum(0))
+    # Double-Routing step 6: index_select with the argsort of gathered_ids_unsort restores arrival order
+    back = r["x_sorted"][np.argsort(r["gathered_ids_unsort"])]
+    assert np.array_equal(back, x)
+    assert np.array_equal(oracle.unsort_rows(r["x_sorted"], r["gathered_ids_unsort"]), x)
+
+
+def test_double_routing_permutations_compose_to_single_routing(oracle):
+    """Init-routing per source rank, block exchange to the expert-owning ranks, then
+    re-routing, puts the rows in exactly the single-routing (stable, by expert) order."""
+    T, k, E, W, H = 48, 3, 8, 4, 10
+    El, Tp = E // W, T // W
+    ids = inputs.random_ids(T, k, E, seed=5).numpy()
+    x = inputs.random_rows(T, H, torch.float32, seed=6).numpy()
+    single = oracle.init_routing(ids, x, E)
+    per_src = [oracle.init_routing(ids[p * Tp:(p + 1) * Tp], x[p * Tp:(p + 1) * Tp], E) for p in range(W)]
+    sorted_all = []
+    for q in range(W):
+        blocks, counts = [], []
+        for p in range(W):
+            off = per_src[p]["expert_offsets"]
+            blocks.append(per_src[p]["expanded_x"][off[q * El]:off[(q + 1) * El]])
+            counts.append(per_src[p]["tokens_per_expert"][q * El:(q + 1) * El])
+        r = oracle.re_routing(np.concatenate(blocks), np.array(counts, np.int32))
+        sorted_all.append(r["x_sorted"])
+    assert np.array_equal(np.concatenate(sorted_all), single["expanded_x"])
