@@ -59,6 +59,14 @@ def _load():
         lib.oracle_init_routing.restype = I
         lib.oracle_expert_ffn_rows.argtypes = [P, I, L, P, P, P, P, I, I, P]
         lib.oracle_re_routing.argtypes = [P, I, P, I, I, I, P, P, P, P]
+        lib.oracle_e4m3_decode.argtypes = [ctypes.c_uint8]
+        lib.oracle_e4m3_decode.restype = ctypes.c_double
+        lib.oracle_e4m3_encode.argtypes = [ctypes.c_float]
+        lib.oracle_e4m3_encode.restype = ctypes.c_uint8
+        lib.oracle_quantize_rows_fp8.argtypes = [P, I, L, I, P, P]
+        lib.oracle_quantize_tiles_fp8.argtypes = [P, I, I, I, P, P]
+        lib.oracle_gemm_fp8.argtypes = [P, P, P, P, I, I, I, P]
+        lib.oracle_layer_fp8.argtypes = [P, I, I, I, I, I, I, I, P, P] + [P] * 12 + [P, I, P, P, P, P, I, I, I]
         lib.oracle_unsort_rows.argtypes = [P, I, P, L, I, P]
         lib.oracle_finalize_routing.argtypes = [P, I, L, P, P, P, I, I, I, P]
         lib.oracle_layer.argtypes = [P, I, I, I, I, I, I, I, I, P, P, P, P, P, P, P, P, P, I,
@@ -185,6 +193,86 @@ def unsort_rows(y_sorted: np.ndarray, gathered_ids_unsort: np.ndarray) -> np.nda
     out = np.zeros_like(y_sorted)
     _load().oracle_unsort_rows(_ptr(y_sorted), _dt(y_sorted), _ptr(gidx), gidx.size, y_sorted.shape[1], _ptr(out))
     return out
+
+
+def e4m3_decode(code: int) -> float:
+    return _load().oracle_e4m3_decode(int(code))
+
+
+def e4m3_encode(v: float) -> int:
+    return int(_load().oracle_e4m3_encode(float(v)))
+
+
+E4M3_VALUES = None
+
+
+def e4m3_table() -> np.ndarray:
+    """Values of all 256 e4m3 codes (fp64; NaN for the two NaN codes)."""
+    global E4M3_VALUES
+    if E4M3_VALUES is None:
+        E4M3_VALUES = np.array([e4m3_decode(c) for c in range(256)])
+    return E4M3_VALUES
+
+
+def quantize_rows_fp8(a: np.ndarray):
+    """1x128 blocks along the columns.  Returns (codes uint8 [rows, cols], scales f32 [rows, ceil(cols/128)])."""
+    a = _c(a)
+    rows, cols = a.shape
+    codes = np.empty((rows, cols), np.uint8)
+    scales = np.empty((rows, (cols + 127) // 128), np.float32)
+    _load().oracle_quantize_rows_fp8(_ptr(a), _dt(a), rows, cols, _ptr(codes), _ptr(scales))
+    return codes, scales
+
+
+def quantize_tiles_fp8(w: np.ndarray):
+    """128x128 tiles of a [n_out, k_in] weight.  Returns (codes, scales [ceil(n/128), ceil(k/128)])."""
+    w = _c(w)
+    n, k = w.shape
+    codes = np.empty((n, k), np.uint8)
+    scales = np.empty(((n + 127) // 128, (k + 127) // 128), np.float32)
+    _load().oracle_quantize_tiles_fp8(_ptr(w), _dt(w), n, k, _ptr(codes), _ptr(scales))
+    return codes, scales
+
+
+def gemm_fp8(qa, sa, qb, sb) -> np.ndarray:
+    """C[m,n] = sum_b sa[m,b] sb[n/128,b] sum_(k in b) e4m3(qa[m,k]) e4m3(qb[n,k])  (fp64)."""
+    qa, qb = _c(qa, np.uint8), _c(qb, np.uint8)
+    sa, sb = _c(sa, np.float32), _c(sb, np.float32)
+    M, K = qa.shape
+    N = qb.shape[0]
+    c = np.empty((M, N), np.float64)
+    _load().oracle_gemm_fp8(_ptr(qa), _ptr(sa), _ptr(qb), _ptr(sb), M, N, K, _ptr(c))
+    return c
+
+
+def quantize_experts_fp8(w: np.ndarray):
+    """[E, n_out, k_in] weights -> (codes [E, n_out, k_in], scales [E, n_out/128, k_in/128])."""
+    E = w.shape[0]
+    pairs = [quantize_tiles_fp8(w[e]) for e in range(E)]
+    return np.stack([p[0] for p in pairs]), np.stack([p[1] for p in pairs])
+
+
+def layer_fp8(x, wg, q: dict, *, k: int, renorm: bool = True, bias=None, tokens=None, n_group: int = 1,
+              topk_group: int = 1, group_rule: str = "max"):
+    """Brute-force layer with FP8 expert weights (x, wg bf16 bit patterns).  q holds the codes
+    and scales from quantize_experts_fp8: gq, gs, uq, us, dq, ds and the shared sgq ... sds."""
+    x, wg = _c(x, np.uint16), _c(wg, np.uint16)
+    T, H = x.shape
+    E, I = q["gq"].shape[0], q["gq"].shape[1]
+    S = 0 if q.get("sgq") is None else q["sgq"].shape[0]
+    arrs = [_c(q[n], np.uint8 if n.endswith("q") else np.float32) if q.get(n) is not None else None
+            for n in ("gq", "gs", "uq", "us", "dq", "ds", "sgq", "sgs", "suq", "sus", "sdq", "sds")]
+    bias = _c(bias, np.float32)
+    toks = None if tokens is None else _c(np.asarray(tokens, np.int32), np.int32)
+    n = T if toks is None else toks.size
+    logits = np.empty((n, E), np.float64)
+    ids = np.empty((n, k), np.int32)
+    w = np.empty((n, k), np.float64)
+    out = np.empty((n, H), np.float64)
+    _load().oracle_layer_fp8(_ptr(x), T, H, E, k, I, S, int(bool(renorm)), _ptr(wg), _ptr(bias),
+                             *[_ptr(a) for a in arrs], _ptr(toks), n, _ptr(logits), _ptr(ids), _ptr(w), _ptr(out),
+                             n_group, topk_group, {"max": 0, "top2_sum": 1}[group_rule])
+    return dict(logits64=logits, ids=ids, w=w, out=out)
 
 
 def expert_ffn_rows(a: np.ndarray, expert: np.ndarray, wgate, wup, w2) -> np.ndarray:

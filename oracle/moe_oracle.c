@@ -112,6 +112,101 @@ void oracle_round_array(const double* in, int dt, int64_t n, double* out) {
     for (int64_t i = 0; i < n; ++i) out[i] = round_to(in[i], dt);
 }
 
+/* ---- FP8 (e4m3) block quantisation ------------------------------------------
+ * [BLOG §Quantization]: DeepSeek-V3/R1 uses per-block FP8 quantisation, with
+ * weights quantised statically and activations on the fly; scales are computed
+ * per 128-element vector for activations and per 128x128 tile for weights.
+ * Readings (the page does not fix them): the FP8 format is e4m3 (1 sign bit,
+ * 4 exponent bits with bias 7, 3 mantissa bits, largest finite 448, no
+ * infinities); a block's scale is amax/448 in fp32 (1 for an all-zero block);
+ * a value's code is round-to-nearest-even of fl32(v / scale) onto the e4m3
+ * grid, saturating at +-448.                                                   */
+
+/* e4m3 code -> value. */
+double oracle_e4m3_decode(uint8_t code) {
+    int sign = code >> 7, e = (code >> 3) & 15, m = code & 7;
+    if (e == 15 && m == 7) return NAN;
+    double v = e == 0 ? ldexp((double)m, -9) : ldexp(8.0 + m, e - 10);
+    return sign ? -v : v;
+}
+
+/* value -> e4m3 code, round to nearest even on the e4m3 grid, saturating. */
+uint8_t oracle_e4m3_encode(float f) {
+    double v = (double)f;
+    int sign = v < 0 || (v == 0 && signbit(v));
+    double a = fabs(v);
+    if (isnan(v)) return 0x7F;
+    if (a >= 448.0) return (uint8_t)((sign << 7) | 0x7E);
+    /* spacing of the grid around a: 2^-9 below 2^-6 (subnormals), else 2^(E-3) */
+    int E = a > 0 ? (int)floor(log2(a)) : -10;
+    if (E < -6) E = -6;
+    double q = ldexp(1.0, E - 3);
+    double n = a / q;                 /* exact: q is a power of two */
+    double r = floor(n);
+    double frac = n - r;
+    if (frac > 0.5 || (frac == 0.5 && fmod(r, 2.0) == 1.0)) r += 1.0;
+    double val = r * q;
+    if (val > 448.0) val = 448.0;
+    /* encode val */
+    uint8_t code;
+    if (val < ldexp(1.0, -6)) {
+        code = (uint8_t)(int)(val / ldexp(1.0, -9));                /* subnormal: e = 0 */
+    } else {
+        int e2 = (int)floor(log2(val));
+        int mant = (int)(val / ldexp(1.0, e2 - 3)) - 8;            /* 0..7 */
+        code = (uint8_t)(((e2 + 7) << 3) | mant);
+    }
+    return (uint8_t)((sign << 7) | code);
+}
+
+/* Scale of one block from its largest magnitude (fp32 arithmetic). */
+static float block_scale(float amax) { return amax > 0.0f ? amax / 448.0f : 1.0f; }
+
+/* Rows of a [rows, cols] matrix (dtype dt) quantised in 1 x 128 blocks along
+ * the columns: codes [rows, cols], scales [rows, ceil(cols/128)] fp32.       */
+void oracle_quantize_rows_fp8(const void* a, int dt, int64_t rows, int cols, uint8_t* codes, float* scales) {
+    int kb = (cols + 127) / 128;
+    #pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < rows; ++r) {
+        for (int b = 0; b < kb; ++b) {
+            int c0 = b * 128, c1 = c0 + 128 < cols ? c0 + 128 : cols;
+            float amax = 0.0f;
+            for (int c = c0; c < c1; ++c) {
+                float v = (float)load(a, dt, (size_t)r * cols + c);
+                if (fabsf(v) > amax) amax = fabsf(v);
+            }
+            float s = block_scale(amax);
+            scales[(size_t)r * kb + b] = s;
+            for (int c = c0; c < c1; ++c)
+                codes[(size_t)r * cols + c] = oracle_e4m3_encode((float)load(a, dt, (size_t)r * cols + c) / s);
+        }
+    }
+}
+
+/* A weight [n_out, k_in] (dtype dt) quantised in 128 x 128 tiles:
+ * codes [n_out, k_in], scales [ceil(n_out/128), ceil(k_in/128)] fp32.        */
+void oracle_quantize_tiles_fp8(const void* w, int dt, int n_out, int k_in, uint8_t* codes, float* scales) {
+    int nb = (n_out + 127) / 128, kb = (k_in + 127) / 128;
+    #pragma omp parallel for schedule(static) collapse(2)
+    for (int bn = 0; bn < nb; ++bn) {
+        for (int bk = 0; bk < kb; ++bk) {
+            int n1 = bn * 128 + 128 < n_out ? bn * 128 + 128 : n_out;
+            int k1 = bk * 128 + 128 < k_in ? bk * 128 + 128 : k_in;
+            float amax = 0.0f;
+            for (int n = bn * 128; n < n1; ++n)
+                for (int k = bk * 128; k < k1; ++k) {
+                    float v = (float)load(w, dt, (size_t)n * k_in + k);
+                    if (fabsf(v) > amax) amax = fabsf(v);
+                }
+            float s = block_scale(amax);
+            scales[(size_t)bn * kb + bk] = s;
+            for (int n = bn * 128; n < n1; ++n)
+                for (int k = bk * 128; k < k1; ++k)
+                    codes[(size_t)n * k_in + k] = oracle_e4m3_encode((float)load(w, dt, (size_t)n * k_in + k) / s);
+        }
+    }
+}
+
 /* ---- gate GEMM ------------------------------------------------------------
  * [BLOG §Roofline / GEMM]: logits = x [T,H] times the router weight; the
  * router weight is stored like a Linear weight, wg [E,H] (H contiguous), so
@@ -404,6 +499,132 @@ void oracle_finalize_routing(const void* y, int dt, int64_t n_rows, const void* 
             }
             out[(size_t)t * H + o] = acc;
         }
+    }
+}
+
+/* ---- FP8 block-scaled GEMM and SwiGLU expert ---------------------------------
+ * [BLOG §Quantization]: with scales per 1x128 activation vector and per 128x128
+ * weight tile, a product [M,K]x[K,N] (weights stored [N,K]) is
+ *   C[m,n] = sum_b sa[m,b] * sb[n/128, b] * sum_{k in block b} qa[m,k] * qb[n,k]
+ * with qa, qb the e4m3 values.  Sums in fp64.                                 */
+static double E4M3[256];
+static void init_e4m3(void) {
+    static int done = 0;
+    if (done) return;
+    for (int c = 0; c < 256; ++c) E4M3[c] = oracle_e4m3_decode((uint8_t)c);
+    done = 1;
+}
+
+static double fp8_dot(const uint8_t* qa, const float* sa, const uint8_t* qb, const float* sb_row, int K) {
+    int kb = (K + 127) / 128;
+    double acc = 0.0;
+    for (int b = 0; b < kb; ++b) {
+        double part = 0.0;
+        int k1 = b * 128 + 128 < K ? b * 128 + 128 : K;
+        for (int k = b * 128; k < k1; ++k) part += E4M3[qa[k]] * E4M3[qb[k]];
+        acc += (double)sa[b] * (double)sb_row[b] * part;
+    }
+    return acc;
+}
+
+void oracle_gemm_fp8(const uint8_t* qa, const float* sa, const uint8_t* qb, const float* sb, int M, int N, int K,
+                     double* c) {
+    init_e4m3();
+    int kb = (K + 127) / 128;
+    #pragma omp parallel for schedule(static)
+    for (int m = 0; m < M; ++m)
+        for (int n = 0; n < N; ++n)
+            c[(size_t)m * N + n] = fp8_dot(qa + (size_t)m * K, sa + (size_t)m * kb, qb + (size_t)n * K,
+                                           sb + (size_t)(n / 128) * kb, K);
+}
+
+/* One SwiGLU expert on one quantised row (bf16 layer with FP8 weights):
+ *   g, u   = FP8 products of the row with the gate and up weights
+ *   h      = silu(g) * u, stored in bf16, then quantised in 1x128 blocks
+ *   y      = FP8 product of h with the down weight (returned unrounded)
+ * Weights of the expert: gq/uq [I,H] with scales [I/128][H/128]; dq [H,I]
+ * with scales [H/128][I/128].                                                 */
+static void expert_ffn_row_fp8(const uint8_t* xq, const float* xs, const uint8_t* gq, const float* gs,
+                               const uint8_t* uq, const float* us, const uint8_t* dq, const float* ds, int H,
+                               int I, double* hbuf, uint8_t* hq, float* hs, double* y) {
+    int kbh = (H + 127) / 128, kbi = (I + 127) / 128;
+    for (int i = 0; i < I; ++i) {
+        double g = fp8_dot(xq, xs, gq + (size_t)i * H, gs + (size_t)(i / 128) * kbh, H);
+        double u = fp8_dot(xq, xs, uq + (size_t)i * H, us + (size_t)(i / 128) * kbh, H);
+        hbuf[i] = round_to(g / (1.0 + exp(-g)) * u, OR_BF16);
+    }
+    for (int b = 0; b < kbi; ++b) {
+        int i1 = b * 128 + 128 < I ? b * 128 + 128 : I;
+        float amax = 0.0f;
+        for (int i = b * 128; i < i1; ++i) if (fabsf((float)hbuf[i]) > amax) amax = fabsf((float)hbuf[i]);
+        float sc = block_scale(amax);
+        hs[b] = sc;
+        for (int i = b * 128; i < i1; ++i) hq[i] = oracle_e4m3_encode((float)hbuf[i] / sc);
+    }
+    for (int o = 0; o < H; ++o) y[o] = fp8_dot(hq, hs, dq + (size_t)o * I, ds + (size_t)(o / 128) * kbi, I);
+}
+
+/* The layer with FP8 expert weights (bf16 activations and outputs), brute force
+ * per token: bf16 gate logits and routing exactly as oracle_layer, x quantised
+ * in 1x128 blocks, each expert (routed and shared) through expert_ffn_row_fp8,
+ * the shared outputs summed and stored in bf16, each routed output stored in
+ * bf16, the weighted sum rounded once to bf16.
+ * Per-expert weight arrays: gq, uq [E][I][H], gs, us [E][I/128][H/128],
+ * dq [E][H][I], ds [E][H/128][I/128]; the shared ones likewise with S.       */
+void oracle_layer_fp8(const void* x, int T, int H, int E, int k, int I, int S, int renorm, const void* wg,
+                      const float* bias, const uint8_t* gq, const float* gs, const uint8_t* uq, const float* us,
+                      const uint8_t* dq, const float* ds, const uint8_t* sgq, const float* sgs, const uint8_t* suq,
+                      const float* sus, const uint8_t* sdq, const float* sds, const int32_t* tokens, int n_tok,
+                      double* logits64, int32_t* ids, double* w, double* out, int n_group, int topk_group,
+                      int group_rule) {
+    init_e4m3();
+    if (!tokens) n_tok = T;
+    const int kbh = (H + 127) / 128, kbi = (I + 127) / 128;
+    const size_t gsz = (size_t)kbi * kbh;  /* scale blocks of one [I,H] weight */
+    #pragma omp parallel
+    {
+        float* l32 = (float*)malloc(sizeof(float) * (size_t)E);
+        uint8_t* xq = (uint8_t*)malloc((size_t)H);
+        float* xs = (float*)malloc(sizeof(float) * (size_t)kbh);
+        double* hbuf = (double*)malloc(sizeof(double) * (size_t)I);
+        uint8_t* hq = (uint8_t*)malloc((size_t)I);
+        float* hs = (float*)malloc(sizeof(float) * (size_t)kbi);
+        double* yr = (double*)malloc(sizeof(double) * (size_t)H);
+        double* ysh = (double*)malloc(sizeof(double) * (size_t)H);
+        #pragma omp for schedule(dynamic, 1)
+        for (int n = 0; n < n_tok; ++n) {
+            int t = tokens ? tokens[n] : n;
+            size_t xo = (size_t)t * H;
+            for (int e = 0; e < E; ++e) {
+                double acc = 0.0;
+                for (int h = 0; h < H; ++h) acc += load(x, OR_BF16, xo + h) * load(wg, OR_BF16, (size_t)e * H + h);
+                l32[e] = (float)acc;
+                if (logits64) logits64[(size_t)n * E + e] = acc;
+            }
+            if (n_group > 1)
+                oracle_route_topk_grouped(l32, bias, 1, E, k, n_group, topk_group, group_rule, renorm,
+                                          ids + (size_t)n * k, w + (size_t)n * k);
+            else
+                oracle_route_topk(l32, bias, 1, E, k, renorm, ids + (size_t)n * k, w + (size_t)n * k);
+            oracle_quantize_rows_fp8((const char*)x + xo * 2, OR_BF16, 1, H, xq, xs);
+            for (int o = 0; o < H; ++o) ysh[o] = 0.0;
+            for (int s2 = 0; s2 < S; ++s2) {
+                expert_ffn_row_fp8(xq, xs, sgq + (size_t)s2 * I * H, sgs + s2 * gsz, suq + (size_t)s2 * I * H,
+                                   sus + s2 * gsz, sdq + (size_t)s2 * H * I, sds + s2 * gsz, H, I, hbuf, hq, hs, yr);
+                for (int o = 0; o < H; ++o) ysh[o] += yr[o];
+            }
+            double* orow = out + (size_t)n * H;
+            for (int o = 0; o < H; ++o) orow[o] = round_to(ysh[o], OR_BF16);
+            for (int j = 0; j < k; ++j) {
+                int e = ids[(size_t)n * k + j];
+                expert_ffn_row_fp8(xq, xs, gq + (size_t)e * I * H, gs + e * gsz, uq + (size_t)e * I * H,
+                                   us + e * gsz, dq + (size_t)e * H * I, ds + e * gsz, H, I, hbuf, hq, hs, yr);
+                double wj = w[(size_t)n * k + j];
+                for (int o = 0; o < H; ++o) orow[o] += wj * round_to(yr[o], OR_BF16);
+            }
+            for (int o = 0; o < H; ++o) orow[o] = round_to(orow[o], OR_BF16);
+        }
+        free(l32); free(xq); free(xs); free(hbuf); free(hq); free(hs); free(yr); free(ysh);
     }
 }
 

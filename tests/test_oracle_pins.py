@@ -408,3 +408,111 @@ def test_double_routing_permutations_compose_to_single_routing(oracle):
         r = oracle.re_routing(np.concatenate(blocks), np.array(counts, np.int32))
         sorted_all.append(r["x_sorted"])
     assert np.array_equal(np.concatenate(sorted_all), single["expanded_x"])
+
+
+# ---- FP8 (e4m3) block quantisation -------------------------------------------------
+
+def test_e4m3_decode_matches_torch_for_every_code(oracle):
+    codes = torch.arange(256, dtype=torch.uint8)
+    want = codes.view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    got = oracle.e4m3_table()
+    assert np.array_equal(np.isnan(got), np.isnan(want))
+    ok = ~np.isnan(want)
+    assert np.array_equal(got[ok], want[ok])
+    assert got[0x7E] == 448.0 and got[0x01] == 2.0 ** -9 and got[0x08] == 2.0 ** -6
+
+
+def test_e4m3_encode_matches_torch_cast(oracle):
+    rng = np.random.default_rng(0)
+    table = oracle.e4m3_table()
+    finite = np.sort(np.unique(table[~np.isnan(table)]))
+    mids = (finite[:-1] + finite[1:]) / 2  # exact ties: round to the even code
+    vals = np.concatenate([rng.standard_normal(20000) * 50, rng.standard_normal(2000) * 1e-2,
+                           finite, mids, -mids]).astype(np.float32)
+    vals = vals[np.abs(vals) <= 448]
+    got = np.array([oracle.e4m3_encode(v) for v in vals], np.uint8)
+    want = torch.from_numpy(vals).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    # +0/-0 both decode to zero; compare values
+    assert np.array_equal(table[got], table[want])
+    assert oracle.e4m3_encode(1000.0) == 0x7E and oracle.e4m3_encode(-1000.0) == 0xFE  # saturation
+
+
+def test_quantize_rows_and_tiles(oracle):
+    x = inputs.random_rows(5, 300, torch.bfloat16, seed=1)
+    codes, scales = oracle.quantize_rows_fp8(inputs.to_numpy(x))
+    assert scales.shape == (5, 3)
+    xf = x.to(torch.float64).numpy()
+    deq = oracle.e4m3_table()[codes] * np.repeat(scales.astype(np.float64), 128, axis=1)[:, :300]
+    # each block's largest magnitude maps to +-448 exactly, every element within half an e4m3 step
+    for r in range(5):
+        for b in range(3):
+            blk = xf[r, b * 128:(b + 1) * 128]
+            assert np.isclose(np.abs(blk).max() / scales[r, b], 448.0, rtol=1e-6)
+    assert np.all(np.abs(deq - xf) <= np.abs(xf) * 2.0 ** -4 + scales.max() * 2.0 ** -9)
+    w = inputs.random_rows(200, 260, torch.float32, seed=2).numpy()
+    wc, ws = oracle.quantize_tiles_fp8(w)
+    assert ws.shape == (2, 3)
+    np.testing.assert_allclose(ws[1, 2], np.abs(w[128:, 256:]).max() / 448, rtol=1e-7)
+    zc, zs = oracle.quantize_rows_fp8(np.zeros((1, 128), np.float32))
+    assert np.all(zc == 0) and zs[0, 0] == 1.0
+
+
+def _dequant_torch(codes, scales, rows_per_scale):
+    """Library dequantisation: torch's float8_e4m3fn values times the block scales."""
+    v = torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    s = np.repeat(np.repeat(scales.astype(np.float64), rows_per_scale, axis=0), 128, axis=1)
+    return v * s[:v.shape[0], :v.shape[1]]
+
+
+def test_gemm_fp8_is_dequantised_matmul(oracle):
+    a = inputs.random_rows(7, 300, torch.bfloat16, seed=3)
+    b = inputs.random_rows(260, 300, torch.float32, seed=4).numpy()
+    qa, sa = oracle.quantize_rows_fp8(inputs.to_numpy(a))
+    qb, sb = oracle.quantize_tiles_fp8(b)
+    got = oracle.gemm_fp8(qa, sa, qb, sb)
+    want = _dequant_torch(qa, sa, 1) @ _dequant_torch(qb, sb, 128).T
+    np.testing.assert_allclose(got, want, rtol=1e-12, atol=1e-12)
+
+
+def test_gemm_fp8_lossless_case_is_exact(oracle):
+    """Small integers with a 448 in every block quantise exactly (scale 1)."""
+    rng = np.random.default_rng(5)
+    A = rng.integers(-8, 9, size=(4, 256)).astype(np.float32)
+    B = rng.integers(-8, 9, size=(128, 256)).astype(np.float32)
+    A[:, 0] = 448.0
+    A[:, 128] = 448.0
+    B[0, :] = 448.0
+    qa, sa = oracle.quantize_rows_fp8(A)
+    qb, sb = oracle.quantize_tiles_fp8(B)
+    assert np.all(sa == 1.0) and np.all(sb == 1.0)
+    assert np.array_equal(oracle.gemm_fp8(qa, sa, qb, sb), A.astype(np.float64) @ B.T.astype(np.float64))
+
+
+def test_layer_fp8_dense_case_composes_the_steps(oracle):
+    """E=1, k=1 + one shared expert: the FP8 layer is two FP8 SwiGLU MLPs built
+    from the quantiser, the FP8 product and torch's SiLU."""
+    cfg = inputs.LayerConfig("t", T=6, H=256, E=1, k=1, I=128, S=1, dtype="bf16", seed=9)
+    d = inputs.make_layer(cfg)
+    n = {k_: inputs.to_numpy(v) for k_, v in d.items() if isinstance(v, torch.Tensor)}
+    q = {}
+    for pre, g, u, w2 in (("", "w_gate", "w_up", "w2"), ("s", "s_gate", "s_up", "s2")):
+        q[pre + "gq"], q[pre + "gs"] = oracle.quantize_experts_fp8(n[g])
+        q[pre + "uq"], q[pre + "us"] = oracle.quantize_experts_fp8(n[u])
+        q[pre + "dq"], q[pre + "ds"] = oracle.quantize_experts_fp8(n[w2])
+    r = oracle.layer_fp8(n["x"], n["wg"], q, k=1)
+    xq, xs = oracle.quantize_rows_fp8(n["x"])
+
+    def mlp(pre):
+        g = oracle.gemm_fp8(xq, xs, q[pre + "gq"][0], q[pre + "gs"][0])
+        u = oracle.gemm_fp8(xq, xs, q[pre + "uq"][0], q[pre + "us"][0])
+        h = (F.silu(torch.from_numpy(g)) * torch.from_numpy(u)).to(torch.bfloat16)
+        hq, hs = oracle.quantize_rows_fp8(inputs.to_numpy(h))
+        y = oracle.gemm_fp8(hq, hs, q[pre + "dq"][0], q[pre + "ds"][0])
+        return oracle.round_to(y, BF16)
+
+    want = oracle.round_to(mlp("s") + mlp(""), BF16)
+    # torch's SiLU and the oracle's may differ in the last bit of h before rounding to bf16
+    assert np.abs(r["out"] - want).max() <= 1e-2 * np.abs(want).max()
+    # and the FP8 layer stays close to the bf16 layer (quantisation error only)
+    ref = oracle.layer(*(n[k_] for k_ in ("x", "wg", "w_gate", "w_up", "w2", "s_gate", "s_up", "s2")), k=1)
+    assert np.linalg.norm(r["out"] - ref["out"]) / np.linalg.norm(ref["out"]) < 0.1
