@@ -232,7 +232,12 @@ def run_ours(args, world, rank, local):
     layer = binding.MoELayer(T=cfg.T, k=cfg.k, w_router=d["wg"], w_gate=d["w_gate"], w_up=d["w_up"], w2=d["w2"],
                              s_gate=d["s_gate"] if cfg.S else None, s_up=d["s_up"] if cfg.S else None,
                              s2=d["s2"] if cfg.S else None, expert_bias=d["bias"], renormalize=cfg.renormalize,
-                             n_group=cfg.n_group, topk_group=cfg.topk_group, group_rule=cfg.group_rule)
+                             n_group=cfg.n_group, topk_group=cfg.topk_group, group_rule=cfg.group_rule,
+                             weight_format=cfg.weight_format)
+    if cfg.weight_format == "fp8":  # the bf16 expert weights are no longer needed on the device
+        for key in ("w_gate", "w_up", "w2"):
+            d[key] = d[key].cpu() if not args.no_cpu_baseline else None
+        torch.cuda.empty_cache()
     x = d["x"]
     out = torch.empty_like(x)
     stream = torch.cuda.current_stream()
@@ -276,11 +281,14 @@ def run_ours(args, world, rank, local):
     # roofline of the dominant kernel
     counts = layer.field("tokens_per_expert").cpu().numpy()
     touched = int((counts > 0).sum())
-    costs = roofline.stage_costs(cfg.T, cfg.H, cfg.E, cfg.k, cfg.I, cfg.S, cfg.esize, touched)
+    fp8 = cfg.weight_format == "fp8"
+    costs = roofline.stage_costs(cfg.T, cfg.H, cfg.E, cfg.k, cfg.I, cfg.S, cfg.esize, touched,
+                                 weight_bytes=1 if fp8 else None)
     peaks = roofline.load_peaks()
     top = max(stage_ms, key=stage_ms.get)
     fl, by = costs[top]
-    rl = roofline.roofline_entry(fl, by, stage_ms[top] / 1e3, peaks, sustained=True)
+    rl = roofline.roofline_entry(fl, by, stage_ms[top] / 1e3, peaks, sustained=True,
+                                 tensor_scale=2.0 if fp8 and top in ("up", "down", "shared") else 1.0)
     rl["traffic"] = measured_traffic(top, cfg.name)
     rl["kernel"] = top
     rl["algorithmic_bytes"] = by
@@ -308,7 +316,7 @@ def run_ours(args, world, rank, local):
     nbytes_io = x.numel() * x.element_size()
 
     cpu = None
-    if world == 1 and rank == 0 and not args.no_cpu_baseline:
+    if world == 1 and rank == 0 and not args.no_cpu_baseline and not fp8:
         import oracle
         oracle.build()
         cpu = cpu_baseline(cfg, host_layer(d), budget_s=args.cpu_budget)

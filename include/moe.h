@@ -206,6 +206,37 @@ moe_status_t moe_grouped_ffn(const void* a, moe_dtype_t dt, const int32_t* exper
                              void* ws, size_t ws_bytes, moe_stream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * FP8 block quantisation.  [BLOG §Quantization]: DeepSeek-V3/R1 quantises per
+ * block -- weights statically with one scale per 128x128 tile, activations on
+ * the fly with one scale per 128-element vector.  Format e4m3 (largest finite
+ * 448); a block's scale is amax/448 in fp32 (1 for an all-zero block); a value's
+ * code is round-to-nearest-even of fl32(v/scale), saturated at +-448.
+ *
+ * moe_quantize_rows_fp8: a [rows, cols] dt -> codes [rows, cols] uint8, scales
+ * [rows, ld_scales] fp32 (ld_scales >= ceil(cols/128); 1x128 blocks).
+ * moe_quantize_weights_fp8: w [G, n_out, k_in] dt -> codes [G, n_out, k_in],
+ * scales [G][ceil(n_out/128)][ceil(k_in/128)] (128x128 tiles).  For w13 pass the
+ * moe_pack_w13 output (n_out = 2*Ip); for the shared experts G = 1. */
+moe_status_t moe_quantize_rows_fp8(const void* a, moe_dtype_t dt, int64_t rows, int cols, uint8_t* codes,
+                                   float* scales, int ld_scales, moe_stream_t stream);
+moe_status_t moe_quantize_weights_fp8(const void* w, moe_dtype_t dt, int G, int n_out, int k_in, uint8_t* codes,
+                                      float* scales, moe_stream_t stream);
+
+/* Grouped SwiGLU expert FFN with FP8 weights and activations ([BLOG
+ * §Quantization], [BLOG §Roofline / GroupGEMM]): products are block-scaled,
+ *   C[m,n] = sum_b sa[m,b] * sb[n/128,b] * sum_{k in block b} qa[m,k] qb[n,k],
+ * h = silu(gate) * up is stored in bf16 and quantised in 1x128 blocks for the
+ * down projection; y [rows, H] bf16.  aq [rows, H] codes with a_scales
+ * [rows, lda_scales]; w13q/w13s and w2q/w2s from moe_quantize_weights_fp8;
+ * expert_offsets as in moe_grouped_ffn.  H % 256 == 0, I % 16 == 0.
+ * ws: moe_grouped_ffn_fp8_workspace_bytes(rows, I) bytes. */
+size_t moe_grouped_ffn_fp8_workspace_bytes(int rows, int I);
+moe_status_t moe_grouped_ffn_fp8(const uint8_t* aq, const float* a_scales, int lda_scales,
+                                 const int32_t* expert_offsets, int E, int rows, int H, int I, const uint8_t* w13q,
+                                 const float* w13s, const uint8_t* w2q, const float* w2s, void* y, void* ws,
+                                 size_t ws_bytes, moe_stream_t stream);
+
+/* ---------------------------------------------------------------------------
  * Finalize-routing.  [CANN §MoE deployment, Double-Routing step 8]: restore
  * the token order through expanded_src_to_dst_row, weight by scales=topk_weight
  * and add the shared expert output (skip1):
@@ -268,7 +299,20 @@ typedef struct moe_layer_desc {
     int n_group;               /* 0 or 1: flat top-k; > 1: group-limited (moe_route_topk_grouped) */
     int topk_group;            /* groups kept when n_group > 1 */
     int group_rule;            /* MOE_GROUP_SCORE_MAX or MOE_GROUP_SCORE_TOP2_SUM */
+    int weight_format;         /* MOE_WEIGHTS_NATIVE or MOE_WEIGHTS_FP8 (bf16 layers only) */
+    const float* w13_scales;   /* FP8: tile scales of w13 [E][2*Ip/128][ceil(H/128)] (moe_quantize_weights_fp8) */
+    const float* w2_scales;    /* FP8: tile scales of w2 [E][H/128][ceil(I/128)] */
+    const float* w13_shared_scales; /* FP8: [1][2*Ips/128][ceil(H/128)], Ips = S*I rounded up to 128 */
+    const float* w2_shared_scales;  /* FP8: [1][H/128][ceil(S*I/128)] */
 } moe_layer_desc;
+
+/* Weight formats of moe_layer_desc.  With MOE_WEIGHTS_FP8 the w13/w2 pointers
+ * (routed and shared) hold e4m3 codes in the same layouts (one byte per
+ * element) with 128x128 tile scales beside them; the activations are quantised
+ * on the fly in 1x128 blocks ([BLOG §Quantization]); the gate GEMM, routing and
+ * all outputs stay bf16.  Requires dtype MOE_BF16, H % 256 == 0, I % 16 == 0. */
+#define MOE_WEIGHTS_NATIVE 0
+#define MOE_WEIGHTS_FP8 1
 
 /* Layer steps timed by moe_layer_forward_timed.  "shared" (both projections of
  * the shared experts) runs on a second stream of the library's, forked after
@@ -293,7 +337,15 @@ typedef enum moe_ws_field {
     MOE_WS_Y_SHARED = 10,         /* [T,H] dt */
     MOE_WS_X_IN = 11,             /* [T,H] dt: staging for moe_layer_forward_host */
     MOE_WS_OUT = 12,              /* [T,H] dt: staging for moe_layer_forward_host */
-    MOE_WS_NUM_FIELDS = 13
+    MOE_WS_XQ = 13,               /* FP8 only: [T,H] e4m3 codes of x */
+    MOE_WS_XQ_SCALES = 14,        /* FP8 only: [T, ceil(H/128) rounded up to 4] fp32 */
+    MOE_WS_EXPANDED_XQ = 15,      /* FP8 only: [T*k,H] codes, expert-sorted */
+    MOE_WS_EXPANDED_XQ_SCALES = 16, /* FP8 only: [T*k, ...] fp32 */
+    MOE_WS_HQ = 17,               /* FP8 only: [T*k,I] codes of h */
+    MOE_WS_HQ_SCALES = 18,        /* FP8 only: [T*k, ceil(I/128) rounded up to 4] fp32 */
+    MOE_WS_HQ_SHARED = 19,        /* FP8 only: [T,S*I] codes of the shared h */
+    MOE_WS_HQ_SHARED_SCALES = 20, /* FP8 only: [T, ceil(S*I/128) rounded up to 4] fp32 */
+    MOE_WS_NUM_FIELDS = 21
 } moe_ws_field;
 
 size_t moe_layer_workspace_bytes(const moe_layer_desc* desc);

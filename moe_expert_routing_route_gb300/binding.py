@@ -22,7 +22,9 @@ MOE_DEVERR_BAD_EXPERT_ID, MOE_DEVERR_BAD_ROW_INDEX, MOE_DEVERR_BAD_OFFSETS, MOE_
 MOE_WS_HEADER_BYTES = 256
 MOE_NUM_STAGES = 8
 WS_FIELDS = ["logits", "topk_ids", "topk_w", "tokens_per_expert", "expert_offsets", "expanded_row_idx",
-             "expanded_x", "h_routed", "h_shared", "y_routed", "y_shared", "x_in", "out"]
+             "expanded_x", "h_routed", "h_shared", "y_routed", "y_shared", "x_in", "out", "xq", "xq_scales",
+             "expanded_xq", "expanded_xq_scales", "hq", "hq_scales", "hq_shared", "hq_shared_scales"]
+MOE_WEIGHTS_NATIVE, MOE_WEIGHTS_FP8 = 0, 1
 
 # The exported entry points (name -> (restype, argtypes)).
 P, I32, I64, SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t
@@ -31,7 +33,9 @@ P, I32, I64, SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t
 class LayerDesc(ctypes.Structure):
     _fields_ = [("T", I32), ("H", I32), ("E", I32), ("k", I32), ("I", I32), ("S", I32), ("dtype", I32),
                 ("renormalize", I32), ("w_router", P), ("expert_bias", P), ("w13", P), ("w2", P),
-                ("w13_shared", P), ("w2_shared", P), ("n_group", I32), ("topk_group", I32), ("group_rule", I32)]
+                ("w13_shared", P), ("w2_shared", P), ("n_group", I32), ("topk_group", I32), ("group_rule", I32),
+                ("weight_format", I32), ("w13_scales", P), ("w2_scales", P), ("w13_shared_scales", P),
+                ("w2_shared_scales", P)]
 
 
 _DP = ctypes.POINTER(LayerDesc)
@@ -56,6 +60,10 @@ SIGNATURES = {
     "moe_unsort_rows": (I32, [P, I32, P, I32, I32, P, P, P]),
     "moe_layer_workspace_bytes_ep": (SZ, [_DP, I32]),
     "moe_layer_forward_ep": (I32, [_DP, I32, P, P, P, SZ, P]),
+    "moe_quantize_rows_fp8": (I32, [P, I32, I64, I32, P, P, I32, P]),
+    "moe_quantize_weights_fp8": (I32, [P, I32, I32, I32, I32, P, P, P]),
+    "moe_grouped_ffn_fp8_workspace_bytes": (SZ, [I32, I32]),
+    "moe_grouped_ffn_fp8": (I32, [P, P, I32, P, I32, I32, I32, I32, P, P, P, P, P, P, SZ, P]),
     "moe_stage_name": (ctypes.c_char_p, [I32]),
     "moe_layer_workspace_bytes": (SZ, [_DP]),
     "moe_layer_workspace_field": (I32, [_DP, I32, ctypes.POINTER(SZ), ctypes.POINTER(SZ)]),
@@ -262,6 +270,43 @@ def moe_unsort_rows(y_sorted: torch.Tensor, gathered_ids_unsort: torch.Tensor, w
     return out
 
 
+def scale_ld(cols: int) -> int:
+    """Row stride (floats) of the 1x128 activation scales the layer uses."""
+    return -(-(-(-cols // 128)) // 4) * 4
+
+
+def moe_quantize_rows_fp8(a: torch.Tensor, ld_scales: int | None = None, stream=None):
+    rows, cols = a.shape
+    ld = ld_scales or -(-cols // 128)
+    codes = torch.empty((rows, cols), dtype=torch.uint8, device=a.device)
+    scales = torch.empty((rows, ld), dtype=torch.float32, device=a.device)
+    _check(lib().moe_quantize_rows_fp8(_ptr(a), _dt(a), rows, cols, _ptr(codes), _ptr(scales), ld, _stream(stream)),
+           "moe_quantize_rows_fp8")
+    return codes, scales
+
+
+def moe_quantize_weights_fp8(w: torch.Tensor, stream=None):
+    """w [G, n_out, k_in] (or [n_out, k_in]) -> (codes, scales [G, n/128, k/128])."""
+    if w.dim() == 2:
+        w = w.unsqueeze(0)
+    G, n, k = w.shape
+    codes = torch.empty((G, n, k), dtype=torch.uint8, device=w.device)
+    scales = torch.empty((G, -(-n // 128), -(-k // 128)), dtype=torch.float32, device=w.device)
+    _check(lib().moe_quantize_weights_fp8(_ptr(w.contiguous()), _dt(w), G, n, k, _ptr(codes), _ptr(scales),
+                                          _stream(stream)), "moe_quantize_weights_fp8")
+    return codes, scales
+
+
+def moe_grouped_ffn_fp8(aq, a_scales, expert_offsets, E: int, I: int, w13q, w13s, w2q, w2s, stream=None):
+    rows, H = aq.shape
+    ws = torch.empty(lib().moe_grouped_ffn_fp8_workspace_bytes(rows, I), dtype=torch.uint8, device=aq.device)
+    y = torch.zeros((rows, H), dtype=torch.bfloat16, device=aq.device)
+    _check(lib().moe_grouped_ffn_fp8(_ptr(aq), _ptr(a_scales), a_scales.shape[1], _ptr(expert_offsets), E, rows, H, I,
+                                     _ptr(w13q), _ptr(w13s), _ptr(w2q), _ptr(w2s), _ptr(y), _ptr(ws), ws.numel(),
+                                     _stream(stream)), "moe_grouped_ffn_fp8")
+    return y, ws
+
+
 def stage_names() -> list[str]:
     return [lib().moe_stage_name(i).decode() for i in range(MOE_NUM_STAGES)]
 
@@ -275,7 +320,7 @@ class MoELayer:
 
     def __init__(self, *, T: int, k: int, w_router, w_gate, w_up, w2, s_gate=None, s_up=None, s2=None,
                  expert_bias=None, renormalize: bool = True, n_group: int = 1, topk_group: int = 1,
-                 group_rule: str = "max", stream=None):
+                 group_rule: str = "max", weight_format: str = "native", stream=None):
         E, I, H = w_gate.shape
         S = 0 if s_gate is None else s_gate.shape[0]
         self.T, self.H, self.E, self.k, self.I, self.S = T, H, E, k, I, S
@@ -291,11 +336,26 @@ class MoELayer:
         else:
             self.w13_shared = self.w2_shared = None
         self.expert_bias = None if expert_bias is None else expert_bias.to(torch.float32).contiguous()
+        self.weight_format = weight_format
+        scales = [None] * 4
+        if weight_format == "fp8":
+            # static 128x128-tile quantisation of the packed gate/up and the down weights
+            self.w13, s13 = moe_quantize_weights_fp8(self.w13, stream)
+            self.w2, s2_ = moe_quantize_weights_fp8(self.w2, stream)
+            scales[0], scales[1] = s13, s2_
+            if S:
+                self.w13_shared, ss13 = moe_quantize_weights_fp8(self.w13_shared, stream)
+                self.w2_shared, ss2 = moe_quantize_weights_fp8(self.w2_shared, stream)
+                scales[2], scales[3] = ss13, ss2
+        elif weight_format != "native":
+            raise ValueError(f"weight_format must be 'native' or 'fp8', got {weight_format!r}")
+        self.scales = scales
+        sp = [0 if t is None else t.data_ptr() for t in scales]
         self.desc = LayerDesc(T, H, E, k, I, S, _dt(w_gate), int(bool(renormalize)), self.w_router.data_ptr(),
                               0 if self.expert_bias is None else self.expert_bias.data_ptr(), self.w13.data_ptr(),
                               self.w2.data_ptr(), 0 if S == 0 else self.w13_shared.data_ptr(),
                               0 if S == 0 else self.w2_shared.data_ptr(), n_group, topk_group,
-                              GROUP_RULES[group_rule])
+                              GROUP_RULES[group_rule], MOE_WEIGHTS_FP8 if weight_format == "fp8" else 0, *sp)
         nbytes = lib().moe_layer_workspace_bytes(ctypes.byref(self.desc))
         if nbytes == 0:
             raise MoEError(MOE_ERR_INVALID_ARG, "moe_layer_workspace_bytes")
@@ -313,7 +373,12 @@ class MoELayer:
                       expert_offsets=((E + 1,), torch.int32), expanded_row_idx=((T * k,), torch.int32),
                       expanded_x=((T * k, H), self.dtype), h_routed=((T * k, I), self.dtype),
                       h_shared=((T, S * I), self.dtype), y_routed=((T * k, H), self.dtype),
-                      y_shared=((T, H), self.dtype), x_in=((T, H), self.dtype), out=((T, H), self.dtype))
+                      y_shared=((T, H), self.dtype), x_in=((T, H), self.dtype), out=((T, H), self.dtype),
+                      xq=((T, H), torch.uint8), xq_scales=((T, scale_ld(H)), torch.float32),
+                      expanded_xq=((T * k, H), torch.uint8), expanded_xq_scales=((T * k, scale_ld(H)), torch.float32),
+                      hq=((T * k, I), torch.uint8), hq_scales=((T * k, scale_ld(I)), torch.float32),
+                      hq_shared=((T, S * I), torch.uint8), hq_shared_scales=((T, scale_ld(S * I) if S else 0),
+                                                                             torch.float32))
         shape, dtype = shapes[name]
         return raw.view(dtype).view(shape)
 

@@ -1,0 +1,373 @@
+// Grouped GEMM with FP8 (e4m3) block-scaled operands on tcgen05 tensor cores.
+//
+// "Lower latency and higher throughput with multi-node DeepSeek deployment"
+// (Perplexity blog), §Quantization: activations carry one fp32 scale per
+// 128-element vector along K (computed on the fly), weights one per 128x128
+// tile, so a product is
+//   C[m,n] = sum_b sa[m,b] * sb[n/128,b] * (sum_{k in block b} qa[m,k] * qb[n,k]).
+// §Roofline / GroupGEMM: the grouped product over expert segments, as in the
+// bf16 kernel (gemm_tc.cu), with the same persistent grid and device-side
+// tile scheduler reading the expert offsets.
+//
+// One 128-wide K block is one pipeline stage and one scale block.  The MMA
+// warp multiplies each K block into a fresh fp32 partial in TMEM (four
+// kind::f8f6f4 instructions, K = 32 each), alternating between two partial
+// buffers.  Eight epilogue warps -- two per TMEM lane group, each owning half of
+// the tile's columns -- fold every partial into register accumulators with
+// sa * sb (the promotion the block scales need), then apply SwiGLU or convert
+// and store once per tile.  Rows of a tile past the expert's segment are
+// computed and never stored, as in the bf16 kernel.  Waits are bounded as in
+// the bf16 kernel (about one second, then abort without trapping).
+#include "tc_ptx.cuh"
+
+#include <climits>
+
+namespace moe {
+namespace {
+
+using namespace tc;
+
+constexpr int BM = 128;
+constexpr int BK = 128;  // bytes (= e4m3 elements) of K per stage: one swizzle row, one scale block
+constexpr int UMMA_K = 32;
+constexpr int BN = 256;
+constexpr int kEpiWarps = 8;
+constexpr int kThreads = 64 + 32 * kEpiWarps;
+constexpr int kMaxGroups = 1024;
+constexpr int A_BYTES = BM * BK;
+constexpr int B_BYTES = BN * BK;
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int STAGES = 4;
+constexpr int TMEM_COLS = 2 * BN;  // two partial buffers
+constexpr int NUM_BARS = 2 * STAGES + 5;
+constexpr size_t SMEM = 1024 + (size_t)STAGES * STAGE_BYTES + NUM_BARS * 8 + 16 + (size_t)(3 * kMaxGroups + 1) * 4;
+
+struct Params {
+    const int32_t* offsets;  // [G+1] or nullptr: one group of M rows
+    int G, M, K, Nb, N, NT, KB;
+    void* C;
+    int64_t ldc;
+    const float* a_scales;  // [M][lda_s]
+    int lda_s;
+    const float* b_scales;  // [G][Nb/128][KB]
+    uint32_t* status;
+};
+
+__device__ __forceinline__ void decode_tile(int tile, const int* prefix, int G, int NT, int& g, int& m, int& n) {
+    int lo = 0, hi = G - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (prefix[mid] <= tile) lo = mid;
+        else hi = mid - 1;
+    }
+    g = lo;
+    const int local = tile - prefix[g];
+    const int mt = (prefix[g + 1] - prefix[g]) / NT;
+    n = local / mt;
+    m = local - n * mt;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// 64 consecutive bf16 outputs of one row (columns col0.., valid below N).
+__device__ __forceinline__ void store_row64(__nv_bfloat16* C, int64_t ldc, int64_t row, int col0, int N,
+                                            const float* v) {
+    __nv_bfloat16* dst = C + row * ldc + col0;
+    if (col0 + 64 <= N) {
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            uint4 u;
+            u.x = pack_bf16x2(v[8 * q + 0], v[8 * q + 1]);
+            u.y = pack_bf16x2(v[8 * q + 2], v[8 * q + 3]);
+            u.z = pack_bf16x2(v[8 * q + 4], v[8 * q + 5]);
+            u.w = pack_bf16x2(v[8 * q + 6], v[8 * q + 7]);
+            reinterpret_cast<uint4*>(dst)[q] = u;
+        }
+    } else {
+#pragma unroll
+        for (int c = 0; c < 64; ++c)
+            if (col0 + c < N) dst[c] = __float2bfloat16_rn(v[c]);
+    }
+}
+
+template <int EPI>
+__global__ void __launch_bounds__(kThreads, 1)
+tc_fp8_grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
+                           const __grid_constant__ Params p) {
+    constexpr uint32_t IDESC = idesc_e4m3(BM, BN);
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_addr = smem_u32(smem_raw);
+    uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
+    uint8_t* sA = smem;
+    uint8_t* sB = smem + STAGES * A_BYTES;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sB + STAGES * B_BYTES);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + NUM_BARS);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    int* prefix = reinterpret_cast<int*>(tmem_slot + 4);
+    int* gstart = prefix + kMaxGroups + 1;
+    int* gend = gstart + kMaxGroups;
+
+    auto full_bar = [&](int s) { return smem_u32(bars + s); };
+    auto empty_bar = [&](int s) { return smem_u32(bars + STAGES + s); };
+    auto pfull_bar = [&](int j) { return smem_u32(bars + 2 * STAGES + j); };
+    auto pempty_bar = [&](int j) { return smem_u32(bars + 2 * STAGES + 2 + j); };
+    const uint32_t drain_bar = smem_u32(bars + 2 * STAGES + 4);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int G = p.G, NT = p.NT, KB = p.KB;
+
+    for (int g = threadIdx.x; g < G; g += kThreads) {
+        int a = 0, b = p.M;
+        if (p.offsets) {
+            a = p.offsets[g];
+            b = p.offsets[g + 1];
+        }
+        if (a < 0 || b < a || b > p.M) {
+            set_status(p.status, MOE_DEVERR_BAD_OFFSETS);
+            a = b = 0;
+        }
+        gstart[g] = a;
+        gend[g] = b;
+    }
+    if (threadIdx.x == 0) *abort_flag = 0;
+    __syncthreads();
+    if (warp == 0) {
+        int run = 0;
+        for (int g0 = 0; g0 < G; g0 += 32) {
+            const int g = g0 + lane;
+            const int v = g < G ? (gend[g] - gstart[g] + BM - 1) / BM * NT : 0;
+            int incl = v;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const int nb = __shfl_up_sync(0xffffffffu, incl, off);
+                if (lane >= off) incl += nb;
+            }
+            if (g < G) prefix[g] = run + incl - v;
+            run += __shfl_sync(0xffffffffu, incl, 31);
+        }
+        if (lane == 0) {
+            prefix[G] = run;
+            for (int s = 0; s < STAGES; ++s) {
+                mbar_init(full_bar(s), 1);
+                mbar_init(empty_bar(s), 1);
+            }
+            for (int j = 0; j < 2; ++j) {
+                mbar_init(pfull_bar(j), 1);
+                mbar_init(pempty_bar(j), kEpiWarps);
+            }
+            mbar_init(drain_bar, 1);
+            asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            prefetch_tensormap(&mapA);
+            prefetch_tensormap(&mapB);
+        }
+    } else if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    const int total = prefix[G];
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ---------------- TMA producer ----------------
+            int s = 0;
+            uint32_t ph = 0, issued = 0, issued_par = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
+                int g, m, n;
+                decode_tile(tile, prefix, G, NT, g, m, n);
+                const int row0 = gstart[g] + m * BM;
+                const int brow = g * p.Nb + n * BN;
+                for (int kb = 0; kb < KB; ++kb) {
+                    if (!wait_phase_fast(empty_bar(s), ph ^ 1u, abort_flag, p.status)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(full_bar(s), STAGE_BYTES);
+                    tma_load_2d(smem_u32(sA + s * A_BYTES), &mapA, full_bar(s), kb * BK, row0);
+                    tma_load_2d(smem_u32(sB + s * B_BYTES), &mapB, full_bar(s), kb * BK, brow);
+                    issued |= 1u << s;
+                    issued_par = (issued_par & ~(1u << s)) | (ph << s);
+                    if (++s == STAGES) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                }
+            }
+            for (int q = 0; q < STAGES; ++q)
+                if ((issued >> q) & 1u) wait_drain(full_bar(q), (issued_par >> q) & 1u, p.status);
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // ---------------- MMA issuer: one partial per K block ----------------
+            int s = 0, j = 0;
+            uint32_t ph = 0, pph = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
+                for (int kb = 0; kb < KB; ++kb) {
+                    if (!wait_phase_fast(full_bar(s), ph, abort_flag, p.status) ||
+                        !wait_phase_fast(pempty_bar(j), pph ^ 1u, abort_flag, p.status)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t d = tmem_base + (uint32_t)(j * BN);
+                    const uint64_t adesc = smem_desc_sw128(smem_u32(sA + s * A_BYTES));
+                    const uint64_t bdesc = smem_desc_sw128(smem_u32(sB + s * B_BYTES));
+#pragma unroll
+                    for (int kk = 0; kk < BK / UMMA_K; ++kk)  // +32 bytes per K=32 slice
+                        mma_e4m3(d, adesc + 2u * kk, bdesc + 2u * kk, IDESC, kk != 0);
+                    mma_commit(empty_bar(s));
+                    mma_commit(pfull_bar(j));
+                    if (++s == STAGES) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                    if (++j == 2) {
+                        j = 0;
+                        pph ^= 1u;
+                    }
+                }
+            }
+            mma_commit(drain_bar);
+            wait_drain(drain_bar, 0, p.status);
+        }
+    } else {
+        // ---------------- epilogue: 8 warps, each (lane group, column half) ----------------
+        const int eg = warp & 3;
+        const int half = (warp - 2) >> 2;
+        const int r = eg * 32 + lane;
+        // the two 64-column chunks of this thread: gate/up halves (SwiGLU) or one 128-column half
+        const int colA = EPI == TC_EPI_SWIGLU ? half * 64 : half * 128;
+        const int colB = EPI == TC_EPI_SWIGLU ? 128 + half * 64 : half * 128 + 64;
+        const int nbA = EPI == TC_EPI_SWIGLU ? 0 : half;  // scale block of each chunk inside the tile
+        const int nbB = EPI == TC_EPI_SWIGLU ? 1 : half;
+        const int nblocks = p.Nb / 128;
+        int j = 0;
+        uint32_t pph = 0;
+        float acc[128];
+        bool ok = true;
+        for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
+            int g, m, n;
+            decode_tile(tile, prefix, G, NT, g, m, n);
+            const int64_t row = (int64_t)gstart[g] + (int64_t)m * BM + r;
+            const bool valid = row < gend[g];
+            const int64_t srow = row < p.M ? row : p.M - 1;  // scale row (rows past M are never stored)
+            const float* sa_row = p.a_scales + srow * p.lda_s;
+            const float* sbA = p.b_scales + ((int64_t)g * nblocks + n * 2 + nbA) * KB;
+            const float* sbB = p.b_scales + ((int64_t)g * nblocks + n * 2 + nbB) * KB;
+#pragma unroll
+            for (int i = 0; i < 128; ++i) acc[i] = 0.0f;
+            float sa_next = __ldg(sa_row), sbA_next = __ldg(sbA), sbB_next = __ldg(sbB);
+            for (int kb = 0; kb < KB; ++kb) {
+                const float fA = sa_next * sbA_next, fB = sa_next * sbB_next;
+                if (kb + 1 < KB) {
+                    sa_next = __ldg(sa_row + kb + 1);
+                    sbA_next = __ldg(sbA + kb + 1);
+                    sbB_next = __ldg(sbB + kb + 1);
+                }
+                if (!__all_sync(0xffffffffu, wait_phase_fast(pfull_bar(j), pph, abort_flag, p.status))) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t taddr = tmem_base + ((uint32_t)(eg * 32) << 16) + (uint32_t)(j * BN);
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {  // column pair q of chunk A and of chunk B
+                    uint32_t va[16], vb[16];
+                    tmem_ld16x2(taddr + colA + 16 * q, taddr + colB + 16 * q, va, vb);
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        acc[16 * q + i] = fmaf(__uint_as_float(va[i]), fA, acc[16 * q + i]);
+                        acc[64 + 16 * q + i] = fmaf(__uint_as_float(vb[i]), fB, acc[64 + 16 * q + i]);
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(pempty_bar(j));
+                if (++j == 2) {
+                    j = 0;
+                    pph ^= 1u;
+                }
+            }
+            if (!ok) break;
+            if (valid) {
+                __nv_bfloat16* C = static_cast<__nv_bfloat16*>(p.C);
+                if (EPI == TC_EPI_SWIGLU) {
+                    float h[64];
+#pragma unroll
+                    for (int i = 0; i < 64; ++i) h[i] = acc[i] / (1.0f + __expf(-acc[i])) * acc[64 + i];
+                    store_row64(C, p.ldc, row, n * 128 + half * 64, p.N, h);
+                } else {
+                    store_row64(C, p.ldc, row, n * BN + colA, p.N, acc);
+                    store_row64(C, p.ldc, row, n * BN + colB, p.N, acc + 64);
+                }
+            }
+        }
+    }
+
+    __syncwarp();
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, TMEM_COLS);
+    }
+}
+
+template <int EPI>
+moe_status_t launch_impl(const TcFp8GroupedGemm& g, cudaStream_t s) {
+    static std::once_flag attr_once[64];
+    int dev = 0;
+    MOE_CUDA_TRY(cudaGetDevice(&dev));
+    cudaError_t attr_err = cudaSuccess;
+    std::call_once(attr_once[dev & 63], [&] {
+        attr_err = cudaFuncSetAttribute(tc_fp8_grouped_gemm_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        (int)SMEM);
+    });
+    MOE_CUDA_TRY(attr_err);
+    CUtensorMap ma, mb;
+    if (!make_map(&ma, g.A, (uint64_t)g.K, (uint64_t)g.M, BM, 1)) return MOE_ERR_CUDA;
+    if (!make_map(&mb, g.B, (uint64_t)g.K, (uint64_t)g.G * g.Nb, BN, 1)) return MOE_ERR_CUDA;
+    Params p;
+    p.offsets = g.offsets;
+    p.G = g.G;
+    p.M = g.M;
+    p.K = g.K;
+    p.Nb = g.Nb;
+    p.N = g.N;
+    p.NT = (int)ceil_div(g.Nb, BN);
+    p.KB = (int)ceil_div(g.K, BK);
+    p.C = g.C;
+    p.ldc = g.ldc;
+    p.a_scales = g.a_scales;
+    p.lda_s = g.lda_scales;
+    p.b_scales = g.b_scales;
+    p.status = g.status;
+    const int64_t max_tiles = (int64_t)p.NT * (ceil_div(g.M, BM) + (g.offsets ? g.G : 0));
+    const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(sm_count(), max_tiles));
+    tc_fp8_grouped_gemm_kernel<EPI><<<grid, kThreads, SMEM, s>>>(ma, mb, p);
+    note_launch();
+    return last_launch_status();
+}
+
+}  // namespace
+
+moe_status_t launch_tc_fp8_grouped_gemm(const TcFp8GroupedGemm& g, cudaStream_t s) {
+    if (g.M == 0 || g.G == 0) return MOE_OK;
+    if (g.G > kMaxGroups) return MOE_ERR_UNSUPPORTED;
+    if (g.Nb % BN != 0 || g.K % 16 != 0) return MOE_ERR_INVALID_ARG;
+    switch (g.epi) {
+        case TC_EPI_SWIGLU: return launch_impl<TC_EPI_SWIGLU>(g, s);
+        case TC_EPI_BF16: return launch_impl<TC_EPI_BF16>(g, s);
+        default: return MOE_ERR_INVALID_ARG;
+    }
+}
+
+}  // namespace moe

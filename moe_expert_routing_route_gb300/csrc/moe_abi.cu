@@ -67,6 +67,28 @@ moe_status_t ffn_down(const void* h, moe_dtype_t dt, const int32_t* offsets, int
                                     H, static_cast<float*>(y), status, s);
 }
 
+// FP8 halves: the up projection (SwiGLU into bf16 h) followed by the 1x128
+// quantisation of h, and the down projection.  Scale rows are padded to a
+// multiple of 4 floats so they can be permuted as 16-byte vectors.
+int scale_ld(int cols) { return (int)round_up((size_t)ceil_div(cols, 128), 4); }
+
+moe_status_t ffn_up_fp8(const uint8_t* aq, const float* as, int lda_s, const int32_t* offsets, int G, int rows, int H,
+                        int I, const void* w13q, const float* w13s, void* h, uint8_t* hq, float* hs,
+                        uint32_t* status, cudaStream_t s) {
+    if (rows == 0) return MOE_OK;
+    TcFp8GroupedGemm up{aq, rows, H, offsets, G, w13q, packed_rows(I), I, h, I, TC_EPI_SWIGLU, as, lda_s,
+                        w13s, status};
+    MOE_TRY(launch_tc_fp8_grouped_gemm(up, s));
+    return launch_quantize_rows_fp8(h, MOE_BF16, rows, I, hq, hs, scale_ld(I), s);
+}
+
+moe_status_t ffn_down_fp8(const uint8_t* hq, const float* hs, const int32_t* offsets, int G, int rows, int H, int I,
+                          const void* w2q, const float* w2s, void* y, uint32_t* status, cudaStream_t s) {
+    if (rows == 0) return MOE_OK;
+    TcFp8GroupedGemm down{hq, rows, I, offsets, G, w2q, H, H, y, H, TC_EPI_BF16, hs, scale_ld(I), w2s, status};
+    return launch_tc_fp8_grouped_gemm(down, s);
+}
+
 moe_status_t gate(const void* x, const void* wr, moe_dtype_t dt, int T, int H, int E, float* logits,
                   cudaStream_t s) {
     if (T == 0) return MOE_OK;
@@ -102,6 +124,18 @@ Layout layout(const moe_layer_desc& d) {
     L.bytes[MOE_WS_Y_SHARED] = T * H * b;
     L.bytes[MOE_WS_X_IN] = T * H * b;
     L.bytes[MOE_WS_OUT] = T * H * b;
+    if (d.weight_format == MOE_WEIGHTS_FP8) {
+        const size_t SI = S * I;
+        L.bytes[MOE_WS_XQ] = T * H;
+        L.bytes[MOE_WS_XQ_SCALES] = T * scale_ld(d.H) * 4;
+        L.bytes[MOE_WS_EXPANDED_XQ] = R * H;
+        L.bytes[MOE_WS_EXPANDED_XQ_SCALES] = R * scale_ld(d.H) * 4;
+        L.bytes[MOE_WS_HQ] = R * I;
+        L.bytes[MOE_WS_HQ_SCALES] = R * scale_ld(d.I) * 4;
+        L.bytes[MOE_WS_HQ_SHARED] = T * SI;
+        L.bytes[MOE_WS_HQ_SHARED_SCALES] = SI ? T * scale_ld((int)SI) * 4 : 0;
+        L.bytes[MOE_WS_EXPANDED_X] = 0;  // the bf16 expanded rows are not used
+    }
     size_t cur = MOE_WS_HEADER_BYTES;
     for (int f = 0; f < MOE_WS_NUM_FIELDS; ++f) {
         L.off[f] = cur;
@@ -132,6 +166,12 @@ moe_status_t check_desc(const moe_layer_desc* d) {
     if (!d->w_router || !d->w13 || !d->w2) return MOE_ERR_INVALID_ARG;
     if (d->S > 0 && (!d->w13_shared || !d->w2_shared)) return MOE_ERR_INVALID_ARG;
     if ((int64_t)d->S * d->I >= INT_MAX / 2) return MOE_ERR_INVALID_ARG;
+    if (d->weight_format != MOE_WEIGHTS_NATIVE && d->weight_format != MOE_WEIGHTS_FP8) return MOE_ERR_INVALID_ARG;
+    if (d->weight_format == MOE_WEIGHTS_FP8) {
+        if (d->dtype != MOE_BF16 || d->H % 256 != 0 || d->I % 16 != 0) return MOE_ERR_UNSUPPORTED;
+        if (!d->w13_scales || !d->w2_scales) return MOE_ERR_INVALID_ARG;
+        if (d->S > 0 && (!d->w13_shared_scales || !d->w2_shared_scales)) return MOE_ERR_INVALID_ARG;
+    }
     if (!aligned16(d->w_router) || !aligned16(d->w13) || !aligned16(d->w2) || !aligned16(d->expert_bias) ||
         !aligned16(d->w13_shared) || !aligned16(d->w2_shared))
         return MOE_ERR_UNSUPPORTED;
@@ -214,6 +254,17 @@ moe_status_t layer_forward(const moe_layer_desc* d, const void* x, void* out, vo
     void* ys = at<void>(ws, L.off[MOE_WS_Y_SHARED]);
     int32_t* scratch = at<int32_t>(ws, L.scratch_off);
 
+    const bool fp8 = d->weight_format == MOE_WEIGHTS_FP8;
+    uint8_t* xq = at<uint8_t>(ws, L.off[MOE_WS_XQ]);
+    float* xs = at<float>(ws, L.off[MOE_WS_XQ_SCALES]);
+    uint8_t* exq = at<uint8_t>(ws, L.off[MOE_WS_EXPANDED_XQ]);
+    float* exs = at<float>(ws, L.off[MOE_WS_EXPANDED_XQ_SCALES]);
+    uint8_t* hq = at<uint8_t>(ws, L.off[MOE_WS_HQ]);
+    float* hqs = at<float>(ws, L.off[MOE_WS_HQ_SCALES]);
+    uint8_t* hsq = at<uint8_t>(ws, L.off[MOE_WS_HQ_SHARED]);
+    float* hss = at<float>(ws, L.off[MOE_WS_HQ_SHARED_SCALES]);
+    const int ldx = scale_ld(H);
+
     SideStream* side = nullptr;
     if (SI > 0) MOE_TRY(side_stream(&side));
     std::unique_lock<std::mutex> side_lock;
@@ -222,6 +273,7 @@ moe_status_t layer_forward(const moe_layer_desc* d, const void* x, void* out, vo
     MOE_TRY(clear_status(ws, s));
     MOE_TRY(mark(ev, ST_GATE, 0, s));
     MOE_TRY(gate(x, d->w_router, dt, T, H, E, logits, s));
+    if (fp8) MOE_TRY(launch_quantize_rows_fp8(x, dt, T, H, xq, xs, ldx, s));  // activations, 1x128 blocks
     MOE_TRY(mark(ev, ST_GATE, 1, s));
     if (side) {
         // fork: shared experts on the side stream, after the gate
@@ -229,8 +281,14 @@ moe_status_t layer_forward(const moe_layer_desc* d, const void* x, void* out, vo
         MOE_CUDA_TRY(cudaStreamWaitEvent(side->stream, side->fork, 0));
         cudaStream_t ss = side->stream;
         MOE_TRY(mark(ev, ST_SHARED, 0, ss));
-        MOE_TRY(ffn_up(x, dt, nullptr, 1, T, H, SI, d->w13_shared, hs, status, ss));
-        MOE_TRY(ffn_down(hs, dt, nullptr, 1, T, H, SI, d->w2_shared, ys, status, ss));
+        if (fp8) {
+            MOE_TRY(ffn_up_fp8(xq, xs, ldx, nullptr, 1, T, H, SI, d->w13_shared, d->w13_shared_scales, hs, hsq, hss,
+                               status, ss));
+            MOE_TRY(ffn_down_fp8(hsq, hss, nullptr, 1, T, H, SI, d->w2_shared, d->w2_shared_scales, ys, status, ss));
+        } else {
+            MOE_TRY(ffn_up(x, dt, nullptr, 1, T, H, SI, d->w13_shared, hs, status, ss));
+            MOE_TRY(ffn_down(hs, dt, nullptr, 1, T, H, SI, d->w2_shared, ys, status, ss));
+        }
         MOE_TRY(mark(ev, ST_SHARED, 1, ss));
         MOE_CUDA_TRY(cudaEventRecord(side->join, ss));
     } else {
@@ -245,15 +303,22 @@ moe_status_t layer_forward(const moe_layer_desc* d, const void* x, void* out, vo
     MOE_TRY(launch_init_routing_index(ids, R, E, counts, offsets, row_idx, scratch, status, s));
     MOE_TRY(mark(ev, ST_INIT, 1, s));
     MOE_TRY(mark(ev, ST_PERMUTE, 0, s));
-    MOE_TRY(launch_permute_rows(x, (size_t)H * dt_size(dt), row_idx, T, k, ex, s));
+    if (fp8) {
+        MOE_TRY(launch_permute_rows(xq, (size_t)H, row_idx, T, k, exq, s));
+        MOE_TRY(launch_permute_rows(xs, (size_t)ldx * 4, row_idx, T, k, exs, s));
+    } else {
+        MOE_TRY(launch_permute_rows(x, (size_t)H * dt_size(dt), row_idx, T, k, ex, s));
+    }
     MOE_TRY(mark(ev, ST_PERMUTE, 1, s));
     // join: the routed GEMMs need every SM, so they start after the shared experts
     if (side) MOE_CUDA_TRY(cudaStreamWaitEvent(s, side->join, 0));
     MOE_TRY(mark(ev, ST_UP, 0, s));
-    MOE_TRY(ffn_up(ex, dt, offsets, E, R, H, I, d->w13, h, status, s));
+    if (fp8) MOE_TRY(ffn_up_fp8(exq, exs, ldx, offsets, E, R, H, I, d->w13, d->w13_scales, h, hq, hqs, status, s));
+    else MOE_TRY(ffn_up(ex, dt, offsets, E, R, H, I, d->w13, h, status, s));
     MOE_TRY(mark(ev, ST_UP, 1, s));
     MOE_TRY(mark(ev, ST_DOWN, 0, s));
-    MOE_TRY(ffn_down(h, dt, offsets, E, R, H, I, d->w2, y, status, s));
+    if (fp8) MOE_TRY(ffn_down_fp8(hq, hqs, offsets, E, R, H, I, d->w2, d->w2_scales, y, status, s));
+    else MOE_TRY(ffn_down(h, dt, offsets, E, R, H, I, d->w2, y, status, s));
     MOE_TRY(mark(ev, ST_DOWN, 1, s));
     MOE_TRY(mark(ev, ST_FINALIZE, 0, s));
     MOE_TRY(launch_finalize(y, R, SI > 0 ? ys : nullptr, w, row_idx, dt, T, H, k, out, status, s));
@@ -284,6 +349,7 @@ EpLayout ep_layout(const moe_layer_desc& d, int W, const Layout& L) {
 
 moe_status_t check_ep(const moe_layer_desc* d, int W) {
     MOE_TRY(check_desc(d));
+    if (d->weight_format != MOE_WEIGHTS_NATIVE) return MOE_ERR_UNSUPPORTED;
     if (W < 1 || W > 32 || d->T % W != 0 || d->E % W != 0) return MOE_ERR_INVALID_ARG;
     return MOE_OK;
 }
@@ -464,6 +530,49 @@ moe_status_t moe_unsort_rows(const void* y_sorted, moe_dtype_t dt, const int32_t
     MOE_TRY(clear_status(ws, s));
     return launch_unsort_rows(y_sorted, (size_t)H * dt_size(dt), gathered_ids_unsort, N, out,
                               ws ? status_word(ws) : nullptr, s);
+}
+
+moe_status_t moe_quantize_rows_fp8(const void* a, moe_dtype_t dt, int64_t rows, int cols, uint8_t* codes,
+                                   float* scales, int ld_scales, moe_stream_t stream) {
+    if (bad_dtype(dt) || rows < 0 || cols <= 0 || ld_scales < (cols + 127) / 128) return MOE_ERR_INVALID_ARG;
+    if (rows == 0) return MOE_OK;
+    if (!a || !codes || !scales) return MOE_ERR_INVALID_ARG;
+    return launch_quantize_rows_fp8(a, dt, rows, cols, codes, scales, ld_scales, reinterpret_cast<cudaStream_t>(stream));
+}
+
+moe_status_t moe_quantize_weights_fp8(const void* w, moe_dtype_t dt, int G, int n_out, int k_in, uint8_t* codes,
+                                      float* scales, moe_stream_t stream) {
+    if (bad_dtype(dt) || G <= 0 || n_out <= 0 || k_in <= 0) return MOE_ERR_INVALID_ARG;
+    if (!w || !codes || !scales) return MOE_ERR_INVALID_ARG;
+    return launch_quantize_tiles_fp8(w, dt, G, n_out, k_in, codes, scales, reinterpret_cast<cudaStream_t>(stream));
+}
+
+size_t moe_grouped_ffn_fp8_workspace_bytes(int rows, int I) {
+    if (rows < 0 || I <= 0) return 0;
+    return MOE_WS_HEADER_BYTES + round_up((size_t)rows * I * 2, kAlign) + round_up((size_t)rows * I, kAlign) +
+           round_up((size_t)rows * scale_ld(I) * 4, kAlign);
+}
+
+moe_status_t moe_grouped_ffn_fp8(const uint8_t* aq, const float* a_scales, int lda_scales,
+                                 const int32_t* expert_offsets, int E, int rows, int H, int I, const uint8_t* w13q,
+                                 const float* w13s, const uint8_t* w2q, const float* w2s, void* y, void* ws,
+                                 size_t ws_bytes, moe_stream_t stream) {
+    if (rows < 0 || H <= 0 || I <= 0 || E <= 0 || E > 1024 || lda_scales < (H + 127) / 128) return MOE_ERR_INVALID_ARG;
+    if (!expert_offsets && E != 1) return MOE_ERR_INVALID_ARG;
+    if (H % 256 != 0 || I % 16 != 0) return MOE_ERR_UNSUPPORTED;
+    if (!ws || ws_bytes < moe_grouped_ffn_fp8_workspace_bytes(rows, I)) return MOE_ERR_INVALID_ARG;
+    if (rows > 0 && (!aq || !a_scales || !w13q || !w13s || !w2q || !w2s || !y)) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(aq) || !aligned16(w13q) || !aligned16(w2q) || !aligned16(y) || !aligned16(ws))
+        return MOE_ERR_UNSUPPORTED;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    MOE_TRY(clear_status(ws, s));
+    void* h = at<void>(ws, MOE_WS_HEADER_BYTES);
+    uint8_t* hq = at<uint8_t>(ws, MOE_WS_HEADER_BYTES + round_up((size_t)rows * I * 2, kAlign));
+    float* hs = at<float>(ws, MOE_WS_HEADER_BYTES + round_up((size_t)rows * I * 2, kAlign) +
+                                  round_up((size_t)rows * I, kAlign));
+    MOE_TRY(ffn_up_fp8(aq, a_scales, lda_scales, expert_offsets, E, rows, H, I, w13q, w13s, h, hq, hs, status_word(ws),
+                       s));
+    return ffn_down_fp8(hq, hs, expert_offsets, E, rows, H, I, w2q, w2s, y, status_word(ws), s);
 }
 
 size_t moe_init_routing_workspace_bytes(int T, int E, int k) {

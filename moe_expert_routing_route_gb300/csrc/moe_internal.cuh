@@ -82,6 +82,12 @@ moe_status_t ep_route_and_dispatch(const EpBuffers& b, cudaStream_t s);
 const int32_t* ep_rank_offsets(const EpBuffers& b, int q);  // [E/W + 1] rows of rank q's experts in `sorted`
 moe_status_t ep_combine(const EpBuffers& b, const void* y_sorted, void* y_recv, void* y_expanded, cudaStream_t s);
 
+// quant.cu: FP8 (e4m3) block quantisation.
+moe_status_t launch_quantize_rows_fp8(const void* a, moe_dtype_t dt, int64_t rows, int cols, uint8_t* codes,
+                                      float* scales, int ld_scales, cudaStream_t s);
+moe_status_t launch_quantize_tiles_fp8(const void* w, moe_dtype_t dt, int G, int rows, int cols, uint8_t* codes,
+                                       float* scales, cudaStream_t s);
+
 // finalize.cu
 moe_status_t launch_finalize(const void* y, int64_t y_rows, const void* skip, const float* w,
                              const int32_t* row_idx, moe_dtype_t dt, int T, int H, int k, void* out,
@@ -104,6 +110,26 @@ struct TcGroupedGemm {
     uint32_t* status;
 };
 moe_status_t launch_tc_grouped_gemm(const TcGroupedGemm& g, cudaStream_t s);
+
+// gemm_fp8.cu: e4m3 block-scaled grouped GEMM (bf16 out), C = A B^T per group.
+struct TcFp8GroupedGemm {
+    const void* A;            // [M, K] e4m3 codes
+    int M;
+    int K;
+    const int32_t* offsets;   // [G+1] device, or nullptr for one group [0, M)
+    int G;
+    const void* B;            // [G * Nb, K] e4m3 codes
+    int Nb;                   // B rows per group (a multiple of 256)
+    int N;                    // valid output columns per group
+    void* C;                  // bf16 output
+    int64_t ldc;
+    TcEpilogue epi;           // TC_EPI_SWIGLU or TC_EPI_BF16
+    const float* a_scales;    // [M][lda_scales]: one per 1x128 block of A
+    int lda_scales;
+    const float* b_scales;    // [G][Nb/128][ceil(K/128)]: one per 128x128 tile of B
+    uint32_t* status;
+};
+moe_status_t launch_tc_fp8_grouped_gemm(const TcFp8GroupedGemm& g, cudaStream_t s);
 int tc_packed_block();        // rows of gate (and of up) per packed block: 128
 
 // gemm_simt.cu: fp32 (FFMA) GEMMs of the same shapes.

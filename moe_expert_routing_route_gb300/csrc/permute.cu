@@ -48,11 +48,33 @@ hist_kernel(const int32_t* __restrict__ ids, int R, int E, int NW, int32_t* __re
     for (int e = threadIdx.x; e < E; e += kChunkThreads) hist[(size_t)c * E + e] = sh[e];
 }
 
-// Exclusive scan of up to 1024 values held one per thread; returns the
-// exclusive prefix of thread tid and writes the total to *total.
-__device__ int block_exclusive_scan_1024(int v, int* warp_tot, int* total) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    int incl = v;
+// 256 threads: small enough in registers and threads to run beside a resident
+// tensor-core GEMM CTA (the shared experts run concurrently on another stream).
+constexpr int kScanThreads = 256;
+
+__global__ void __launch_bounds__(kScanThreads)
+scan_kernel(int32_t* __restrict__ hist, int NW, int E, int32_t* __restrict__ counts,
+            int32_t* __restrict__ offsets) {
+    __shared__ int cnt[1024];
+    __shared__ int warp_tot[kScanThreads / 32];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    // per-expert totals over the chunks (coalesced across experts)
+    for (int e = tid; e < E; e += kScanThreads) {
+        int sum = 0;
+        for (int c = 0; c < NW; ++c) sum += hist[(size_t)c * E + e];
+        cnt[e] = sum;
+        counts[e] = sum;
+    }
+    __syncthreads();
+    // exclusive scan over experts: 4 consecutive experts per thread, then across threads
+    const int e0 = tid * 4;
+    int loc[4], run = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        loc[i] = run;
+        run += e0 + i < E ? cnt[e0 + i] : 0;
+    }
+    int incl = run;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
         const int n = __shfl_up_sync(0xffffffffu, incl, off);
@@ -60,66 +82,24 @@ __device__ int block_exclusive_scan_1024(int v, int* warp_tot, int* total) {
     }
     if (lane == 31) warp_tot[warp] = incl;
     __syncthreads();
-    if (warp == 0) {
-        const int wv = lane < (int)(blockDim.x >> 5) ? warp_tot[lane] : 0;
-        int wincl = wv;
+    int wbase = 0;
+    for (int w = 0; w < warp; ++w) wbase += warp_tot[w];
+    const int tbase = wbase + incl - run;
+    __syncthreads();
 #pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-            const int n = __shfl_up_sync(0xffffffffu, wincl, off);
-            if (lane >= off) wincl += n;
-        }
-        warp_tot[lane] = wincl - wv;  // exclusive prefix of warp totals
-        if (lane == 31) *total = wincl;
-    }
+    for (int i = 0; i < 4; ++i)
+        if (e0 + i < E) cnt[e0 + i] = tbase + loc[i];
+    if (tid == kScanThreads - 1) offsets[E] = tbase + run;
     __syncthreads();
-    return warp_tot[warp] + incl - v;
-}
-
-__global__ void __launch_bounds__(1024)
-scan_kernel(int32_t* __restrict__ hist, int NW, int E, int32_t* __restrict__ counts,
-            int32_t* __restrict__ offsets) {
-    __shared__ int part[1024];
-    __shared__ int warp_tot[32];
-    __shared__ int total;
-    const int tid = threadIdx.x;
-    const int P = max(1, 1024 / E);  // parts per expert along the chunk axis
-    const bool active = tid < P * E;
-    const int e = tid % E, p = tid / E;
-    const int per = (NW + P - 1) / P;
-    const int c0 = min(NW, p * per), c1 = min(NW, c0 + per);
-
-    int sum = 0;
-    if (active)
-        for (int c = c0; c < c1; ++c) sum += hist[(size_t)c * E + e];
-    part[tid] = active ? sum : 0;
-    __syncthreads();
-    int cnt = 0;
-    if (tid < E) {
-        int run = 0;
-        for (int q = 0; q < P; ++q) {
-            const int v = part[q * E + tid];
-            part[q * E + tid] = run;
-            run += v;
-        }
-        cnt = run;
-        counts[tid] = run;
-    }
-    __syncthreads();
-    const int excl = block_exclusive_scan_1024(tid < E ? cnt : 0, warp_tot, &total);
-    __shared__ int base_sh[1024];
-    if (tid < E) {
-        base_sh[tid] = excl;
-        offsets[tid] = excl;
-    }
-    if (tid == 0) offsets[E] = total;
-    __syncthreads();
-    if (active) {
-        int run = base_sh[e] + part[tid];
-        for (int c = c0; c < c1; ++c) {
+    // first destination row of every (chunk, expert), in chunk order inside an expert
+    for (int e = tid; e < E; e += kScanThreads) {
+        offsets[e] = cnt[e];
+        int r = cnt[e];
+        for (int c = 0; c < NW; ++c) {
             const size_t i = (size_t)c * E + e;
             const int v = hist[i];
-            hist[i] = run;
-            run += v;
+            hist[i] = r;
+            r += v;
         }
     }
 }
@@ -239,7 +219,7 @@ moe_status_t launch_init_routing_index(const int32_t* ids, int R, int E, int32_t
         note_launch();
         MOE_TRY(last_launch_status());
     }
-    scan_kernel<<<1, 1024, 0, s>>>(scratch, NW, E, counts, offsets);
+    scan_kernel<<<1, kScanThreads, 0, s>>>(scratch, NW, E, counts, offsets);
     note_launch();
     MOE_TRY(last_launch_status());
     if (NW > 0) {

@@ -1,0 +1,143 @@
+// FP8 (e4m3) block quantisation.
+//
+// "Lower latency and higher throughput with multi-node DeepSeek deployment"
+// (Perplexity blog), §Quantization: DeepSeek-V3/R1 quantises per block, with
+// scales per 128-element vector for activations (computed on the fly) and per
+// 128x128 tile for weights (static).  A block's scale is amax/448 in fp32 (1
+// for an all-zero block); each value becomes the e4m3 code of fl32(v / scale),
+// rounded to nearest even and saturated at +-448.
+#include "moe_internal.cuh"
+
+#include <cuda_fp8.h>
+
+namespace moe {
+namespace {
+
+__device__ __forceinline__ float to_f(__nv_bfloat16 v) { return __bfloat162float(v); }
+__device__ __forceinline__ float to_f(float v) { return v; }
+__device__ __forceinline__ uint32_t e4m3(float v) {
+    return (uint32_t)__nv_cvt_float_to_fp8(v, __NV_SATFINITE, __NV_E4M3);
+}
+__device__ __forceinline__ float block_scale(float amax) { return amax > 0.0f ? amax / 448.0f : 1.0f; }
+
+__device__ __forceinline__ void load4(const __nv_bfloat16* p, float (&v)[4]) {
+    const uint2 u = __ldg(reinterpret_cast<const uint2*>(p));
+    v[0] = __uint_as_float(u.x << 16);
+    v[1] = __uint_as_float(u.x & 0xffff0000u);
+    v[2] = __uint_as_float(u.y << 16);
+    v[3] = __uint_as_float(u.y & 0xffff0000u);
+}
+__device__ __forceinline__ void load4(const float* p, float (&v)[4]) {
+    const float4 f = __ldg(reinterpret_cast<const float4*>(p));
+    v[0] = f.x;
+    v[1] = f.y;
+    v[2] = f.z;
+    v[3] = f.w;
+}
+
+// One warp per (row, 128-column block), four values per lane.
+template <typename T>
+__global__ void __launch_bounds__(256)
+quantize_rows_kernel(const T* __restrict__ a, int64_t rows, int cols, int kb, int ld_scales,
+                     uint8_t* __restrict__ codes, float* __restrict__ scales) {
+    const int lane = threadIdx.x & 31;
+    const int64_t nw = (int64_t)gridDim.x * (blockDim.x / 32);
+    for (int64_t item = (int64_t)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5); item < rows * kb;
+         item += nw) {
+        const int64_t r = item / kb;
+        const int b = (int)(item - r * kb);
+        const int c0 = b * 128 + lane * 4;
+        const T* row = a + r * cols;
+        float v[4];
+        if (c0 + 4 <= cols && (cols & 3) == 0) {
+            load4(row + c0, v);  // one 8- or 16-byte load
+        } else {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) v[i] = c0 + i < cols ? to_f(row[c0 + i]) : 0.0f;
+        }
+        float amax = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) amax = fmaxf(amax, fabsf(v[i]));
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+        const float s = block_scale(amax);
+        uint8_t* crow = codes + r * cols;
+        if (c0 + 4 <= cols && (cols & 3) == 0) {
+            uint32_t packed = 0;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) packed |= e4m3(v[i] / s) << (8 * i);
+            *reinterpret_cast<uint32_t*>(crow + c0) = packed;
+        } else {
+            for (int i = 0; i < 4; ++i)
+                if (c0 + i < cols) crow[c0 + i] = (uint8_t)e4m3(v[i] / s);
+        }
+        if (lane == 0) scales[r * ld_scales + b] = s;
+    }
+}
+
+// One block per 128x128 tile of a [G][rows][cols] matrix.
+template <typename T>
+__global__ void __launch_bounds__(256)
+quantize_tiles_kernel(const T* __restrict__ w, int rows, int cols, int nb, int kb, uint8_t* __restrict__ codes,
+                      float* __restrict__ scales) {
+    __shared__ float red[8];
+    const int64_t tile = blockIdx.x;
+    const int64_t g = tile / ((int64_t)nb * kb);
+    const int bn = (int)((tile / kb) % nb), bk = (int)(tile % kb);
+    const int r0 = bn * 128, c0 = bk * 128;
+    const int r1 = min(rows, r0 + 128), c1 = min(cols, c0 + 128);
+    const T* base = w + g * rows * (int64_t)cols;
+    float amax = 0.0f;
+    for (int i = threadIdx.x; i < 128 * 128; i += blockDim.x) {
+        const int r = r0 + i / 128, c = c0 + i % 128;
+        if (r < r1 && c < c1) amax = fmaxf(amax, fabsf(to_f(base[(int64_t)r * cols + c])));
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = amax;
+    __syncthreads();
+    amax = red[0];
+    for (int i = 1; i < (int)(blockDim.x >> 5); ++i) amax = fmaxf(amax, red[i]);
+    const float s = block_scale(amax);
+    uint8_t* cbase = codes + g * rows * (int64_t)cols;
+    for (int i = threadIdx.x; i < 128 * 128; i += blockDim.x) {
+        const int r = r0 + i / 128, c = c0 + i % 128;
+        if (r < r1 && c < c1) cbase[(int64_t)r * cols + c] = (uint8_t)e4m3(to_f(base[(int64_t)r * cols + c]) / s);
+    }
+    if (threadIdx.x == 0) scales[(g * nb + bn) * kb + bk] = s;
+}
+
+}  // namespace
+
+moe_status_t launch_quantize_rows_fp8(const void* a, moe_dtype_t dt, int64_t rows, int cols, uint8_t* codes,
+                                      float* scales, int ld_scales, cudaStream_t s) {
+    if (rows == 0) return MOE_OK;
+    const int kb = (cols + 127) / 128;
+    const int64_t items = rows * kb;
+    const int grid = (int)std::min<int64_t>(ceil_div(items, 8), (int64_t)sm_count() * 16);
+    if (dt == MOE_BF16)
+        quantize_rows_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(a), rows, cols, kb,
+                                                                 ld_scales, codes, scales);
+    else
+        quantize_rows_kernel<float><<<grid, 256, 0, s>>>(static_cast<const float*>(a), rows, cols, kb, ld_scales,
+                                                         codes, scales);
+    note_launch();
+    return last_launch_status();
+}
+
+moe_status_t launch_quantize_tiles_fp8(const void* w, moe_dtype_t dt, int G, int rows, int cols, uint8_t* codes,
+                                       float* scales, cudaStream_t s) {
+    const int nb = (rows + 127) / 128, kb = (cols + 127) / 128;
+    const int64_t tiles = (int64_t)G * nb * kb;
+    if (tiles == 0) return MOE_OK;
+    if (dt == MOE_BF16)
+        quantize_tiles_kernel<__nv_bfloat16><<<(unsigned)tiles, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(w),
+                                                                             rows, cols, nb, kb, codes, scales);
+    else
+        quantize_tiles_kernel<float><<<(unsigned)tiles, 256, 0, s>>>(static_cast<const float*>(w), rows, cols, nb, kb,
+                                                                     codes, scales);
+    note_launch();
+    return last_launch_status();
+}
+
+}  // namespace moe

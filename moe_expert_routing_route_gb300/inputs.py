@@ -42,6 +42,7 @@ class LayerConfig:
     n_group: int = 1          # > 1: group-limited routing
     topk_group: int = 1
     group_rule: str = "max"   # "max" | "top2_sum"
+    weight_format: str = "native"  # "native" | "fp8" (e4m3 expert weights, 128x128 tile scales)
 
     @property
     def R(self) -> int:
@@ -74,6 +75,13 @@ CONFIGS = {
     # experts, 4 groups kept, group score = sum of its two best scores).
     "dsv3_prefill_grouped": LayerConfig("dsv3_prefill_grouped", T=4096, H=7168, E=256, k=8, I=2048, S=1,
                                         dtype="bf16", seed=2, n_group=8, topk_group=4, group_rule="top2_sum"),
+    # The prefill and decode layers with FP8 (e4m3) block-quantised expert weights.
+    "dsv3_prefill_fp8": LayerConfig("dsv3_prefill_fp8", T=4096, H=7168, E=256, k=8, I=2048, S=1, dtype="bf16",
+                                    seed=2, weight_format="fp8"),
+    "dsv3_decode_fp8": LayerConfig("dsv3_decode_fp8", T=128, H=7168, E=256, k=8, I=2048, S=1, dtype="bf16",
+                                   seed=3, weight_format="fp8"),
+    "dsv3_prefill_slice_fp8": LayerConfig("dsv3_prefill_slice_fp8", T=512, H=7168, E=32, k=8, I=2048, S=1,
+                                          dtype="bf16", seed=2, weight_format="fp8"),
     # Profiling slice: the DeepSeek-V3 prefill layer's per-expert shape (about 128 rows
     # per expert) on 32 experts, small enough for ncu captures (~5 GB on the device).
     "dsv3_prefill_slice": LayerConfig("dsv3_prefill_slice", T=512, H=7168, E=32, k=8, I=2048, S=1,

@@ -35,25 +35,40 @@ def balanced_tokens_per_expert(batch: int, q_len: int, top_k: int, ranks: int, e
     return batch * q_len * top_k * ranks / experts
 
 
-def gemm_part_costs(T: int, H: int, E: int, k: int, I: int, S: int, esize: int, touched: int) -> dict:
-    """{part: (flops, bytes)} of the four expert GEMMs: up/down x routed/shared."""
+def gemm_part_costs(T: int, H: int, E: int, k: int, I: int, S: int, esize: int, touched: int,
+                    weight_bytes: int | None = None) -> dict:
+    """{part: (flops, bytes)} of the four expert GEMMs: up/down x routed/shared.
+
+    weight_bytes = 1 (FP8): weights and GEMM inputs are e4m3 codes (plus one fp32
+    scale per 128x128 weight tile and per 1x128 input block); outputs stay esize."""
     R = T * k
     b = esize
     SI = S * I
+    if weight_bytes is None:
+        return {
+            "up_routed": (2 * R * H * 2 * I, touched * 2 * I * H * b + R * H * b + R * I * b),
+            "up_shared": (2 * T * H * 2 * SI, (2 * SI * H + T * H + T * SI) * b if S else 0),
+            "down_routed": (2 * R * I * H, touched * H * I * b + R * I * b + R * H * b),
+            "down_shared": (2 * T * SI * H, (H * SI + T * SI + T * H) * b if S else 0),
+        }
+    wb = weight_bytes
+    ws = lambda n, kk: n * kk * wb + (n // 128) * ((kk + 127) // 128) * 4  # noqa: E731  codes + tile scales
+    xs = lambda rows, kk: rows * kk * wb + rows * ((kk + 127) // 128) * 4  # noqa: E731  codes + block scales
     return {
-        "up_routed": (2 * R * H * 2 * I, touched * 2 * I * H * b + R * H * b + R * I * b),
-        "up_shared": (2 * T * H * 2 * SI, (2 * SI * H + T * H + T * SI) * b if S else 0),
-        "down_routed": (2 * R * I * H, touched * H * I * b + R * I * b + R * H * b),
-        "down_shared": (2 * T * SI * H, (H * SI + T * SI + T * H) * b if S else 0),
+        "up_routed": (2 * R * H * 2 * I, touched * ws(2 * I, H) + xs(R, H) + R * I * b),
+        "up_shared": (2 * T * H * 2 * SI, (ws(2 * SI, H) + xs(T, H) + T * SI * b) if S else 0),
+        "down_routed": (2 * R * I * H, touched * ws(H, I) + xs(R, I) + R * H * b),
+        "down_shared": (2 * T * SI * H, (ws(H, SI) + xs(T, SI) + T * H * b) if S else 0),
     }
 
 
-def stage_costs(T: int, H: int, E: int, k: int, I: int, S: int, esize: int, touched: int) -> dict:
+def stage_costs(T: int, H: int, E: int, k: int, I: int, S: int, esize: int, touched: int,
+                weight_bytes: int | None = None) -> dict:
     """{stage: (flops, bytes)} for the eight layer stages.  touched = experts with >= 1 row.
     "shared" is both projections of the shared experts; "up"/"down" the routed ones."""
     R = T * k
     b = esize
-    g = gemm_part_costs(T, H, E, k, I, S, esize, touched)
+    g = gemm_part_costs(T, H, E, k, I, S, esize, touched, weight_bytes)
     add = lambda a, c: (a[0] + c[0], a[1] + c[1])  # noqa: E731
     return {
         "gate": (2 * T * H * E, T * H * b + E * H * b + T * E * 4),
@@ -84,10 +99,13 @@ def load_peaks(path: str | None = None) -> dict:
     return dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0, source="fallback")
 
 
-def roofline_entry(flops: float, nbytes: float, seconds: float, peaks: dict, sustained: bool = True) -> dict:
+def roofline_entry(flops: float, nbytes: float, seconds: float, peaks: dict, sustained: bool = True,
+                   tensor_scale: float = 1.0) -> dict:
     """The binding roofline of one kernel: whichever of compute time at the
-    tensor peak and byte time at HBM bandwidth is larger."""
-    tf = peaks["bf16_tflops_sustained"] if sustained else peaks["bf16_tflops"]
+    tensor peak and byte time at HBM bandwidth is larger.  tensor_scale converts
+    the measured bf16 peak to another operand type's (FP8: 2, the nominal
+    4.5/2.25 PFLOP/s ratio)."""
+    tf = (peaks["bf16_tflops_sustained"] if sustained else peaks["bf16_tflops"]) * tensor_scale
     t_compute = flops / (tf * 1e12) if flops else 0.0
     t_bytes = nbytes / (peaks["hbm_gbs"] * 1e9)
     if t_compute > t_bytes:

@@ -66,6 +66,7 @@ def _load():
         lib.oracle_quantize_rows_fp8.argtypes = [P, I, L, I, P, P]
         lib.oracle_quantize_tiles_fp8.argtypes = [P, I, I, I, P, P]
         lib.oracle_gemm_fp8.argtypes = [P, P, P, P, I, I, I, P]
+        lib.oracle_expert_ffn_rows_fp8.argtypes = [P, P, L, P, P, P, P, P, P, P, I, I, P]
         lib.oracle_layer_fp8.argtypes = [P, I, I, I, I, I, I, I, P, P] + [P] * 12 + [P, I, P, P, P, P, I, I, I]
         lib.oracle_unsort_rows.argtypes = [P, I, P, L, I, P]
         lib.oracle_finalize_routing.argtypes = [P, I, L, P, P, P, I, I, I, P]
@@ -250,6 +251,19 @@ def quantize_experts_fp8(w: np.ndarray):
     E = w.shape[0]
     pairs = [quantize_tiles_fp8(w[e]) for e in range(E)]
     return np.stack([p[0] for p in pairs]), np.stack([p[1] for p in pairs])
+
+
+def expert_ffn_rows_fp8(xq, xs, expert, q: dict) -> np.ndarray:
+    """y[r] = FP8 SwiGLU expert expert[r] on quantised row r, stored in bf16 (fp64 out)."""
+    xq, xs = _c(xq, np.uint8), _c(xs, np.float32)
+    expert = _c(expert, np.int32)
+    n, H = xq.shape
+    I = q["gq"].shape[1]
+    assert xs.shape[1] == (H + 127) // 128
+    arrs = [_c(q[k_], np.uint8 if k_.endswith("q") else np.float32) for k_ in ("gq", "gs", "uq", "us", "dq", "ds")]
+    y = np.zeros((n, H), np.float64)
+    _load().oracle_expert_ffn_rows_fp8(_ptr(xq), _ptr(xs), n, _ptr(expert), *[_ptr(a) for a in arrs], H, I, _ptr(y))
+    return y
 
 
 def layer_fp8(x, wg, q: dict, *, k: int, renorm: bool = True, bias=None, tokens=None, n_group: int = 1,

@@ -564,6 +564,34 @@ static void expert_ffn_row_fp8(const uint8_t* xq, const float* xs, const uint8_t
     for (int o = 0; o < H; ++o) y[o] = fp8_dot(hq, hs, dq + (size_t)o * I, ds + (size_t)(o / 128) * kbi, I);
 }
 
+/* Expert FFN on quantised rows: y[r] = FFN_fp8_{expert[r]}(xq[r]) stored in bf16
+ * (rows with expert < 0 untouched).  xs [n][ceil(H/128)]; weights per expert as
+ * in oracle_layer_fp8.                                                        */
+void oracle_expert_ffn_rows_fp8(const uint8_t* xq, const float* xs, int64_t n, const int32_t* expert,
+                                const uint8_t* gq, const float* gs, const uint8_t* uq, const float* us,
+                                const uint8_t* dq, const float* ds, int H, int I, double* y) {
+    init_e4m3();
+    const int kbh = (H + 127) / 128, kbi = (I + 127) / 128;
+    const size_t gsz = (size_t)kbi * kbh;
+    #pragma omp parallel
+    {
+        double* hbuf = (double*)malloc(sizeof(double) * (size_t)I);
+        uint8_t* hq = (uint8_t*)malloc((size_t)I);
+        float* hs = (float*)malloc(sizeof(float) * (size_t)kbi);
+        double* yr = (double*)malloc(sizeof(double) * (size_t)H);
+        #pragma omp for schedule(dynamic, 1)
+        for (int64_t r = 0; r < n; ++r) {
+            int e = expert[r];
+            if (e < 0) continue;
+            expert_ffn_row_fp8(xq + (size_t)r * H, xs + (size_t)r * kbh, gq + (size_t)e * I * H, gs + e * gsz,
+                               uq + (size_t)e * I * H, us + e * gsz, dq + (size_t)e * H * I, ds + e * gsz, H, I,
+                               hbuf, hq, hs, yr);
+            for (int o = 0; o < H; ++o) y[(size_t)r * H + o] = round_to(yr[o], OR_BF16);
+        }
+        free(hbuf); free(hq); free(hs); free(yr);
+    }
+}
+
 /* The layer with FP8 expert weights (bf16 activations and outputs), brute force
  * per token: bf16 gate logits and routing exactly as oracle_layer, x quantised
  * in 1x128 blocks, each expert (routed and shared) through expert_ffn_row_fp8,

@@ -1,0 +1,152 @@
+"""GPU parity of the FP8 (e4m3, block-scaled) path against the CPU oracle, through
+the C ABI: quantisers bit for bit, the FP8 grouped FFN and the FP8-weight layer
+within the bf16 tolerance of the oracle's FP8 definition."""
+import numpy as np
+import pytest
+import torch
+
+from moe_expert_routing_route_gb300 import binding, inputs
+from tests._cmp import f64, np_, rel_l2, routing_ambiguity
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    import __graft_entry__
+    __graft_entry__.build_library()
+    binding.lib()
+
+
+@pytest.mark.parametrize("rows,cols,dtype", [(1, 128, torch.bfloat16), (37, 7168, torch.bfloat16),
+                                             (100, 300, torch.float32), (5, 2048, torch.bfloat16),
+                                             (64, 40, torch.float32)])
+def test_quantize_rows_fp8(oracle, rows, cols, dtype):
+    a = inputs.random_rows(rows, cols, dtype, seed=rows + cols) * 3
+    a[0, :5] = 0  # zeros and a partly zero block
+    codes, scales = binding.moe_quantize_rows_fp8(a.to(DEV))
+    rc, rs = oracle.quantize_rows_fp8(np_(a))
+    assert np.array_equal(codes.cpu().numpy(), rc)
+    assert np.array_equal(scales.cpu().numpy(), rs)
+
+
+def test_quantize_rows_fp8_all_zero_block(oracle):
+    a = torch.zeros((2, 256), dtype=torch.bfloat16)
+    a[1, 200] = 1.5
+    codes, scales = binding.moe_quantize_rows_fp8(a.to(DEV))
+    want = np.array([[1.0, 1.0], [1.0, np.float32(1.5) / np.float32(448)]], np.float32)
+    assert np.array_equal(scales.cpu().numpy(), want)
+    assert np.array_equal(codes.cpu().numpy(), oracle.quantize_rows_fp8(np_(a))[0])
+
+
+@pytest.mark.parametrize("G,n,k", [(2, 256, 512), (1, 200, 300), (3, 384, 7168)])
+def test_quantize_weights_fp8(oracle, G, n, k):
+    w = inputs.random_rows(G * n, k, torch.bfloat16, seed=G * n + k).view(G, n, k)
+    codes, scales = binding.moe_quantize_weights_fp8(w.to(DEV))
+    for g in range(G):
+        rc, rs = oracle.quantize_tiles_fp8(np_(w[g]))
+        assert np.array_equal(codes[g].cpu().numpy(), rc)
+        assert np.array_equal(scales[g].cpu().numpy(), rs)
+
+
+def _oracle_fp8_weights(oracle, n: dict, shared: bool = True):
+    q = {}
+    parts = [("", "w_gate", "w_up", "w2")] + ([("s", "s_gate", "s_up", "s2")] if shared else [])
+    for pre, g, u, d in parts:
+        q[pre + "gq"], q[pre + "gs"] = oracle.quantize_experts_fp8(n[g])
+        q[pre + "uq"], q[pre + "us"] = oracle.quantize_experts_fp8(n[u])
+        q[pre + "dq"], q[pre + "ds"] = oracle.quantize_experts_fp8(n[d])
+    return q
+
+
+@pytest.mark.parametrize("T,k,E,H,I", [(300, 6, 16, 512, 256), (1000, 2, 8, 256, 384), (64, 8, 64, 256, 128),
+                                       (3, 1, 4, 256, 128), (120, 4, 8, 512, 208)])
+def test_grouped_ffn_fp8(oracle, T, k, E, H, I):
+    """I=208: a K tail of 80 in the down projection and padded gate/up packing."""
+    cfg = inputs.LayerConfig("f", T=T, H=H, E=E, k=k, I=I, S=0, dtype="bf16", seed=T + E)
+    d = inputs.make_layer(cfg, "cpu")
+    n = {key: np_(v) for key, v in d.items() if isinstance(v, torch.Tensor)}
+    ids = inputs.random_ids(T, k, E, seed=T)
+    ir = oracle.init_routing(ids.numpy(), n["x"], E)
+    xq, xs = oracle.quantize_rows_fp8(ir["expanded_x"])
+    q = _oracle_fp8_weights(oracle, n, shared=False)
+    # the GPU quantises the packed gate/up weight; its codes are the oracle's, re-packed
+    w13 = binding.moe_pack_w13(d["w_gate"].to(DEV), d["w_up"].to(DEV))
+    w13q, w13s = binding.moe_quantize_weights_fp8(w13)
+    w2q, w2s = binding.moe_quantize_weights_fp8(d["w2"].to(DEV))
+    if I % 128 == 0:
+        e0 = w13q[0].cpu().numpy()
+        assert np.array_equal(e0[0:128], q["gq"][0][0:128]) and np.array_equal(e0[128:256], q["uq"][0][0:128])
+    y, ws = binding.moe_grouped_ffn_fp8(torch.from_numpy(xq).to(DEV), torch.from_numpy(xs).to(DEV),
+                                        torch.from_numpy(ir["expert_offsets"]).to(DEV), E, I, w13q, w13s, w2q, w2s)
+    assert binding.moe_check_device_status(ws) == 0
+    expert_of_row = np.repeat(np.arange(E, dtype=np.int32), ir["tokens_per_expert"])
+    ref = oracle.expert_ffn_rows_fp8(xq, xs, expert_of_row, q)
+    assert rel_l2(y, ref) <= 1e-2
+
+
+FP8_LAYERS = [
+    inputs.LayerConfig("fp8_small", T=256, H=512, E=64, k=6, I=256, S=2, dtype="bf16", seed=51,
+                       weight_format="fp8"),
+    inputs.LayerConfig("fp8_grouped", T=200, H=256, E=32, k=4, I=128, S=1, dtype="bf16", seed=52, n_group=4,
+                       topk_group=2, group_rule="top2_sum", weight_format="fp8"),
+    inputs.LayerConfig("fp8_noshared", T=130, H=256, E=16, k=2, I=384, S=0, dtype="bf16", seed=53,
+                       weight_format="fp8"),
+]
+
+
+def _check_fp8_layer(oracle, cfg, d, layer, out, tokens=None):
+    n = {key: np_(v) for key, v in d.items() if isinstance(v, torch.Tensor)}
+    q = _oracle_fp8_weights(oracle, n, shared=cfg.S > 0)
+    toks = np.arange(cfg.T, dtype=np.int32) if tokens is None else np.asarray(tokens, np.int32)
+    ref = oracle.layer_fp8(n["x"], n["wg"], q, k=cfg.k, renorm=cfg.renormalize, bias=n.get("bias"),
+                           tokens=None if tokens is None else toks, n_group=cfg.n_group, topk_group=cfg.topk_group,
+                           group_rule=cfg.group_rule)
+    ids = layer.field("topk_ids").cpu().numpy()[toks]
+    same = np.array([set(ids[i]) == set(ref["ids"][i]) for i in range(len(toks))])
+    assert (~same).sum() <= max(1, len(toks) // 100)
+    err = rel_l2(f64(out)[toks][same], ref["out"][same])
+    assert err <= 1e-2, f"{cfg.name}: rel-L2 {err:.3e}"
+    assert binding.moe_check_device_status(layer.ws) == 0
+    return err
+
+
+def _make(cfg):
+    d = inputs.make_layer(cfg, DEV)
+    layer = binding.MoELayer(T=cfg.T, k=cfg.k, w_router=d["wg"], w_gate=d["w_gate"], w_up=d["w_up"], w2=d["w2"],
+                             s_gate=d["s_gate"] if cfg.S else None, s_up=d["s_up"] if cfg.S else None,
+                             s2=d["s2"] if cfg.S else None, expert_bias=d["bias"], renormalize=cfg.renormalize,
+                             n_group=cfg.n_group, topk_group=cfg.topk_group, group_rule=cfg.group_rule,
+                             weight_format=cfg.weight_format)
+    return d, layer
+
+
+@pytest.mark.parametrize("cfg", FP8_LAYERS, ids=[c.name for c in FP8_LAYERS])
+def test_layer_fp8_small(oracle, cfg):
+    d, layer = _make(cfg)
+    out = layer.forward(d["x"])
+    _check_fp8_layer(oracle, cfg, d, layer, out)
+    # deterministic: a second forward gives the same bits
+    assert torch.equal(layer.forward(d["x"]), out)
+
+
+@pytest.mark.parametrize("name,n_sample", [("dsv3_prefill_fp8", 32), ("dsv3_decode_fp8", 16)])
+def test_layer_fp8_full_size_sampled(oracle, name, n_sample):
+    cfg = inputs.CONFIGS[name]
+    d, layer = _make(cfg)
+    out = layer.forward(d["x"])
+    g = inputs.generator("cpu", cfg.seed, "misc")
+    toks = torch.randperm(cfg.T, generator=g)[:n_sample].sort().values.numpy().astype(np.int32)
+    _check_fp8_layer(oracle, cfg, d, layer, out, tokens=toks)
+    del layer, d
+    torch.cuda.empty_cache()
+
+
+def test_grouped_ffn_fp8_rejects_unsupported_shapes():
+    a = torch.zeros((8, 512), dtype=torch.uint8, device=DEV)
+    sc = torch.ones((8, 4), dtype=torch.float32, device=DEV)
+    with pytest.raises(binding.MoEError):  # I % 16 != 0
+        binding.moe_grouped_ffn_fp8(a, sc, None, 1, 200, a, sc, a, sc)
