@@ -178,12 +178,17 @@ def host_layer(d: dict) -> dict:
     return {k: inputs.to_numpy(v) for k, v in d.items() if isinstance(v, torch.Tensor)}
 
 
-def cpu_baseline(cfg, host: dict, budget_s: float = 12.0) -> dict:
+def cpu_baseline(cfg, host: dict, budget_s: float = 15.0) -> dict:
     import oracle
-    n = 4
+    # probe with one token per thread (the oracle parallelises over tokens), then
+    # scale the sample to the budget; rescale once if it still ran short
+    n = min(cfg.T, max(4, oracle.num_threads()))
     t = oracle_layer_time(cfg, host, sample_tokens(cfg, n))
-    n = int(max(4, min(cfg.T, n * budget_s / max(t, 1e-3))))
-    t = oracle_layer_time(cfg, host, sample_tokens(cfg, n, offset=1))
+    for attempt in range(2):
+        if t >= 0.7 * budget_s or n >= cfg.T:
+            break
+        n = int(max(4, min(cfg.T, n * budget_s / max(t, 1e-3))))
+        t = oracle_layer_time(cfg, host, sample_tokens(cfg, n, offset=1 + attempt))
     return dict(value=n / t, unit=UNIT, cores=min(oracle.num_threads(), n), kind="oracle",
                 sample=f"{n} of {cfg.T} tokens of {cfg.name}, whole layer per token in fp64 "
                        f"(gate, routing, shared + {cfg.k} routed SwiGLU experts), {t:.1f} s")
@@ -393,7 +398,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="dsv3_prefill", choices=sorted(inputs.CONFIGS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
+    ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--ref-tokens", type=int, default=16, help="tokens per step for --impl reference")
     ap.add_argument("--ep", type=int, default=1,
                     help="run the layer through expert-parallel Double-Routing with this many virtual ranks")

@@ -81,6 +81,15 @@ const char* moe_status_string(moe_status_t status);
 /* Number of kernels this library has launched in this process (all devices). */
 uint64_t moe_kernel_launch_count(void);
 
+/* Diagnostic of the bounded on-chip waits (no counterpart on the pages): one
+ * CTA waits on an mbarrier that nothing arrives on.  Its first warp gives up
+ * after limit_ns (1 ns .. 10 s) and sets MOE_DEVERR_TIMEOUT in the status word
+ * of `ws` (cleared first); its second warp, which has no limit of its own,
+ * leaves through the shared abort flag the first one raises.  *outcome
+ * (device, uint32) receives bit 0 when the first warp timed out and bit 1 when
+ * the second left through the flag.  No trap, no hang; asynchronous. */
+moe_status_t moe_diag_bounded_wait(uint64_t limit_ns, void* ws, uint32_t* outcome, moe_stream_t stream);
+
 /* Synchronises `stream`, then reads and returns the status word of `ws` in
  * *word (may be NULL).  Returns MOE_OK if the word is zero, MOE_ERR_DEVICE if
  * not, MOE_ERR_CUDA if the synchronisation failed.  This call blocks. */
@@ -324,7 +333,7 @@ const char* moe_stage_name(int stage); /* "gate", "route", "init_routing", "perm
 
 /* Workspace fields of the layer (intermediates a caller may inspect). */
 typedef enum moe_ws_field {
-    MOE_WS_LOGITS = 0,            /* [T,E] fp32 */
+    MOE_WS_LOGITS = 0,            /* [T,E] fp32 (bf16 layers: room for 8 K slices, the sums in the first) */
     MOE_WS_TOPK_IDS = 1,          /* [T,k] int32 */
     MOE_WS_TOPK_W = 2,            /* [T,k] fp32 */
     MOE_WS_TOKENS_PER_EXPERT = 3, /* [E] int32 */

@@ -44,6 +44,7 @@ SIGNATURES = {
     "moe_status_string": (ctypes.c_char_p, [I32]),
     "moe_kernel_launch_count": (ctypes.c_uint64, []),
     "moe_check_device_status": (I32, [P, P, ctypes.POINTER(ctypes.c_uint32)]),
+    "moe_diag_bounded_wait": (I32, [ctypes.c_uint64, P, P, P]),
     "moe_gate_logits": (I32, [P, P, I32, I32, I32, I32, P, P]),
     "moe_route_topk": (I32, [P, P, I32, I32, I32, I32, P, P, P]),
     "moe_route_topk_grouped": (I32, [P, P, I32, I32, I32, I32, I32, I32, I32, P, P, P]),
@@ -380,7 +381,10 @@ class MoELayer:
                       hq_shared=((T, S * I), torch.uint8), hq_shared_scales=((T, scale_ld(S * I) if S else 0),
                                                                              torch.float32))
         shape, dtype = shapes[name]
-        return raw.view(dtype).view(shape)
+        n = 1
+        for dim in shape:
+            n *= dim
+        return raw.view(dtype)[:n].view(shape)  # the logits region also holds the gate's K slices
 
     def forward(self, x: torch.Tensor, out: torch.Tensor | None = None, stream=None, events=None):
         if out is None:

@@ -36,6 +36,7 @@
 // is freed before the CTA exits.  No trap, no unbounded spin.
 #include "tc_ptx.cuh"
 
+#include <algorithm>
 #include <climits>
 
 namespace moe {
@@ -65,14 +66,17 @@ struct Cfg {
 struct Params {
     const int32_t* offsets;
     int G, M, K, Nb, N, NT;
+    int ksplit;               // K split into this many slices (fp32 outputs only), each written at
+    int64_t c_split_stride;   // C + slice * c_split_stride
     void* C;
     int64_t ldc;
     uint32_t* status;
 };
 
-// tile -> (group, m-tile, n-tile).  prefix[g] = first tile of group g,
-// prefix[G] = total; tiles of a group are n-major, m fastest.
-__device__ __forceinline__ void decode_tile(int tile, const int* prefix, int G, int NT, int& g, int& m, int& n) {
+// tile -> (group, m-tile, n-tile, K slice).  prefix[g] = first tile of group g,
+// prefix[G] = total; tiles of a group are n-major, then m, K slice fastest.
+__device__ __forceinline__ void decode_tile(int tile, const int* prefix, int G, int NT, int S, int& g, int& m,
+                                            int& n, int& ks) {
     int lo = 0, hi = G - 1;
     while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
@@ -81,9 +85,11 @@ __device__ __forceinline__ void decode_tile(int tile, const int* prefix, int G, 
     }
     g = lo;
     const int local = tile - prefix[g];
-    const int mt = (prefix[g + 1] - prefix[g]) / NT;
-    n = local / mt;
-    m = local - n * mt;
+    const int mts = (prefix[g + 1] - prefix[g]) / NT;  // m-tiles x slices
+    n = local / mts;
+    const int rem = local - n * mts;
+    m = rem / S;
+    ks = rem - m * S;
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
@@ -176,7 +182,7 @@ tc_grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_co
         int run = 0;
         for (int g0 = 0; g0 < G; g0 += 32) {
             const int g = g0 + lane;
-            const int v = g < G ? (gend[g] - gstart[g] + BM - 1) / BM * NT : 0;
+            const int v = g < G ? (gend[g] - gstart[g] + BM - 1) / BM * NT * p.ksplit : 0;
             int incl = v;
 #pragma unroll
             for (int off = 1; off < 32; off <<= 1) {
@@ -211,6 +217,7 @@ tc_grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_co
     const uint32_t tmem_base = *tmem_slot;
     const int total = prefix[G];
     const int KB = (p.K + BK - 1) / BK;
+    const int KBS = (KB + p.ksplit - 1) / p.ksplit;  // k-blocks per slice (the host keeps every slice non-empty)
 
     if (warp == 0) {
         if (lane == 0) {
@@ -219,11 +226,12 @@ tc_grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_co
             uint32_t ph = 0, issued = 0, issued_par = 0;
             bool ok = true;
             for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
-                int g, m, n;
-                decode_tile(tile, prefix, G, NT, g, m, n);
+                int g, m, n, ks;
+                decode_tile(tile, prefix, G, NT, p.ksplit, g, m, n, ks);
                 const int row0 = gstart[g] + m * BM;
                 const int brow = g * p.Nb + n * BN;
-                for (int kb = 0; kb < KB; ++kb) {
+                const int kb1 = min(KB, (ks + 1) * KBS);
+                for (int kb = ks * KBS; kb < kb1; ++kb) {
                     if (!wait_phase(empty_bar(s), ph ^ 1u, abort_flag, p.status)) {
                         ok = false;
                         break;
@@ -250,10 +258,13 @@ tc_grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_co
             uint32_t ph = 0, aph = 0;
             bool ok = true;
             for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
+                int g, m, n, ks;
+                decode_tile(tile, prefix, G, NT, p.ksplit, g, m, n, ks);
+                const int kb0 = ks * KBS, kb1 = min(KB, kb0 + KBS);
                 if (!wait_phase(tempty_bar(acc), aph ^ 1u, abort_flag, p.status)) break;
                 tc_fence_after();
                 const uint32_t d = tmem_base + (uint32_t)(acc * BN);
-                for (int kb = 0; kb < KB; ++kb) {
+                for (int kb = kb0; kb < kb1; ++kb) {
                     if (!wait_phase(full_bar(s), ph, abort_flag, p.status)) {
                         ok = false;
                         break;
@@ -263,7 +274,7 @@ tc_grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_co
                     const uint64_t bdesc = smem_desc_sw128(smem_u32(sB + s * Cf::B_BYTES));
 #pragma unroll
                     for (int kk = 0; kk < BK / UMMA_K; ++kk)  // +32 bytes per K=16 slice
-                        mma_bf16(d, adesc + 2u * kk, bdesc + 2u * kk, IDESC, (kb | kk) != 0);
+                        mma_bf16(d, adesc + 2u * kk, bdesc + 2u * kk, IDESC, (kb != kb0) | (kk != 0));
                     mma_commit(empty_bar(s));
                     if (++s == STAGES) {
                         s = 0;
@@ -288,8 +299,9 @@ tc_grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_co
         int acc = 0;
         uint32_t aph = 0;
         for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
-            int g, m, n;
-            decode_tile(tile, prefix, G, NT, g, m, n);
+            int g, m, n, ks;
+            decode_tile(tile, prefix, G, NT, p.ksplit, g, m, n, ks);
+            void* C = static_cast<char*>(p.C) + ks * p.c_split_stride * (EPI == TC_EPI_F32 ? 4 : 2);
             const int64_t row = (int64_t)gstart[g] + (int64_t)m * BM + r;
             const bool valid = row < gend[g];
             // warp-uniform decision: the TMEM loads below are .sync.aligned
@@ -308,7 +320,7 @@ tc_grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_co
                         const float gv = __uint_as_float(gr[i]);
                         h[i] = gv / (1.0f + __expf(-gv)) * __uint_as_float(ur[i]);
                     }
-                    if (valid) store_row32<EPI>(p.C, p.ldc, row, n * kPackBlock + c, p.N, h);
+                    if (valid) store_row32<EPI>(C, p.ldc, row, n * kPackBlock + c, p.N, h);
                 }
             } else {
 #pragma unroll 1
@@ -318,7 +330,7 @@ tc_grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_co
                     float v[32];
 #pragma unroll
                     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(vr[i]);
-                    if (valid) store_row32<EPI>(p.C, p.ldc, row, n * BN + c, p.N, v);
+                    if (valid) store_row32<EPI>(C, p.ldc, row, n * BN + c, p.N, v);
                 }
             }
             tc_fence_before();
@@ -338,6 +350,14 @@ tc_grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_co
         tc_fence_after();
         tmem_dealloc(tmem_base, Cf::TMEM_COLS);
     }
+}
+
+// K slices actually launched for a requested count: each slice takes
+// ceil(KB / requested) k-blocks, so none is left empty.
+int effective_splits(int K, int requested) {
+    const int KB = (int)ceil_div(K, BK);
+    const int S = std::max(1, std::min(requested, KB));
+    return (int)ceil_div(KB, ceil_div(KB, S));
 }
 
 template <int BN, int EPI>
@@ -365,41 +385,55 @@ moe_status_t launch_impl(const TcGroupedGemm& g, cudaStream_t s) {
     p.Nb = g.Nb;
     p.N = g.N;
     p.NT = EPI == TC_EPI_SWIGLU ? g.Nb / BN : (int)ceil_div(g.N, BN);
+    p.ksplit = EPI == TC_EPI_F32 ? effective_splits(g.K, g.ksplit) : 1;
+    p.c_split_stride = g.c_split_stride;
     p.C = g.C;
     p.ldc = g.ldc;
     p.status = g.status;
 
-    const int64_t max_tiles = (int64_t)p.NT * (ceil_div(g.M, BM) + (g.offsets ? g.G : 0));
+    const int64_t max_tiles = (int64_t)p.NT * p.ksplit * (ceil_div(g.M, BM) + (g.offsets ? g.G : 0));
     const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(sm_count(), max_tiles));
     tc_grouped_gemm_kernel<BN, EPI><<<grid, kThreads, Cf::SMEM, s>>>(ma, mb, p);
     note_launch();
     return last_launch_status();
 }
 
-// Gate-style launches (one dense problem, fp32 out): pick the n-tile width
-// that minimises waves x per-k-block time, where a k-block costs the larger of
-// its MMA time (M=128, N=BN, K=64: 2*BN cycles) and its operand fill
-// ((16 KB + BN*128 B) at ~128 B per cycle per SM).  Ties go to the wider tile.
-int pick_bn_f32(int M, int N) {
+// Gate-style launches (one dense problem, fp32 out): pick the n-tile width and
+// the number of K slices.  A CTA's k-blocks run at roughly the larger of their
+// MMA time (2*BN cycles), their operand fill ((16 KB + BN*128 B) at ~128 B per
+// cycle) and a floor of ~700 cycles set by the load latency one pipeline
+// covers; cost = waves x k-blocks per tile x that.  Ties go to fewer slices,
+// then to the wider tile.
+void plan_f32(int M, int N, int K, int max_split, int& bn_out, int& split_out) {
     const int sms = sm_count();
-    int best = 256;
+    const int64_t KB = ceil_div(K, BK);
     int64_t best_cost = INT64_MAX;
-    for (int bn : {256, 128, 64}) {
-        const int64_t tiles = ceil_div(M, BM) * ceil_div(N, bn);
-        const int64_t waves = ceil_div(tiles, sms);
-        const int64_t per_kb = std::max<int64_t>(2 * bn, (16384 + (int64_t)bn * 128) / 128);
-        const int64_t cost = waves * per_kb;
-        if (cost < best_cost) {
-            best_cost = cost;
-            best = bn;
+    bn_out = 256;
+    split_out = 1;
+    for (int S = 1; S <= max_split; S *= 2) {
+        for (int bn : {256, 128, 64}) {
+            const int64_t tiles = ceil_div(M, BM) * ceil_div(N, bn) * S;
+            const int64_t waves = ceil_div(tiles, sms);
+            const int64_t per_kb = std::max<int64_t>({2 * bn, (16384 + (int64_t)bn * 128) / 128, 700});
+            const int64_t cost = waves * ceil_div(KB, S) * per_kb;
+            if (cost < best_cost) {
+                best_cost = cost;
+                bn_out = bn;
+                split_out = S;
+            }
         }
     }
-    return best;
 }
 
 }  // namespace
 
 int tc_packed_block() { return kPackBlock; }
+
+int tc_gate_splits(int M, int N, int K, int max_split) {
+    int bn, split;
+    plan_f32(M, N, K, std::max(1, max_split), bn, split);
+    return effective_splits(K, split);
+}
 
 moe_status_t launch_tc_grouped_gemm(const TcGroupedGemm& g, cudaStream_t s) {
     if (g.M == 0 || g.G == 0) return MOE_OK;
@@ -410,12 +444,17 @@ moe_status_t launch_tc_grouped_gemm(const TcGroupedGemm& g, cudaStream_t s) {
             return launch_impl<256, TC_EPI_SWIGLU>(g, s);
         case TC_EPI_BF16:
             return launch_impl<256, TC_EPI_BF16>(g, s);
-        case TC_EPI_F32:
-            switch (pick_bn_f32(g.M, g.N)) {
-                case 64: return launch_impl<64, TC_EPI_F32>(g, s);
-                case 128: return launch_impl<128, TC_EPI_F32>(g, s);
-                default: return launch_impl<256, TC_EPI_F32>(g, s);
+        case TC_EPI_F32: {
+            int bn, split;
+            plan_f32(g.M, g.N, g.K, std::max(1, g.ksplit), bn, split);
+            TcGroupedGemm gs = g;
+            gs.ksplit = split;
+            switch (bn) {
+                case 64: return launch_impl<64, TC_EPI_F32>(gs, s);
+                case 128: return launch_impl<128, TC_EPI_F32>(gs, s);
+                default: return launch_impl<256, TC_EPI_F32>(gs, s);
             }
+        }
     }
     return MOE_ERR_INVALID_ARG;
 }

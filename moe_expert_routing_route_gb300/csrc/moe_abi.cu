@@ -99,6 +99,29 @@ moe_status_t gate(const void* x, const void* wr, moe_dtype_t dt, int T, int H, i
     return launch_simt_gate(static_cast<const float*>(x), static_cast<const float*>(wr), T, H, E, logits, s);
 }
 
+// K slices of the layer's gate GEMM (bf16 on tensor cores only); the route
+// kernel adds them.  The workspace holds kMaxGateSplits slices so that its size
+// does not depend on the device; the launch picks at most that many.
+constexpr int kMaxGateSplits = 8;
+int gate_splits(const moe_layer_desc& d) {
+    if (d.dtype != MOE_BF16 || d.T <= 0) return 1;
+    return tc_gate_splits(d.T, d.E, d.H, kMaxGateSplits);
+}
+
+// The layer's gate GEMM: bf16 splits K (the route kernel adds the slices), fp32
+// runs unsplit.  Every layer path uses this so that their logits agree bit for bit.
+// The launch plans from the same maximum as gate_splits, so both arrive at the
+// same slice count.
+moe_status_t layer_gate(const moe_layer_desc& d, const void* x, float* logits, int* nsplit, cudaStream_t s) {
+    *nsplit = gate_splits(d);
+    if (d.dtype == MOE_BF16) {
+        TcGroupedGemm g{x, d.T, d.H, nullptr, 1, d.w_router, d.E, d.E, logits, d.E, TC_EPI_F32, nullptr,
+                        kMaxGateSplits, (int64_t)d.T * d.E};
+        return launch_tc_grouped_gemm(g, s);
+    }
+    return gate(x, d.w_router, d.dtype, d.T, d.H, d.E, logits, s);
+}
+
 // ---- layer workspace layout ----
 struct Layout {
     size_t off[MOE_WS_NUM_FIELDS];
@@ -111,7 +134,7 @@ Layout layout(const moe_layer_desc& d) {
     const size_t b = dt_size(d.dtype);
     const size_t T = (size_t)d.T, H = (size_t)d.H, E = (size_t)d.E, R = (size_t)d.T * d.k, I = (size_t)d.I,
                  S = (size_t)d.S;
-    L.bytes[MOE_WS_LOGITS] = T * E * 4;
+    L.bytes[MOE_WS_LOGITS] = T * E * 4 * (d.dtype == MOE_BF16 ? kMaxGateSplits : 1);
     L.bytes[MOE_WS_TOPK_IDS] = R * 4;
     L.bytes[MOE_WS_TOPK_W] = R * 4;
     L.bytes[MOE_WS_TOKENS_PER_EXPERT] = E * 4;
@@ -272,7 +295,8 @@ moe_status_t layer_forward(const moe_layer_desc* d, const void* x, void* out, vo
 
     MOE_TRY(clear_status(ws, s));
     MOE_TRY(mark(ev, ST_GATE, 0, s));
-    MOE_TRY(gate(x, d->w_router, dt, T, H, E, logits, s));
+    int nsplit = 1;
+    MOE_TRY(layer_gate(*d, x, logits, &nsplit, s));
     if (fp8) MOE_TRY(launch_quantize_rows_fp8(x, dt, T, H, xq, xs, ldx, s));  // activations, 1x128 blocks
     MOE_TRY(mark(ev, ST_GATE, 1, s));
     if (side) {
@@ -297,7 +321,7 @@ moe_status_t layer_forward(const moe_layer_desc* d, const void* x, void* out, vo
     }
     MOE_TRY(mark(ev, ST_ROUTE, 0, s));
     MOE_TRY(launch_route_topk(logits, d->expert_bias, T, E, k, d->renormalize, ids, w, s, d->n_group,
-                              d->topk_group, d->group_rule));
+                              d->topk_group, d->group_rule, nsplit));
     MOE_TRY(mark(ev, ST_ROUTE, 1, s));
     MOE_TRY(mark(ev, ST_INIT, 0, s));
     MOE_TRY(launch_init_routing_index(ids, R, E, counts, offsets, row_idx, scratch, status, s));
@@ -385,7 +409,8 @@ moe_status_t layer_forward_ep(const moe_layer_desc* d, int W, const void* x, voi
     if (side) side_lock = std::unique_lock<std::mutex>(side->mu);
 
     MOE_TRY(clear_status(ws, s));
-    MOE_TRY(gate(x, d->w_router, dt, T, H, E, logits, s));
+    int nsplit = 1;
+    MOE_TRY(layer_gate(*d, x, logits, &nsplit, s));
     if (side) {
         MOE_CUDA_TRY(cudaEventRecord(side->fork, s));
         MOE_CUDA_TRY(cudaStreamWaitEvent(side->stream, side->fork, 0));
@@ -394,7 +419,7 @@ moe_status_t layer_forward_ep(const moe_layer_desc* d, int W, const void* x, voi
         MOE_CUDA_TRY(cudaEventRecord(side->join, side->stream));
     }
     MOE_TRY(launch_route_topk(logits, d->expert_bias, T, E, k, d->renormalize, ids, w, s, d->n_group, d->topk_group,
-                              d->group_rule));
+                              d->group_rule, nsplit));
     MOE_TRY(ep_route_and_dispatch(b, s));  // steps 1-4
     if (side) MOE_CUDA_TRY(cudaStreamWaitEvent(s, side->join, 0));
     // step 5: each rank's experts on its sorted rows

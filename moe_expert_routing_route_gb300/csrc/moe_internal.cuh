@@ -42,9 +42,11 @@ __device__ __forceinline__ void set_status(uint32_t* status, uint32_t bit) {
 // route.cu
 // n_group <= 1: flat top-k; otherwise group-limited (topk_group groups kept,
 // rule 0 = group max, rule 1 = sum of the group's two largest scores).
+// nsplit > 1: the logits arrive as nsplit partial sums, slice i at logits + i*T*E;
+// they are added in slice order and the sums written back to slice 0.
 moe_status_t launch_route_topk(const float* logits, const float* bias, int T, int E, int k, int renorm,
                                int32_t* ids, float* w, cudaStream_t s, int n_group = 1, int topk_group = 1,
-                               int rule = 0);
+                               int rule = 0, int nsplit = 1);
 
 // permute.cu
 size_t init_routing_scratch_bytes(int T, int E, int k);
@@ -108,8 +110,11 @@ struct TcGroupedGemm {
     int64_t ldc;              // elements
     TcEpilogue epi;
     uint32_t* status;
+    int ksplit = 1;               // fp32 output only: at most this many K slices, slice s written at
+    int64_t c_split_stride = 0;   // C + s * c_split_stride (elements); the caller sums the slices
 };
 moe_status_t launch_tc_grouped_gemm(const TcGroupedGemm& g, cudaStream_t s);
+int tc_gate_splits(int M, int N, int K, int max_split);  // K slices the fp32 launch will use
 
 // gemm_fp8.cu: e4m3 block-scaled grouped GEMM (bf16 out), C = A B^T per group.
 struct TcFp8GroupedGemm {

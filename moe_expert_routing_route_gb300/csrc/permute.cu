@@ -211,8 +211,7 @@ size_t init_routing_scratch_bytes(int T, int E, int k) {
 }
 
 moe_status_t launch_init_routing_index(const int32_t* ids, int R, int E, int32_t* counts, int32_t* offsets,
-                                       int32_t* row_idx, int32_t* scratch, uint32_t* status,
-                                       cudaStream_t s) {
+                                       int32_t* row_idx, int32_t* scratch, uint32_t* status, cudaStream_t s) {
     const int NW = (int)ceil_div(R, kChunk);
     if (NW > 0) {
         hist_kernel<<<NW, kChunkThreads, (size_t)E * sizeof(int32_t), s>>>(ids, R, E, NW, scratch, status);

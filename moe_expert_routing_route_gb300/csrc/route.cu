@@ -18,6 +18,9 @@
 // largest score, or the largest two added in fp32), topk_group rounds of the
 // warp argmax keep the best groups, and the experts of the other groups are
 // excluded before the top-k rounds.
+//
+// The gate GEMM may hand over its logits as K-sliced partial sums; they are
+// added here in slice order while loading (deterministic, no extra kernel).
 #include "moe_internal.cuh"
 
 #include <climits>
@@ -53,8 +56,8 @@ __device__ __forceinline__ void warp_argmax(float& bv, int& bi) {
 
 template <int VPL>
 __global__ void __launch_bounds__(kWarps * 32)
-route_topk_kernel(const float* __restrict__ logits, const float* __restrict__ bias, int T, int E, int k,
-                  Grouping grp, int renorm, int32_t* __restrict__ ids, float* __restrict__ w) {
+route_topk_kernel(const float* logits, const float* __restrict__ bias, int T, int E, int k, Grouping grp,
+                  int renorm, int nsplit, int32_t* __restrict__ ids, float* __restrict__ w) {
     extern __shared__ float sh_scores[];  // [kWarps][E], grouped routing only
     const int lane = threadIdx.x & 31;
     const int t = blockIdx.x * kWarps + (threadIdx.x >> 5);
@@ -63,14 +66,26 @@ route_topk_kernel(const float* __restrict__ logits, const float* __restrict__ bi
 
     float v[VPL];
 #pragma unroll
+    for (int i = 0; i < VPL; ++i) v[i] = i * 32 + lane < E ? row[i * 32 + lane] : 0.0f;
+    if (nsplit > 1) {
+        // K slices of the gate GEMM, added in slice order; each round issues all
+        // of a lane's loads before any add, and the sums go back to slice 0 last
+        for (int q = 1; q < nsplit; ++q) {
+            const float* sl = row + (size_t)q * T * E;
+            float p[VPL];
+#pragma unroll
+            for (int i = 0; i < VPL; ++i) p[i] = i * 32 + lane < E ? sl[i * 32 + lane] : 0.0f;
+#pragma unroll
+            for (int i = 0; i < VPL; ++i) v[i] += p[i];
+        }
+#pragma unroll
+        for (int i = 0; i < VPL; ++i)
+            if (i * 32 + lane < E) const_cast<float*>(row)[i * 32 + lane] = v[i];
+    }
+#pragma unroll
     for (int i = 0; i < VPL; ++i) {
         const int e = i * 32 + lane;
-        if (e < E) {
-            const float b = bias ? __ldg(bias + e) : 0.0f;
-            v[i] = __ldg(row + e) + b;
-        } else {
-            v[i] = -INFINITY;
-        }
+        v[i] = e < E ? v[i] + (bias ? __ldg(bias + e) : 0.0f) : -INFINITY;
     }
 
     uint32_t taken = 0;  // bit i: register slot i is no longer a candidate
@@ -169,26 +184,28 @@ route_topk_kernel(const float* __restrict__ logits, const float* __restrict__ bi
 
 template <int VPL>
 cudaError_t launch(const float* logits, const float* bias, int T, int E, int k, Grouping grp, int renorm,
-                   int32_t* ids, float* w, cudaStream_t s) {
+                   int nsplit, int32_t* ids, float* w, cudaStream_t s) {
     const int blocks = (int)ceil_div(T, kWarps);
     const size_t smem = grp.n_group > 1 ? (size_t)kWarps * E * sizeof(float) : 0;
-    route_topk_kernel<VPL><<<blocks, kWarps * 32, smem, s>>>(logits, bias, T, E, k, grp, renorm, ids, w);
+    route_topk_kernel<VPL><<<blocks, kWarps * 32, smem, s>>>(logits, bias, T, E, k, grp, renorm, nsplit, ids, w);
     return cudaGetLastError();
 }
 
 }  // namespace
 
 moe_status_t launch_route_topk(const float* logits, const float* bias, int T, int E, int k, int renorm,
-                               int32_t* ids, float* w, cudaStream_t s, int n_group, int topk_group, int rule) {
+                               int32_t* ids, float* w, cudaStream_t s, int n_group, int topk_group, int rule,
+                               int nsplit) {
     if (T == 0) return MOE_OK;
     const Grouping grp{n_group > 1 ? n_group : 1, topk_group, rule};
+    const int ns = nsplit > 1 ? nsplit : 1;
     cudaError_t err;
-    if (E <= 32) err = launch<1>(logits, bias, T, E, k, grp, renorm, ids, w, s);
-    else if (E <= 64) err = launch<2>(logits, bias, T, E, k, grp, renorm, ids, w, s);
-    else if (E <= 128) err = launch<4>(logits, bias, T, E, k, grp, renorm, ids, w, s);
-    else if (E <= 256) err = launch<8>(logits, bias, T, E, k, grp, renorm, ids, w, s);
-    else if (E <= 512) err = launch<16>(logits, bias, T, E, k, grp, renorm, ids, w, s);
-    else err = launch<32>(logits, bias, T, E, k, grp, renorm, ids, w, s);
+    if (E <= 32) err = launch<1>(logits, bias, T, E, k, grp, renorm, ns, ids, w, s);
+    else if (E <= 64) err = launch<2>(logits, bias, T, E, k, grp, renorm, ns, ids, w, s);
+    else if (E <= 128) err = launch<4>(logits, bias, T, E, k, grp, renorm, ns, ids, w, s);
+    else if (E <= 256) err = launch<8>(logits, bias, T, E, k, grp, renorm, ns, ids, w, s);
+    else if (E <= 512) err = launch<16>(logits, bias, T, E, k, grp, renorm, ns, ids, w, s);
+    else err = launch<32>(logits, bias, T, E, k, grp, renorm, ns, ids, w, s);
     note_launch();
     return err == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }

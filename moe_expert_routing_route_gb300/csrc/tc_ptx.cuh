@@ -149,14 +149,14 @@ __host__ __device__ constexpr uint32_t idesc_e4m3(int M, int N) {
 // Bounded wait on an mbarrier phase.  Returns false when the wait ran out (and
 // then raises the abort flag) or when another role already aborted.
 static __device__ __noinline__ bool wait_phase(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                        uint32_t* status) {
+                                               uint32_t* status, uint64_t limit_ns = kWaitLimitNs) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer();
     for (uint32_t it = 1;; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
         if ((it & 31u) == 0) {
             if (*abort_flag) return false;
-            if (globaltimer() - t0 > kWaitLimitNs) {
+            if (globaltimer() - t0 > limit_ns) {
                 *abort_flag = 1;
                 set_status(status, MOE_DEVERR_TIMEOUT);
                 return false;

@@ -79,10 +79,14 @@ def test_layer_workspace_layout(lib):
         assert off.value % 256 == 0 and off.value >= prev_end
         prev_end = off.value + nb.value
     assert prev_end <= total
-    off, nb = ctypes.c_size_t(), ctypes.c_size_t()
-    lib.moe_layer_workspace_field(ctypes.byref(d), binding.WS_FIELDS.index("expanded_x"), ctypes.byref(off),
-                                  ctypes.byref(nb))
-    assert nb.value == R * 7168 * 2
+    sizes = {}
+    for name in ("expanded_x", "y_routed", "logits"):
+        off, nb = ctypes.c_size_t(), ctypes.c_size_t()
+        lib.moe_layer_workspace_field(ctypes.byref(d), binding.WS_FIELDS.index(name), ctypes.byref(off),
+                                      ctypes.byref(nb))
+        sizes[name] = nb.value
+    # the logits region has room for the gate GEMM's K slices (8 at most)
+    assert sizes == {"expanded_x": R * 7168 * 2, "y_routed": R * 7168 * 2, "logits": 8 * 4096 * 256 * 4}
 
 
 def test_packed_weight_size(lib):

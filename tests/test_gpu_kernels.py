@@ -277,3 +277,25 @@ def test_grouped_ffn_flags_bad_offsets():
     w2 = torch.zeros((E, H, I), dtype=torch.bfloat16, device=DEV)
     _, ws = binding.moe_grouped_ffn(a, offs, E, I, w13, w2)
     assert binding.moe_check_device_status(ws) & binding.MOE_DEVERR_BAD_OFFSETS
+
+
+# ---- failure detection: a bounded wait that runs out ------------------------------------
+
+def test_bounded_wait_times_out_and_aborts_without_trapping():
+    """An mbarrier nothing arrives on: the limited wait gives up, sets the timeout bit
+    and raises the abort flag, and the unlimited waiter leaves through the flag."""
+    import time
+    ws = torch.zeros(256, dtype=torch.uint8, device=DEV)
+    outcome = torch.zeros(1, dtype=torch.int32, device=DEV)
+    t0 = time.perf_counter()
+    st = binding.lib().moe_diag_bounded_wait(50_000_000, binding._ptr(ws), binding._ptr(outcome), binding._stream())
+    assert st == binding.MOE_OK
+    torch.cuda.synchronize()
+    elapsed = time.perf_counter() - t0
+    assert binding.moe_check_device_status(ws) == binding.MOE_DEVERR_TIMEOUT
+    assert int(outcome.item()) == 3
+    assert 0.04 < elapsed < 5.0
+    # the context is still usable
+    ids, w = binding.moe_route_topk(torch.randn(8, 16, device=DEV), 2)
+    torch.cuda.synchronize()
+    assert ids.shape == (8, 2)

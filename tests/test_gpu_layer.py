@@ -126,6 +126,26 @@ def test_layer_small(oracle, cfg):
     check_layer(oracle, cfg, d, layer, out)
 
 
+# H sweeps the gate GEMM's k-block count (1 .. 17, with K tails) and T its tile
+# count, so the K-split plan takes several slice counts, each slice non-empty.
+GATE_SPLIT = [(T, H) for T in (40, 700) for H in (24, 136, 264, 328, 584, 1096)]
+
+
+@pytest.mark.parametrize("T,H", GATE_SPLIT, ids=[f"T{T}_H{H}" for T, H in GATE_SPLIT])
+def test_layer_gate_split_k(oracle, T, H):
+    cfg = inputs.LayerConfig(f"gate_{T}_{H}", T=T, H=H, E=40, k=3, I=64, S=0, dtype="bf16", seed=T + H)
+    d, layer = make(cfg)
+    gl = None
+    for _ in range(2):  # the logits region holds stale slices from the first call
+        layer.forward(d["x"])
+        got = layer.field("logits").cpu().numpy().copy()
+        if gl is not None:
+            assert np.array_equal(got, gl)
+        gl = got
+    assert rel_l2(gl, oracle.gate_logits(np_(d["x"]), np_(d["wg"]))) <= 1e-5
+    assert binding.moe_check_device_status(layer.ws) == 0
+
+
 FULL = [("mid_bf16", 96), ("dsv3_prefill", 48), ("dsv3_decode", 32), ("dsv3_zipf_prefill", 32),
         ("dsv3_prefill_grouped", 32)]
 
