@@ -208,7 +208,11 @@ moe_status_t moe_pack_w13(const void* w_gate, const void* w_up, moe_dtype_t dt, 
  * y [rows,H] dt (rows outside every segment are left untouched).
  * ws: at least moe_grouped_ffn_workspace_bytes(dt,rows,I) bytes (h + status).
  * bf16 runs on tcgen05 tensor cores (TMA-fed, persistent, device-side tile
- * scheduler); fp32 runs on the FFMA pipes. */
+ * scheduler); fp32 runs on the FFMA pipes.  bf16 tiles are 128 rows on one SM,
+ * or 256 rows on a two-CTA cluster (tcgen05.mma.cta_group::2) once the groups
+ * average 256 rows or more; the environment variable MOE_GEMM_TILE=single or
+ * MOE_GEMM_TILE=pair, read at every launch, forces one shape.  Both give the
+ * same result up to fp32 summation order. */
 size_t moe_grouped_ffn_workspace_bytes(moe_dtype_t dt, int rows, int I);
 moe_status_t moe_grouped_ffn(const void* a, moe_dtype_t dt, const int32_t* expert_offsets, int E,
                              int rows, int H, int I, const void* w13_packed, const void* w2, void* y,

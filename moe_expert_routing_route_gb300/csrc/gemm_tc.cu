@@ -38,6 +38,8 @@
 
 #include <algorithm>
 #include <climits>
+#include <cstdlib>
+#include <cstring>
 
 namespace moe {
 namespace {
@@ -352,6 +354,270 @@ tc_grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_co
     }
 }
 
+// ---------------------------------------------------------------------------
+// Pair tiles: a cluster of two CTAs on one tcgen05.mma.cta_group::2 (M = 256).
+//
+// A tile is 256 rows x 256 columns.  Each CTA of the pair loads its own 128
+// rows of A and its own half of the 256 B rows (SwiGLU: rank 0 the 128 gate
+// rows, rank 1 the 128 up rows of the packed block), i.e. 32 KB per k-block
+// instead of the 48 KB a 128 x 256 tile on one SM needs.  The fill rate one SM
+// sustains is bounded by the bytes it keeps in flight, so the same 192 KB of
+// stages now cover 6 k-blocks and feed the tensor core for 3/2 as long.
+//
+// Protocol (rank = %cluster_ctarank; rank 0 is the leader):
+//   both producers   wait their own empty[s]; the leader arms its full[s] with
+//                    the bytes of both CTAs; both load into their own shared
+//                    memory with completion counted on the leader's full[s]
+//   leader MMA       waits full[s], issues 4 x mma.cta_group::2, commits with
+//                    multicast to empty[s] of both CTAs; after a tile, commits
+//                    to tfull[acc] of both CTAs; waits tempty[acc] (8 warps:
+//                    4 local + 4 remote) before reusing an accumulator
+//   both epilogues   wait their own tfull[acc], read their own TMEM lanes
+//                    (their 128 rows), store, arrive on the leader's tempty
+// Cluster barriers after setup (barriers initialised, TMEM allocated) and
+// before TMEM is freed (every pair MMA drained).  Waits are bounded as in the
+// single-CTA kernel; a CTA that aborts stops signalling and its peer's waits
+// run out in turn.
+constexpr int BM2 = 256;  // rows per pair tile
+constexpr int BN2 = 256;  // columns per pair tile (each CTA holds BN2 / 2 B rows)
+
+struct Cfg2 {
+    static constexpr int A_BYTES = 128 * BK * 2;
+    static constexpr int B_BYTES = (BN2 / 2) * BK * 2;
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;  // per CTA
+    static constexpr int STAGES = 6;
+    static constexpr int TMEM_COLS = 2 * BN2;
+    static constexpr int NUM_BARS = 2 * STAGES + 5;
+    static constexpr size_t SMEM = 1024 + (size_t)STAGES * STAGE_BYTES + NUM_BARS * 8 + 16 +
+                                   (size_t)(3 * kMaxGroups + 1) * 4;
+};
+static_assert(Cfg2::SMEM <= 232448, "pair-tile stages exceed shared memory");
+
+template <int EPI>
+__global__ void __launch_bounds__(kThreads, 1)
+tc_pair_gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
+                    const __grid_constant__ Params p) {
+    using Cf = Cfg2;
+    constexpr int STAGES = Cf::STAGES;
+    constexpr uint32_t IDESC = idesc_bf16(BM2, BN2);
+    static_assert(EPI != TC_EPI_F32, "fp32 outputs use the single-CTA kernel");
+
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_addr = smem_u32(smem_raw);
+    uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
+    uint8_t* sA = smem;
+    uint8_t* sB = smem + STAGES * Cf::A_BYTES;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sB + STAGES * Cf::B_BYTES);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + Cf::NUM_BARS);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    int* prefix = reinterpret_cast<int*>(tmem_slot + 4);
+    int* gstart = prefix + kMaxGroups + 1;
+    int* gend = gstart + kMaxGroups;
+
+    auto full_bar = [&](int s) { return smem_u32(bars + s); };
+    auto empty_bar = [&](int s) { return smem_u32(bars + STAGES + s); };
+    auto tfull_bar = [&](int a) { return smem_u32(bars + 2 * STAGES + a); };
+    auto tempty_bar = [&](int a) { return smem_u32(bars + 2 * STAGES + 2 + a); };
+    const uint32_t drain_bar = smem_u32(bars + 2 * STAGES + 4);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();
+    const bool leader = rank == 0;
+    const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
+    const int G = p.G, NT = p.NT;
+
+    for (int g = threadIdx.x; g < G; g += kThreads) {
+        int a = 0, b = p.M;
+        if (p.offsets) {
+            a = p.offsets[g];
+            b = p.offsets[g + 1];
+        }
+        if (a < 0 || b < a || b > p.M) {
+            set_status(p.status, MOE_DEVERR_BAD_OFFSETS);
+            a = b = 0;
+        }
+        gstart[g] = a;
+        gend[g] = b;
+    }
+    if (threadIdx.x == 0) *abort_flag = 0;
+    __syncthreads();
+    if (warp == 0) {
+        int run = 0;
+        for (int g0 = 0; g0 < G; g0 += 32) {
+            const int g = g0 + lane;
+            const int v = g < G ? (gend[g] - gstart[g] + BM2 - 1) / BM2 * NT : 0;
+            int incl = v;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const int nb = __shfl_up_sync(0xffffffffu, incl, off);
+                if (lane >= off) incl += nb;
+            }
+            if (g < G) prefix[g] = run + incl - v;
+            run += __shfl_sync(0xffffffffu, incl, 31);
+        }
+        if (lane == 0) {
+            prefix[G] = run;
+            for (int s = 0; s < STAGES; ++s) {
+                mbar_init(full_bar(s), 1);
+                mbar_init(empty_bar(s), 1);
+            }
+            for (int a = 0; a < 2; ++a) {
+                mbar_init(tfull_bar(a), 1);
+                mbar_init(tempty_bar(a), 8);
+            }
+            mbar_init(drain_bar, 1);
+            asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            prefetch_tensormap(&mapA);
+            prefetch_tensormap(&mapB);
+        }
+    } else if (warp == 1) {
+        tmem_alloc_pair(smem_u32(tmem_slot), Cf::TMEM_COLS);
+    }
+    tc_fence_before();
+    cluster_sync_all();  // the peer's barriers exist before anything signals them
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    const int total = prefix[G];
+    const int KB = (p.K + BK - 1) / BK;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ---------------- TMA producer (both CTAs) ----------------
+            int s = 0;
+            uint32_t ph = 0, issued = 0, issued_par = 0;
+            bool ok = true;
+            for (int tile = pair; ok && tile < total; tile += npairs) {
+                int g, m, n, ks;
+                decode_tile(tile, prefix, G, NT, 1, g, m, n, ks);
+                const int row0 = gstart[g] + m * BM2 + (int)rank * 128;
+                const int brow = g * p.Nb + n * BN2 + (int)rank * (BN2 / 2);
+                for (int kb = 0; kb < KB; ++kb) {
+                    if (!wait_phase(empty_bar(s), ph ^ 1u, abort_flag, p.status)) {
+                        ok = false;
+                        break;
+                    }
+                    if (leader) mbar_arrive_expect_tx(full_bar(s), 2 * Cf::STAGE_BYTES);
+                    const uint32_t fb = mapa_shared(full_bar(s), 0);  // the leader's full[s]
+                    tma_load_2d_pair(smem_u32(sA + s * Cf::A_BYTES), &mapA, fb, kb * BK, row0);
+                    tma_load_2d_pair(smem_u32(sB + s * Cf::B_BYTES), &mapB, fb, kb * BK, brow);
+                    issued |= 1u << s;
+                    issued_par = (issued_par & ~(1u << s)) | (ph << s);
+                    if (++s == STAGES) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                }
+            }
+            if (leader) {
+                // the leader's full barriers count both CTAs' bytes of every stage it armed
+                for (int q = 0; q < STAGES; ++q)
+                    if ((issued >> q) & 1u) wait_drain(full_bar(q), (issued_par >> q) & 1u, p.status);
+            } else if (!ok) {
+                // stopped early: give copies still in flight time to land before exit
+                const uint64_t t0 = globaltimer();
+                while (globaltimer() - t0 < 200000ull) {
+                }
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0 && leader) {
+            // ---------------- MMA issuer (leader only) ----------------
+            int s = 0, acc = 0;
+            uint32_t ph = 0, aph = 0;
+            bool ok = true;
+            for (int tile = pair; ok && tile < total; tile += npairs) {
+                if (!wait_phase(tempty_bar(acc), aph ^ 1u, abort_flag, p.status)) break;
+                tc_fence_after();
+                const uint32_t d = tmem_base + (uint32_t)(acc * BN2);
+                for (int kb = 0; kb < KB; ++kb) {
+                    if (!wait_phase(full_bar(s), ph, abort_flag, p.status)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint64_t adesc = smem_desc_sw128(smem_u32(sA + s * Cf::A_BYTES));
+                    const uint64_t bdesc = smem_desc_sw128(smem_u32(sB + s * Cf::B_BYTES));
+#pragma unroll
+                    for (int kk = 0; kk < BK / UMMA_K; ++kk)
+                        mma_bf16_pair(d, adesc + 2u * kk, bdesc + 2u * kk, IDESC, (kb | kk) != 0);
+                    mma_commit_pair_mc(empty_bar(s), 0x3);
+                    if (++s == STAGES) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                mma_commit_pair_mc(tfull_bar(acc), 0x3);
+                if (++acc == 2) {
+                    acc = 0;
+                    aph ^= 1u;
+                }
+            }
+            mma_commit_pair(drain_bar);
+            wait_drain(drain_bar, 0, p.status);
+        }
+    } else {
+        // ---------------- epilogue: warps 2..5 of both CTAs ----------------
+        const int eg = warp & 3;
+        const int r = eg * 32 + lane;
+        int acc = 0;
+        uint32_t aph = 0;
+        for (int tile = pair; tile < total; tile += npairs) {
+            int g, m, n, ks;
+            decode_tile(tile, prefix, G, NT, 1, g, m, n, ks);
+            const int64_t row = (int64_t)gstart[g] + (int64_t)m * BM2 + (int64_t)rank * 128 + r;
+            const bool valid = row < gend[g];
+            if (!__all_sync(0xffffffffu, wait_phase(tfull_bar(acc), aph, abort_flag, p.status))) break;
+            tc_fence_after();
+            const uint32_t taddr = tmem_base + ((uint32_t)(eg * 32) << 16) + (uint32_t)(acc * BN2);
+            if (EPI == TC_EPI_SWIGLU) {
+#pragma unroll 1
+                for (int c = 0; c < kPackBlock; c += 32) {
+                    uint32_t gr[32], ur[32];
+                    tmem_ld32(taddr + c, gr);
+                    tmem_ld32(taddr + kPackBlock + c, ur);
+                    float h[32];
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        const float gv = __uint_as_float(gr[i]);
+                        h[i] = gv / (1.0f + __expf(-gv)) * __uint_as_float(ur[i]);
+                    }
+                    if (valid) store_row32<EPI>(p.C, p.ldc, row, n * kPackBlock + c, p.N, h);
+                }
+            } else {
+#pragma unroll 1
+                for (int c = 0; c < BN2; c += 32) {
+                    uint32_t vr[32];
+                    tmem_ld32(taddr + c, vr);
+                    float v[32];
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(vr[i]);
+                    if (valid) store_row32<EPI>(p.C, p.ldc, row, n * BN2 + c, p.N, v);
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                if (leader) mbar_arrive(tempty_bar(acc));
+                else mbar_arrive_cluster(mapa_shared(tempty_bar(acc), 0));
+            }
+            if (++acc == 2) {
+                acc = 0;
+                aph ^= 1u;
+            }
+        }
+    }
+
+    __syncwarp();
+    tc_fence_before();
+    cluster_sync_all();  // every pair MMA has completed and no CTA signals the other any more
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc_pair(tmem_base, Cf::TMEM_COLS);
+    }
+}
+
 // K slices actually launched for a requested count: each slice takes
 // ceil(KB / requested) k-blocks, so none is left empty.
 int effective_splits(int K, int requested) {
@@ -398,6 +664,81 @@ moe_status_t launch_impl(const TcGroupedGemm& g, cudaStream_t s) {
     return last_launch_status();
 }
 
+template <int EPI>
+moe_status_t launch_pair(const TcGroupedGemm& g, cudaStream_t s) {
+    using Cf = Cfg2;
+    static std::once_flag attr_once[64];
+    static int max_clusters[64];
+    int dev = 0;
+    MOE_CUDA_TRY(cudaGetDevice(&dev));
+    cudaError_t attr_err = cudaSuccess;
+
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = Cf::SMEM;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+
+    std::call_once(attr_once[dev & 63], [&] {
+        attr_err = cudaFuncSetAttribute(tc_pair_gemm_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        (int)Cf::SMEM);
+        if (attr_err != cudaSuccess) return;
+        // pairs that fit on the device at once (clusters live within one GPC)
+        cudaLaunchConfig_t q = cfg;
+        q.gridDim = dim3(2 * (sm_count() / 2));
+        int n = 0;
+        attr_err = cudaOccupancyMaxActiveClusters(&n, tc_pair_gemm_kernel<EPI>, &q);
+        max_clusters[dev & 63] = n;
+    });
+    MOE_CUDA_TRY(attr_err);
+    const int pairs_max = max_clusters[dev & 63];
+    if (pairs_max < 1) return MOE_ERR_UNSUPPORTED;
+
+    CUtensorMap ma, mb;
+    if (!make_map(&ma, g.A, (uint64_t)g.K, (uint64_t)g.M, 128)) return MOE_ERR_CUDA;
+    if (!make_map(&mb, g.B, (uint64_t)g.K, (uint64_t)g.G * g.Nb, BN2 / 2)) return MOE_ERR_CUDA;
+
+    Params p;
+    p.offsets = g.offsets;
+    p.G = g.G;
+    p.M = g.M;
+    p.K = g.K;
+    p.Nb = g.Nb;
+    p.N = g.N;
+    p.NT = EPI == TC_EPI_SWIGLU ? g.Nb / BN2 : (int)ceil_div(g.N, BN2);
+    p.ksplit = 1;
+    p.c_split_stride = 0;
+    p.C = g.C;
+    p.ldc = g.ldc;
+    p.status = g.status;
+
+    const int64_t max_tiles = (int64_t)p.NT * (ceil_div(g.M, BM2) + (g.offsets ? g.G : 0));
+    const int pairs = (int)std::max<int64_t>(1, std::min<int64_t>(pairs_max, max_tiles));
+    cfg.gridDim = dim3(2 * pairs);
+    MOE_CUDA_TRY(cudaLaunchKernelEx(&cfg, tc_pair_gemm_kernel<EPI>, ma, mb, p));
+    note_launch();
+    return last_launch_status();
+}
+
+// Tile shape for the bf16 / SwiGLU outputs.  MOE_GEMM_TILE = "single" or "pair"
+// forces one; otherwise pair tiles (256 rows) are used once the groups average
+// 256 rows or more, where the halved operand fill per SM pays, and single-CTA
+// tiles (128 rows) below that, where a pair tile would mostly hold the next
+// group's rows and double the A traffic.
+bool use_pair_tiles(const TcGroupedGemm& g) {
+    if (const char* e = std::getenv("MOE_GEMM_TILE")) {
+        if (std::strcmp(e, "single") == 0) return false;
+        if (std::strcmp(e, "pair") == 0) return true;
+    }
+    return (int64_t)g.M >= (int64_t)BM2 * g.G;
+}
+
 // Gate-style launches (one dense problem, fp32 out): pick the n-tile width and
 // the number of K slices.  A CTA's k-blocks run at roughly the larger of their
 // MMA time (2*BN cycles), their operand fill ((16 KB + BN*128 B) at ~128 B per
@@ -441,9 +782,9 @@ moe_status_t launch_tc_grouped_gemm(const TcGroupedGemm& g, cudaStream_t s) {
     switch (g.epi) {
         case TC_EPI_SWIGLU:
             if (g.Nb % (2 * kPackBlock) != 0) return MOE_ERR_INVALID_ARG;
-            return launch_impl<256, TC_EPI_SWIGLU>(g, s);
+            return use_pair_tiles(g) ? launch_pair<TC_EPI_SWIGLU>(g, s) : launch_impl<256, TC_EPI_SWIGLU>(g, s);
         case TC_EPI_BF16:
-            return launch_impl<256, TC_EPI_BF16>(g, s);
+            return use_pair_tiles(g) ? launch_pair<TC_EPI_BF16>(g, s) : launch_impl<256, TC_EPI_BF16>(g, s);
         case TC_EPI_F32: {
             int bn, split;
             plan_f32(g.M, g.N, g.K, std::max(1, g.ksplit), bn, split);

@@ -263,6 +263,45 @@ def test_grouped_ffn_dense_single_group(oracle):
     assert rel_l2(y, ref) <= 1e-2
 
 
+# Both tile shapes of the bf16 GEMM on the same cases: 128-row tiles on one SM,
+# and 256-row pair tiles on a two-CTA cluster (tcgen05.mma.cta_group::2).
+TILE_CASES = [
+    (1000, 2, 8, 512, 384),    # ~250 rows per expert: pair tiles cut inside the peer's half
+    (2000, 4, 8, 264, 200),    # ~1000 rows: several pair tiles; K tails; down N tail (264 = 256 + 8)
+    (300, 6, 64, 512, 256),    # ~28 rows per expert: the peer's rows lie past the expert
+    (64, 8, 256, 128, 128),    # most experts empty
+    (3, 1, 4, 64, 128),        # tiny
+]
+
+
+@pytest.mark.parametrize("tile", ["single", "pair"])
+@pytest.mark.parametrize("T,k,E,H,I", TILE_CASES)
+def test_grouped_ffn_bf16_tile_shapes(oracle, monkeypatch, tile, T, k, E, H, I):
+    monkeypatch.setenv("MOE_GEMM_TILE", tile)
+    y, ref, _ = _ffn_case(oracle, T, k, E, H, I, torch.bfloat16, seed=T + E + 1)
+    assert rel_l2(y, ref) <= 1e-2
+
+
+@pytest.mark.parametrize("tile", ["single", "pair"])
+def test_grouped_ffn_bf16_tile_shapes_skewed_and_dense(oracle, monkeypatch, tile):
+    monkeypatch.setenv("MOE_GEMM_TILE", tile)
+    T, k, E = 1500, 2, 16
+    w = torch.tensor([40.0] + [1.0] * 7 + [0.5] * 8)
+    ids = inputs.random_ids(T, k, E, seed=21, weights=w)
+    y, ref, ir = _ffn_case(oracle, T, k, E, 256, 128, torch.bfloat16, seed=5, ids=ids)
+    assert ir["tokens_per_expert"].max() > 1000
+    assert rel_l2(y, ref) <= 1e-2
+    # one group of all rows, no offsets (the shared-expert call)
+    cfg = inputs.LayerConfig("s", T=777, H=320, E=1, k=1, I=256, S=0, dtype="bf16", seed=6)
+    d = inputs.make_layer(cfg, DEV)
+    w13 = binding.moe_pack_w13(d["w_gate"], d["w_up"])
+    y, ws = binding.moe_grouped_ffn(d["x"], None, 1, 256, w13, d["w2"])
+    assert binding.moe_check_device_status(ws) == 0
+    ref = oracle.expert_ffn_rows(np_(d["x"]), np.zeros(777, np.int32), np_(d["w_gate"]), np_(d["w_up"]),
+                                 np_(d["w2"]))
+    assert rel_l2(y, ref) <= 1e-2
+
+
 @pytest.mark.parametrize("T,k,E,H,I", [(64, 2, 16, 256, 128), (100, 3, 7, 72, 40)])
 def test_grouped_ffn_fp32(oracle, T, k, E, H, I):
     y, ref, _ = _ffn_case(oracle, T, k, E, H, I, torch.float32, seed=T)

@@ -126,6 +126,19 @@ def test_layer_small(oracle, cfg):
     check_layer(oracle, cfg, d, layer, out)
 
 
+PAIR = [c for c in SMALL if c.dtype == "bf16" and c.name in ("small_bf16", "ragged_bf16", "zipf_bf16",
+                                                                 "grouped_bf16", "dense_E1_bf16")]
+
+
+@pytest.mark.parametrize("cfg", PAIR, ids=[c.name for c in PAIR])
+def test_layer_small_pair_tiles(oracle, monkeypatch, cfg):
+    """The whole layer with every bf16 expert GEMM on 256-row pair tiles."""
+    monkeypatch.setenv("MOE_GEMM_TILE", "pair")
+    d, layer = make(cfg)
+    out = layer.forward(d["x"])
+    check_layer(oracle, cfg, d, layer, out)
+
+
 # H sweeps the gate GEMM's k-block count (1 .. 17, with K tails) and T its tile
 # count, so the K-split plan takes several slice counts, each slice non-empty.
 GATE_SPLIT = [(T, H) for T in (40, 700) for H in (24, 136, 264, 328, 584, 1096)]
