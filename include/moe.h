@@ -238,8 +238,9 @@ moe_status_t moe_quantize_weights_fp8(const void* w, moe_dtype_t dt, int G, int 
 /* Grouped SwiGLU expert FFN with FP8 weights and activations ([BLOG
  * §Quantization], [BLOG §Roofline / GroupGEMM]): products are block-scaled,
  *   C[m,n] = sum_b sa[m,b] * sb[n/128,b] * sum_{k in block b} qa[m,k] qb[n,k],
- * h = silu(gate) * up is stored in bf16 and quantised in 1x128 blocks for the
- * down projection; y [rows, H] bf16.  aq [rows, H] codes with a_scales
+ * h = silu(gate) * up is rounded to bf16 and quantised in 1x128 blocks for the
+ * down projection by the up GEMM's own epilogue (the workspace keeps the bf16
+ * h, its codes and its scales); y [rows, H] bf16.  aq [rows, H] codes with a_scales
  * [rows, lda_scales]; w13q/w13s and w2q/w2s from moe_quantize_weights_fp8;
  * expert_offsets as in moe_grouped_ffn.  H % 256 == 0, I % 16 == 0.
  * ws: moe_grouped_ffn_fp8_workspace_bytes(rows, I) bytes. */

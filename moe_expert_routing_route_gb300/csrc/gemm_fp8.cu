@@ -15,9 +15,16 @@
 // buffers.  Eight epilogue warps -- two per TMEM lane group, each owning half of
 // the tile's columns -- fold every partial into register accumulators with
 // sa * sb (the promotion the block scales need), then apply SwiGLU or convert
-// and store once per tile.  Rows of a tile past the expert's segment are
+// and store once per tile.  With a code buffer, the SwiGLU epilogue also
+// quantises h for the down projection in place (the 1x128 activation blocks of
+// §Quantization, computed on the fly): h is rounded to bf16, the two warps that
+// hold the two 64-column halves of a 128-column block swap their partial amax
+// through shared memory (an mbarrier per TMEM lane group, bounded wait), and
+// each writes its 64 e4m3 codes; the half-0 warp writes the block's scale.
+// Rows of a tile past the expert's segment are
 // computed and never stored, as in the bf16 kernel.  Waits are bounded as in
 // the bf16 kernel (about one second, then abort without trapping).
+#include "fp8_codec.cuh"
 #include "tc_ptx.cuh"
 
 #include <climits>
@@ -39,8 +46,10 @@ constexpr int B_BYTES = BN * BK;
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int STAGES = 4;
 constexpr int TMEM_COLS = 2 * BN;  // two partial buffers
-constexpr int NUM_BARS = 2 * STAGES + 5;
-constexpr size_t SMEM = 1024 + (size_t)STAGES * STAGE_BYTES + NUM_BARS * 8 + 16 + (size_t)(3 * kMaxGroups + 1) * 4;
+constexpr int NUM_BARS = 2 * STAGES + 9;  // full, empty, partial full/empty, drain, 4 amax exchanges
+constexpr int XAMAX_FLOATS = 2 * 2 * BM;   // [tile parity][column half][row]
+constexpr size_t SMEM = 1024 + (size_t)STAGES * STAGE_BYTES + NUM_BARS * 8 + 16 + (size_t)(3 * kMaxGroups + 1) * 4 +
+                        (size_t)XAMAX_FLOATS * 4;
 
 struct Params {
     const int32_t* offsets;  // [G+1] or nullptr: one group of M rows
@@ -50,6 +59,9 @@ struct Params {
     const float* a_scales;  // [M][lda_s]
     int lda_s;
     const float* b_scales;  // [G][Nb/128][KB]
+    uint8_t* q;             // SwiGLU only, nullable: e4m3 codes of h [M][N]
+    float* q_scales;        // [M][ldq]: one per 1x128 block of h
+    int ldq;
     uint32_t* status;
 };
 
@@ -66,6 +78,9 @@ __device__ __forceinline__ void decode_tile(int tile, const int* prefix, int G, 
     n = local / mt;
     m = local - n * mt;
 }
+
+// Parity of the index of `tile` among this CTA's tiles (blockIdx.x, +gridDim.x, ...).
+__device__ __forceinline__ int tile_parity(int tile, int first, int stride) { return ((tile - first) / stride) & 1; }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
     __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
@@ -109,12 +124,14 @@ tc_fp8_grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __gri
     int* prefix = reinterpret_cast<int*>(tmem_slot + 4);
     int* gstart = prefix + kMaxGroups + 1;
     int* gend = gstart + kMaxGroups;
+    float* xamax = reinterpret_cast<float*>(gend + kMaxGroups);  // [2][2][BM]
 
     auto full_bar = [&](int s) { return smem_u32(bars + s); };
     auto empty_bar = [&](int s) { return smem_u32(bars + STAGES + s); };
     auto pfull_bar = [&](int j) { return smem_u32(bars + 2 * STAGES + j); };
     auto pempty_bar = [&](int j) { return smem_u32(bars + 2 * STAGES + 2 + j); };
     const uint32_t drain_bar = smem_u32(bars + 2 * STAGES + 4);
+    auto xchg_bar = [&](int eg) { return smem_u32(bars + 2 * STAGES + 5 + eg); };
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int G = p.G, NT = p.NT, KB = p.KB;
@@ -159,6 +176,7 @@ tc_fp8_grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __gri
                 mbar_init(pempty_bar(j), kEpiWarps);
             }
             mbar_init(drain_bar, 1);
+            for (int eg = 0; eg < 4; ++eg) mbar_init(xchg_bar(eg), 2);  // the two warps of a lane group
             asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             prefetch_tensormap(&mapA);
@@ -250,7 +268,7 @@ tc_fp8_grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __gri
         const int nbB = EPI == TC_EPI_SWIGLU ? 1 : half;
         const int nblocks = p.Nb / 128;
         int j = 0;
-        uint32_t pph = 0;
+        uint32_t pph = 0, xph = 0;
         float acc[128];
         bool ok = true;
         for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
@@ -297,17 +315,48 @@ tc_fp8_grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __gri
                 }
             }
             if (!ok) break;
-            if (valid) {
-                __nv_bfloat16* C = static_cast<__nv_bfloat16*>(p.C);
-                if (EPI == TC_EPI_SWIGLU) {
-                    float h[64];
+            __nv_bfloat16* C = static_cast<__nv_bfloat16*>(p.C);
+            if (EPI == TC_EPI_SWIGLU) {
+                // h in bf16 (the precision it is stored and quantised in)
+                float h[64];
+                float am = 0.0f;
 #pragma unroll
-                    for (int i = 0; i < 64; ++i) h[i] = acc[i] / (1.0f + __expf(-acc[i])) * acc[64 + i];
-                    store_row64(C, p.ldc, row, n * 128 + half * 64, p.N, h);
-                } else {
-                    store_row64(C, p.ldc, row, n * BN + colA, p.N, acc);
-                    store_row64(C, p.ldc, row, n * BN + colB, p.N, acc + 64);
+                for (int i = 0; i < 64; ++i) {
+                    h[i] = __bfloat162float(__float2bfloat16_rn(acc[i] / (1.0f + __expf(-acc[i])) * acc[64 + i]));
+                    am = fmaxf(am, fabsf(h[i]));
                 }
+                const int col0 = n * 128 + half * 64;
+                if (valid && C) store_row64(C, p.ldc, row, col0, p.N, h);
+                if (p.q) {
+                    // amax of the 128-column block: this half's and the other warp's
+                    float* slot = xamax + (tile_parity(tile, blockIdx.x, gridDim.x) * 2) * BM;
+                    slot[half * BM + r] = am;
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(xchg_bar(eg));
+                    if (!__all_sync(0xffffffffu, wait_phase_fast(xchg_bar(eg), xph, abort_flag, p.status))) break;
+                    xph ^= 1u;
+                    const float sc = fp8::block_scale(fmaxf(am, slot[(1 - half) * BM + r]));
+                    if (valid) {
+                        uint8_t* qrow = p.q + row * (int64_t)p.N + col0;
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) {  // 16 codes per store; N % 16 == 0
+                            if (col0 + 16 * c < p.N) {
+                                uint32_t w4[4];
+#pragma unroll
+                                for (int t = 0; t < 4; ++t)
+                                    w4[t] = fp8::e4m3(h[16 * c + 4 * t] / sc) |
+                                            (fp8::e4m3(h[16 * c + 4 * t + 1] / sc) << 8) |
+                                            (fp8::e4m3(h[16 * c + 4 * t + 2] / sc) << 16) |
+                                            (fp8::e4m3(h[16 * c + 4 * t + 3] / sc) << 24);
+                                reinterpret_cast<uint4*>(qrow)[c] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+                            }
+                        }
+                        if (half == 0) p.q_scales[row * (int64_t)p.ldq + n] = sc;
+                    }
+                }
+            } else if (valid) {
+                store_row64(C, p.ldc, row, n * BN + colA, p.N, acc);
+                store_row64(C, p.ldc, row, n * BN + colB, p.N, acc + 64);
             }
         }
     }
@@ -349,6 +398,9 @@ moe_status_t launch_impl(const TcFp8GroupedGemm& g, cudaStream_t s) {
     p.a_scales = g.a_scales;
     p.lda_s = g.lda_scales;
     p.b_scales = g.b_scales;
+    p.q = g.q;
+    p.q_scales = g.q_scales;
+    p.ldq = g.ldq;
     p.status = g.status;
     const int64_t max_tiles = (int64_t)p.NT * (ceil_div(g.M, BM) + (g.offsets ? g.G : 0));
     const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(sm_count(), max_tiles));
@@ -363,6 +415,9 @@ moe_status_t launch_tc_fp8_grouped_gemm(const TcFp8GroupedGemm& g, cudaStream_t 
     if (g.M == 0 || g.G == 0) return MOE_OK;
     if (g.G > kMaxGroups) return MOE_ERR_UNSUPPORTED;
     if (g.Nb % BN != 0 || g.K % 16 != 0) return MOE_ERR_INVALID_ARG;
+    if (g.q && (g.epi != TC_EPI_SWIGLU || g.N % 16 != 0 || !g.q_scales || g.ldq < (int)ceil_div(g.N, 128)))
+        return MOE_ERR_INVALID_ARG;
+    if (!g.q && !g.C) return MOE_ERR_INVALID_ARG;
     switch (g.epi) {
         case TC_EPI_SWIGLU: return launch_impl<TC_EPI_SWIGLU>(g, s);
         case TC_EPI_BF16: return launch_impl<TC_EPI_BF16>(g, s);

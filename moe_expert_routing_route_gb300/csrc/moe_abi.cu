@@ -76,10 +76,11 @@ moe_status_t ffn_up_fp8(const uint8_t* aq, const float* as, int lda_s, const int
                         int I, const void* w13q, const float* w13s, void* h, uint8_t* hq, float* hs,
                         uint32_t* status, cudaStream_t s) {
     if (rows == 0) return MOE_OK;
+    // the SwiGLU epilogue writes the down projection's FP8 input directly; bf16 h
+    // is stored too only when the caller gives a buffer for it (h may be null)
     TcFp8GroupedGemm up{aq, rows, H, offsets, G, w13q, packed_rows(I), I, h, I, TC_EPI_SWIGLU, as, lda_s,
-                        w13s, status};
-    MOE_TRY(launch_tc_fp8_grouped_gemm(up, s));
-    return launch_quantize_rows_fp8(h, MOE_BF16, rows, I, hq, hs, scale_ld(I), s);
+                        w13s, status, hq, hs, scale_ld(I)};
+    return launch_tc_fp8_grouped_gemm(up, s);
 }
 
 moe_status_t ffn_down_fp8(const uint8_t* hq, const float* hs, const int32_t* offsets, int G, int rows, int H, int I,
@@ -246,8 +247,52 @@ moe_status_t side_stream(SideStream** out) {
     return MOE_OK;
 }
 
+// Host-buffer path: x arrives and out leaves in row chunks on two library-owned
+// copy streams, so the copies overlap the shared experts (x side) and the
+// finalize kernel (out side) instead of bracketing the whole layer.
+constexpr int kMaxIoChunks = 8;
+struct HostPipe {
+    cudaStream_t h2d = nullptr, d2h = nullptr;
+    cudaEvent_t entry = nullptr, done = nullptr, in[kMaxIoChunks] = {}, out[kMaxIoChunks] = {};
+    std::mutex mu;
+};
+HostPipe g_pipe[64];
+std::mutex g_pipe_init;
+
+moe_status_t host_pipe(HostPipe** out) {
+    int dev = 0;
+    MOE_CUDA_TRY(cudaGetDevice(&dev));
+    if (dev < 0 || dev >= 64) return MOE_ERR_UNSUPPORTED;
+    HostPipe& hp = g_pipe[dev];
+    std::lock_guard<std::mutex> lock(g_pipe_init);
+    if (!hp.h2d) {
+        MOE_CUDA_TRY(cudaStreamCreateWithFlags(&hp.h2d, cudaStreamNonBlocking));
+        MOE_CUDA_TRY(cudaStreamCreateWithFlags(&hp.d2h, cudaStreamNonBlocking));
+        MOE_CUDA_TRY(cudaEventCreateWithFlags(&hp.entry, cudaEventDisableTiming));
+        MOE_CUDA_TRY(cudaEventCreateWithFlags(&hp.done, cudaEventDisableTiming));
+        for (int c = 0; c < kMaxIoChunks; ++c) {
+            MOE_CUDA_TRY(cudaEventCreateWithFlags(&hp.in[c], cudaEventDisableTiming));
+            MOE_CUDA_TRY(cudaEventCreateWithFlags(&hp.out[c], cudaEventDisableTiming));
+        }
+    }
+    *out = &hp;
+    return MOE_OK;
+}
+
+struct HostIO {
+    const void* x_host;  // [T,H] dt, copied into the x buffer the layer reads
+    void* out_host;      // [T,H] dt, receives the layer's output
+    HostPipe* pipe;
+};
+
+// Rows [c0, c1) of chunk c when T rows are cut into n nearly equal chunks.
+inline void chunk_rows(int T, int n, int c, int& c0, int& c1) {
+    c0 = (int)((int64_t)T * c / n);
+    c1 = (int)((int64_t)T * (c + 1) / n);
+}
+
 moe_status_t layer_forward(const moe_layer_desc* d, const void* x, void* out, void* ws, size_t ws_bytes,
-                           cudaStream_t s, void* const* ev) {
+                           cudaStream_t s, void* const* ev, const HostIO* io = nullptr) {
     MOE_TRY(check_desc(d));
     if (!x || !out || !ws) return MOE_ERR_INVALID_ARG;
     if (!aligned16(x) || !aligned16(out) || !aligned16(ws)) return MOE_ERR_UNSUPPORTED;
@@ -294,19 +339,57 @@ moe_status_t layer_forward(const moe_layer_desc* d, const void* x, void* out, vo
     if (side) side_lock = std::unique_lock<std::mutex>(side->mu);
 
     MOE_TRY(clear_status(ws, s));
+    const size_t row_bytes = (size_t)H * dt_size(dt);
+    // host path: chunks of T/1024 rows (at most kMaxIoChunks), one when T is small
+    const int io_chunks = io ? std::max(1, std::min(kMaxIoChunks, (T + 1023) / 1024)) : 0;
+    const bool chunked_shared = io && side && !fp8;  // FP8 shared experts read x quantised on the main stream
+    if (io) {
+        HostPipe* hp = io->pipe;
+        MOE_CUDA_TRY(cudaEventRecord(hp->entry, s));  // after the status reset and all earlier work on s
+        MOE_CUDA_TRY(cudaStreamWaitEvent(hp->h2d, hp->entry, 0));
+        for (int c = 0; c < io_chunks; ++c) {
+            int c0, c1;
+            chunk_rows(T, io_chunks, c, c0, c1);
+            MOE_CUDA_TRY(cudaMemcpyAsync(static_cast<char*>(const_cast<void*>(x)) + (size_t)c0 * row_bytes,
+                                         static_cast<const char*>(io->x_host) + (size_t)c0 * row_bytes,
+                                         (size_t)(c1 - c0) * row_bytes, cudaMemcpyHostToDevice, hp->h2d));
+            MOE_CUDA_TRY(cudaEventRecord(hp->in[c], hp->h2d));
+        }
+        if (chunked_shared) {
+            // shared experts chunk by chunk as x arrives (they depend on x alone)
+            cudaStream_t ss = side->stream;
+            MOE_CUDA_TRY(cudaStreamWaitEvent(ss, hp->entry, 0));
+            MOE_TRY(mark(ev, ST_SHARED, 0, ss));
+            for (int c = 0; c < io_chunks; ++c) {
+                int c0, c1;
+                chunk_rows(T, io_chunks, c, c0, c1);
+                MOE_CUDA_TRY(cudaStreamWaitEvent(ss, hp->in[c], 0));
+                const char* xc = static_cast<const char*>(x) + (size_t)c0 * row_bytes;
+                char* hsc = static_cast<char*>(hs) + (size_t)c0 * SI * dt_size(dt);
+                char* ysc = static_cast<char*>(ys) + (size_t)c0 * row_bytes;
+                MOE_TRY(ffn_up(xc, dt, nullptr, 1, c1 - c0, H, SI, d->w13_shared, hsc, status, ss));
+                MOE_TRY(ffn_down(hsc, dt, nullptr, 1, c1 - c0, H, SI, d->w2_shared, ysc, status, ss));
+            }
+            MOE_TRY(mark(ev, ST_SHARED, 1, ss));
+            MOE_CUDA_TRY(cudaEventRecord(side->join, ss));
+        }
+        MOE_CUDA_TRY(cudaStreamWaitEvent(s, hp->in[io_chunks - 1], 0));  // the gate reads all of x
+    }
     MOE_TRY(mark(ev, ST_GATE, 0, s));
     int nsplit = 1;
     MOE_TRY(layer_gate(*d, x, logits, &nsplit, s));
     if (fp8) MOE_TRY(launch_quantize_rows_fp8(x, dt, T, H, xq, xs, ldx, s));  // activations, 1x128 blocks
     MOE_TRY(mark(ev, ST_GATE, 1, s));
-    if (side) {
+    if (chunked_shared) {
+        // launched above
+    } else if (side) {
         // fork: shared experts on the side stream, after the gate
         MOE_CUDA_TRY(cudaEventRecord(side->fork, s));
         MOE_CUDA_TRY(cudaStreamWaitEvent(side->stream, side->fork, 0));
         cudaStream_t ss = side->stream;
         MOE_TRY(mark(ev, ST_SHARED, 0, ss));
         if (fp8) {
-            MOE_TRY(ffn_up_fp8(xq, xs, ldx, nullptr, 1, T, H, SI, d->w13_shared, d->w13_shared_scales, hs, hsq, hss,
+            MOE_TRY(ffn_up_fp8(xq, xs, ldx, nullptr, 1, T, H, SI, d->w13_shared, d->w13_shared_scales, nullptr, hsq, hss,
                                status, ss));
             MOE_TRY(ffn_down_fp8(hsq, hss, nullptr, 1, T, H, SI, d->w2_shared, d->w2_shared_scales, ys, status, ss));
         } else {
@@ -337,7 +420,7 @@ moe_status_t layer_forward(const moe_layer_desc* d, const void* x, void* out, vo
     // join: the routed GEMMs need every SM, so they start after the shared experts
     if (side) MOE_CUDA_TRY(cudaStreamWaitEvent(s, side->join, 0));
     MOE_TRY(mark(ev, ST_UP, 0, s));
-    if (fp8) MOE_TRY(ffn_up_fp8(exq, exs, ldx, offsets, E, R, H, I, d->w13, d->w13_scales, h, hq, hqs, status, s));
+    if (fp8) MOE_TRY(ffn_up_fp8(exq, exs, ldx, offsets, E, R, H, I, d->w13, d->w13_scales, nullptr, hq, hqs, status, s));
     else MOE_TRY(ffn_up(ex, dt, offsets, E, R, H, I, d->w13, h, status, s));
     MOE_TRY(mark(ev, ST_UP, 1, s));
     MOE_TRY(mark(ev, ST_DOWN, 0, s));
@@ -345,7 +428,26 @@ moe_status_t layer_forward(const moe_layer_desc* d, const void* x, void* out, vo
     else MOE_TRY(ffn_down(h, dt, offsets, E, R, H, I, d->w2, y, status, s));
     MOE_TRY(mark(ev, ST_DOWN, 1, s));
     MOE_TRY(mark(ev, ST_FINALIZE, 0, s));
-    MOE_TRY(launch_finalize(y, R, SI > 0 ? ys : nullptr, w, row_idx, dt, T, H, k, out, status, s));
+    if (!io) {
+        MOE_TRY(launch_finalize(y, R, SI > 0 ? ys : nullptr, w, row_idx, dt, T, H, k, out, status, s));
+    } else {
+        // finalize chunk c, then its rows leave on the copy stream while chunk c+1 runs
+        HostPipe* hp = io->pipe;
+        for (int c = 0; c < io_chunks; ++c) {
+            int c0, c1;
+            chunk_rows(T, io_chunks, c, c0, c1);
+            const size_t o = (size_t)c0 * row_bytes;
+            MOE_TRY(launch_finalize(y, R, SI > 0 ? static_cast<const char*>(ys) + o : nullptr, w + (size_t)c0 * k,
+                                    row_idx + (size_t)c0 * k, dt, c1 - c0, H, k, static_cast<char*>(out) + o,
+                                    status, s));
+            MOE_CUDA_TRY(cudaEventRecord(hp->out[c], s));
+            MOE_CUDA_TRY(cudaStreamWaitEvent(hp->d2h, hp->out[c], 0));
+            MOE_CUDA_TRY(cudaMemcpyAsync(static_cast<char*>(io->out_host) + o, static_cast<const char*>(out) + o,
+                                         (size_t)(c1 - c0) * row_bytes, cudaMemcpyDeviceToHost, hp->d2h));
+        }
+        MOE_CUDA_TRY(cudaEventRecord(hp->done, hp->d2h));
+        MOE_CUDA_TRY(cudaStreamWaitEvent(s, hp->done, 0));  // the caller's stream covers the copies
+    }
     MOE_TRY(mark(ev, ST_FINALIZE, 1, s));
     return MOE_OK;
 }
@@ -726,10 +828,12 @@ moe_status_t moe_layer_forward_host(const moe_layer_desc* desc, const void* x_ho
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     void* xin = at<void>(ws, L.off[MOE_WS_X_IN]);
     void* xout = at<void>(ws, L.off[MOE_WS_OUT]);
-    const size_t bytes = L.bytes[MOE_WS_X_IN];
-    if (bytes) MOE_CUDA_TRY(cudaMemcpyAsync(xin, x_host, bytes, cudaMemcpyHostToDevice, s));
-    MOE_TRY(layer_forward(desc, xin, xout, ws, ws_bytes, s, nullptr));
-    if (bytes) MOE_CUDA_TRY(cudaMemcpyAsync(out_host, xout, bytes, cudaMemcpyDeviceToHost, s));
+    if (desc->T == 0) return MOE_OK;
+    HostPipe* hp = nullptr;
+    MOE_TRY(host_pipe(&hp));
+    std::lock_guard<std::mutex> lock(hp->mu);
+    const HostIO io{x_host, out_host, hp};
+    MOE_TRY(layer_forward(desc, xin, xout, ws, ws_bytes, s, nullptr, &io));
     MOE_CUDA_TRY(cudaStreamSynchronize(s));
     return MOE_OK;
 }

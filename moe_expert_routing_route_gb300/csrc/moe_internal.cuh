@@ -133,6 +133,9 @@ struct TcFp8GroupedGemm {
     int lda_scales;
     const float* b_scales;    // [G][Nb/128][ceil(K/128)]: one per 128x128 tile of B
     uint32_t* status;
+    uint8_t* q = nullptr;     // SwiGLU: also quantise h in 1x128 blocks into codes [M, N] (C may then be null)
+    float* q_scales = nullptr;  // [M][ldq]
+    int ldq = 0;
 };
 moe_status_t launch_tc_fp8_grouped_gemm(const TcFp8GroupedGemm& g, cudaStream_t s);
 int tc_packed_block();        // rows of gate (and of up) per packed block: 128

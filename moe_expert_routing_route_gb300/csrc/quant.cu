@@ -6,19 +6,17 @@
 // 128x128 tile for weights (static).  A block's scale is amax/448 in fp32 (1
 // for an all-zero block); each value becomes the e4m3 code of fl32(v / scale),
 // rounded to nearest even and saturated at +-448.
+#include "fp8_codec.cuh"
 #include "moe_internal.cuh"
-
-#include <cuda_fp8.h>
 
 namespace moe {
 namespace {
 
+using fp8::block_scale;
+using fp8::e4m3;
+
 __device__ __forceinline__ float to_f(__nv_bfloat16 v) { return __bfloat162float(v); }
 __device__ __forceinline__ float to_f(float v) { return v; }
-__device__ __forceinline__ uint32_t e4m3(float v) {
-    return (uint32_t)__nv_cvt_float_to_fp8(v, __NV_SATFINITE, __NV_E4M3);
-}
-__device__ __forceinline__ float block_scale(float amax) { return amax > 0.0f ? amax / 448.0f : 1.0f; }
 
 __device__ __forceinline__ void load4(const __nv_bfloat16* p, float (&v)[4]) {
     const uint2 u = __ldg(reinterpret_cast<const uint2*>(p));

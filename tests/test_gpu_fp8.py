@@ -86,6 +86,23 @@ def test_grouped_ffn_fp8(oracle, T, k, E, H, I):
     expert_of_row = np.repeat(np.arange(E, dtype=np.int32), ir["tokens_per_expert"])
     ref = oracle.expert_ffn_rows_fp8(xq, xs, expert_of_row, q)
     assert rel_l2(y, ref) <= 1e-2
+    # The up GEMM's epilogue quantises h itself; its codes and scales are those the
+    # 1x128 quantiser gives for the bf16 h stored beside them.  Workspace of this
+    # entry point: 256-byte header, h [rows, I] bf16, codes [rows, I], scales
+    # [rows, scale_ld(I)], each region 256-byte aligned.
+    rows, ld = T * k, binding.scale_ld(I)
+    up = lambda b: -(-b // 256) * 256  # noqa: E731
+    h = ws[256:256 + rows * I * 2].view(torch.bfloat16).view(rows, I)
+    o = 256 + up(rows * I * 2)
+    hq = ws[o:o + rows * I].view(rows, I)
+    o += up(rows * I)
+    hs = ws[o:o + rows * ld * 4].view(torch.float32).view(rows, ld)
+    rq, rs = binding.moe_quantize_rows_fp8(h, ld_scales=ld)
+    nb = -(-I // 128)
+    assert torch.equal(hq, rq) and torch.equal(hs[:, :nb], rs[:, :nb])
+    # and both are the oracle's quantisation of that h
+    oq, os_ = oracle.quantize_rows_fp8(np_(h))
+    assert np.array_equal(hq.cpu().numpy(), oq) and np.array_equal(hs[:, :nb].cpu().numpy(), os_)
 
 
 FP8_LAYERS = [

@@ -205,14 +205,34 @@ def test_layer_deterministic_and_graph_capturable(oracle):
     check_layer(oracle, cfg, d, layer, static_out)
 
 
-def test_layer_forward_host_matches_device():
-    cfg = inputs.LayerConfig("host_bf16", T=256, H=256, E=32, k=4, I=128, S=1, dtype="bf16", seed=22)
-    d, layer = make(cfg)
-    dev_out = layer.forward(d["x"])
+HOST = [
+    inputs.LayerConfig("host_bf16", T=256, H=256, E=32, k=4, I=128, S=1, dtype="bf16", seed=22),  # one chunk
+    # x and out move in 3 uneven row chunks; the shared experts run chunk by chunk
+    inputs.LayerConfig("host_bf16_chunks", T=3001, H=512, E=64, k=6, I=256, S=2, dtype="bf16", seed=24),
+    inputs.LayerConfig("host_bf16_noshared", T=2100, H=256, E=16, k=2, I=128, S=0, dtype="bf16", seed=25),
+    inputs.LayerConfig("host_fp32_chunks", T=1500, H=128, E=16, k=2, I=64, S=1, dtype="f32", seed=26),
+    inputs.LayerConfig("host_fp8_chunks", T=2048, H=512, E=32, k=4, I=256, S=1, dtype="bf16", seed=27,
+                       weight_format="fp8"),
+]
+
+
+@pytest.mark.parametrize("cfg", HOST, ids=[c.name for c in HOST])
+def test_layer_forward_host_matches_device(cfg):
+    """The host-buffer entry point (chunked copies overlapping the shared experts and
+    the finalize kernel) gives the device-buffer result bit for bit."""
+    d = inputs.make_layer(cfg, DEV)
+    layer = binding.MoELayer(T=cfg.T, k=cfg.k, w_router=d["wg"], w_gate=d["w_gate"], w_up=d["w_up"], w2=d["w2"],
+                             s_gate=d["s_gate"] if cfg.S else None, s_up=d["s_up"] if cfg.S else None,
+                             s2=d["s2"] if cfg.S else None, expert_bias=d["bias"], renormalize=cfg.renormalize,
+                             weight_format=cfg.weight_format)
+    dev_out = layer.forward(d["x"]).cpu()
     x_host = d["x"].cpu().pin_memory()
     out_host = torch.empty_like(x_host).pin_memory()
-    layer.forward_host(x_host, out_host)
-    assert torch.equal(out_host, dev_out.cpu())
+    for _ in range(2):  # the second call reuses the buffers the first one filled
+        out_host.zero_()
+        layer.forward_host(x_host, out_host)
+        assert layer.device_status() == 0
+        assert torch.equal(out_host, dev_out)
 
 
 def test_layer_stage_events():
