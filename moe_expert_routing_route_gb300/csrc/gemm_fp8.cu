@@ -79,6 +79,19 @@ __device__ __forceinline__ void decode_tile(int tile, const int* prefix, int G, 
     m = local - n * mt;
 }
 
+// (d0, d1) += (a0, a1) * f on the packed two-lane fp32 FMA; each lane rounds
+// like fmaf, so the promotion costs half the issue slots of scalar FMAs.
+__device__ __forceinline__ void ffma2(float& d0, float& d1, uint32_t a0, uint32_t a1, float f) {
+    asm("{\n\t.reg .b64 ra, rf, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\t"
+        "mov.b64 rf, {%4, %4};\n\t"
+        "mov.b64 rd, {%0, %1};\n\t"
+        "fma.rn.f32x2 rd, ra, rf, rd;\n\t"
+        "mov.b64 {%0, %1}, rd;\n\t}"
+        : "+f"(d0), "+f"(d1)
+        : "r"(a0), "r"(a1), "f"(f));
+}
+
 // Parity of the index of `tile` among this CTA's tiles (blockIdx.x, +gridDim.x, ...).
 __device__ __forceinline__ int tile_parity(int tile, int first, int stride) { return ((tile - first) / stride) & 1; }
 
@@ -301,9 +314,9 @@ tc_fp8_grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __gri
                     uint32_t va[16], vb[16];
                     tmem_ld16x2(taddr + colA + 16 * q, taddr + colB + 16 * q, va, vb);
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        acc[16 * q + i] = fmaf(__uint_as_float(va[i]), fA, acc[16 * q + i]);
-                        acc[64 + 16 * q + i] = fmaf(__uint_as_float(vb[i]), fB, acc[64 + 16 * q + i]);
+                    for (int i = 0; i < 16; i += 2) {  // two columns per packed FMA
+                        ffma2(acc[16 * q + i], acc[16 * q + i + 1], va[i], va[i + 1], fA);
+                        ffma2(acc[64 + 16 * q + i], acc[64 + 16 * q + i + 1], vb[i], vb[i + 1], fB);
                     }
                 }
                 tc_fence_before();
