@@ -381,23 +381,28 @@ tc_grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_co
 constexpr int BM2 = 256;  // rows per pair tile
 constexpr int BN2 = 256;  // columns per pair tile (each CTA holds BN2 / 2 B rows)
 
+// Shared memory: the stage ring, the barriers and a tile prefix over the
+// groups (segment bounds are read from the offsets themselves).  Up to 256
+// groups leave room for 7 stages; more groups take 6.
+template <int STAGES_, int MAXG_>
 struct Cfg2 {
     static constexpr int A_BYTES = 128 * BK * 2;
     static constexpr int B_BYTES = (BN2 / 2) * BK * 2;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;  // per CTA
-    static constexpr int STAGES = 6;
+    static constexpr int STAGES = STAGES_;
+    static constexpr int MAXG = MAXG_;
     static constexpr int TMEM_COLS = 2 * BN2;
     static constexpr int NUM_BARS = 2 * STAGES + 5;
-    static constexpr size_t SMEM = 1024 + (size_t)STAGES * STAGE_BYTES + NUM_BARS * 8 + 16 +
-                                   (size_t)(3 * kMaxGroups + 1) * 4;
+    static constexpr size_t SMEM = 1024 + (size_t)STAGES * STAGE_BYTES + NUM_BARS * 8 + 16 + (size_t)(MAXG + 1) * 4;
 };
-static_assert(Cfg2::SMEM <= 232448, "pair-tile stages exceed shared memory");
+static_assert(Cfg2<7, 256>::SMEM <= 232448, "pair-tile stages exceed shared memory");
+static_assert(Cfg2<6, 1024>::SMEM <= 232448, "pair-tile stages exceed shared memory");
 
-template <int EPI>
+template <int EPI, int STAGES_, int MAXG_>
 __global__ void __launch_bounds__(kThreads, 1)
 tc_pair_gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
                     const __grid_constant__ Params p) {
-    using Cf = Cfg2;
+    using Cf = Cfg2<STAGES_, MAXG_>;
     constexpr int STAGES = Cf::STAGES;
     constexpr uint32_t IDESC = idesc_bf16(BM2, BN2);
     static_assert(EPI != TC_EPI_F32, "fp32 outputs use the single-CTA kernel");
@@ -410,9 +415,7 @@ tc_pair_gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_const
     uint64_t* bars = reinterpret_cast<uint64_t*>(sB + STAGES * Cf::B_BYTES);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + Cf::NUM_BARS);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-    int* prefix = reinterpret_cast<int*>(tmem_slot + 4);
-    int* gstart = prefix + kMaxGroups + 1;
-    int* gend = gstart + kMaxGroups;
+    int* prefix = reinterpret_cast<int*>(tmem_slot + 4);  // [G+1]
 
     auto full_bar = [&](int s) { return smem_u32(bars + s); };
     auto empty_bar = [&](int s) { return smem_u32(bars + STAGES + s); };
@@ -425,27 +428,25 @@ tc_pair_gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_const
     const bool leader = rank == 0;
     const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
     const int G = p.G, NT = p.NT;
+    // rows [a, b) of group g; a group with bad offsets gets no tiles, so every
+    // decoded tile's group has valid bounds
+    auto seg = [&](int g, int& a, int& b) {
+        a = p.offsets ? __ldg(p.offsets + g) : 0;
+        b = p.offsets ? __ldg(p.offsets + g + 1) : p.M;
+    };
 
-    for (int g = threadIdx.x; g < G; g += kThreads) {
-        int a = 0, b = p.M;
-        if (p.offsets) {
-            a = p.offsets[g];
-            b = p.offsets[g + 1];
-        }
-        if (a < 0 || b < a || b > p.M) {
-            set_status(p.status, MOE_DEVERR_BAD_OFFSETS);
-            a = b = 0;
-        }
-        gstart[g] = a;
-        gend[g] = b;
-    }
     if (threadIdx.x == 0) *abort_flag = 0;
-    __syncthreads();
     if (warp == 0) {
         int run = 0;
         for (int g0 = 0; g0 < G; g0 += 32) {
             const int g = g0 + lane;
-            const int v = g < G ? (gend[g] - gstart[g] + BM2 - 1) / BM2 * NT : 0;
+            int v = 0;
+            if (g < G) {
+                int a, b;
+                seg(g, a, b);
+                if (a < 0 || b < a || b > p.M) set_status(p.status, MOE_DEVERR_BAD_OFFSETS);
+                else v = (b - a + BM2 - 1) / BM2 * NT;
+            }
             int incl = v;
 #pragma unroll
             for (int off = 1; off < 32; off <<= 1) {
@@ -490,7 +491,9 @@ tc_pair_gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_const
             for (int tile = pair; ok && tile < total; tile += npairs) {
                 int g, m, n, ks;
                 decode_tile(tile, prefix, G, NT, 1, g, m, n, ks);
-                const int row0 = gstart[g] + m * BM2 + (int)rank * 128;
+                int ga, gb;
+                seg(g, ga, gb);
+                const int row0 = ga + m * BM2 + (int)rank * 128;
                 const int brow = g * p.Nb + n * BN2 + (int)rank * (BN2 / 2);
                 for (int kb = 0; kb < KB; ++kb) {
                     if (!wait_phase(empty_bar(s), ph ^ 1u, abort_flag, p.status)) {
@@ -566,8 +569,10 @@ tc_pair_gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_const
         for (int tile = pair; tile < total; tile += npairs) {
             int g, m, n, ks;
             decode_tile(tile, prefix, G, NT, 1, g, m, n, ks);
-            const int64_t row = (int64_t)gstart[g] + (int64_t)m * BM2 + (int64_t)rank * 128 + r;
-            const bool valid = row < gend[g];
+            int ga, gb;
+            seg(g, ga, gb);
+            const int64_t row = (int64_t)ga + (int64_t)m * BM2 + (int64_t)rank * 128 + r;
+            const bool valid = row < gb;
             if (!__all_sync(0xffffffffu, wait_phase(tfull_bar(acc), aph, abort_flag, p.status))) break;
             tc_fence_after();
             const uint32_t taddr = tmem_base + ((uint32_t)(eg * 32) << 16) + (uint32_t)(acc * BN2);
@@ -664,9 +669,9 @@ moe_status_t launch_impl(const TcGroupedGemm& g, cudaStream_t s) {
     return last_launch_status();
 }
 
-template <int EPI>
-moe_status_t launch_pair(const TcGroupedGemm& g, cudaStream_t s) {
-    using Cf = Cfg2;
+template <int EPI, int STAGES, int MAXG>
+moe_status_t launch_pair_impl(const TcGroupedGemm& g, cudaStream_t s) {
+    using Cf = Cfg2<STAGES, MAXG>;
     static std::once_flag attr_once[64];
     static int max_clusters[64];
     int dev = 0;
@@ -686,14 +691,14 @@ moe_status_t launch_pair(const TcGroupedGemm& g, cudaStream_t s) {
     cfg.numAttrs = 1;
 
     std::call_once(attr_once[dev & 63], [&] {
-        attr_err = cudaFuncSetAttribute(tc_pair_gemm_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        (int)Cf::SMEM);
+        attr_err = cudaFuncSetAttribute(tc_pair_gemm_kernel<EPI, STAGES, MAXG>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cf::SMEM);
         if (attr_err != cudaSuccess) return;
         // pairs that fit on the device at once (clusters live within one GPC)
         cudaLaunchConfig_t q = cfg;
         q.gridDim = dim3(2 * (sm_count() / 2));
         int n = 0;
-        attr_err = cudaOccupancyMaxActiveClusters(&n, tc_pair_gemm_kernel<EPI>, &q);
+        attr_err = cudaOccupancyMaxActiveClusters(&n, tc_pair_gemm_kernel<EPI, STAGES, MAXG>, &q);
         max_clusters[dev & 63] = n;
     });
     MOE_CUDA_TRY(attr_err);
@@ -721,9 +726,14 @@ moe_status_t launch_pair(const TcGroupedGemm& g, cudaStream_t s) {
     const int64_t max_tiles = (int64_t)p.NT * (ceil_div(g.M, BM2) + (g.offsets ? g.G : 0));
     const int pairs = (int)std::max<int64_t>(1, std::min<int64_t>(pairs_max, max_tiles));
     cfg.gridDim = dim3(2 * pairs);
-    MOE_CUDA_TRY(cudaLaunchKernelEx(&cfg, tc_pair_gemm_kernel<EPI>, ma, mb, p));
+    MOE_CUDA_TRY(cudaLaunchKernelEx(&cfg, tc_pair_gemm_kernel<EPI, STAGES, MAXG>, ma, mb, p));
     note_launch();
     return last_launch_status();
+}
+
+template <int EPI>
+moe_status_t launch_pair(const TcGroupedGemm& g, cudaStream_t s) {
+    return g.G <= 256 ? launch_pair_impl<EPI, 7, 256>(g, s) : launch_pair_impl<EPI, 6, 1024>(g, s);
 }
 
 // Tile shape for the bf16 / SwiGLU outputs.  MOE_GEMM_TILE = "single" or "pair"
