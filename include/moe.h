@@ -367,6 +367,7 @@ moe_status_t moe_layer_workspace_field(const moe_layer_desc* desc, moe_ws_field 
                                        size_t* bytes);
 
 /* x [T,H] dt, out [T,H] dt, ws of moe_layer_workspace_bytes(desc) bytes.
+ * T == 0 is a no-op that returns MOE_OK (x, out and ws may then be NULL).
  * With S > 0 the first call on a device creates the library's second stream
  * and two events for that device (no device memory is allocated); make that
  * first call outside stream capture.  The call's work forks onto that stream
@@ -395,7 +396,12 @@ moe_status_t moe_layer_forward_ep(const moe_layer_desc* desc, int W, const void*
 
 /* End to end from HOST memory: copies x_host [T,H] into the workspace, runs
  * the layer, copies the result to out_host [T,H] and synchronises `stream`
- * (this call blocks).  Pinned host buffers give asynchronous copies. */
+ * (this call blocks).  Pinned host buffers give asynchronous copies.  The
+ * copies run on two library-owned copy streams in row chunks of 1024 tokens,
+ * overlapping the shared experts (input side) and finalize (output side); the
+ * result equals moe_layer_forward's bit for bit.  The first call on a device
+ * creates those streams and their events (make it outside stream capture).
+ * T == 0 returns MOE_OK without touching any buffer. */
 moe_status_t moe_layer_forward_host(const moe_layer_desc* desc, const void* x_host, void* out_host,
                                     void* ws, size_t ws_bytes, moe_stream_t stream);
 

@@ -294,17 +294,17 @@ inline void chunk_rows(int T, int n, int c, int& c0, int& c1) {
 moe_status_t layer_forward(const moe_layer_desc* d, const void* x, void* out, void* ws, size_t ws_bytes,
                            cudaStream_t s, void* const* ev, const HostIO* io = nullptr) {
     MOE_TRY(check_desc(d));
-    if (!x || !out || !ws) return MOE_ERR_INVALID_ARG;
-    if (!aligned16(x) || !aligned16(out) || !aligned16(ws)) return MOE_ERR_UNSUPPORTED;
-    const Layout L = layout(*d);
-    if (ws_bytes < L.total) return MOE_ERR_INVALID_ARG;
-    if (d->T == 0) {
+    if (d->T == 0) {  // an empty batch: nothing to read or write (pointers may be null)
         for (int i = 0; i < MOE_NUM_STAGES; ++i) {
             MOE_TRY(mark(ev, i, 0, s));
             MOE_TRY(mark(ev, i, 1, s));
         }
         return MOE_OK;
     }
+    if (!x || !out || !ws) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(out) || !aligned16(ws)) return MOE_ERR_UNSUPPORTED;
+    const Layout L = layout(*d);
+    if (ws_bytes < L.total) return MOE_ERR_INVALID_ARG;
     const int T = d->T, H = d->H, E = d->E, k = d->k, I = d->I, R = T * k;
     const int SI = d->S * d->I;
     const moe_dtype_t dt = d->dtype;
@@ -822,13 +822,13 @@ moe_status_t moe_layer_forward_ep(const moe_layer_desc* desc, int W, const void*
 moe_status_t moe_layer_forward_host(const moe_layer_desc* desc, const void* x_host, void* out_host, void* ws,
                                     size_t ws_bytes, moe_stream_t stream) {
     MOE_TRY(check_desc(desc));
+    if (desc->T == 0) return MOE_OK;  // an empty batch (pointers may be null)
     if (!x_host || !out_host || !ws) return MOE_ERR_INVALID_ARG;
     if (ws_bytes < layout(*desc).total) return MOE_ERR_INVALID_ARG;
     const Layout L = layout(*desc);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     void* xin = at<void>(ws, L.off[MOE_WS_X_IN]);
     void* xout = at<void>(ws, L.off[MOE_WS_OUT]);
-    if (desc->T == 0) return MOE_OK;
     HostPipe* hp = nullptr;
     MOE_TRY(host_pipe(&hp));
     std::lock_guard<std::mutex> lock(hp->mu);

@@ -18,58 +18,63 @@ using fp8::e4m3;
 __device__ __forceinline__ float to_f(__nv_bfloat16 v) { return __bfloat162float(v); }
 __device__ __forceinline__ float to_f(float v) { return v; }
 
-__device__ __forceinline__ void load4(const __nv_bfloat16* p, float (&v)[4]) {
-    const uint2 u = __ldg(reinterpret_cast<const uint2*>(p));
-    v[0] = __uint_as_float(u.x << 16);
-    v[1] = __uint_as_float(u.x & 0xffff0000u);
-    v[2] = __uint_as_float(u.y << 16);
-    v[3] = __uint_as_float(u.y & 0xffff0000u);
+__device__ __forceinline__ void load8(const __nv_bfloat16* p, float (&v)[8]) {
+    const uint4 u = __ldg(reinterpret_cast<const uint4*>(p));
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        v[2 * i] = __uint_as_float(w[i] << 16);
+        v[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+    }
 }
-__device__ __forceinline__ void load4(const float* p, float (&v)[4]) {
-    const float4 f = __ldg(reinterpret_cast<const float4*>(p));
-    v[0] = f.x;
-    v[1] = f.y;
-    v[2] = f.z;
-    v[3] = f.w;
+__device__ __forceinline__ void load8(const float* p, float (&v)[8]) {
+    const float4 a = __ldg(reinterpret_cast<const float4*>(p)), b = __ldg(reinterpret_cast<const float4*>(p) + 1);
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+    v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
 }
 
-// One warp per (row, 128-column block), four values per lane.
+// Half a warp per (row, 128-column block), eight values per lane, so a warp
+// takes two blocks of one row per step with one 16-byte load per lane (8 bf16).
+// Rows whose width is not a multiple of 8 take the guarded scalar path.
 template <typename T>
 __global__ void __launch_bounds__(256)
 quantize_rows_kernel(const T* __restrict__ a, int64_t rows, int cols, int kb, int ld_scales,
                      uint8_t* __restrict__ codes, float* __restrict__ scales) {
-    const int lane = threadIdx.x & 31;
+    const int lane = threadIdx.x & 31, hl = lane & 15;
+    const int kb2 = (kb + 1) / 2;  // block pairs per row
+    const bool vec = (cols & 7) == 0;
     const int64_t nw = (int64_t)gridDim.x * (blockDim.x / 32);
-    for (int64_t item = (int64_t)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5); item < rows * kb;
+    for (int64_t item = (int64_t)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5); item < rows * kb2;
          item += nw) {
-        const int64_t r = item / kb;
-        const int b = (int)(item - r * kb);
-        const int c0 = b * 128 + lane * 4;
+        const int64_t r = item / kb2;
+        const int b = (int)(item - r * kb2) * 2 + (lane >> 4);
+        const int c0 = b * 128 + hl * 8;
         const T* row = a + r * cols;
-        float v[4];
-        if (c0 + 4 <= cols && (cols & 3) == 0) {
-            load4(row + c0, v);  // one 8- or 16-byte load
+        float v[8];
+        if (vec && b < kb && c0 + 8 <= cols) {
+            load8(row + c0, v);
         } else {
 #pragma unroll
-            for (int i = 0; i < 4; ++i) v[i] = c0 + i < cols ? to_f(row[c0 + i]) : 0.0f;
+            for (int i = 0; i < 8; ++i) v[i] = b < kb && c0 + i < cols ? to_f(row[c0 + i]) : 0.0f;
         }
         float amax = 0.0f;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) amax = fmaxf(amax, fabsf(v[i]));
+        for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(v[i]));
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+        for (int off = 8; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+        if (b >= kb) continue;  // the second half of the last pair of an odd block count
         const float s = block_scale(amax);
         uint8_t* crow = codes + r * cols;
-        if (c0 + 4 <= cols && (cols & 3) == 0) {
-            uint32_t packed = 0;
-#pragma unroll
-            for (int i = 0; i < 4; ++i) packed |= e4m3(v[i] / s) << (8 * i);
-            *reinterpret_cast<uint32_t*>(crow + c0) = packed;
+        if (vec && c0 + 8 <= cols) {
+            uint2 packed;
+            packed.x = e4m3(v[0] / s) | (e4m3(v[1] / s) << 8) | (e4m3(v[2] / s) << 16) | (e4m3(v[3] / s) << 24);
+            packed.y = e4m3(v[4] / s) | (e4m3(v[5] / s) << 8) | (e4m3(v[6] / s) << 16) | (e4m3(v[7] / s) << 24);
+            *reinterpret_cast<uint2*>(crow + c0) = packed;
         } else {
-            for (int i = 0; i < 4; ++i)
+            for (int i = 0; i < 8; ++i)
                 if (c0 + i < cols) crow[c0 + i] = (uint8_t)e4m3(v[i] / s);
         }
-        if (lane == 0) scales[r * ld_scales + b] = s;
+        if (hl == 0) scales[r * ld_scales + b] = s;
     }
 }
 
@@ -111,7 +116,7 @@ moe_status_t launch_quantize_rows_fp8(const void* a, moe_dtype_t dt, int64_t row
                                       float* scales, int ld_scales, cudaStream_t s) {
     if (rows == 0) return MOE_OK;
     const int kb = (cols + 127) / 128;
-    const int64_t items = rows * kb;
+    const int64_t items = rows * ((kb + 1) / 2);  // one warp per pair of blocks
     const int grid = (int)std::min<int64_t>(ceil_div(items, 8), (int64_t)sm_count() * 16);
     if (dt == MOE_BF16)
         quantize_rows_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(a), rows, cols, kb,
