@@ -95,7 +95,7 @@ class ClockSampler:
         except Exception:
             pass
         cmd = ["nvidia-smi", "--query-gpu=" + ",".join(self.FIELDS), "--format=csv,noheader,nounits",
-               "-lms", "20"]
+               "-lms", "10"]
         if uuid:
             cmd += ["-i", uuid]
         try:

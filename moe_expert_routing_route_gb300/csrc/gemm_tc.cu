@@ -733,7 +733,7 @@ moe_status_t launch_pair_impl(const TcGroupedGemm& g, cudaStream_t s) {
 
 template <int EPI>
 moe_status_t launch_pair(const TcGroupedGemm& g, cudaStream_t s) {
-    return g.G <= 256 ? launch_pair_impl<EPI, 7, 256>(g, s) : launch_pair_impl<EPI, 6, 1024>(g, s);
+    return g.G <= 256 && !g.smem_headroom ? launch_pair_impl<EPI, 7, 256>(g, s) : launch_pair_impl<EPI, 6, 1024>(g, s);
 }
 
 // Tile shape for the bf16 / SwiGLU outputs.  MOE_GEMM_TILE = "single" or "pair"

@@ -44,11 +44,13 @@ int packed_rows(int I) { return 2 * (int)round_up((size_t)I, (size_t)tc_packed_b
 
 // Grouped FFN halves: up (SwiGLU into h) and down (h into y); bf16 on tcgen05,
 // fp32 on the FFMA pipes.  offsets == nullptr means one dense group of `rows`.
+// headroom: leave shared memory on every SM for kernels running beside this one
 moe_status_t ffn_up(const void* a, moe_dtype_t dt, const int32_t* offsets, int G, int rows, int H, int I,
-                    const void* w13p, void* h, uint32_t* status, cudaStream_t s) {
+                    const void* w13p, void* h, uint32_t* status, cudaStream_t s, bool headroom = false) {
     if (rows == 0) return MOE_OK;
     if (dt == MOE_BF16) {
         TcGroupedGemm up{a, rows, H, offsets, G, w13p, packed_rows(I), I, h, I, TC_EPI_SWIGLU, status};
+        up.smem_headroom = headroom;
         return launch_tc_grouped_gemm(up, s);
     }
     return launch_simt_grouped_ffn_up(static_cast<const float*>(a), rows, H, offsets, G,
@@ -57,10 +59,11 @@ moe_status_t ffn_up(const void* a, moe_dtype_t dt, const int32_t* offsets, int G
 }
 
 moe_status_t ffn_down(const void* h, moe_dtype_t dt, const int32_t* offsets, int G, int rows, int H, int I,
-                      const void* w2, void* y, uint32_t* status, cudaStream_t s) {
+                      const void* w2, void* y, uint32_t* status, cudaStream_t s, bool headroom = false) {
     if (rows == 0) return MOE_OK;
     if (dt == MOE_BF16) {
         TcGroupedGemm down{h, rows, I, offsets, G, w2, H, H, y, H, TC_EPI_BF16, status};
+        down.smem_headroom = headroom;
         return launch_tc_grouped_gemm(down, s);
     }
     return launch_simt_grouped_down(static_cast<const float*>(h), rows, I, offsets, G, static_cast<const float*>(w2),
@@ -393,8 +396,9 @@ moe_status_t layer_forward(const moe_layer_desc* d, const void* x, void* out, vo
                                status, ss));
             MOE_TRY(ffn_down_fp8(hsq, hss, nullptr, 1, T, H, SI, d->w2_shared, d->w2_shared_scales, ys, status, ss));
         } else {
-            MOE_TRY(ffn_up(x, dt, nullptr, 1, T, H, SI, d->w13_shared, hs, status, ss));
-            MOE_TRY(ffn_down(hs, dt, nullptr, 1, T, H, SI, d->w2_shared, ys, status, ss));
+            // the routing kernels (histogram and scatter use shared memory) run beside them
+            MOE_TRY(ffn_up(x, dt, nullptr, 1, T, H, SI, d->w13_shared, hs, status, ss, true));
+            MOE_TRY(ffn_down(hs, dt, nullptr, 1, T, H, SI, d->w2_shared, ys, status, ss, true));
         }
         MOE_TRY(mark(ev, ST_SHARED, 1, ss));
         MOE_CUDA_TRY(cudaEventRecord(side->join, ss));

@@ -112,6 +112,8 @@ struct TcGroupedGemm {
     uint32_t* status;
     int ksplit = 1;               // fp32 output only: at most this many K slices, slice s written at
     int64_t c_split_stride = 0;   // C + s * c_split_stride (elements); the caller sums the slices
+    bool smem_headroom = false;   // pair tiles: take the 6-stage ring, leaving ~24 KB of shared memory per SM
+                                  // for kernels of other streams (the 7-stage ring leaves under 1 KB)
 };
 moe_status_t launch_tc_grouped_gemm(const TcGroupedGemm& g, cudaStream_t s);
 int tc_gate_splits(int M, int N, int K, int max_split);  // K slices the fp32 launch will use
