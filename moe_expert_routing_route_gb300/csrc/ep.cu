@@ -78,12 +78,16 @@ ep_dispatch_plan_kernel(const int32_t* __restrict__ counts_all, int W, int E, in
 //   rr [Q][P][El][3]: (src row, dst row, rows) of block (p, e) of rank q
 //   tokens_per_local_expert [Q][El], local_offsets [Q][El+1] (from 0),
 //   goff [Q][El+1] (= base + local_offsets: rows in the whole sorted buffer)
+//   eoff [Q*El+1] (nullable): the same offsets as one array over all ranks' experts
+//     in rank order; with ranks laid out contiguously (base[q+1] = base[q] + rows
+//     of rank q) it segments the whole sorted buffer by global expert
 // expect_rows >= 0: the rank's rows must add up to it, else every block is
 // emptied and the status bit is set.
 __global__ void __launch_bounds__(kPlanThreads)
 re_routing_plan_kernel(const int32_t* __restrict__ counts_recv, const int32_t* __restrict__ recv_start, int P,
                        int El, int expect_rows, int32_t* __restrict__ rr, int32_t* __restrict__ tpl,
-                       int32_t* __restrict__ local_off, int32_t* __restrict__ goff, uint32_t* status) {
+                       int32_t* __restrict__ local_off, int32_t* __restrict__ goff, int32_t* __restrict__ eoff,
+                       uint32_t* status) {
     __shared__ int scan_buf[1025];
     __shared__ int arrive_base;  // rows of earlier sources
     __shared__ int total_rows;
@@ -114,6 +118,8 @@ re_routing_plan_kernel(const int32_t* __restrict__ counts_recv, const int32_t* _
     if (tid <= El) {
         local_off[(size_t)q * (El + 1) + tid] = ok ? scan_buf[tid] : 0;
         goff[(size_t)q * (El + 1) + tid] = base + (ok ? scan_buf[tid] : 0);
+        // rank q writes its El starts; the last rank also writes the end
+        if (eoff && (tid < El || q == gridDim.x - 1)) eoff[(size_t)q * El + tid] = base + (ok ? scan_buf[tid] : 0);
     }
     if (tid < El) tpl[(size_t)q * El + tid] = ok ? t_e : 0;
     int dst_run = tid < El ? scan_buf[tid] : 0;  // next sorted row of expert tid
@@ -212,7 +218,8 @@ moe_status_t launch_re_routing(const void* x_recv, size_t row_bytes, const int32
                                uint32_t* status, cudaStream_t s) {
     int32_t* rr = plan;
     int32_t* goff = plan + (size_t)W * El * 3;
-    re_routing_plan_kernel<<<1, kPlanThreads, 0, s>>>(counts, nullptr, W, El, N, rr, tpl, local_off, goff, status);
+    re_routing_plan_kernel<<<1, kPlanThreads, 0, s>>>(counts, nullptr, W, El, N, rr, tpl, local_off, goff, nullptr,
+                                                      status);
     note_launch();
     MOE_TRY(last_launch_status());
     if (N == 0) return MOE_OK;
@@ -237,7 +244,8 @@ size_t ep_scratch_ints(int W, int E) {
            + (size_t)W * W * El             // counts_recv
            + (size_t)W * W * El * 3         // re-routing blocks
            + (size_t)W * El                 // tokens per local expert
-           + 2 * (size_t)W * (El + 1);      // local and global offsets
+           + 2 * (size_t)W * (El + 1)       // local and global offsets
+           + (size_t)E + 1;                 // global offsets by global expert
 }
 
 moe_status_t ep_route_and_dispatch(const EpBuffers& b, cudaStream_t s) {
@@ -251,6 +259,7 @@ moe_status_t ep_route_and_dispatch(const EpBuffers& b, cudaStream_t s) {
     int32_t* tpl = rr + (size_t)W * W * El * 3;
     int32_t* local_off = tpl + (size_t)W * El;
     int32_t* goff = local_off + (size_t)W * (El + 1);
+    int32_t* eoff = goff + (size_t)W * (El + 1);
     // step 1: init-routing per source rank (row indices local to the rank)
     for (int p = 0; p < W; ++p) {
         MOE_TRY(launch_init_routing_index(b.ids + (size_t)p * Rp, Rp, E, counts_all + (size_t)p * E,
@@ -267,7 +276,7 @@ moe_status_t ep_route_and_dispatch(const EpBuffers& b, cudaStream_t s) {
     MOE_TRY(launch_copy_blocks(b.expanded, b.recv, b.row_bytes, xfer, W * W, 0, nullptr, Rp / W, s));
     // step 4: re-routing on every receiving rank
     re_routing_plan_kernel<<<W, kPlanThreads, 0, s>>>(counts_recv, recv_start, W, El, -1, rr, tpl, local_off, goff,
-                                                      b.status);
+                                                      eoff, b.status);
     note_launch();
     MOE_TRY(last_launch_status());
     MOE_TRY(launch_copy_blocks(b.recv, b.sorted, b.row_bytes, rr, W * W * El, 0, b.gidx,
@@ -280,6 +289,11 @@ const int32_t* ep_rank_offsets(const EpBuffers& b, int q) {
     const int32_t* goff = b.scratch + (size_t)W * E + (size_t)W * (E + 1) + (size_t)W * W * 3 + W + 1 +
                           (size_t)W * W * El + (size_t)W * W * El * 3 + (size_t)W * El + (size_t)W * (El + 1);
     return goff + (size_t)q * (El + 1);
+}
+
+const int32_t* ep_expert_offsets(const EpBuffers& b) {
+    const int W = b.W, E = b.E, El = E / W;
+    return ep_rank_offsets(b, 0) + (size_t)W * (El + 1);
 }
 
 moe_status_t ep_combine(const EpBuffers& b, const void* y_sorted, void* y_recv, void* y_expanded, cudaStream_t s) {

@@ -528,14 +528,13 @@ moe_status_t layer_forward_ep(const moe_layer_desc* d, int W, const void* x, voi
                               d->group_rule, nsplit));
     MOE_TRY(ep_route_and_dispatch(b, s));  // steps 1-4
     if (side) MOE_CUDA_TRY(cudaStreamWaitEvent(s, side->join, 0));
-    // step 5: each rank's experts on its sorted rows
-    const size_t w13_expert = (size_t)packed_rows(I) * H * eb, w2_expert = (size_t)H * I * eb;
-    for (int q = 0; q < W; ++q)
-        MOE_TRY(ffn_up(b.sorted, dt, ep_rank_offsets(b, q), El, R, H, I,
-                       static_cast<const char*>(d->w13) + (size_t)q * El * w13_expert, h, status, s));
-    for (int q = 0; q < W; ++q)
-        MOE_TRY(ffn_down(h, dt, ep_rank_offsets(b, q), El, R, H, I,
-                         static_cast<const char*>(d->w2) + (size_t)q * El * w2_expert, y, status, s));
+    // step 5: each rank's experts on its sorted rows.  The ranks' sorted rows lie
+    // rank after rank in one buffer and rank q owns experts [q*El, (q+1)*El), so
+    // the ranks' local segments together segment the buffer by global expert: on
+    // one GPU all ranks' expert GEMMs run as one persistent launch per projection
+    // (the same tiles as W launches of El experts, without W tails).
+    MOE_TRY(ffn_up(b.sorted, dt, ep_expert_offsets(b), E, R, H, I, d->w13, h, status, s));
+    MOE_TRY(ffn_down(h, dt, ep_expert_offsets(b), E, R, H, I, d->w2, y, status, s));
     // steps 6-7: back to received order, back to the source ranks (into the free buffers)
     MOE_TRY(ep_combine(b, y, b.recv, b.expanded, s));
     // step 8: finalize on each source rank
