@@ -52,3 +52,27 @@ def test_clock_summary_window():
     # a window shorter than the sampling period falls back to the nearest sample
     s = cs.summary(8.9, 8.95)
     assert s["reasons"] == ["hw_slowdown"]
+
+
+def test_reference_arm_json_line_on_cpu():
+    """`bench.py --impl reference` times the oracle on host cores; its one JSON line
+    carries the contract's keys (run here on the small fp32 workload)."""
+    import json
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = dict(os.environ, CUDA_VISIBLE_DEVICES="")
+    r = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--workload", "tiny_fp32", "--steps", "2",
+                        "--warmup", "1", "--ref-tokens", "8"], cwd=root, env=env, capture_output=True, text=True,
+                       timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better", "scaling",
+                "vs_baseline", "dtype", "data", "config", "impl", "cpu_baseline", "e2e"):
+        assert key in d, key
+    assert d["impl"] == "reference" and d["steps"] == 2 and d["warmup"] == 1 and d["value"] > 0
+    assert d["config"]["workload"] == "tiny_fp32"
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] == d["value"]
+    assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
