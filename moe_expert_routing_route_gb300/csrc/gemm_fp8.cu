@@ -20,7 +20,7 @@
 // §Quantization, computed on the fly): h is rounded to bf16, the two warps that
 // hold the two 64-column halves of a 128-column block swap their partial amax
 // through shared memory (an mbarrier per TMEM lane group, bounded wait), and
-// each writes its 64 e4m3 codes; the half-0 warp writes the block's scale.
+// each writes its 64 e4m3 codes; the first warp writes the block's scale.
 // Rows of a tile past the expert's segment are
 // computed and never stored, as in the bf16 kernel.  Waits are bounded as in
 // the bf16 kernel (about one second, then abort without trapping).
@@ -38,8 +38,11 @@ constexpr int BM = 128;
 constexpr int BK = 128;  // bytes (= e4m3 elements) of K per stage: one swizzle row, one scale block
 constexpr int UMMA_K = 32;
 constexpr int BN = 256;
-constexpr int kEpiWarps = 8;
+constexpr int kEpiWarps = 8;              // epilogue warps: kSplit per TMEM lane group
+constexpr int kSplit = kEpiWarps / 4;     // warps sharing a lane group, each on 128/kSplit columns of a chunk
+constexpr int kCols = 128 / kSplit;       // columns of each of a thread's two chunks
 constexpr int kThreads = 64 + 32 * kEpiWarps;
+static_assert(kSplit >= 2 && kCols % 16 == 0, "epilogue split");
 constexpr int kMaxGroups = 1024;
 constexpr int A_BYTES = BM * BK;
 constexpr int B_BYTES = BN * BK;
@@ -47,7 +50,7 @@ constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int STAGES = 4;
 constexpr int TMEM_COLS = 2 * BN;  // two partial buffers
 constexpr int NUM_BARS = 2 * STAGES + 9;  // full, empty, partial full/empty, drain, 4 amax exchanges
-constexpr int XAMAX_FLOATS = 2 * 2 * BM;   // [tile parity][column half][row]
+constexpr int XAMAX_FLOATS = 2 * kSplit * BM;  // [tile parity][column part][row]
 constexpr size_t SMEM = 1024 + (size_t)STAGES * STAGE_BYTES + NUM_BARS * 8 + 16 + (size_t)(3 * kMaxGroups + 1) * 4 +
                         (size_t)XAMAX_FLOATS * 4;
 
@@ -100,13 +103,14 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
     return *reinterpret_cast<uint32_t*>(&v);
 }
 
-// 64 consecutive bf16 outputs of one row (columns col0.., valid below N).
-__device__ __forceinline__ void store_row64(__nv_bfloat16* C, int64_t ldc, int64_t row, int col0, int N,
-                                            const float* v) {
+// NV consecutive bf16 outputs of one row (columns col0.., valid below N).
+template <int NV>
+__device__ __forceinline__ void store_row(__nv_bfloat16* C, int64_t ldc, int64_t row, int col0, int N,
+                                          const float* v) {
     __nv_bfloat16* dst = C + row * ldc + col0;
-    if (col0 + 64 <= N) {
+    if (col0 + NV <= N) {
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
+        for (int q = 0; q < NV / 8; ++q) {
             uint4 u;
             u.x = pack_bf16x2(v[8 * q + 0], v[8 * q + 1]);
             u.y = pack_bf16x2(v[8 * q + 2], v[8 * q + 3]);
@@ -116,7 +120,7 @@ __device__ __forceinline__ void store_row64(__nv_bfloat16* C, int64_t ldc, int64
         }
     } else {
 #pragma unroll
-        for (int c = 0; c < 64; ++c)
+        for (int c = 0; c < NV; ++c)
             if (col0 + c < N) dst[c] = __float2bfloat16_rn(v[c]);
     }
 }
@@ -189,7 +193,7 @@ tc_fp8_grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __gri
                 mbar_init(pempty_bar(j), kEpiWarps);
             }
             mbar_init(drain_bar, 1);
-            for (int eg = 0; eg < 4; ++eg) mbar_init(xchg_bar(eg), 2);  // the two warps of a lane group
+            for (int eg = 0; eg < 4; ++eg) mbar_init(xchg_bar(eg), kSplit);  // the warps of a lane group
             asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             prefetch_tensormap(&mapA);
@@ -270,19 +274,20 @@ tc_fp8_grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __gri
             wait_drain(drain_bar, 0, p.status);
         }
     } else {
-        // ---------------- epilogue: 8 warps, each (lane group, column half) ----------------
+        // ---------------- epilogue: kEpiWarps warps, each (lane group, column part) ----------------
         const int eg = warp & 3;
-        const int half = (warp - 2) >> 2;
+        const int part = (warp - 2) >> 2;  // 0 .. kSplit-1
         const int r = eg * 32 + lane;
-        // the two 64-column chunks of this thread: gate/up halves (SwiGLU) or one 128-column half
-        const int colA = EPI == TC_EPI_SWIGLU ? half * 64 : half * 128;
-        const int colB = EPI == TC_EPI_SWIGLU ? 128 + half * 64 : half * 128 + 64;
-        const int nbA = EPI == TC_EPI_SWIGLU ? 0 : half;  // scale block of each chunk inside the tile
-        const int nbB = EPI == TC_EPI_SWIGLU ? 1 : half;
+        // the thread's two kCols-column chunks: gate and up slices of a packed block (SwiGLU), or two
+        // adjacent slices of one 128-column block
+        const int colA = EPI == TC_EPI_SWIGLU ? part * kCols : part * 2 * kCols;
+        const int colB = EPI == TC_EPI_SWIGLU ? 128 + part * kCols : part * 2 * kCols + kCols;
+        const int nbA = EPI == TC_EPI_SWIGLU ? 0 : colA / 128;  // scale block of each chunk inside the tile
+        const int nbB = EPI == TC_EPI_SWIGLU ? 1 : colB / 128;
         const int nblocks = p.Nb / 128;
         int j = 0;
         uint32_t pph = 0, xph = 0;
-        float acc[128];
+        float acc[2 * kCols];
         bool ok = true;
         for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
             int g, m, n;
@@ -294,7 +299,7 @@ tc_fp8_grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __gri
             const float* sbA = p.b_scales + ((int64_t)g * nblocks + n * 2 + nbA) * KB;
             const float* sbB = p.b_scales + ((int64_t)g * nblocks + n * 2 + nbB) * KB;
 #pragma unroll
-            for (int i = 0; i < 128; ++i) acc[i] = 0.0f;
+            for (int i = 0; i < 2 * kCols; ++i) acc[i] = 0.0f;
             float sa_next = __ldg(sa_row), sbA_next = __ldg(sbA), sbB_next = __ldg(sbB);
             for (int kb = 0; kb < KB; ++kb) {
                 const float fA = sa_next * sbA_next, fB = sa_next * sbB_next;
@@ -310,13 +315,13 @@ tc_fp8_grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __gri
                 tc_fence_after();
                 const uint32_t taddr = tmem_base + ((uint32_t)(eg * 32) << 16) + (uint32_t)(j * BN);
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {  // column pair q of chunk A and of chunk B
+                for (int q = 0; q < kCols / 16; ++q) {  // 16 columns of chunk A and of chunk B
                     uint32_t va[16], vb[16];
                     tmem_ld16x2(taddr + colA + 16 * q, taddr + colB + 16 * q, va, vb);
 #pragma unroll
                     for (int i = 0; i < 16; i += 2) {  // two columns per packed FMA
                         ffma2(acc[16 * q + i], acc[16 * q + i + 1], va[i], va[i + 1], fA);
-                        ffma2(acc[64 + 16 * q + i], acc[64 + 16 * q + i + 1], vb[i], vb[i + 1], fB);
+                        ffma2(acc[kCols + 16 * q + i], acc[kCols + 16 * q + i + 1], vb[i], vb[i + 1], fB);
                     }
                 }
                 tc_fence_before();
@@ -331,28 +336,31 @@ tc_fp8_grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __gri
             __nv_bfloat16* C = static_cast<__nv_bfloat16*>(p.C);
             if (EPI == TC_EPI_SWIGLU) {
                 // h in bf16 (the precision it is stored and quantised in)
-                float h[64];
+                float h[kCols];
                 float am = 0.0f;
 #pragma unroll
-                for (int i = 0; i < 64; ++i) {
-                    h[i] = __bfloat162float(__float2bfloat16_rn(acc[i] / (1.0f + __expf(-acc[i])) * acc[64 + i]));
+                for (int i = 0; i < kCols; ++i) {
+                    h[i] = __bfloat162float(
+                        __float2bfloat16_rn(acc[i] / (1.0f + __expf(-acc[i])) * acc[kCols + i]));
                     am = fmaxf(am, fabsf(h[i]));
                 }
-                const int col0 = n * 128 + half * 64;
-                if (valid && C) store_row64(C, p.ldc, row, col0, p.N, h);
+                const int col0 = n * 128 + part * kCols;
+                if (valid && C) store_row<kCols>(C, p.ldc, row, col0, p.N, h);
                 if (p.q) {
-                    // amax of the 128-column block: this half's and the other warp's
-                    float* slot = xamax + (tile_parity(tile, blockIdx.x, gridDim.x) * 2) * BM;
-                    slot[half * BM + r] = am;
+                    // amax of the 128-column block: the maximum over the kSplit warps' parts
+                    float* slot = xamax + tile_parity(tile, blockIdx.x, gridDim.x) * kSplit * BM;
+                    slot[part * BM + r] = am;
                     __syncwarp();
                     if (lane == 0) mbar_arrive(xchg_bar(eg));
                     if (!__all_sync(0xffffffffu, wait_phase_fast(xchg_bar(eg), xph, abort_flag, p.status))) break;
                     xph ^= 1u;
-                    const float sc = fp8::block_scale(fmaxf(am, slot[(1 - half) * BM + r]));
+#pragma unroll
+                    for (int o = 0; o < kSplit; ++o) am = fmaxf(am, slot[o * BM + r]);
+                    const float sc = fp8::block_scale(am);
                     if (valid) {
                         uint8_t* qrow = p.q + row * (int64_t)p.N + col0;
 #pragma unroll
-                        for (int c = 0; c < 4; ++c) {  // 16 codes per store; N % 16 == 0
+                        for (int c = 0; c < kCols / 16; ++c) {  // 16 codes per store; N % 16 == 0
                             if (col0 + 16 * c < p.N) {
                                 uint32_t w4[4];
 #pragma unroll
@@ -364,12 +372,12 @@ tc_fp8_grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __gri
                                 reinterpret_cast<uint4*>(qrow)[c] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
                             }
                         }
-                        if (half == 0) p.q_scales[row * (int64_t)p.ldq + n] = sc;
+                        if (part == 0) p.q_scales[row * (int64_t)p.ldq + n] = sc;
                     }
                 }
             } else if (valid) {
-                store_row64(C, p.ldc, row, n * BN + colA, p.N, acc);
-                store_row64(C, p.ldc, row, n * BN + colB, p.N, acc + 64);
+                store_row<kCols>(C, p.ldc, row, n * BN + colA, p.N, acc);
+                store_row<kCols>(C, p.ldc, row, n * BN + colB, p.N, acc + kCols);
             }
         }
     }
