@@ -271,6 +271,7 @@ TILE_CASES = [
     (300, 6, 64, 512, 256),    # ~28 rows per expert: the peer's rows lie past the expert
     (64, 8, 256, 128, 128),    # most experts empty
     (3, 1, 4, 64, 128),        # tiny
+    (2000, 8, 300, 256, 128),  # more than 256 groups: the pair kernel's 6-stage instantiation
 ]
 
 
