@@ -330,7 +330,9 @@ def run_ours(args, world, rank, local):
         tokens = cfg.T * world
         line = dict(metric=METRIC, value=tokens / (ms_max / 1e3), unit=UNIT, n_gpus=world, steps=args.steps,
                     warmup=args.warmup, ms_per_step=ms_max, higher_is_better=True, scaling="weak",
-                    vs_baseline=None, dtype=cfg.dtype, data="synthetic (seeded N(0,1) x, N(0,1/sqrt(fan_in)) "
+                    vs_baseline=None,
+                    # FP8 layers multiply e4m3 codes in the expert GEMMs; gate, routing and outputs stay bf16
+                    dtype="e4m3+bf16" if fp8 else cfg.dtype, data="synthetic (seeded N(0,1) x, N(0,1/sqrt(fan_in)) "
                     "weights, random-init DeepSeek-V3-shaped MoE layer)",
                     config=dict(workload=cfg.name, T=cfg.T, H=cfg.H, E=cfg.E, k=cfg.k, I=cfg.I, S=cfg.S,
                                 global_batch=tokens, parallelism=f"replicas{world}",
