@@ -283,6 +283,32 @@ def run_ours(args, world, rank, local):
     if layer.device_status() != 0:
         raise RuntimeError("device status word set during the timed region")
 
+    graph_ms = None
+    if args.graph:
+        # the same forward captured once into a CUDA graph ([BLOG §CUDA Graph]) and replayed K times:
+        # what a serving loop pays per layer once launch costs are gone
+        cs = torch.cuda.Stream()
+        cs.wait_stream(stream)
+        with torch.cuda.stream(cs):
+            layer.forward(x, out)  # warm-up on the capture stream
+        stream.wait_stream(cs)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            layer.forward(x, out)
+        for _ in range(args.warmup):
+            graph.replay()
+        g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier(world)
+        torch.cuda.synchronize()
+        g0.record()
+        for _ in range(args.steps):
+            graph.replay()
+        g1.record()
+        torch.cuda.synchronize()
+        graph_ms = max_over_ranks(g0.elapsed_time(g1) / args.steps, world)
+        if layer.device_status() != 0:
+            raise RuntimeError("device status word set during graph replay")
+
     # roofline of the dominant kernel
     counts = layer.field("tokens_per_expert").cpu().numpy()
     touched = int((counts > 0).sum())
@@ -346,6 +372,8 @@ def run_ours(args, world, rank, local):
                                       frac_of_bf16_peak=round(gemm_fl / (gemm_ms / 1e3) / 1e12 /
                                                               peaks["bf16_tflops_sustained"], 3)),
                     layer_tflops=round(layer_fl / (ms_max / 1e3) / 1e12, 1))
+        if graph_ms is not None:
+            line["graph"] = dict(ms_per_step=graph_ms, value=tokens / (graph_ms / 1e3), unit=UNIT)
         print(json.dumps(line), flush=True)
 
 
@@ -402,6 +430,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--ref-tokens", type=int, default=16, help="tokens per step for --impl reference")
+    ap.add_argument("--graph", action="store_true",
+                    help="also time K replays of one forward captured into a CUDA graph")
     ap.add_argument("--ep", type=int, default=1,
                     help="run the layer through expert-parallel Double-Routing with this many virtual ranks")
     args = ap.parse_args()
