@@ -63,16 +63,33 @@ simt_grouped_kernel(const float* __restrict__ A, int M, int K, const int32_t* __
         return (int64_t)g * Nb + (c / 128) * 256 + (up ? 128 : 0) + (c & 127);
     };
 
-    for (int k0 = 0; k0 < K; k0 += BK) {
-        for (int i = threadIdx.x; i < BM * BK; i += 256) {
+    // each thread stages 4 elements of A, B (and U) per k-tile; the next tile's
+    // loads are issued before the current tile's FMAs, so their latency overlaps
+    constexpr int PER = BM * BK / 256;
+    float ra[PER], rb[PER], ru[PER];
+    auto fetch = [&](int k0) {
+#pragma unroll
+        for (int q = 0; q < PER; ++q) {
+            const int i = threadIdx.x + q * 256;
             const int r = i / BK, kk = i % BK;
-            const int row = r0 + r, kc = k0 + kk;
-            As[kk][r] = (row < r1 && kc < K) ? A[(int64_t)row * K + kc] : 0.f;
-            const int c = c0 + r;
-            Bs[kk][r] = (c < N && kc < K) ? B[brow(c, false) * K + kc] : 0.f;
-            if (SWIGLU) Us[kk][r] = (c < N && kc < K) ? B[brow(c, true) * K + kc] : 0.f;
+            const int row = r0 + r, kc = k0 + kk, c = c0 + r;
+            ra[q] = (row < r1 && kc < K) ? A[(int64_t)row * K + kc] : 0.f;
+            rb[q] = (c < N && kc < K) ? B[brow(c, false) * K + kc] : 0.f;
+            if (SWIGLU) ru[q] = (c < N && kc < K) ? B[brow(c, true) * K + kc] : 0.f;
+        }
+    };
+    fetch(0);
+    for (int k0 = 0; k0 < K; k0 += BK) {
+#pragma unroll
+        for (int q = 0; q < PER; ++q) {
+            const int i = threadIdx.x + q * 256;
+            const int r = i / BK, kk = i % BK;
+            As[kk][r] = ra[q];
+            Bs[kk][r] = rb[q];
+            if (SWIGLU) Us[kk][r] = ru[q];
         }
         __syncthreads();
+        if (k0 + BK < K) fetch(k0 + BK);
 #pragma unroll
         for (int kk = 0; kk < BK; ++kk) {
             float a[4], b[4], u[4];
