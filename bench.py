@@ -325,6 +325,11 @@ def run_ours(args, world, rank, local):
     rl["algorithmic_bytes"] = by
     rl["algorithmic_flops"] = fl
     rl["peak_source"] = peaks["source"]
+    # the whole layer against the slower of its summed FLOPs at the tensor peak and
+    # its summed bytes at HBM bandwidth
+    rl.update(roofline.layer_roofline(costs, ms_max / 1e3, peaks, sustained=True,
+                                      gemm_tensor_scale=2.0 if fp8 else 1.0))
+    rl["stage_costs"] = {name: dict(flops=f_, bytes=b_) for name, (f_, b_) in costs.items()}
     stages = {}
     for name, t in stage_ms.items():
         f_, b_ = costs[name]
@@ -408,8 +413,10 @@ def run_ours_ep(args, world, rank, local, cfg, layer, x, out):
     counts = layer.field("tokens_per_expert").cpu().numpy()
     costs = roofline.stage_costs(cfg.T, cfg.H, cfg.E, cfg.k, cfg.I, cfg.S, cfg.esize, int((counts > 0).sum()))
     fl, by = sum(c[0] for c in costs.values()), sum(c[1] for c in costs.values())
-    rl = roofline.roofline_entry(fl, by, ms_max / 1e3, roofline.load_peaks(), sustained=True)
+    peaks = roofline.load_peaks()
+    rl = roofline.roofline_entry(fl, by, ms_max / 1e3, peaks, sustained=True)
     rl.update(kernel="whole layer (double routing)", traffic=None, algorithmic_bytes=by, algorithmic_flops=fl)
+    rl.update(roofline.layer_roofline(costs, ms_max / 1e3, peaks, sustained=True))
     if rank == 0:
         tokens = cfg.T * world
         print(json.dumps(dict(metric=METRIC, value=tokens / (ms_max / 1e3), unit=UNIT, n_gpus=world,

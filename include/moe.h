@@ -169,7 +169,9 @@ moe_status_t moe_init_routing(const void* x, moe_dtype_t dt, const int32_t* topk
  * a larger call returns MOE_ERR_UNSUPPORTED.  No allocation of any kind is made.
  * The first call on a device looks up the array's device address (with that
  * device current) and keeps it; make that first call before any stream
- * capture.  All calls share the array and it keeps the last call's contents
+ * capture.  The address is tied to the device's context: the first call after
+ * a cudaDeviceReset of that device (a new context) looks it up again, so make
+ * that call outside stream capture too.  All calls share the array and it keeps the last call's contents
  * (every entry a call reads is rewritten by that call, so nothing needs
  * clearing), but calls whose kernels overlap on the GPU race on it.  There is
  * no status word: an id outside [0,E) shows as expanded_row_idx = -1 and is not
@@ -329,9 +331,9 @@ typedef struct moe_layer_desc {
 #define MOE_WEIGHTS_FP8 1
 
 /* Layer steps timed by moe_layer_forward_timed.  "shared" (both projections of
- * the shared experts) runs on a second stream of the library's, forked after
- * the gate and joined before "up", concurrently with route, init_routing and
- * permute_rows; "up" and "down" are the routed experts. */
+ * the shared experts) runs on a second stream of the library's, forked when
+ * the gate starts and joined before "up", concurrently with gate, route,
+ * init_routing and permute_rows; "up" and "down" are the routed experts. */
 #define MOE_NUM_STAGES 8
 const char* moe_stage_name(int stage); /* "gate", "route", "init_routing", "permute_rows",
                                           "shared", "up", "down", "finalize" */
@@ -393,6 +395,23 @@ moe_status_t moe_layer_forward_timed(const moe_layer_desc* desc, const void* x, 
 size_t moe_layer_workspace_bytes_ep(const moe_layer_desc* desc, int W);
 moe_status_t moe_layer_forward_ep(const moe_layer_desc* desc, int W, const void* x, void* out, void* ws,
                                   size_t ws_bytes, moe_stream_t stream);
+
+/* Intermediates of moe_layer_forward_ep that stay in its workspace after the
+ * call (for inspection; the routing fields MOE_WS_LOGITS, MOE_WS_TOPK_IDS and
+ * MOE_WS_TOPK_W sit at the offsets moe_layer_workspace_field gives).
+ * [CANN §MoE deployment], steps 3-4: rank q's received rows arrive grouped by
+ * source rank, each source's rows in global-expert order; re-routing sorts them
+ * by local expert (stable), remembering where each sorted row came from. */
+typedef enum moe_ws_field_ep {
+    MOE_WS_EP_X_SORTED = 0,              /* [T*k,H] dt: every rank's re-routed rows, rank after rank */
+    MOE_WS_EP_GATHERED_IDS_UNSORT = 1,   /* [T*k] int32: the receive-buffer row (all ranks, rank after
+                                            rank) each sorted row was taken from */
+    MOE_WS_EP_RECV_START = 2,            /* [W+1] int32: first received row of each rank */
+    MOE_WS_EP_EXPERT_OFFSETS = 3,        /* [E+1] int32: rows of each global expert in X_SORTED */
+    MOE_WS_EP_NUM_FIELDS = 4
+} moe_ws_field_ep;
+moe_status_t moe_layer_workspace_field_ep(const moe_layer_desc* desc, int W, moe_ws_field_ep field,
+                                          size_t* offset, size_t* bytes);
 
 /* End to end from HOST memory: copies x_host [T,H] into the workspace, runs
  * the layer, copies the result to out_host [T,H] and synchronises `stream`

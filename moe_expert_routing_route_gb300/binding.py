@@ -24,6 +24,7 @@ MOE_NUM_STAGES = 8
 WS_FIELDS = ["logits", "topk_ids", "topk_w", "tokens_per_expert", "expert_offsets", "expanded_row_idx",
              "expanded_x", "h_routed", "h_shared", "y_routed", "y_shared", "x_in", "out", "xq", "xq_scales",
              "expanded_xq", "expanded_xq_scales", "hq", "hq_scales", "hq_shared", "hq_shared_scales"]
+WS_FIELDS_EP = ["x_sorted", "gathered_ids_unsort", "recv_start", "expert_offsets"]
 MOE_WEIGHTS_NATIVE, MOE_WEIGHTS_FP8 = 0, 1
 
 # The exported entry points (name -> (restype, argtypes)).
@@ -61,6 +62,7 @@ SIGNATURES = {
     "moe_unsort_rows": (I32, [P, I32, P, I32, I32, P, P, P]),
     "moe_layer_workspace_bytes_ep": (SZ, [_DP, I32]),
     "moe_layer_forward_ep": (I32, [_DP, I32, P, P, P, SZ, P]),
+    "moe_layer_workspace_field_ep": (I32, [_DP, I32, I32, ctypes.POINTER(SZ), ctypes.POINTER(SZ)]),
     "moe_quantize_rows_fp8": (I32, [P, I32, I64, I32, P, P, I32, P]),
     "moe_quantize_weights_fp8": (I32, [P, I32, I32, I32, I32, P, P, P]),
     "moe_grouped_ffn_fp8_workspace_bytes": (SZ, [I32, I32]),
@@ -362,12 +364,13 @@ class MoELayer:
             raise MoEError(MOE_ERR_INVALID_ARG, "moe_layer_workspace_bytes")
         self.ws = torch.empty(nbytes, dtype=torch.uint8, device=w_gate.device)
 
-    def field(self, name: str) -> torch.Tensor:
-        """A view of one intermediate in the workspace (see moe_ws_field)."""
+    def field(self, name: str, ws: torch.Tensor | None = None) -> torch.Tensor:
+        """A view of one intermediate in the workspace (see moe_ws_field); ws: another
+        workspace laid out from the same descriptor (forward_ep's), else the layer's."""
         off, nb = SZ(0), SZ(0)
         _check(lib().moe_layer_workspace_field(ctypes.byref(self.desc), WS_FIELDS.index(name), ctypes.byref(off),
                                                ctypes.byref(nb)), "moe_layer_workspace_field")
-        raw = self.ws[off.value:off.value + nb.value]
+        raw = (self.ws if ws is None else ws)[off.value:off.value + nb.value]
         T, H, E, k, I, S = self.T, self.H, self.E, self.k, self.I, self.S
         shapes = dict(logits=((T, E), torch.float32), topk_ids=((T, k), torch.int32),
                       topk_w=((T, k), torch.float32), tokens_per_expert=((E,), torch.int32),
@@ -426,6 +429,19 @@ class MoELayer:
         _check(lib().moe_layer_forward_ep(ctypes.byref(self.desc), W, _ptr(x), _ptr(out), _ptr(self.ws_ep),
                                           self.ws_ep.numel(), _stream(stream)), "moe_layer_forward_ep")
         return out
+
+    def field_ep(self, name: str, W: int) -> torch.Tensor:
+        """A view of one intermediate left in the workspace by forward_ep(x, W)
+        (see moe_ws_field_ep)."""
+        off, nb = SZ(0), SZ(0)
+        _check(lib().moe_layer_workspace_field_ep(ctypes.byref(self.desc), W, WS_FIELDS_EP.index(name),
+                                                  ctypes.byref(off), ctypes.byref(nb)), "moe_layer_workspace_field_ep")
+        raw = self.ws_ep[off.value:off.value + nb.value]
+        R = self.T * self.k
+        shapes = dict(x_sorted=((R, self.H), self.dtype), gathered_ids_unsort=((R,), torch.int32),
+                      recv_start=((W + 1,), torch.int32), expert_offsets=((self.E + 1,), torch.int32))
+        shape, dtype = shapes[name]
+        return raw.view(dtype).view(shape)
 
     def device_status(self, stream=None) -> int:
         return moe_check_device_status(self.ws, stream)

@@ -284,6 +284,14 @@ moe_status_t ep_route_and_dispatch(const EpBuffers& b, cudaStream_t s) {
     return MOE_OK;
 }
 
+size_t ep_recv_start_int(int W, int E) { return (size_t)W * E + (size_t)W * (E + 1) + (size_t)W * W * 3; }
+
+size_t ep_expert_offsets_int(int W, int E) {
+    const int El = E / W;
+    return ep_recv_start_int(W, E) + W + 1 + (size_t)W * W * El + (size_t)W * W * El * 3 + (size_t)W * El +
+           2 * (size_t)W * (El + 1);
+}
+
 const int32_t* ep_rank_offsets(const EpBuffers& b, int q) {
     const int W = b.W, E = b.E, El = E / W;
     const int32_t* goff = b.scratch + (size_t)W * E + (size_t)W * (E + 1) + (size_t)W * W * 3 + W + 1 +

@@ -220,7 +220,7 @@ moe_status_t mark(void* const* ev, int stage, int end, cudaStream_t s) {
 
 // Per-device side stream for the shared experts, with the fork/join events.
 // The shared experts depend only on x, so they run on the side stream while
-// the main stream routes and permutes the tokens -- kernels that leave most of
+// the main stream computes the gate logits, routes and permutes the tokens -- kernels that leave most of
 // the SMs idle ("Lower latency and higher throughput with multi-node DeepSeek
 // deployment", §Dispatch Overlap: the shared expert is computed while the
 // tokens are being dispatched).  The mutex keeps each call's record/wait pairs
@@ -379,15 +379,18 @@ moe_status_t layer_forward(const moe_layer_desc* d, const void* x, void* out, vo
         MOE_CUDA_TRY(cudaStreamWaitEvent(s, hp->in[io_chunks - 1], 0));  // the gate reads all of x
     }
     MOE_TRY(mark(ev, ST_GATE, 0, s));
+    if (fp8) MOE_TRY(launch_quantize_rows_fp8(x, dt, T, H, xq, xs, ldx, s));  // activations, 1x128 blocks
+    // fork: the shared experts need x alone (FP8: its codes), so they branch off
+    // before the gate; the gate is enqueued first and starts first
+    const bool fork = side && !chunked_shared;
+    if (fork) MOE_CUDA_TRY(cudaEventRecord(side->fork, s));
     int nsplit = 1;
     MOE_TRY(layer_gate(*d, x, logits, &nsplit, s));
-    if (fp8) MOE_TRY(launch_quantize_rows_fp8(x, dt, T, H, xq, xs, ldx, s));  // activations, 1x128 blocks
     MOE_TRY(mark(ev, ST_GATE, 1, s));
     if (chunked_shared) {
         // launched above
-    } else if (side) {
-        // fork: shared experts on the side stream, after the gate
-        MOE_CUDA_TRY(cudaEventRecord(side->fork, s));
+    } else if (fork) {
+        // shared experts on the side stream, beside the gate and the routing steps
         MOE_CUDA_TRY(cudaStreamWaitEvent(side->stream, side->fork, 0));
         cudaStream_t ss = side->stream;
         MOE_TRY(mark(ev, ST_SHARED, 0, ss));
@@ -515,10 +518,10 @@ moe_status_t layer_forward_ep(const moe_layer_desc* d, int W, const void* x, voi
     if (side) side_lock = std::unique_lock<std::mutex>(side->mu);
 
     MOE_TRY(clear_status(ws, s));
+    if (side) MOE_CUDA_TRY(cudaEventRecord(side->fork, s));  // the shared experts need x alone
     int nsplit = 1;
     MOE_TRY(layer_gate(*d, x, logits, &nsplit, s));
     if (side) {
-        MOE_CUDA_TRY(cudaEventRecord(side->fork, s));
         MOE_CUDA_TRY(cudaStreamWaitEvent(side->stream, side->fork, 0));
         MOE_TRY(ffn_up(x, dt, nullptr, 1, T, H, SI, d->w13_shared, hs, status, side->stream));
         MOE_TRY(ffn_down(hs, dt, nullptr, 1, T, H, SI, d->w2_shared, ys, status, side->stream));
@@ -815,6 +818,27 @@ moe_status_t moe_layer_forward_timed(const moe_layer_desc* desc, const void* x, 
 size_t moe_layer_workspace_bytes_ep(const moe_layer_desc* desc, int W) {
     if (check_ep(desc, W) != MOE_OK) return 0;
     return ep_layout(*desc, W, layout(*desc)).total;
+}
+
+moe_status_t moe_layer_workspace_field_ep(const moe_layer_desc* desc, int W, moe_ws_field_ep field, size_t* offset,
+                                          size_t* bytes) {
+    MOE_TRY(check_ep(desc, W));
+    const EpLayout EL = ep_layout(*desc, W, layout(*desc));
+    const size_t R = (size_t)desc->T * desc->k;
+    size_t off = 0, nb = 0;
+    switch (field) {
+        case MOE_WS_EP_X_SORTED: off = EL.sorted_off; nb = R * desc->H * dt_size(desc->dtype); break;
+        case MOE_WS_EP_GATHERED_IDS_UNSORT: off = EL.gidx_off; nb = R * 4; break;
+        case MOE_WS_EP_RECV_START: off = EL.scratch_off + 4 * ep_recv_start_int(W, desc->E); nb = (W + 1) * 4; break;
+        case MOE_WS_EP_EXPERT_OFFSETS:
+            off = EL.scratch_off + 4 * ep_expert_offsets_int(W, desc->E);
+            nb = ((size_t)desc->E + 1) * 4;
+            break;
+        default: return MOE_ERR_INVALID_ARG;
+    }
+    if (offset) *offset = off;
+    if (bytes) *bytes = nb;
+    return MOE_OK;
 }
 
 moe_status_t moe_layer_forward_ep(const moe_layer_desc* desc, int W, const void* x, void* out, void* ws,

@@ -81,6 +81,8 @@ struct EpBuffers {
 };
 size_t ep_scratch_ints(int W, int E);
 moe_status_t ep_route_and_dispatch(const EpBuffers& b, cudaStream_t s);
+size_t ep_recv_start_int(int W, int E);      // int offsets of recv_start and of the global
+size_t ep_expert_offsets_int(int W, int E);  // expert offsets inside the EP scratch
 const int32_t* ep_rank_offsets(const EpBuffers& b, int q);  // [E/W + 1] rows of rank q's experts in `sorted`
 const int32_t* ep_expert_offsets(const EpBuffers& b);       // [E + 1] rows of every expert in `sorted`
 moe_status_t ep_combine(const EpBuffers& b, const void* y_sorted, void* y_recv, void* y_expanded, cudaStream_t s);

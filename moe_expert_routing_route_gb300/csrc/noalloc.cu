@@ -12,12 +12,18 @@
 // library holds it (1 MiB) until the process exits.  Host code cannot use the
 // array's name as a device address, so the first call on each device looks the
 // address up with cudaGetSymbolAddress while that device is current and keeps
-// it; later calls on that device reuse it.  All calls share the one array and
-// it keeps whatever the last call left there.  The histogram kernel rewrites
-// every entry a call reads, so nothing has to be cleared between calls, but two
-// calls whose kernels overlap on the GPU (different streams, or different host
-// threads on one device) race on the array and corrupt each other's results.
+// it; later calls on that device reuse it.  The address belongs to the device's
+// context: after a cudaDeviceReset the module is loaded again into a new
+// context, possibly elsewhere, so the kept address is tagged with the context's
+// process-unique id and looked up again when the current context's id differs.
+// All calls share the one array and it keeps whatever the last call left
+// there.  The histogram kernel rewrites every entry a call reads, so nothing
+// has to be cleared between calls, but two calls whose kernels overlap on the
+// GPU (different streams, or different host threads on one device) race on the
+// array and corrupt each other's results.
 #include "moe_internal.cuh"
+
+#include <cuda.h>
 
 #include <mutex>
 
@@ -29,20 +35,55 @@ static __device__ __align__(256) int32_t g_noalloc_scratch[kNoAllocScratchInts];
 
 constexpr int kMaxDevices = 64;
 std::mutex g_setup_mutex;
-int32_t* g_scratch_ptr[kMaxDevices] = {};
+struct ScratchAddr {
+    int32_t* ptr = nullptr;
+    unsigned long long ctx_id = 0;  // id of the context the address belongs to (0: unknown)
+};
+ScratchAddr g_scratch[kMaxDevices];
 
-// Device address of the array for the current device (set up on first use).
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long*);
+
+// Id of the calling thread's current context, 0 when there is none or the
+// driver cannot say (then a kept address is trusted as it is).
+unsigned long long current_context_id() {
+    static CtxGetCurrentFn get_current = nullptr;
+    static CtxGetIdFn get_id = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_current = reinterpret_cast<CtxGetCurrentFn>(p);
+        p = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<CtxGetIdFn>(p);
+    });
+    if (!get_current || !get_id) return 0;
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (get_current(&ctx) != CUDA_SUCCESS || !ctx || get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+    return id;
+}
+
+// Device address of the array for the current device (set up on first use in
+// each context of that device).
 moe_status_t scratch_for_current_device(int32_t** out) {
     int dev = 0;
     MOE_CUDA_TRY(cudaGetDevice(&dev));
     if (dev < 0 || dev >= kMaxDevices) return MOE_ERR_UNSUPPORTED;
     std::lock_guard<std::mutex> lock(g_setup_mutex);
-    if (!g_scratch_ptr[dev]) {
+    ScratchAddr& a = g_scratch[dev];
+    const unsigned long long id = current_context_id();
+    if (!a.ptr || (id != 0 && id != a.ctx_id)) {
         void* p = nullptr;
         if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return MOE_ERR_CUDA;
-        g_scratch_ptr[dev] = static_cast<int32_t*>(p);
+        a.ptr = static_cast<int32_t*>(p);
+        a.ctx_id = current_context_id();  // the lookup made the device's context current
     }
-    *out = g_scratch_ptr[dev];
+    *out = a.ptr;
     return MOE_OK;
 }
 

@@ -86,6 +86,11 @@ CONFIGS = {
     # per expert) on 32 experts, small enough for ncu captures (~5 GB on the device).
     "dsv3_prefill_slice": LayerConfig("dsv3_prefill_slice", T=512, H=7168, E=32, k=8, I=2048, S=1,
                                       dtype="bf16", seed=2),
+    # Profiling slice of the skewed long prefill: 512 rows per expert on average over
+    # 32 experts with the Zipf(1.2) popularity bias (~3 GB of weights on the device),
+    # so the routed GEMMs are compute-bound and unevenly loaded as in the full layer.
+    "dsv3_zipf_prefill_slice": LayerConfig("dsv3_zipf_prefill_slice", T=2048, H=7168, E=32, k=8, I=2048, S=1,
+                                           dtype="bf16", seed=4, zipf_s=1.2),
 }
 CONFIG_ORDER = ["tiny_fp32", "mid_bf16", "dsv3_prefill", "dsv3_decode", "dsv3_zipf_prefill"]
 

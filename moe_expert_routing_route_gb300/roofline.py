@@ -99,6 +99,34 @@ def load_peaks(path: str | None = None) -> dict:
     return dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0, source="fallback")
 
 
+GEMM_STAGES = ("shared", "up", "down")
+
+
+def layer_roofline(costs: dict, seconds: float, peaks: dict, sustained: bool = True,
+                   gemm_tensor_scale: float = 1.0) -> dict:
+    """The whole layer against its roofline: the ideal time is the slower of all
+    stages' FLOPs at the tensor peak and all stages' bytes at HBM bandwidth
+    (§Roofline: a kernel cannot beat either ceiling, and the layer's stages run
+    back to back on one GPU); frac = ideal time / measured time.
+
+    costs: stage_costs() output.  gemm_tensor_scale applies to the expert GEMM
+    stages only (FP8 expert weights: 2, the nominal FP8/bf16 ratio); the gate
+    GEMM stays on the bf16 peak."""
+    tf = (peaks["bf16_tflops_sustained"] if sustained else peaks["bf16_tflops"]) * 1e12
+    flops = sum(f for f, _ in costs.values())
+    nbytes = sum(b for _, b in costs.values())
+    t_compute = sum(f / (tf * (gemm_tensor_scale if s in GEMM_STAGES else 1.0)) for s, (f, _) in costs.items())
+    t_bytes = nbytes / (peaks["hbm_gbs"] * 1e9)
+    ideal = max(t_compute, t_bytes)
+    # the stricter per-stage form: each stage at its own ceiling, stages not overlapped
+    staged = sum(max(f / (tf * (gemm_tensor_scale if s in GEMM_STAGES else 1.0)), b / (peaks["hbm_gbs"] * 1e9))
+                 for s, (f, b) in costs.items())
+    return dict(layer_frac=ideal / seconds, layer_bound="tensor" if t_compute > t_bytes else "hbm",
+                layer_ideal_ms=ideal * 1e3, layer_flops=flops, layer_bytes=nbytes,
+                layer_compute_ms=t_compute * 1e3, layer_bytes_ms=t_bytes * 1e3,
+                layer_frac_stagewise=staged / seconds)
+
+
 def roofline_entry(flops: float, nbytes: float, seconds: float, peaks: dict, sustained: bool = True,
                    tensor_scale: float = 1.0) -> dict:
     """The binding roofline of one kernel: whichever of compute time at the

@@ -65,3 +65,57 @@ def check_permutation_properties(ids: np.ndarray, E: int, counts, offsets, row_i
     if x is not None:
         k = ids.shape[1]
         assert np.array_equal(ex[row_idx], x[np.arange(R) // k])
+
+
+def per_row_rel_l2(got, want) -> np.ndarray:
+    """rel-L2 of each row (token) separately: ||got_r - want_r|| / ||want_r||."""
+    got, want = f64(got), f64(want)
+    got, want = got.reshape(len(got), -1), want.reshape(len(want), -1)
+    den = np.linalg.norm(want, axis=1)
+    return np.linalg.norm(got - want, axis=1) / np.where(den > 0, den, 1.0)
+
+
+# Per-token (per-row) tolerance next to the aggregate one: one wrong row among
+# thousands barely moves an aggregate rel-L2, but fails this.
+ROW_TOL = {"bf16": 3e-2, "f32": 1e-5}
+
+
+def group_scores(scores: np.ndarray, n_group: int, rule: str) -> np.ndarray:
+    """Group score of each expert group: its best score ("max") or the sum of its
+    two best ("top2_sum").  scores [E] or [T,E]."""
+    s = np.atleast_2d(scores)
+    g = -np.sort(-s.reshape(len(s), n_group, -1), axis=2)
+    out = g[:, :, 0] + (g[:, :, 1] if rule == "top2_sum" else 0.0)
+    return out if scores.ndim == 2 else out[0]
+
+
+def check_grouped_topk_valid(ids: np.ndarray, scores: np.ndarray, n_group: int, topk_group: int, rule: str,
+                             err: float):
+    """Group-limited routing, valid within a score error of `err` per expert: there
+    is a set K of topk_group groups that is a top-topk_group set of the group
+    scores (within the error of a group score: 2*err for "max", 4*err for a sum
+    of two), such that ids lie in K and are a valid top-k of the scores of K's
+    experts (within 2*err).  K exists iff the greedy choice exists: the groups of
+    ids, plus the best-scoring other groups whose experts all score no more than
+    the weakest chosen one (+ 2*err)."""
+    E = scores.size
+    gs = E // n_group
+    k = ids.size
+    assert len(set(ids.tolist())) == k, "duplicate expert ids"
+    s = scores[ids]
+    assert np.all(s[:-1] >= s[1:] - 2 * err), "slots not in descending order"
+    gsc = group_scores(scores, n_group, rule)
+    gtol = (4 if rule == "top2_sum" else 2) * err
+    chosen = sorted(set((ids // gs).tolist()))
+    assert len(chosen) <= topk_group, "ids span more groups than are kept"
+    gmax = scores.reshape(n_group, gs).max(axis=1)
+    cand = [g for g in np.argsort(-gsc, kind="stable") if g not in chosen and gmax[g] <= s.min() + 2 * err]
+    K = chosen + [int(g) for g in cand[:topk_group - len(chosen)]]
+    assert len(K) == topk_group, "no valid set of kept groups holds these ids"
+    rest = [g for g in range(n_group) if g not in K]
+    if rest:
+        assert gsc[K].min() >= gsc[rest].max() - gtol, "a better group was left out"
+    in_k = np.concatenate([np.arange(g * gs, (g + 1) * gs) for g in K])
+    others = np.setdiff1d(in_k, ids)
+    if others.size:
+        assert s.min() >= scores[others].max() - 2 * err, "a better expert of a kept group was left out"

@@ -69,3 +69,33 @@ def test_stage_costs_sum_the_parts():
     assert st["shared"] == tuple(a + b for a, b in zip(parts["up_shared"], parts["down_shared"]))
     assert st["up"] == parts["up_routed"] and st["down"] == parts["down_routed"]
     assert list(st) == ["gate", "route", "init_routing", "permute_rows", "shared", "up", "down", "finalize"]
+
+
+def test_layer_roofline_is_the_slower_ceiling_over_all_stages():
+    """dsv3 prefill: the summed bytes at HBM bandwidth exceed the summed FLOPs at the
+    sustained tensor peak, so the layer is HBM-bound and frac = (bytes / BW) / time."""
+    T, H, E, k, I, S = 4096, 7168, 256, 8, 2048, 1
+    costs = roofline.stage_costs(T, H, E, k, I, S, 2, touched=E)
+    peaks = dict(hbm_gbs=6787.2, bf16_tflops=1927.2, bf16_tflops_sustained=1721.0)
+    lr = roofline.layer_roofline(costs, 4.169e-3, peaks)
+    nbytes = sum(b for _, b in costs.values())
+    flops = sum(f for f, _ in costs.values())
+    assert lr["layer_bound"] == "hbm"
+    assert lr["layer_bytes"] == nbytes and lr["layer_flops"] == flops
+    assert lr["layer_frac"] == pytest.approx(nbytes / 6787.2e9 / 4.169e-3)
+    assert 0.85 < lr["layer_frac"] < 0.95  # 25.2 GB in 4.169 ms
+    # the compute ceiling alone: 3.26 TFLOP at 1721 TFLOP/s
+    assert lr["layer_compute_ms"] == pytest.approx(flops / 1721e12 * 1e3)
+
+
+def test_layer_roofline_compute_bound_and_fp8_scale():
+    """A skewed 16K-token layer is compute-bound; FP8 expert GEMMs halve the GEMM
+    stages' compute time but not the gate's."""
+    T, H, E, k, I, S = 16384, 7168, 256, 8, 2048, 1
+    costs = roofline.stage_costs(T, H, E, k, I, S, 2, touched=E)
+    peaks = dict(hbm_gbs=6787.2, bf16_tflops=1927.2, bf16_tflops_sustained=1721.0)
+    lr = roofline.layer_roofline(costs, 12e-3, peaks)
+    assert lr["layer_bound"] == "tensor"
+    lr8 = roofline.layer_roofline(costs, 12e-3, peaks, gemm_tensor_scale=2.0)
+    gate_ms = costs["gate"][0] / 1721e12 * 1e3
+    assert lr8["layer_compute_ms"] == pytest.approx(gate_ms + (lr["layer_compute_ms"] - gate_ms) / 2)

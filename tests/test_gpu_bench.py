@@ -31,6 +31,12 @@ def test_bench_json_line_keys():
     assert rl["bound"] in ("hbm", "tensor") and rl["unit"] in ("GB/s", "TFLOP/s")
     assert rl["achieved"] > 0 and rl["peak"] > 0 and abs(rl["frac"] - rl["achieved"] / rl["peak"]) < 1e-9
     assert "traffic" in rl
+    # whole-layer roofline: reproducible from the stage costs in the line
+    sc = rl["stage_costs"]
+    assert rl["layer_bytes"] == sum(v["bytes"] for v in sc.values())
+    assert rl["layer_flops"] == sum(v["flops"] for v in sc.values())
+    assert abs(rl["layer_frac"] - rl["layer_ideal_ms"] / d["ms_per_step"]) < 1e-9
+    assert 0 < rl["layer_frac_stagewise"] and rl["layer_frac"] <= rl["layer_frac_stagewise"] + 1e-12
     e = d["e2e"]
     assert e["value"] > 0 and e["h2d_bytes_per_step"] == e["d2h_bytes_per_step"] == 64 * 256 * 4
     assert d["gpu_launches"] > 0

@@ -50,3 +50,43 @@ def test_noalloc_rejects_requests_beyond_its_scratch():
                                                 binding._ptr(out), binding._ptr(out), binding._ptr(out),
                                                 binding._ptr(out), binding._stream())
     assert st == binding.MOE_ERR_UNSUPPORTED
+
+
+def test_noalloc_bad_ids_match_workspace_version():
+    """Ids outside [0,E): not counted, expanded_row_idx = -1, the same outputs as the
+    workspace version (whose status word flags them) on the rows both write."""
+    T, k, E, H = 300, 4, 16, 64
+    ids = inputs.random_ids(T, k, E, seed=31)
+    ids[7, 2] = -1
+    ids[100, 0] = E
+    ids[299, 3] = E + 40
+    ids = ids.to(DEV)
+    x = inputs.random_rows(T, H, torch.bfloat16, seed=32, tag="x").to(DEV)
+    for _ in range(2):
+        got = binding.moe_init_routing_noalloc(x, ids, E)
+        want = binding.moe_init_routing(x, ids, E)
+        assert binding.moe_check_device_status(want["ws"]) & binding.MOE_DEVERR_BAD_EXPERT_ID
+        for key in ("tokens_per_expert", "expert_offsets", "expanded_row_idx"):
+            assert torch.equal(got[key], want[key]), key
+        idx = got["expanded_row_idx"].cpu()
+        assert idx[7 * k + 2] == -1 and idx[100 * k] == -1 and idx[299 * k + 3] == -1
+        assert int(got["tokens_per_expert"].sum()) == T * k - 3
+        n = int(got["expert_offsets"][E])
+        assert n == T * k - 3
+        assert torch.equal(got["expanded_x"][:n], want["expanded_x"][:n])
+
+
+def test_noalloc_empty_batch_writes_zero_counts():
+    """T = 0: every count and offset is written as 0, whatever the buffers held."""
+    E, k, H = 40, 3, 16
+    x = torch.empty((0, H), dtype=torch.bfloat16, device=DEV)
+    ids = torch.empty((0, k), dtype=torch.int32, device=DEV)
+    for _ in range(2):
+        counts = torch.full((E,), 7, dtype=torch.int32, device=DEV)
+        offsets = torch.full((E + 1,), 7, dtype=torch.int32, device=DEV)
+        st = binding.lib().moe_init_routing_noalloc(binding._ptr(x), binding.MOE_BF16, binding._ptr(ids), 0, H, E,
+                                                    k, None, None, binding._ptr(counts), binding._ptr(offsets),
+                                                    binding._stream())
+        assert st == binding.MOE_OK
+        torch.cuda.synchronize()
+        assert torch.all(counts == 0) and torch.all(offsets == 0)
