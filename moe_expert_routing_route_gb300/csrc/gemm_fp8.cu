@@ -47,12 +47,24 @@ constexpr int kMaxGroups = 1024;
 constexpr int A_BYTES = BM * BK;
 constexpr int B_BYTES = BN * BK;
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-constexpr int STAGES = 4;
 constexpr int TMEM_COLS = 2 * BN;  // two partial buffers
-constexpr int NUM_BARS = 2 * STAGES + 9;  // full, empty, partial full/empty, drain, 4 amax exchanges
 constexpr int XAMAX_FLOATS = 2 * kSplit * BM;  // [tile parity][column part][row]
-constexpr size_t SMEM = 1024 + (size_t)STAGES * STAGE_BYTES + NUM_BARS * 8 + 16 + (size_t)(3 * kMaxGroups + 1) * 4 +
-                        (size_t)XAMAX_FLOATS * 4;
+constexpr int kOutBox = 32 * kCols * 2;        // one warp's 32 rows x kCols bf16 columns (128-byte rows)
+static_assert(kCols * 2 == 128, "a staged output row is one 128-byte swizzle row");
+
+// Shared-memory plan per epilogue.  The bf16 epilogue (the down projection)
+// stages each finished tile in shared memory and writes it with TMA stores, so
+// its warps go straight back to folding the next tile's partials instead of
+// waiting on 16-byte row-by-row global stores; the 64 KB staging area takes the
+// place of one pipeline stage.
+template <int EPI>
+struct Plan {
+    static constexpr int STAGES = EPI == TC_EPI_BF16 ? 3 : 4;
+    static constexpr int OUT_BYTES = EPI == TC_EPI_BF16 ? kEpiWarps * 2 * kOutBox : 0;
+    static constexpr int NUM_BARS = 2 * STAGES + 9;  // full, empty, partial full/empty, drain, 4 amax exchanges
+    static constexpr size_t SMEM = 1024 + (size_t)STAGES * STAGE_BYTES + OUT_BYTES + NUM_BARS * 8 + 16 +
+                                   (size_t)(3 * kMaxGroups + 1) * 4 + (size_t)XAMAX_FLOATS * 4;
+};
 
 struct Params {
     const int32_t* offsets;  // [G+1] or nullptr: one group of M rows
@@ -62,6 +74,7 @@ struct Params {
     const float* a_scales;  // [M][lda_s]
     int lda_s;
     const float* b_scales;  // [G][Nb/128][KB]
+    int c_tma;              // bf16 epilogue: C is written through mapC (TMA stores of staged tiles)
     uint8_t* q;             // SwiGLU only, nullable: e4m3 codes of h [M][N]
     float* q_scales;        // [M][ldq]: one per 1x128 block of h
     int ldq;
@@ -125,18 +138,35 @@ __device__ __forceinline__ void store_row(__nv_bfloat16* C, int64_t ldc, int64_t
     }
 }
 
+// One warp's 32 x 64 bf16 block into a staging box laid out as the 128-byte
+// swizzled TMA box expects: 16-byte chunk c of row r at r*128 + ((c ^ (r % 8)) * 16).
+// Lane r writes its row; eight consecutive rows cover all banks.
+__device__ __forceinline__ void stage_row_sw128(uint8_t* box, int r, const float* v) {
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+        uint4 u;
+        u.x = pack_bf16x2(v[8 * c + 0], v[8 * c + 1]);
+        u.y = pack_bf16x2(v[8 * c + 2], v[8 * c + 3]);
+        u.z = pack_bf16x2(v[8 * c + 4], v[8 * c + 5]);
+        u.w = pack_bf16x2(v[8 * c + 6], v[8 * c + 7]);
+        *reinterpret_cast<uint4*>(box + r * 128 + ((c ^ (r & 7)) << 4)) = u;
+    }
+}
+
 template <int EPI>
 __global__ void __launch_bounds__(kThreads, 1)
 tc_fp8_grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
-                           const __grid_constant__ Params p) {
+                           const __grid_constant__ CUtensorMap mapC, const __grid_constant__ Params p) {
     constexpr uint32_t IDESC = idesc_e4m3(BM, BN);
+    constexpr int STAGES = Plan<EPI>::STAGES;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_u32(smem_raw);
     uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
     uint8_t* sA = smem;
     uint8_t* sB = smem + STAGES * A_BYTES;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(sB + STAGES * B_BYTES);
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + NUM_BARS);
+    uint8_t* sOut = sB + STAGES * B_BYTES;  // bf16 epilogue: kEpiWarps x 2 staging boxes (1024-aligned)
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sOut + Plan<EPI>::OUT_BYTES);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + Plan<EPI>::NUM_BARS);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     int* prefix = reinterpret_cast<int*>(tmem_slot + 4);
     int* gstart = prefix + kMaxGroups + 1;
@@ -375,11 +405,31 @@ tc_fp8_grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __gri
                         if (part == 0) p.q_scales[row * (int64_t)p.ldq + n] = sc;
                     }
                 }
-            } else if (valid) {
-                store_row<kCols>(C, p.ldc, row, n * BN + colA, p.N, acc);
-                store_row<kCols>(C, p.ldc, row, n * BN + colB, p.N, acc + kCols);
+            } else {
+                // all 32 rows of this warp inside the expert's segment: stage and TMA-store
+                // the two 32 x 64 blocks; a warp holding rows past the segment (they belong
+                // to the next expert) stores its valid rows directly
+                if (p.c_tma && __all_sync(0xffffffffu, valid)) {
+                    uint8_t* box = sOut + (warp - 2) * 2 * kOutBox;
+                    if (lane == 0) bulk_wait_read_all();  // the previous tile's boxes have left
+                    __syncwarp();
+                    stage_row_sw128(box, lane, acc);
+                    stage_row_sw128(box + kOutBox, lane, acc + kCols);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        const int row0 = gstart[g] + m * BM + eg * 32;
+                        if (n * BN + colA < p.N) tma_store_2d(&mapC, smem_u32(box), n * BN + colA, row0);
+                        if (n * BN + colB < p.N) tma_store_2d(&mapC, smem_u32(box + kOutBox), n * BN + colB, row0);
+                        bulk_commit();
+                    }
+                } else if (valid) {
+                    store_row<kCols>(C, p.ldc, row, n * BN + colA, p.N, acc);
+                    store_row<kCols>(C, p.ldc, row, n * BN + colB, p.N, acc + kCols);
+                }
             }
         }
+        if (EPI == TC_EPI_BF16 && lane == 0) bulk_wait_all();  // staged stores done before the CTA leaves
     }
 
     __syncwarp();
@@ -399,12 +449,16 @@ moe_status_t launch_impl(const TcFp8GroupedGemm& g, cudaStream_t s) {
     cudaError_t attr_err = cudaSuccess;
     std::call_once(attr_once[dev & 63], [&] {
         attr_err = cudaFuncSetAttribute(tc_fp8_grouped_gemm_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        (int)SMEM);
+                                        (int)Plan<EPI>::SMEM);
     });
     MOE_CUDA_TRY(attr_err);
-    CUtensorMap ma, mb;
+    CUtensorMap ma, mb, mc;
     if (!make_map(&ma, g.A, (uint64_t)g.K, (uint64_t)g.M, BM, 1)) return MOE_ERR_CUDA;
     if (!make_map(&mb, g.B, (uint64_t)g.K, (uint64_t)g.G * g.Nb, BN, 1)) return MOE_ERR_CUDA;
+    // bf16 output through TMA stores when the map can describe it (else direct stores)
+    const bool c_tma = EPI == TC_EPI_BF16 && g.C &&
+                       make_store_map_bf16(&mc, g.C, (uint64_t)g.N, (uint64_t)g.M, (uint64_t)g.ldc, 32);
+    if (!c_tma) mc = ma;  // never read
     Params p;
     p.offsets = g.offsets;
     p.G = g.G;
@@ -419,13 +473,14 @@ moe_status_t launch_impl(const TcFp8GroupedGemm& g, cudaStream_t s) {
     p.a_scales = g.a_scales;
     p.lda_s = g.lda_scales;
     p.b_scales = g.b_scales;
+    p.c_tma = c_tma ? 1 : 0;
     p.q = g.q;
     p.q_scales = g.q_scales;
     p.ldq = g.ldq;
     p.status = g.status;
     const int64_t max_tiles = (int64_t)p.NT * (ceil_div(g.M, BM) + (g.offsets ? g.G : 0));
     const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(sm_count(), max_tiles));
-    tc_fp8_grouped_gemm_kernel<EPI><<<grid, kThreads, SMEM, s>>>(ma, mb, p);
+    tc_fp8_grouped_gemm_kernel<EPI><<<grid, kThreads, Plan<EPI>::SMEM, s>>>(ma, mb, mc, p);
     note_launch();
     return last_launch_status();
 }

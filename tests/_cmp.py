@@ -1,6 +1,9 @@
 """Comparison helpers shared by the tests (no arithmetic of the method here)."""
 from __future__ import annotations
 
+import json
+import os
+
 import numpy as np
 import torch
 
@@ -75,9 +78,10 @@ def per_row_rel_l2(got, want) -> np.ndarray:
     return np.linalg.norm(got - want, axis=1) / np.where(den > 0, den, 1.0)
 
 
-# Per-token (per-row) tolerance next to the aggregate one: one wrong row among
-# thousands barely moves an aggregate rel-L2, but fails this.
-ROW_TOL = {"bf16": 3e-2, "f32": 1e-5}
+# Per-token (per-row) tolerance next to the aggregate one: the layer tolerance
+# (rel-L2 <= 1e-2 bf16, 1e-5 fp32) held by every token, not only on average.  One
+# wrong row among thousands barely moves an aggregate rel-L2, but fails this.
+ROW_TOL = {"bf16": 1e-2, "f32": 1e-5}
 
 
 def group_scores(scores: np.ndarray, n_group: int, rule: str) -> np.ndarray:
@@ -119,3 +123,12 @@ def check_grouped_topk_valid(ids: np.ndarray, scores: np.ndarray, n_group: int, 
     others = np.setdiff1d(in_k, ids)
     if others.size:
         assert s.min() >= scores[others].max() - 2 * err, "a better expert of a kept group was left out"
+
+
+def log_parity(name: str, **values):
+    """Append the measured errors of one comparison to the file MOE_PARITY_LOG names
+    (nothing when it is unset): the record behind the tolerances."""
+    path = os.environ.get("MOE_PARITY_LOG")
+    if path:
+        with open(path, "a") as f:
+            f.write(json.dumps(dict(config=name, **values)) + "\n")

@@ -10,15 +10,12 @@ Outputs: aggregate rel-L2 within the layer tolerance (1e-2 bf16, 1e-5 fp32) and,
 for every compared token, its own rel-L2 within the per-token bound."""
 from __future__ import annotations
 
-import json
-import os
-
 import numpy as np
 import torch
 
 from moe_expert_routing_route_gb300 import binding
 from tests._cmp import (ROW_TOL, check_grouped_topk_valid, check_permutation_properties, check_topk_valid, f64,
-                        group_scores, np_, per_row_rel_l2, rel_l2, routing_ambiguity)
+                        group_scores, log_parity, np_, per_row_rel_l2, rel_l2, routing_ambiguity)
 
 LAYER_TOL = {"bf16": 1e-2, "f32": 1e-5}
 
@@ -83,10 +80,7 @@ def check_output(cfg, ids: np.ndarray, out, ref: dict, toks: np.ndarray) -> dict
     assert rows.size == 0 or rows.max() <= ROW_TOL[cfg.dtype], \
         f"{cfg.name}: token {toks[same][worst]} rel-L2 {rows.max():.3e}"
     res = dict(rel_l2=err, worst_token_rel_l2=float(rows.max()) if rows.size else 0.0, compared=int(same.sum()))
-    log = os.environ.get("MOE_PARITY_LOG")  # optional record of the measured errors
-    if log:
-        with open(log, "a") as f:
-            f.write(json.dumps(dict(config=cfg.name, **res)) + "\n")
+    log_parity(cfg.name, **res)
     return res
 
 

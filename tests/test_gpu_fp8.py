@@ -6,7 +6,7 @@ import pytest
 import torch
 
 from moe_expert_routing_route_gb300 import binding, inputs
-from tests._cmp import ROW_TOL, np_, per_row_rel_l2, rel_l2
+from tests._cmp import ROW_TOL, log_parity, np_, per_row_rel_l2, rel_l2
 from tests._layer_check import check_output, check_routing, host_arrays
 
 pytestmark = pytest.mark.gpu
@@ -87,7 +87,9 @@ def test_grouped_ffn_fp8(oracle, T, k, E, H, I):
     expert_of_row = np.repeat(np.arange(E, dtype=np.int32), ir["tokens_per_expert"])
     ref = oracle.expert_ffn_rows_fp8(xq, xs, expert_of_row, q)
     assert rel_l2(y, ref) <= 1e-2
-    assert per_row_rel_l2(y, ref).max() <= ROW_TOL["bf16"]
+    rows_err = per_row_rel_l2(y, ref)
+    log_parity("ffn_fp8", rel_l2=rel_l2(y, ref), worst_token_rel_l2=float(rows_err.max()), compared=len(rows_err))
+    assert rows_err.max() <= ROW_TOL["bf16"]
     # The up GEMM's epilogue quantises h itself; its codes and scales are those the
     # 1x128 quantiser gives for the bf16 h stored beside them.  Workspace of this
     # entry point: 256-byte header, h [rows, I] bf16, codes [rows, I], scales

@@ -8,7 +8,7 @@ import pytest
 import torch
 
 from moe_expert_routing_route_gb300 import binding, inputs
-from tests._cmp import ROW_TOL, check_permutation_properties, f64, np_, per_row_rel_l2, rel_l2
+from tests._cmp import ROW_TOL, check_permutation_properties, f64, log_parity, np_, per_row_rel_l2, rel_l2
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -217,6 +217,7 @@ def _close(y, ref, dtype_key: str):
     err = rel_l2(y, ref)
     assert err <= tol, err
     rows = per_row_rel_l2(y, ref)
+    log_parity("ffn_" + dtype_key, rel_l2=err, worst_token_rel_l2=float(rows.max()), compared=len(rows))
     assert rows.max() <= ROW_TOL[dtype_key], f"row {int(rows.argmax())}: rel-L2 {rows.max():.3e}"
     return err
 
