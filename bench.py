@@ -312,6 +312,8 @@ def run_ours(args, world, rank, local):
     # roofline of the dominant kernel
     counts = layer.field("tokens_per_expert").cpu().numpy()
     touched = int((counts > 0).sum())
+    load = dict(max=int(counts.max()), mean=float(counts.mean()), min=int(counts.min()),
+                empty=int((counts == 0).sum()))  # the realised expert histogram of this batch
     fp8 = cfg.weight_format == "fp8"
     costs = roofline.stage_costs(cfg.T, cfg.H, cfg.E, cfg.k, cfg.I, cfg.S, cfg.esize, touched,
                                  weight_bytes=1 if fp8 else None)
@@ -366,7 +368,7 @@ def run_ours(args, world, rank, local):
                     dtype="e4m3+bf16" if fp8 else cfg.dtype, data="synthetic (seeded N(0,1) x, N(0,1/sqrt(fan_in)) "
                     "weights, random-init DeepSeek-V3-shaped MoE layer)",
                     config=dict(workload=cfg.name, T=cfg.T, H=cfg.H, E=cfg.E, k=cfg.k, I=cfg.I, S=cfg.S,
-                                global_batch=tokens, parallelism=f"replicas{world}",
+                                global_batch=tokens, parallelism=f"replicas{world}", expert_load=load,
                                 l2="inputs larger than L2: 22.6 GB of expert weights streamed every step"
                                 if cfg.H == 7168 else "small workload"),
                     roofline=rl, cpu_baseline=cpu,
