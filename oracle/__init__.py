@@ -63,11 +63,11 @@ def _load():
         lib.oracle_e4m3_decode.restype = ctypes.c_double
         lib.oracle_e4m3_encode.argtypes = [ctypes.c_float]
         lib.oracle_e4m3_encode.restype = ctypes.c_uint8
-        lib.oracle_quantize_rows_fp8.argtypes = [P, I, L, I, P, P]
-        lib.oracle_quantize_tiles_fp8.argtypes = [P, I, I, I, P, P]
+        lib.oracle_quantize_rows_fp8.argtypes = [P, I, L, I, P, P, I]
+        lib.oracle_quantize_tiles_fp8.argtypes = [P, I, I, I, P, P, I]
         lib.oracle_gemm_fp8.argtypes = [P, P, P, P, I, I, I, P]
-        lib.oracle_expert_ffn_rows_fp8.argtypes = [P, P, L, P, P, P, P, P, P, P, I, I, P]
-        lib.oracle_layer_fp8.argtypes = [P, I, I, I, I, I, I, I, P, P] + [P] * 12 + [P, I, P, P, P, P, I, I, I]
+        lib.oracle_expert_ffn_rows_fp8.argtypes = [P, P, L, P, P, P, P, P, P, P, I, I, P, I]
+        lib.oracle_layer_fp8.argtypes = [P, I, I, I, I, I, I, I, P, P] + [P] * 12 + [P, I, P, P, P, P, I, I, I, I]
         lib.oracle_unsort_rows.argtypes = [P, I, P, L, I, P]
         lib.oracle_finalize_routing.argtypes = [P, I, L, P, P, P, I, I, I, P]
         lib.oracle_layer.argtypes = [P, I, I, I, I, I, I, I, I, P, P, P, P, P, P, P, P, P, I,
@@ -215,23 +215,25 @@ def e4m3_table() -> np.ndarray:
     return E4M3_VALUES
 
 
-def quantize_rows_fp8(a: np.ndarray):
-    """1x128 blocks along the columns.  Returns (codes uint8 [rows, cols], scales f32 [rows, ceil(cols/128)])."""
+def quantize_rows_fp8(a: np.ndarray, pow2: bool = False):
+    """1x128 blocks along the columns.  Returns (codes uint8 [rows, cols], scales f32 [rows, ceil(cols/128)]).
+    pow2: each scale the smallest power of two that brings the block's largest magnitude to <= 448."""
     a = _c(a)
     rows, cols = a.shape
     codes = np.empty((rows, cols), np.uint8)
     scales = np.empty((rows, (cols + 127) // 128), np.float32)
-    _load().oracle_quantize_rows_fp8(_ptr(a), _dt(a), rows, cols, _ptr(codes), _ptr(scales))
+    _load().oracle_quantize_rows_fp8(_ptr(a), _dt(a), rows, cols, _ptr(codes), _ptr(scales), int(bool(pow2)))
     return codes, scales
 
 
-def quantize_tiles_fp8(w: np.ndarray):
-    """128x128 tiles of a [n_out, k_in] weight.  Returns (codes, scales [ceil(n/128), ceil(k/128)])."""
+def quantize_tiles_fp8(w: np.ndarray, pow2: bool = False):
+    """128x128 tiles of a [n_out, k_in] weight.  Returns (codes, scales [ceil(n/128), ceil(k/128)]).
+    pow2: power-of-two tile scales, as quantize_rows_fp8."""
     w = _c(w)
     n, k = w.shape
     codes = np.empty((n, k), np.uint8)
     scales = np.empty(((n + 127) // 128, (k + 127) // 128), np.float32)
-    _load().oracle_quantize_tiles_fp8(_ptr(w), _dt(w), n, k, _ptr(codes), _ptr(scales))
+    _load().oracle_quantize_tiles_fp8(_ptr(w), _dt(w), n, k, _ptr(codes), _ptr(scales), int(bool(pow2)))
     return codes, scales
 
 
@@ -246,15 +248,16 @@ def gemm_fp8(qa, sa, qb, sb) -> np.ndarray:
     return c
 
 
-def quantize_experts_fp8(w: np.ndarray):
+def quantize_experts_fp8(w: np.ndarray, pow2: bool = False):
     """[E, n_out, k_in] weights -> (codes [E, n_out, k_in], scales [E, n_out/128, k_in/128])."""
     E = w.shape[0]
-    pairs = [quantize_tiles_fp8(w[e]) for e in range(E)]
+    pairs = [quantize_tiles_fp8(w[e], pow2) for e in range(E)]
     return np.stack([p[0] for p in pairs]), np.stack([p[1] for p in pairs])
 
 
-def expert_ffn_rows_fp8(xq, xs, expert, q: dict) -> np.ndarray:
-    """y[r] = FP8 SwiGLU expert expert[r] on quantised row r, stored in bf16 (fp64 out)."""
+def expert_ffn_rows_fp8(xq, xs, expert, q: dict, pow2: bool = False) -> np.ndarray:
+    """y[r] = FP8 SwiGLU expert expert[r] on quantised row r, stored in bf16 (fp64 out).
+    pow2: h is quantised with power-of-two block scales."""
     xq, xs = _c(xq, np.uint8), _c(xs, np.float32)
     expert = _c(expert, np.int32)
     n, H = xq.shape
@@ -262,14 +265,16 @@ def expert_ffn_rows_fp8(xq, xs, expert, q: dict) -> np.ndarray:
     assert xs.shape[1] == (H + 127) // 128
     arrs = [_c(q[k_], np.uint8 if k_.endswith("q") else np.float32) for k_ in ("gq", "gs", "uq", "us", "dq", "ds")]
     y = np.zeros((n, H), np.float64)
-    _load().oracle_expert_ffn_rows_fp8(_ptr(xq), _ptr(xs), n, _ptr(expert), *[_ptr(a) for a in arrs], H, I, _ptr(y))
+    _load().oracle_expert_ffn_rows_fp8(_ptr(xq), _ptr(xs), n, _ptr(expert), *[_ptr(a) for a in arrs], H, I, _ptr(y),
+                                       int(bool(pow2)))
     return y
 
 
 def layer_fp8(x, wg, q: dict, *, k: int, renorm: bool = True, bias=None, tokens=None, n_group: int = 1,
-              topk_group: int = 1, group_rule: str = "max"):
+              topk_group: int = 1, group_rule: str = "max", pow2: bool = False):
     """Brute-force layer with FP8 expert weights (x, wg bf16 bit patterns).  q holds the codes
-    and scales from quantize_experts_fp8: gq, gs, uq, us, dq, ds and the shared sgq ... sds."""
+    and scales from quantize_experts_fp8: gq, gs, uq, us, dq, ds and the shared sgq ... sds.
+    pow2: the activations (x and h) get power-of-two block scales."""
     x, wg = _c(x, np.uint16), _c(wg, np.uint16)
     T, H = x.shape
     E, I = q["gq"].shape[0], q["gq"].shape[1]
@@ -285,7 +290,7 @@ def layer_fp8(x, wg, q: dict, *, k: int, renorm: bool = True, bias=None, tokens=
     out = np.empty((n, H), np.float64)
     _load().oracle_layer_fp8(_ptr(x), T, H, E, k, I, S, int(bool(renorm)), _ptr(wg), _ptr(bias),
                              *[_ptr(a) for a in arrs], _ptr(toks), n, _ptr(logits), _ptr(ids), _ptr(w), _ptr(out),
-                             n_group, topk_group, {"max": 0, "top2_sum": 1}[group_rule])
+                             n_group, topk_group, {"max": 0, "top2_sum": 1}[group_rule], int(bool(pow2)))
     return dict(logits64=logits, ids=ids, w=w, out=out)
 
 

@@ -162,9 +162,29 @@ uint8_t oracle_e4m3_encode(float f) {
 /* Scale of one block from its largest magnitude (fp32 arithmetic). */
 static float block_scale(float amax) { return amax > 0.0f ? amax / 448.0f : 1.0f; }
 
+/* Power-of-two block scales (the second scale format).  [BLOG §Quantization]
+ * fixes per-block scales but not their number format; this reading stores each
+ * scale as a power of two, an 8-bit exponent with no mantissa, which is what
+ * block-scaled tensor-core instructions take.  A block's scale is the smallest
+ * power of two s with amax / s <= 448, so the block's largest magnitude lands
+ * in (224, 448] (1 for an all-zero block; exponent at least -127).  Dividing by
+ * s is exact, so a code is round-to-nearest-even of v / s.                    */
+static float block_scale_pow2(float amax) {
+    if (!(amax > 0.0f)) return 1.0f;
+    int e = (int)ceil(log2((double)amax / 448.0));
+    while (e > -127 && ldexp(448.0, e - 1) >= (double)amax) --e; /* smallest e with amax <= 448 * 2^e */
+    while (ldexp(448.0, e) < (double)amax) ++e;
+    if (e < -127) e = -127;
+    return (float)ldexp(1.0, e);
+}
+
+static float scale_of(float amax, int pow2) { return pow2 ? block_scale_pow2(amax) : block_scale(amax); }
+
 /* Rows of a [rows, cols] matrix (dtype dt) quantised in 1 x 128 blocks along
- * the columns: codes [rows, cols], scales [rows, ceil(cols/128)] fp32.       */
-void oracle_quantize_rows_fp8(const void* a, int dt, int64_t rows, int cols, uint8_t* codes, float* scales) {
+ * the columns: codes [rows, cols], scales [rows, ceil(cols/128)] fp32 (powers
+ * of two when pow2 != 0).                                                    */
+void oracle_quantize_rows_fp8(const void* a, int dt, int64_t rows, int cols, uint8_t* codes, float* scales,
+                              int pow2) {
     int kb = (cols + 127) / 128;
     #pragma omp parallel for schedule(static)
     for (int64_t r = 0; r < rows; ++r) {
@@ -175,7 +195,7 @@ void oracle_quantize_rows_fp8(const void* a, int dt, int64_t rows, int cols, uin
                 float v = (float)load(a, dt, (size_t)r * cols + c);
                 if (fabsf(v) > amax) amax = fabsf(v);
             }
-            float s = block_scale(amax);
+            float s = scale_of(amax, pow2);
             scales[(size_t)r * kb + b] = s;
             for (int c = c0; c < c1; ++c)
                 codes[(size_t)r * cols + c] = oracle_e4m3_encode((float)load(a, dt, (size_t)r * cols + c) / s);
@@ -184,8 +204,9 @@ void oracle_quantize_rows_fp8(const void* a, int dt, int64_t rows, int cols, uin
 }
 
 /* A weight [n_out, k_in] (dtype dt) quantised in 128 x 128 tiles:
- * codes [n_out, k_in], scales [ceil(n_out/128), ceil(k_in/128)] fp32.        */
-void oracle_quantize_tiles_fp8(const void* w, int dt, int n_out, int k_in, uint8_t* codes, float* scales) {
+ * codes [n_out, k_in], scales [ceil(n_out/128), ceil(k_in/128)] fp32 (powers
+ * of two when pow2 != 0).                                                    */
+void oracle_quantize_tiles_fp8(const void* w, int dt, int n_out, int k_in, uint8_t* codes, float* scales, int pow2) {
     int nb = (n_out + 127) / 128, kb = (k_in + 127) / 128;
     #pragma omp parallel for schedule(static) collapse(2)
     for (int bn = 0; bn < nb; ++bn) {
@@ -198,7 +219,7 @@ void oracle_quantize_tiles_fp8(const void* w, int dt, int n_out, int k_in, uint8
                     float v = (float)load(w, dt, (size_t)n * k_in + k);
                     if (fabsf(v) > amax) amax = fabsf(v);
                 }
-            float s = block_scale(amax);
+            float s = scale_of(amax, pow2);
             scales[(size_t)bn * kb + bk] = s;
             for (int n = bn * 128; n < n1; ++n)
                 for (int k = bk * 128; k < k1; ++k)
@@ -541,12 +562,13 @@ void oracle_gemm_fp8(const uint8_t* qa, const float* sa, const uint8_t* qb, cons
 /* One SwiGLU expert on one quantised row (bf16 layer with FP8 weights):
  *   g, u   = FP8 products of the row with the gate and up weights
  *   h      = silu(g) * u, stored in bf16, then quantised in 1x128 blocks
+ *            (power-of-two scales when pow2 != 0)
  *   y      = FP8 product of h with the down weight (returned unrounded)
  * Weights of the expert: gq/uq [I,H] with scales [I/128][H/128]; dq [H,I]
  * with scales [H/128][I/128].                                                 */
 static void expert_ffn_row_fp8(const uint8_t* xq, const float* xs, const uint8_t* gq, const float* gs,
                                const uint8_t* uq, const float* us, const uint8_t* dq, const float* ds, int H,
-                               int I, double* hbuf, uint8_t* hq, float* hs, double* y) {
+                               int I, double* hbuf, uint8_t* hq, float* hs, double* y, int pow2) {
     int kbh = (H + 127) / 128, kbi = (I + 127) / 128;
     for (int i = 0; i < I; ++i) {
         double g = fp8_dot(xq, xs, gq + (size_t)i * H, gs + (size_t)(i / 128) * kbh, H);
@@ -557,7 +579,7 @@ static void expert_ffn_row_fp8(const uint8_t* xq, const float* xs, const uint8_t
         int i1 = b * 128 + 128 < I ? b * 128 + 128 : I;
         float amax = 0.0f;
         for (int i = b * 128; i < i1; ++i) if (fabsf((float)hbuf[i]) > amax) amax = fabsf((float)hbuf[i]);
-        float sc = block_scale(amax);
+        float sc = scale_of(amax, pow2);
         hs[b] = sc;
         for (int i = b * 128; i < i1; ++i) hq[i] = oracle_e4m3_encode((float)hbuf[i] / sc);
     }
@@ -569,7 +591,7 @@ static void expert_ffn_row_fp8(const uint8_t* xq, const float* xs, const uint8_t
  * in oracle_layer_fp8.                                                        */
 void oracle_expert_ffn_rows_fp8(const uint8_t* xq, const float* xs, int64_t n, const int32_t* expert,
                                 const uint8_t* gq, const float* gs, const uint8_t* uq, const float* us,
-                                const uint8_t* dq, const float* ds, int H, int I, double* y) {
+                                const uint8_t* dq, const float* ds, int H, int I, double* y, int pow2) {
     init_e4m3();
     const int kbh = (H + 127) / 128, kbi = (I + 127) / 128;
     const size_t gsz = (size_t)kbi * kbh;
@@ -585,7 +607,7 @@ void oracle_expert_ffn_rows_fp8(const uint8_t* xq, const float* xs, int64_t n, c
             if (e < 0) continue;
             expert_ffn_row_fp8(xq + (size_t)r * H, xs + (size_t)r * kbh, gq + (size_t)e * I * H, gs + e * gsz,
                                uq + (size_t)e * I * H, us + e * gsz, dq + (size_t)e * H * I, ds + e * gsz, H, I,
-                               hbuf, hq, hs, yr);
+                               hbuf, hq, hs, yr, pow2);
             for (int o = 0; o < H; ++o) y[(size_t)r * H + o] = round_to(yr[o], OR_BF16);
         }
         free(hbuf); free(hq); free(hs); free(yr);
@@ -598,13 +620,15 @@ void oracle_expert_ffn_rows_fp8(const uint8_t* xq, const float* xs, int64_t n, c
  * the shared outputs summed and stored in bf16, each routed output stored in
  * bf16, the weighted sum rounded once to bf16.
  * Per-expert weight arrays: gq, uq [E][I][H], gs, us [E][I/128][H/128],
- * dq [E][H][I], ds [E][H/128][I/128]; the shared ones likewise with S.       */
+ * dq [E][H][I], ds [E][H/128][I/128]; the shared ones likewise with S.  With
+ * pow2 != 0 the activations (x and h) get power-of-two block scales; the weight
+ * codes and scales are whatever the caller quantised them with.              */
 void oracle_layer_fp8(const void* x, int T, int H, int E, int k, int I, int S, int renorm, const void* wg,
                       const float* bias, const uint8_t* gq, const float* gs, const uint8_t* uq, const float* us,
                       const uint8_t* dq, const float* ds, const uint8_t* sgq, const float* sgs, const uint8_t* suq,
                       const float* sus, const uint8_t* sdq, const float* sds, const int32_t* tokens, int n_tok,
                       double* logits64, int32_t* ids, double* w, double* out, int n_group, int topk_group,
-                      int group_rule) {
+                      int group_rule, int pow2) {
     init_e4m3();
     if (!tokens) n_tok = T;
     const int kbh = (H + 127) / 128, kbi = (I + 127) / 128;
@@ -634,11 +658,12 @@ void oracle_layer_fp8(const void* x, int T, int H, int E, int k, int I, int S, i
                                           ids + (size_t)n * k, w + (size_t)n * k);
             else
                 oracle_route_topk(l32, bias, 1, E, k, renorm, ids + (size_t)n * k, w + (size_t)n * k);
-            oracle_quantize_rows_fp8((const char*)x + xo * 2, OR_BF16, 1, H, xq, xs);
+            oracle_quantize_rows_fp8((const char*)x + xo * 2, OR_BF16, 1, H, xq, xs, pow2);
             for (int o = 0; o < H; ++o) ysh[o] = 0.0;
             for (int s2 = 0; s2 < S; ++s2) {
                 expert_ffn_row_fp8(xq, xs, sgq + (size_t)s2 * I * H, sgs + s2 * gsz, suq + (size_t)s2 * I * H,
-                                   sus + s2 * gsz, sdq + (size_t)s2 * H * I, sds + s2 * gsz, H, I, hbuf, hq, hs, yr);
+                                   sus + s2 * gsz, sdq + (size_t)s2 * H * I, sds + s2 * gsz, H, I, hbuf, hq, hs, yr,
+                                   pow2);
                 for (int o = 0; o < H; ++o) ysh[o] += yr[o];
             }
             double* orow = out + (size_t)n * H;
@@ -646,7 +671,8 @@ void oracle_layer_fp8(const void* x, int T, int H, int E, int k, int I, int S, i
             for (int j = 0; j < k; ++j) {
                 int e = ids[(size_t)n * k + j];
                 expert_ffn_row_fp8(xq, xs, gq + (size_t)e * I * H, gs + e * gsz, uq + (size_t)e * I * H,
-                                   us + e * gsz, dq + (size_t)e * H * I, ds + e * gsz, H, I, hbuf, hq, hs, yr);
+                                   us + e * gsz, dq + (size_t)e * H * I, ds + e * gsz, H, I, hbuf, hq, hs, yr,
+                                   pow2);
                 double wj = w[(size_t)n * k + j];
                 for (int o = 0; o < H; ++o) orow[o] += wj * round_to(yr[o], OR_BF16);
             }

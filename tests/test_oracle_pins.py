@@ -516,3 +516,106 @@ def test_layer_fp8_dense_case_composes_the_steps(oracle):
     # and the FP8 layer stays close to the bf16 layer (quantisation error only)
     ref = oracle.layer(*(n[k_] for k_ in ("x", "wg", "w_gate", "w_up", "w2", "s_gate", "s_up", "s2")), k=1)
     assert np.linalg.norm(r["out"] - ref["out"]) / np.linalg.norm(ref["out"]) < 0.1
+
+
+# ---- FP8 with power-of-two block scales -------------------------------------------------
+
+def _is_pow2(s: np.ndarray) -> bool:
+    m, _ = np.frexp(s.astype(np.float64))
+    return bool(np.all(m == 0.5))
+
+
+def test_pow2_scales_are_the_smallest_powers_of_two(oracle):
+    """Each scale is a power of two s with amax / s <= 448 < amax / (s / 2): the block's
+    largest magnitude lands in (224, 448]; an all-zero block gets 1."""
+    x = inputs.random_rows(9, 700, torch.float32, seed=21).numpy() * np.logspace(-3, 3, 9)[:, None]
+    x[0, :128] = 0.0
+    codes, scales = oracle.quantize_rows_fp8(x.astype(np.float32), pow2=True)
+    assert _is_pow2(scales) and scales[0, 0] == 1.0 and np.all(codes[0, :128] == 0)
+    for r in range(9):
+        for b in range(scales.shape[1]):
+            amax = np.abs(x[r, b * 128:(b + 1) * 128]).max()
+            if amax == 0:
+                continue
+            s = float(scales[r, b])
+            assert amax / s <= 448.0 < amax / (s / 2)
+    # boundaries: exactly 448 * 2^e keeps 2^e, one fp32 step above doubles it
+    for e in (-20, -1, 0, 3, 40):
+        edge = np.float32(448.0 * 2.0 ** e)
+        blk = np.zeros((2, 128), np.float32)
+        blk[0, 5] = edge
+        blk[1, 5] = np.nextafter(edge, np.float32(np.inf))
+        _, s = oracle.quantize_rows_fp8(blk, pow2=True)
+        assert s[0, 0] == np.float32(2.0 ** e) and s[1, 0] == np.float32(2.0 ** (e + 1))
+
+
+def test_pow2_quantisation_is_lossless_on_grid_values(oracle):
+    """Values c * s with c on the e4m3 grid and a 448 * s in the block come back as the
+    same codes and scale (dividing by a power of two is exact)."""
+    rng = np.random.default_rng(22)
+    table = oracle.e4m3_table()
+    finite = np.flatnonzero(~np.isnan(table) & (np.abs(table) <= 448))
+    for e in (-9, 0, 5):
+        c = rng.choice(finite, size=(3, 256)).astype(np.uint8)
+        c[:, 0] = 0x7E  # 448 in every block
+        c[:, 128] = 0xFE  # -448
+        v = (table[c] * 2.0 ** e).astype(np.float32)
+        codes, scales = oracle.quantize_rows_fp8(v, pow2=True)
+        assert np.all(scales == np.float32(2.0 ** e))
+        assert np.array_equal(table[codes], table[c])  # +0 / -0 compare equal as values
+        wc, ws = oracle.quantize_tiles_fp8(np.tile(v, (43, 1))[:128], pow2=True)
+        assert np.all(ws == np.float32(2.0 ** e)) and np.array_equal(table[wc], table[np.tile(c, (43, 1))[:128]])
+
+
+def test_pow2_dequantised_within_half_a_step(oracle):
+    x = inputs.random_rows(6, 300, torch.bfloat16, seed=23)
+    xf = x.to(torch.float64).numpy()
+    codes, scales = oracle.quantize_rows_fp8(inputs.to_numpy(x), pow2=True)
+    deq = oracle.e4m3_table()[codes] * np.repeat(scales.astype(np.float64), 128, axis=1)[:, :300]
+    # the code is the nearest grid point of v / s: within half an e4m3 step (relative 2^-4, or the
+    # subnormal spacing 2^-9 times s)
+    assert np.all(np.abs(deq - xf) <= np.abs(xf) * 2.0 ** -4 + np.repeat(scales, 128, axis=1)[:, :300] * 2.0 ** -10)
+    # a power-of-two scale wastes at most one bit of range: amax / s > 224
+    assert np.all(np.abs(xf).reshape(6, -1)[:, :256].reshape(6, 2, 128).max(axis=2) / scales[:, :2] > 224)
+
+
+def test_gemm_fp8_pow2_is_dequantised_matmul(oracle):
+    a = inputs.random_rows(7, 300, torch.bfloat16, seed=24)
+    b = inputs.random_rows(260, 300, torch.float32, seed=25).numpy()
+    qa, sa = oracle.quantize_rows_fp8(inputs.to_numpy(a), pow2=True)
+    qb, sb = oracle.quantize_tiles_fp8(b, pow2=True)
+    assert _is_pow2(sa) and _is_pow2(sb)
+    want = _dequant_torch(qa, sa, 1) @ _dequant_torch(qb, sb, 128).T
+    np.testing.assert_allclose(oracle.gemm_fp8(qa, sa, qb, sb), want, rtol=1e-12, atol=1e-12)
+
+
+def test_layer_fp8_pow2_dense_case_composes_the_steps(oracle):
+    """E=1, k=1 + one shared expert with power-of-two scales everywhere: the layer is two
+    FP8 SwiGLU MLPs built from the power-of-two quantiser, the FP8 product and torch's SiLU."""
+    cfg = inputs.LayerConfig("t", T=6, H=256, E=1, k=1, I=128, S=1, dtype="bf16", seed=26)
+    d = inputs.make_layer(cfg)
+    n = {k_: inputs.to_numpy(v) for k_, v in d.items() if isinstance(v, torch.Tensor)}
+    q = {}
+    for pre, g, u, w2 in (("", "w_gate", "w_up", "w2"), ("s", "s_gate", "s_up", "s2")):
+        q[pre + "gq"], q[pre + "gs"] = oracle.quantize_experts_fp8(n[g], pow2=True)
+        q[pre + "uq"], q[pre + "us"] = oracle.quantize_experts_fp8(n[u], pow2=True)
+        q[pre + "dq"], q[pre + "ds"] = oracle.quantize_experts_fp8(n[w2], pow2=True)
+    r = oracle.layer_fp8(n["x"], n["wg"], q, k=1, pow2=True)
+    xq, xs = oracle.quantize_rows_fp8(n["x"], pow2=True)
+
+    def mlp(pre):
+        g = oracle.gemm_fp8(xq, xs, q[pre + "gq"][0], q[pre + "gs"][0])
+        u = oracle.gemm_fp8(xq, xs, q[pre + "uq"][0], q[pre + "us"][0])
+        h = (F.silu(torch.from_numpy(g)) * torch.from_numpy(u)).to(torch.bfloat16)
+        hq, hs = oracle.quantize_rows_fp8(inputs.to_numpy(h), pow2=True)
+        assert _is_pow2(hs)
+        y = oracle.gemm_fp8(hq, hs, q[pre + "dq"][0], q[pre + "ds"][0])
+        return oracle.round_to(y, BF16)
+
+    want = oracle.round_to(mlp("s") + mlp(""), BF16)
+    assert np.abs(r["out"] - want).max() <= 1e-2 * np.abs(want).max()
+    ref = oracle.layer(*(n[k_] for k_ in ("x", "wg", "w_gate", "w_up", "w2", "s_gate", "s_up", "s2")), k=1)
+    assert np.linalg.norm(r["out"] - ref["out"]) / np.linalg.norm(ref["out"]) < 0.1
+    # a wrong scale format in the layer (fp32 scales for h) is visible
+    r32 = oracle.layer_fp8(n["x"], n["wg"], q, k=1, pow2=False)
+    assert not np.array_equal(r32["out"], r["out"])
