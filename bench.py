@@ -239,7 +239,7 @@ def run_ours(args, world, rank, local):
                              s2=d["s2"] if cfg.S else None, expert_bias=d["bias"], renormalize=cfg.renormalize,
                              n_group=cfg.n_group, topk_group=cfg.topk_group, group_rule=cfg.group_rule,
                              weight_format=cfg.weight_format)
-    if cfg.weight_format == "fp8":  # the bf16 expert weights are no longer needed on the device
+    if cfg.weight_format in ("fp8", "fp8_pow2"):  # the bf16 expert weights are no longer needed on the device
         for key in ("w_gate", "w_up", "w2"):
             d[key] = d[key].cpu() if not args.no_cpu_baseline else None
         torch.cuda.empty_cache()
@@ -314,7 +314,7 @@ def run_ours(args, world, rank, local):
     touched = int((counts > 0).sum())
     load = dict(max=int(counts.max()), mean=float(counts.mean()), min=int(counts.min()),
                 empty=int((counts == 0).sum()))  # the realised expert histogram of this batch
-    fp8 = cfg.weight_format == "fp8"
+    fp8 = cfg.weight_format in ("fp8", "fp8_pow2")
     costs = roofline.stage_costs(cfg.T, cfg.H, cfg.E, cfg.k, cfg.I, cfg.S, cfg.esize, touched,
                                  weight_bytes=1 if fp8 else None)
     peaks = roofline.load_peaks()

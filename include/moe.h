@@ -237,6 +237,17 @@ moe_status_t moe_quantize_rows_fp8(const void* a, moe_dtype_t dt, int64_t rows, 
 moe_status_t moe_quantize_weights_fp8(const void* w, moe_dtype_t dt, int G, int n_out, int k_in, uint8_t* codes,
                                       float* scales, moe_stream_t stream);
 
+/* The same two quantisers with power-of-two block scales (the second scale
+ * format).  [BLOG §Quantization] fixes the blocks but not the scales' number
+ * format; here each scale is the smallest power of two 2^e with amax/2^e <= 448
+ * (1 for an all-zero block, e >= -127), so a block's largest magnitude lands in
+ * (224, 448] and a code is the nearest e4m3 value of an exact division.  The
+ * scales are still written as fp32 values.  Arguments as above. */
+moe_status_t moe_quantize_rows_fp8_pow2(const void* a, moe_dtype_t dt, int64_t rows, int cols, uint8_t* codes,
+                                        float* scales, int ld_scales, moe_stream_t stream);
+moe_status_t moe_quantize_weights_fp8_pow2(const void* w, moe_dtype_t dt, int G, int n_out, int k_in,
+                                           uint8_t* codes, float* scales, moe_stream_t stream);
+
 /* Grouped SwiGLU expert FFN with FP8 weights and activations ([BLOG
  * §Quantization], [BLOG §Roofline / GroupGEMM]): products are block-scaled,
  *   C[m,n] = sum_b sa[m,b] * sb[n/128,b] * sum_{k in block b} qa[m,k] qb[n,k],
@@ -251,6 +262,18 @@ moe_status_t moe_grouped_ffn_fp8(const uint8_t* aq, const float* a_scales, int l
                                  const int32_t* expert_offsets, int E, int rows, int H, int I, const uint8_t* w13q,
                                  const float* w13s, const uint8_t* w2q, const float* w2s, void* y, void* ws,
                                  size_t ws_bytes, moe_stream_t stream);
+
+/* moe_grouped_ffn_fp8 with power-of-two scales on every operand (from the _pow2
+ * quantisers): the same product, but the tensor cores apply the scales
+ * (block-scaled MMA taking one 8-bit exponent per 32 K elements of every row of
+ * A and column of B), so each tile accumulates in one TMEM accumulator with no
+ * per-block promotion on CUDA cores; h is quantised with power-of-two scales.
+ * A scale that is not a power of two acts as its exponent (rounded down to a
+ * power of two).  Arguments, workspace and sizes as moe_grouped_ffn_fp8. */
+moe_status_t moe_grouped_ffn_fp8_pow2(const uint8_t* aq, const float* a_scales, int lda_scales,
+                                      const int32_t* expert_offsets, int E, int rows, int H, int I,
+                                      const uint8_t* w13q, const float* w13s, const uint8_t* w2q, const float* w2s,
+                                      void* y, void* ws, size_t ws_bytes, moe_stream_t stream);
 
 /* ---------------------------------------------------------------------------
  * Finalize-routing.  [CANN §MoE deployment, Double-Routing step 8]: restore
@@ -315,7 +338,7 @@ typedef struct moe_layer_desc {
     int n_group;               /* 0 or 1: flat top-k; > 1: group-limited (moe_route_topk_grouped) */
     int topk_group;            /* groups kept when n_group > 1 */
     int group_rule;            /* MOE_GROUP_SCORE_MAX or MOE_GROUP_SCORE_TOP2_SUM */
-    int weight_format;         /* MOE_WEIGHTS_NATIVE or MOE_WEIGHTS_FP8 (bf16 layers only) */
+    int weight_format;         /* MOE_WEIGHTS_NATIVE, MOE_WEIGHTS_FP8 or MOE_WEIGHTS_FP8_POW2 (bf16 layers only) */
     const float* w13_scales;   /* FP8: tile scales of w13 [E][2*Ip/128][ceil(H/128)] (moe_quantize_weights_fp8) */
     const float* w2_scales;    /* FP8: tile scales of w2 [E][H/128][ceil(I/128)] */
     const float* w13_shared_scales; /* FP8: [1][2*Ips/128][ceil(H/128)], Ips = S*I rounded up to 128 */
@@ -329,6 +352,10 @@ typedef struct moe_layer_desc {
  * all outputs stay bf16.  Requires dtype MOE_BF16, H % 256 == 0, I % 16 == 0. */
 #define MOE_WEIGHTS_NATIVE 0
 #define MOE_WEIGHTS_FP8 1
+/* As MOE_WEIGHTS_FP8 with power-of-two scales everywhere (weights quantised
+ * with moe_quantize_weights_fp8_pow2; x and h quantised on the fly the same
+ * way), so the expert GEMMs run as block-scaled tensor-core MMAs. */
+#define MOE_WEIGHTS_FP8_POW2 2
 
 /* Layer steps timed by moe_layer_forward_timed.  "shared" (both projections of
  * the shared experts) runs on a second stream of the library's, forked when

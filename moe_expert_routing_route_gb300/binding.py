@@ -25,7 +25,8 @@ WS_FIELDS = ["logits", "topk_ids", "topk_w", "tokens_per_expert", "expert_offset
              "expanded_x", "h_routed", "h_shared", "y_routed", "y_shared", "x_in", "out", "xq", "xq_scales",
              "expanded_xq", "expanded_xq_scales", "hq", "hq_scales", "hq_shared", "hq_shared_scales"]
 WS_FIELDS_EP = ["x_sorted", "gathered_ids_unsort", "recv_start", "expert_offsets"]
-MOE_WEIGHTS_NATIVE, MOE_WEIGHTS_FP8 = 0, 1
+MOE_WEIGHTS_NATIVE, MOE_WEIGHTS_FP8, MOE_WEIGHTS_FP8_POW2 = 0, 1, 2
+WEIGHT_FORMATS = {"native": MOE_WEIGHTS_NATIVE, "fp8": MOE_WEIGHTS_FP8, "fp8_pow2": MOE_WEIGHTS_FP8_POW2}
 
 # The exported entry points (name -> (restype, argtypes)).
 P, I32, I64, SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t
@@ -65,8 +66,11 @@ SIGNATURES = {
     "moe_layer_workspace_field_ep": (I32, [_DP, I32, I32, ctypes.POINTER(SZ), ctypes.POINTER(SZ)]),
     "moe_quantize_rows_fp8": (I32, [P, I32, I64, I32, P, P, I32, P]),
     "moe_quantize_weights_fp8": (I32, [P, I32, I32, I32, I32, P, P, P]),
+    "moe_quantize_rows_fp8_pow2": (I32, [P, I32, I64, I32, P, P, I32, P]),
+    "moe_quantize_weights_fp8_pow2": (I32, [P, I32, I32, I32, I32, P, P, P]),
     "moe_grouped_ffn_fp8_workspace_bytes": (SZ, [I32, I32]),
     "moe_grouped_ffn_fp8": (I32, [P, P, I32, P, I32, I32, I32, I32, P, P, P, P, P, P, SZ, P]),
+    "moe_grouped_ffn_fp8_pow2": (I32, [P, P, I32, P, I32, I32, I32, I32, P, P, P, P, P, P, SZ, P]),
     "moe_stage_name": (ctypes.c_char_p, [I32]),
     "moe_layer_workspace_bytes": (SZ, [_DP]),
     "moe_layer_workspace_field": (I32, [_DP, I32, ctypes.POINTER(SZ), ctypes.POINTER(SZ)]),
@@ -278,35 +282,40 @@ def scale_ld(cols: int) -> int:
     return -(-(-(-cols // 128)) // 4) * 4
 
 
-def moe_quantize_rows_fp8(a: torch.Tensor, ld_scales: int | None = None, stream=None):
+def moe_quantize_rows_fp8(a: torch.Tensor, ld_scales: int | None = None, stream=None, pow2: bool = False):
+    """1x128 blocks; pow2 selects the power-of-two scale format (moe_quantize_rows_fp8_pow2)."""
     rows, cols = a.shape
     ld = ld_scales or -(-cols // 128)
     codes = torch.empty((rows, cols), dtype=torch.uint8, device=a.device)
     scales = torch.empty((rows, ld), dtype=torch.float32, device=a.device)
-    _check(lib().moe_quantize_rows_fp8(_ptr(a), _dt(a), rows, cols, _ptr(codes), _ptr(scales), ld, _stream(stream)),
-           "moe_quantize_rows_fp8")
+    name = "moe_quantize_rows_fp8_pow2" if pow2 else "moe_quantize_rows_fp8"
+    _check(getattr(lib(), name)(_ptr(a), _dt(a), rows, cols, _ptr(codes), _ptr(scales), ld, _stream(stream)), name)
     return codes, scales
 
 
-def moe_quantize_weights_fp8(w: torch.Tensor, stream=None):
-    """w [G, n_out, k_in] (or [n_out, k_in]) -> (codes, scales [G, n/128, k/128])."""
+def moe_quantize_weights_fp8(w: torch.Tensor, stream=None, pow2: bool = False):
+    """w [G, n_out, k_in] (or [n_out, k_in]) -> (codes, scales [G, n/128, k/128]); pow2 as above."""
     if w.dim() == 2:
         w = w.unsqueeze(0)
     G, n, k = w.shape
     codes = torch.empty((G, n, k), dtype=torch.uint8, device=w.device)
     scales = torch.empty((G, -(-n // 128), -(-k // 128)), dtype=torch.float32, device=w.device)
-    _check(lib().moe_quantize_weights_fp8(_ptr(w.contiguous()), _dt(w), G, n, k, _ptr(codes), _ptr(scales),
-                                          _stream(stream)), "moe_quantize_weights_fp8")
+    name = "moe_quantize_weights_fp8_pow2" if pow2 else "moe_quantize_weights_fp8"
+    _check(getattr(lib(), name)(_ptr(w.contiguous()), _dt(w), G, n, k, _ptr(codes), _ptr(scales), _stream(stream)),
+           name)
     return codes, scales
 
 
-def moe_grouped_ffn_fp8(aq, a_scales, expert_offsets, E: int, I: int, w13q, w13s, w2q, w2s, stream=None):
+def moe_grouped_ffn_fp8(aq, a_scales, expert_offsets, E: int, I: int, w13q, w13s, w2q, w2s, stream=None,
+                        pow2: bool = False):
+    """pow2: every scale a power of two, products on block-scaled MMAs (moe_grouped_ffn_fp8_pow2)."""
     rows, H = aq.shape
     ws = torch.empty(lib().moe_grouped_ffn_fp8_workspace_bytes(rows, I), dtype=torch.uint8, device=aq.device)
     y = torch.zeros((rows, H), dtype=torch.bfloat16, device=aq.device)
-    _check(lib().moe_grouped_ffn_fp8(_ptr(aq), _ptr(a_scales), a_scales.shape[1], _ptr(expert_offsets), E, rows, H, I,
-                                     _ptr(w13q), _ptr(w13s), _ptr(w2q), _ptr(w2s), _ptr(y), _ptr(ws), ws.numel(),
-                                     _stream(stream)), "moe_grouped_ffn_fp8")
+    name = "moe_grouped_ffn_fp8_pow2" if pow2 else "moe_grouped_ffn_fp8"
+    _check(getattr(lib(), name)(_ptr(aq), _ptr(a_scales), a_scales.shape[1], _ptr(expert_offsets), E, rows, H, I,
+                                _ptr(w13q), _ptr(w13s), _ptr(w2q), _ptr(w2s), _ptr(y), _ptr(ws), ws.numel(),
+                                _stream(stream)), name)
     return y, ws
 
 
@@ -341,24 +350,25 @@ class MoELayer:
         self.expert_bias = None if expert_bias is None else expert_bias.to(torch.float32).contiguous()
         self.weight_format = weight_format
         scales = [None] * 4
-        if weight_format == "fp8":
+        if weight_format not in WEIGHT_FORMATS:
+            raise ValueError(f"weight_format must be one of {sorted(WEIGHT_FORMATS)}, got {weight_format!r}")
+        if weight_format != "native":
             # static 128x128-tile quantisation of the packed gate/up and the down weights
-            self.w13, s13 = moe_quantize_weights_fp8(self.w13, stream)
-            self.w2, s2_ = moe_quantize_weights_fp8(self.w2, stream)
+            p2 = weight_format == "fp8_pow2"
+            self.w13, s13 = moe_quantize_weights_fp8(self.w13, stream, pow2=p2)
+            self.w2, s2_ = moe_quantize_weights_fp8(self.w2, stream, pow2=p2)
             scales[0], scales[1] = s13, s2_
             if S:
-                self.w13_shared, ss13 = moe_quantize_weights_fp8(self.w13_shared, stream)
-                self.w2_shared, ss2 = moe_quantize_weights_fp8(self.w2_shared, stream)
+                self.w13_shared, ss13 = moe_quantize_weights_fp8(self.w13_shared, stream, pow2=p2)
+                self.w2_shared, ss2 = moe_quantize_weights_fp8(self.w2_shared, stream, pow2=p2)
                 scales[2], scales[3] = ss13, ss2
-        elif weight_format != "native":
-            raise ValueError(f"weight_format must be 'native' or 'fp8', got {weight_format!r}")
         self.scales = scales
         sp = [0 if t is None else t.data_ptr() for t in scales]
         self.desc = LayerDesc(T, H, E, k, I, S, _dt(w_gate), int(bool(renormalize)), self.w_router.data_ptr(),
                               0 if self.expert_bias is None else self.expert_bias.data_ptr(), self.w13.data_ptr(),
                               self.w2.data_ptr(), 0 if S == 0 else self.w13_shared.data_ptr(),
                               0 if S == 0 else self.w2_shared.data_ptr(), n_group, topk_group,
-                              GROUP_RULES[group_rule], MOE_WEIGHTS_FP8 if weight_format == "fp8" else 0, *sp)
+                              GROUP_RULES[group_rule], WEIGHT_FORMATS[weight_format], *sp)
         nbytes = lib().moe_layer_workspace_bytes(ctypes.byref(self.desc))
         if nbytes == 0:
             raise MoEError(MOE_ERR_INVALID_ARG, "moe_layer_workspace_bytes")

@@ -24,6 +24,25 @@
 // Rows of a tile past the expert's segment are
 // computed and never stored, as in the bf16 kernel.  Waits are bounded as in
 // the bf16 kernel (about one second, then abort without trapping).
+//
+// With power-of-two scales (the MX instantiation) the tensor cores apply the
+// scales themselves: kind::mxf8f6f4 block-scaled MMAs take one UE8M0 exponent
+// per 32 K elements for every row of A and every column of B, read from TMEM,
+// and accumulate the whole tile in one TMEM accumulator, so nothing is promoted
+// on CUDA cores.  A 128-element scale block covers four MMAs, so each 32-bit
+// TMEM word holds the exponents of four consecutive K blocks and the
+// instruction's scale-factor ids pick the byte.  Layout (the tensor cores read
+// the A exponent of row m at lane m, column sfa + m/32, and the B exponent of
+// column n at lane n%32 of the reading row's lane group, column sfb + n/32):
+// per group of 16 K blocks there are four slots (one per four K blocks), each
+// starting on an 8-column boundary: the A exponents of slot s at columns
+// [8s, 8s+8) (a row's word repeated over them, so lane group w finds it at
+// column 8s + w) and the B exponents at [32+8s, 40+8s) (the same eight words in
+// all four lane groups).  Two such groups alternate; the first epilogue warp of
+// each lane group writes them from the scale arrays while the MMAs run, and
+// hands each over through an mbarrier.  The tile's accumulator is drained into
+// registers once, at the end of the tile, after which the MMAs of the next tile
+// start while the epilogue finishes this one.
 #include "fp8_codec.cuh"
 #include "tc_ptx.cuh"
 
@@ -47,7 +66,10 @@ constexpr int kMaxGroups = 1024;
 constexpr int A_BYTES = BM * BK;
 constexpr int B_BYTES = BN * BK;
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-constexpr int TMEM_COLS = 2 * BN;  // two partial buffers
+constexpr int TMEM_COLS = 2 * BN;  // two partial buffers (MX: the accumulator and the scale factors)
+constexpr int kSfGroup = 16;       // MX: K blocks per scale-factor group (4 per 32-bit TMEM word)
+constexpr int kSfCols = 64;        // MX: TMEM columns of one group: A slots at +8s, B slots at +32+8s (s < 4)
+constexpr int kSfBase = BN;        // MX: the two groups at columns 256 and 320
 constexpr int XAMAX_FLOATS = 2 * kSplit * BM;  // [tile parity][column part][row]
 constexpr int kOutBox = 32 * kCols * 2;        // one warp's 32 rows x kCols bf16 columns (128-byte rows)
 static_assert(kCols * 2 == 128, "a staged output row is one 128-byte swizzle row");
@@ -61,7 +83,8 @@ template <int EPI>
 struct Plan {
     static constexpr int STAGES = EPI == TC_EPI_BF16 ? 3 : 4;
     static constexpr int OUT_BYTES = EPI == TC_EPI_BF16 ? kEpiWarps * 2 * kOutBox : 0;
-    static constexpr int NUM_BARS = 2 * STAGES + 9;  // full, empty, partial full/empty, drain, 4 amax exchanges
+    // full, empty, partial (MX: accumulator) full/empty, drain, 4 amax exchanges, MX scale groups full/empty
+    static constexpr int NUM_BARS = 2 * STAGES + 13;
     static constexpr size_t SMEM = 1024 + (size_t)STAGES * STAGE_BYTES + OUT_BYTES + NUM_BARS * 8 + 16 +
                                    (size_t)(3 * kMaxGroups + 1) * 4 + (size_t)XAMAX_FLOATS * 4;
 };
@@ -153,11 +176,19 @@ __device__ __forceinline__ void stage_row_sw128(uint8_t* box, int r, const float
     }
 }
 
-template <int EPI>
+// Four exponent bytes (UE8M0) of the power-of-two scales v[kb0 .. kb0+3] (127 past kb_end).
+__device__ __forceinline__ uint32_t pack_exponents(const float* v, int kb0, int kb_end) {
+    uint32_t w = 0;
+#pragma unroll
+    for (int b = 0; b < 4; ++b) w |= (kb0 + b < kb_end ? fp8::ue8m0(__ldg(v + kb0 + b)) : 127u) << (8 * b);
+    return w;
+}
+
+template <int EPI, bool MX>
 __global__ void __launch_bounds__(kThreads, 1)
 tc_fp8_grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
                            const __grid_constant__ CUtensorMap mapC, const __grid_constant__ Params p) {
-    constexpr uint32_t IDESC = idesc_e4m3(BM, BN);
+    constexpr uint32_t IDESC = MX ? idesc_mx_e4m3(BM, BN) : idesc_e4m3(BM, BN);
     constexpr int STAGES = Plan<EPI>::STAGES;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_u32(smem_raw);
@@ -179,6 +210,8 @@ tc_fp8_grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __gri
     auto pempty_bar = [&](int j) { return smem_u32(bars + 2 * STAGES + 2 + j); };
     const uint32_t drain_bar = smem_u32(bars + 2 * STAGES + 4);
     auto xchg_bar = [&](int eg) { return smem_u32(bars + 2 * STAGES + 5 + eg); };
+    auto sffull_bar = [&](int q) { return smem_u32(bars + 2 * STAGES + 9 + q); };    // MX
+    auto sfempty_bar = [&](int q) { return smem_u32(bars + 2 * STAGES + 11 + q); };  // MX
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int G = p.G, NT = p.NT, KB = p.KB;
@@ -224,6 +257,10 @@ tc_fp8_grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __gri
             }
             mbar_init(drain_bar, 1);
             for (int eg = 0; eg < 4; ++eg) mbar_init(xchg_bar(eg), kSplit);  // the warps of a lane group
+            for (int q = 0; q < 2; ++q) {
+                mbar_init(sffull_bar(q), 4);  // the scale writer of each lane group
+                mbar_init(sfempty_bar(q), 1);
+            }
             asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             prefetch_tensormap(&mapA);
@@ -267,6 +304,58 @@ tc_fp8_grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __gri
             }
             for (int q = 0; q < STAGES; ++q)
                 if ((issued >> q) & 1u) wait_drain(full_bar(q), (issued_par >> q) & 1u, p.status);
+        }
+    } else if (warp == 1 && MX) {
+        if (lane == 0) {
+            // ---------------- MMA issuer, block-scaled: one accumulator per tile ----------------
+            int s = 0, sq = 0;
+            uint32_t ph = 0, dph = 0, sph = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
+                // the epilogue has drained the previous tile's accumulator
+                if (!wait_phase_fast(pempty_bar(0), dph ^ 1u, abort_flag, p.status)) break;
+                tc_fence_after();
+                for (int kb = 0; kb < KB; ++kb) {
+                    if ((kb % kSfGroup) == 0) {
+                        if (!wait_phase_fast(sffull_bar(sq), sph, abort_flag, p.status)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                    }
+                    if (!wait_phase_fast(full_bar(s), ph, abort_flag, p.status)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sf = tmem_base + (uint32_t)(kSfBase + sq * kSfCols);
+                    const uint32_t slot = (uint32_t)((kb % kSfGroup) >> 2), id = (uint32_t)(kb & 3);
+                    const uint32_t idesc = IDESC | idesc_sf_ids(id, id);
+                    const uint64_t adesc = smem_desc_sw128(smem_u32(sA + s * A_BYTES));
+                    const uint64_t bdesc = smem_desc_sw128(smem_u32(sB + s * B_BYTES));
+#pragma unroll
+                    for (int kk = 0; kk < BK / UMMA_K; ++kk)
+                        mma_mx_e4m3(tmem_base, adesc + 2u * kk, bdesc + 2u * kk, idesc, sf + 8u * slot,
+                                    sf + 32u + 8u * slot, (kb | kk) != 0);
+                    mma_commit(empty_bar(s));
+                    if ((kb % kSfGroup) == kSfGroup - 1 || kb == KB - 1) {
+                        mma_commit(sfempty_bar(sq));
+                        if (++sq == 2) {
+                            sq = 0;
+                            sph ^= 1u;
+                        }
+                    }
+                    if (++s == STAGES) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                mma_commit(pfull_bar(0));  // the tile's accumulator is complete
+                dph ^= 1u;
+            }
+            mma_commit(drain_bar);
+            wait_drain(drain_bar, 0, p.status);
         }
     } else if (warp == 1) {
         if (lane == 0) {
@@ -319,6 +408,47 @@ tc_fp8_grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __gri
         uint32_t pph = 0, xph = 0;
         float acc[2 * kCols];
         bool ok = true;
+        // MX: the first warp of each lane group writes the scale-factor groups, in
+        // the order the MMAs consume them (two buffers)
+        int wq = 0;
+        uint32_t wph = 0, dph = 0;
+        const int n_sf_groups = (KB + kSfGroup - 1) / kSfGroup;
+        auto write_sf_group = [&](int tile, int grp) -> bool {
+            if (!__all_sync(0xffffffffu, wait_phase_fast(sfempty_bar(wq), wph ^ 1u, abort_flag, p.status)))
+                return false;
+            int g, m, n;
+            decode_tile(tile, prefix, G, NT, g, m, n);
+            const int64_t row = (int64_t)gstart[g] + (int64_t)m * BM + r;
+            const int64_t srow = row < p.M ? row : p.M - 1;
+            const float* sa_row = p.a_scales + srow * p.lda_s;
+            const float* sb0 = p.b_scales + ((int64_t)g * nblocks + n * 2) * KB;  // columns 0..127 of the tile
+            const float* sb1 = sb0 + KB;                                          // columns 128..255
+            const int kb0 = grp * kSfGroup;
+            uint32_t aw[32], bw[32];
+#pragma unroll
+            for (int sl = 0; sl < 4; ++sl) {
+                const uint32_t a = pack_exponents(sa_row, kb0 + 4 * sl, KB);
+                const uint32_t w0 = pack_exponents(sb0, kb0 + 4 * sl, KB), w1 = pack_exponents(sb1, kb0 + 4 * sl, KB);
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    aw[8 * sl + c] = a;  // lane group eg reads column 8*slot + eg
+                    bw[8 * sl + c] = c < 4 ? w0 : w1;
+                }
+            }
+            const uint32_t t = tmem_base + ((uint32_t)(eg * 32) << 16) + (uint32_t)(kSfBase + wq * kSfCols);
+            tmem_st32(t, aw);        // A slots: columns [0, 32) of the group
+            tmem_st32(t + 32u, bw);  // B slots: columns [32, 64), in every lane group
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(sffull_bar(wq));
+            if (++wq == 2) {
+                wq = 0;
+                wph ^= 1u;
+            }
+            return true;
+        };
+        if (MX && part == 0 && (int)blockIdx.x < total) ok = write_sf_group(blockIdx.x, 0);
         for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
             int g, m, n;
             decode_tile(tile, prefix, G, NT, g, m, n);
@@ -328,6 +458,34 @@ tc_fp8_grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __gri
             const float* sa_row = p.a_scales + srow * p.lda_s;
             const float* sbA = p.b_scales + ((int64_t)g * nblocks + n * 2 + nbA) * KB;
             const float* sbB = p.b_scales + ((int64_t)g * nblocks + n * 2 + nbB) * KB;
+            if constexpr (MX) {
+                // the rest of this tile's scale groups and the next tile's first, then the accumulator
+                if (part == 0) {
+                    for (int grp = 1; ok && grp < n_sf_groups; ++grp) ok = write_sf_group(tile, grp);
+                    if (ok && tile + (int)gridDim.x < total) ok = write_sf_group(tile + gridDim.x, 0);
+                }
+                if (!ok) break;
+                if (!__all_sync(0xffffffffu, wait_phase_fast(pfull_bar(0), dph, abort_flag, p.status))) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t taddr = tmem_base + ((uint32_t)(eg * 32) << 16);
+#pragma unroll
+                for (int q = 0; q < kCols / 16; ++q) {
+                    uint32_t va[16], vb[16];
+                    tmem_ld16x2(taddr + colA + 16 * q, taddr + colB + 16 * q, va, vb);
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        acc[16 * q + i] = __uint_as_float(va[i]);
+                        acc[kCols + 16 * q + i] = __uint_as_float(vb[i]);
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(pempty_bar(0));  // the next tile's MMAs may overwrite it
+                dph ^= 1u;
+            } else {
 #pragma unroll
             for (int i = 0; i < 2 * kCols; ++i) acc[i] = 0.0f;
             float sa_next = __ldg(sa_row), sbA_next = __ldg(sbA), sbB_next = __ldg(sbB);
@@ -363,6 +521,7 @@ tc_fp8_grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __gri
                 }
             }
             if (!ok) break;
+            }
             __nv_bfloat16* C = static_cast<__nv_bfloat16*>(p.C);
             if (EPI == TC_EPI_SWIGLU) {
                 // h in bf16 (the precision it is stored and quantised in)
@@ -386,7 +545,7 @@ tc_fp8_grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __gri
                     xph ^= 1u;
 #pragma unroll
                     for (int o = 0; o < kSplit; ++o) am = fmaxf(am, slot[o * BM + r]);
-                    const float sc = fp8::block_scale(am);
+                    const float sc = fp8::scale_for(am, MX);
                     if (valid) {
                         uint8_t* qrow = p.q + row * (int64_t)p.N + col0;
 #pragma unroll
@@ -441,15 +600,15 @@ tc_fp8_grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __gri
     }
 }
 
-template <int EPI>
+template <int EPI, bool MX>
 moe_status_t launch_impl(const TcFp8GroupedGemm& g, cudaStream_t s) {
     static std::once_flag attr_once[64];
     int dev = 0;
     MOE_CUDA_TRY(cudaGetDevice(&dev));
     cudaError_t attr_err = cudaSuccess;
     std::call_once(attr_once[dev & 63], [&] {
-        attr_err = cudaFuncSetAttribute(tc_fp8_grouped_gemm_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        (int)Plan<EPI>::SMEM);
+        attr_err = cudaFuncSetAttribute(tc_fp8_grouped_gemm_kernel<EPI, MX>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Plan<EPI>::SMEM);
     });
     MOE_CUDA_TRY(attr_err);
     CUtensorMap ma, mb, mc;
@@ -480,7 +639,7 @@ moe_status_t launch_impl(const TcFp8GroupedGemm& g, cudaStream_t s) {
     p.status = g.status;
     const int64_t max_tiles = (int64_t)p.NT * (ceil_div(g.M, BM) + (g.offsets ? g.G : 0));
     const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(sm_count(), max_tiles));
-    tc_fp8_grouped_gemm_kernel<EPI><<<grid, kThreads, Plan<EPI>::SMEM, s>>>(ma, mb, mc, p);
+    tc_fp8_grouped_gemm_kernel<EPI, MX><<<grid, kThreads, Plan<EPI>::SMEM, s>>>(ma, mb, mc, p);
     note_launch();
     return last_launch_status();
 }
@@ -495,8 +654,9 @@ moe_status_t launch_tc_fp8_grouped_gemm(const TcFp8GroupedGemm& g, cudaStream_t 
         return MOE_ERR_INVALID_ARG;
     if (!g.q && !g.C) return MOE_ERR_INVALID_ARG;
     switch (g.epi) {
-        case TC_EPI_SWIGLU: return launch_impl<TC_EPI_SWIGLU>(g, s);
-        case TC_EPI_BF16: return launch_impl<TC_EPI_BF16>(g, s);
+        case TC_EPI_SWIGLU:
+            return g.pow2 ? launch_impl<TC_EPI_SWIGLU, true>(g, s) : launch_impl<TC_EPI_SWIGLU, false>(g, s);
+        case TC_EPI_BF16: return g.pow2 ? launch_impl<TC_EPI_BF16, true>(g, s) : launch_impl<TC_EPI_BF16, false>(g, s);
         default: return MOE_ERR_INVALID_ARG;
     }
 }

@@ -75,21 +75,23 @@ moe_status_t ffn_down(const void* h, moe_dtype_t dt, const int32_t* offsets, int
 // multiple of 4 floats so they can be permuted as 16-byte vectors.
 int scale_ld(int cols) { return (int)round_up((size_t)ceil_div(cols, 128), 4); }
 
+// pow2: power-of-two scales throughout (block-scaled tensor-core MMAs).
 moe_status_t ffn_up_fp8(const uint8_t* aq, const float* as, int lda_s, const int32_t* offsets, int G, int rows, int H,
                         int I, const void* w13q, const float* w13s, void* h, uint8_t* hq, float* hs,
-                        uint32_t* status, cudaStream_t s) {
+                        uint32_t* status, cudaStream_t s, bool pow2) {
     if (rows == 0) return MOE_OK;
     // the SwiGLU epilogue writes the down projection's FP8 input directly; bf16 h
     // is stored too only when the caller gives a buffer for it (h may be null)
     TcFp8GroupedGemm up{aq, rows, H, offsets, G, w13q, packed_rows(I), I, h, I, TC_EPI_SWIGLU, as, lda_s,
-                        w13s, status, hq, hs, scale_ld(I)};
+                        w13s, status, hq, hs, scale_ld(I), pow2};
     return launch_tc_fp8_grouped_gemm(up, s);
 }
 
 moe_status_t ffn_down_fp8(const uint8_t* hq, const float* hs, const int32_t* offsets, int G, int rows, int H, int I,
-                          const void* w2q, const float* w2s, void* y, uint32_t* status, cudaStream_t s) {
+                          const void* w2q, const float* w2s, void* y, uint32_t* status, cudaStream_t s, bool pow2) {
     if (rows == 0) return MOE_OK;
-    TcFp8GroupedGemm down{hq, rows, I, offsets, G, w2q, H, H, y, H, TC_EPI_BF16, hs, scale_ld(I), w2s, status};
+    TcFp8GroupedGemm down{hq, rows, I, offsets, G, w2q, H, H, y, H, TC_EPI_BF16, hs, scale_ld(I), w2s, status,
+                          nullptr, nullptr, 0, pow2};
     return launch_tc_fp8_grouped_gemm(down, s);
 }
 
@@ -151,7 +153,7 @@ Layout layout(const moe_layer_desc& d) {
     L.bytes[MOE_WS_Y_SHARED] = T * H * b;
     L.bytes[MOE_WS_X_IN] = T * H * b;
     L.bytes[MOE_WS_OUT] = T * H * b;
-    if (d.weight_format == MOE_WEIGHTS_FP8) {
+    if (d.weight_format == MOE_WEIGHTS_FP8 || d.weight_format == MOE_WEIGHTS_FP8_POW2) {
         const size_t SI = S * I;
         L.bytes[MOE_WS_XQ] = T * H;
         L.bytes[MOE_WS_XQ_SCALES] = T * scale_ld(d.H) * 4;
@@ -193,8 +195,10 @@ moe_status_t check_desc(const moe_layer_desc* d) {
     if (!d->w_router || !d->w13 || !d->w2) return MOE_ERR_INVALID_ARG;
     if (d->S > 0 && (!d->w13_shared || !d->w2_shared)) return MOE_ERR_INVALID_ARG;
     if ((int64_t)d->S * d->I >= INT_MAX / 2) return MOE_ERR_INVALID_ARG;
-    if (d->weight_format != MOE_WEIGHTS_NATIVE && d->weight_format != MOE_WEIGHTS_FP8) return MOE_ERR_INVALID_ARG;
-    if (d->weight_format == MOE_WEIGHTS_FP8) {
+    if (d->weight_format != MOE_WEIGHTS_NATIVE && d->weight_format != MOE_WEIGHTS_FP8 &&
+        d->weight_format != MOE_WEIGHTS_FP8_POW2)
+        return MOE_ERR_INVALID_ARG;
+    if (d->weight_format != MOE_WEIGHTS_NATIVE) {
         if (d->dtype != MOE_BF16 || d->H % 256 != 0 || d->I % 16 != 0) return MOE_ERR_UNSUPPORTED;
         if (!d->w13_scales || !d->w2_scales) return MOE_ERR_INVALID_ARG;
         if (d->S > 0 && (!d->w13_shared_scales || !d->w2_shared_scales)) return MOE_ERR_INVALID_ARG;
@@ -325,7 +329,8 @@ moe_status_t layer_forward(const moe_layer_desc* d, const void* x, void* out, vo
     void* ys = at<void>(ws, L.off[MOE_WS_Y_SHARED]);
     int32_t* scratch = at<int32_t>(ws, L.scratch_off);
 
-    const bool fp8 = d->weight_format == MOE_WEIGHTS_FP8;
+    const bool fp8 = d->weight_format == MOE_WEIGHTS_FP8 || d->weight_format == MOE_WEIGHTS_FP8_POW2;
+    const bool pow2 = d->weight_format == MOE_WEIGHTS_FP8_POW2;
     uint8_t* xq = at<uint8_t>(ws, L.off[MOE_WS_XQ]);
     float* xs = at<float>(ws, L.off[MOE_WS_XQ_SCALES]);
     uint8_t* exq = at<uint8_t>(ws, L.off[MOE_WS_EXPANDED_XQ]);
@@ -379,7 +384,7 @@ moe_status_t layer_forward(const moe_layer_desc* d, const void* x, void* out, vo
         MOE_CUDA_TRY(cudaStreamWaitEvent(s, hp->in[io_chunks - 1], 0));  // the gate reads all of x
     }
     MOE_TRY(mark(ev, ST_GATE, 0, s));
-    if (fp8) MOE_TRY(launch_quantize_rows_fp8(x, dt, T, H, xq, xs, ldx, s));  // activations, 1x128 blocks
+    if (fp8) MOE_TRY(launch_quantize_rows_fp8(x, dt, T, H, xq, xs, ldx, s, pow2));  // activations, 1x128 blocks
     // fork: the shared experts need x alone (FP8: its codes), so they branch off
     // before the gate; the gate is enqueued first and starts first
     const bool fork = side && !chunked_shared;
@@ -396,8 +401,9 @@ moe_status_t layer_forward(const moe_layer_desc* d, const void* x, void* out, vo
         MOE_TRY(mark(ev, ST_SHARED, 0, ss));
         if (fp8) {
             MOE_TRY(ffn_up_fp8(xq, xs, ldx, nullptr, 1, T, H, SI, d->w13_shared, d->w13_shared_scales, nullptr, hsq, hss,
-                               status, ss));
-            MOE_TRY(ffn_down_fp8(hsq, hss, nullptr, 1, T, H, SI, d->w2_shared, d->w2_shared_scales, ys, status, ss));
+                               status, ss, pow2));
+            MOE_TRY(ffn_down_fp8(hsq, hss, nullptr, 1, T, H, SI, d->w2_shared, d->w2_shared_scales, ys, status, ss,
+                                 pow2));
         } else {
             // the routing kernels (histogram and scatter use shared memory) run beside them
             MOE_TRY(ffn_up(x, dt, nullptr, 1, T, H, SI, d->w13_shared, hs, status, ss, true));
@@ -427,11 +433,12 @@ moe_status_t layer_forward(const moe_layer_desc* d, const void* x, void* out, vo
     // join: the routed GEMMs need every SM, so they start after the shared experts
     if (side) MOE_CUDA_TRY(cudaStreamWaitEvent(s, side->join, 0));
     MOE_TRY(mark(ev, ST_UP, 0, s));
-    if (fp8) MOE_TRY(ffn_up_fp8(exq, exs, ldx, offsets, E, R, H, I, d->w13, d->w13_scales, nullptr, hq, hqs, status, s));
+    if (fp8)
+        MOE_TRY(ffn_up_fp8(exq, exs, ldx, offsets, E, R, H, I, d->w13, d->w13_scales, nullptr, hq, hqs, status, s, pow2));
     else MOE_TRY(ffn_up(ex, dt, offsets, E, R, H, I, d->w13, h, status, s));
     MOE_TRY(mark(ev, ST_UP, 1, s));
     MOE_TRY(mark(ev, ST_DOWN, 0, s));
-    if (fp8) MOE_TRY(ffn_down_fp8(hq, hqs, offsets, E, R, H, I, d->w2, d->w2_scales, y, status, s));
+    if (fp8) MOE_TRY(ffn_down_fp8(hq, hqs, offsets, E, R, H, I, d->w2, d->w2_scales, y, status, s, pow2));
     else MOE_TRY(ffn_down(h, dt, offsets, E, R, H, I, d->w2, y, status, s));
     MOE_TRY(mark(ev, ST_DOWN, 1, s));
     MOE_TRY(mark(ev, ST_FINALIZE, 0, s));
@@ -569,6 +576,49 @@ int sm_count() {
 
 }  // namespace moe
 
+namespace moe {
+namespace {
+
+moe_status_t quantize_rows(const void* a, moe_dtype_t dt, int64_t rows, int cols, uint8_t* codes, float* scales,
+                           int ld_scales, moe_stream_t stream, bool pow2) {
+    if (bad_dtype(dt) || rows < 0 || cols <= 0 || ld_scales < (cols + 127) / 128) return MOE_ERR_INVALID_ARG;
+    if (rows == 0) return MOE_OK;
+    if (!a || !codes || !scales) return MOE_ERR_INVALID_ARG;
+    return launch_quantize_rows_fp8(a, dt, rows, cols, codes, scales, ld_scales, reinterpret_cast<cudaStream_t>(stream),
+                                    pow2);
+}
+
+moe_status_t quantize_weights(const void* w, moe_dtype_t dt, int G, int n_out, int k_in, uint8_t* codes,
+                              float* scales, moe_stream_t stream, bool pow2) {
+    if (bad_dtype(dt) || G <= 0 || n_out <= 0 || k_in <= 0) return MOE_ERR_INVALID_ARG;
+    if (!w || !codes || !scales) return MOE_ERR_INVALID_ARG;
+    return launch_quantize_tiles_fp8(w, dt, G, n_out, k_in, codes, scales, reinterpret_cast<cudaStream_t>(stream),
+                                     pow2);
+}
+moe_status_t grouped_ffn_fp8(const uint8_t* aq, const float* a_scales, int lda_scales, const int32_t* expert_offsets,
+                             int E, int rows, int H, int I, const uint8_t* w13q, const float* w13s, const uint8_t* w2q,
+                             const float* w2s, void* y, void* ws, size_t ws_bytes, moe_stream_t stream, bool pow2) {
+    if (rows < 0 || H <= 0 || I <= 0 || E <= 0 || E > 1024 || lda_scales < (H + 127) / 128) return MOE_ERR_INVALID_ARG;
+    if (!expert_offsets && E != 1) return MOE_ERR_INVALID_ARG;
+    if (H % 256 != 0 || I % 16 != 0) return MOE_ERR_UNSUPPORTED;
+    if (!ws || ws_bytes < moe_grouped_ffn_fp8_workspace_bytes(rows, I)) return MOE_ERR_INVALID_ARG;
+    if (rows > 0 && (!aq || !a_scales || !w13q || !w13s || !w2q || !w2s || !y)) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(aq) || !aligned16(w13q) || !aligned16(w2q) || !aligned16(y) || !aligned16(ws))
+        return MOE_ERR_UNSUPPORTED;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    MOE_TRY(clear_status(ws, s));
+    void* h = at<void>(ws, MOE_WS_HEADER_BYTES);
+    uint8_t* hq = at<uint8_t>(ws, MOE_WS_HEADER_BYTES + round_up((size_t)rows * I * 2, kAlign));
+    float* hs = at<float>(ws, MOE_WS_HEADER_BYTES + round_up((size_t)rows * I * 2, kAlign) +
+                                  round_up((size_t)rows * I, kAlign));
+    MOE_TRY(ffn_up_fp8(aq, a_scales, lda_scales, expert_offsets, E, rows, H, I, w13q, w13s, h, hq, hs, status_word(ws),
+                       s, pow2));
+    return ffn_down_fp8(hq, hs, expert_offsets, E, rows, H, I, w2q, w2s, y, status_word(ws), s, pow2);
+}
+
+}  // namespace
+}  // namespace moe
+
 using namespace moe;
 
 extern "C" {
@@ -665,19 +715,25 @@ moe_status_t moe_unsort_rows(const void* y_sorted, moe_dtype_t dt, const int32_t
                               ws ? status_word(ws) : nullptr, s);
 }
 
+
 moe_status_t moe_quantize_rows_fp8(const void* a, moe_dtype_t dt, int64_t rows, int cols, uint8_t* codes,
                                    float* scales, int ld_scales, moe_stream_t stream) {
-    if (bad_dtype(dt) || rows < 0 || cols <= 0 || ld_scales < (cols + 127) / 128) return MOE_ERR_INVALID_ARG;
-    if (rows == 0) return MOE_OK;
-    if (!a || !codes || !scales) return MOE_ERR_INVALID_ARG;
-    return launch_quantize_rows_fp8(a, dt, rows, cols, codes, scales, ld_scales, reinterpret_cast<cudaStream_t>(stream));
+    return quantize_rows(a, dt, rows, cols, codes, scales, ld_scales, stream, false);
+}
+
+moe_status_t moe_quantize_rows_fp8_pow2(const void* a, moe_dtype_t dt, int64_t rows, int cols, uint8_t* codes,
+                                        float* scales, int ld_scales, moe_stream_t stream) {
+    return quantize_rows(a, dt, rows, cols, codes, scales, ld_scales, stream, true);
 }
 
 moe_status_t moe_quantize_weights_fp8(const void* w, moe_dtype_t dt, int G, int n_out, int k_in, uint8_t* codes,
                                       float* scales, moe_stream_t stream) {
-    if (bad_dtype(dt) || G <= 0 || n_out <= 0 || k_in <= 0) return MOE_ERR_INVALID_ARG;
-    if (!w || !codes || !scales) return MOE_ERR_INVALID_ARG;
-    return launch_quantize_tiles_fp8(w, dt, G, n_out, k_in, codes, scales, reinterpret_cast<cudaStream_t>(stream));
+    return quantize_weights(w, dt, G, n_out, k_in, codes, scales, stream, false);
+}
+
+moe_status_t moe_quantize_weights_fp8_pow2(const void* w, moe_dtype_t dt, int G, int n_out, int k_in,
+                                           uint8_t* codes, float* scales, moe_stream_t stream) {
+    return quantize_weights(w, dt, G, n_out, k_in, codes, scales, stream, true);
 }
 
 size_t moe_grouped_ffn_fp8_workspace_bytes(int rows, int I) {
@@ -686,26 +742,21 @@ size_t moe_grouped_ffn_fp8_workspace_bytes(int rows, int I) {
            round_up((size_t)rows * scale_ld(I) * 4, kAlign);
 }
 
+
 moe_status_t moe_grouped_ffn_fp8(const uint8_t* aq, const float* a_scales, int lda_scales,
                                  const int32_t* expert_offsets, int E, int rows, int H, int I, const uint8_t* w13q,
                                  const float* w13s, const uint8_t* w2q, const float* w2s, void* y, void* ws,
                                  size_t ws_bytes, moe_stream_t stream) {
-    if (rows < 0 || H <= 0 || I <= 0 || E <= 0 || E > 1024 || lda_scales < (H + 127) / 128) return MOE_ERR_INVALID_ARG;
-    if (!expert_offsets && E != 1) return MOE_ERR_INVALID_ARG;
-    if (H % 256 != 0 || I % 16 != 0) return MOE_ERR_UNSUPPORTED;
-    if (!ws || ws_bytes < moe_grouped_ffn_fp8_workspace_bytes(rows, I)) return MOE_ERR_INVALID_ARG;
-    if (rows > 0 && (!aq || !a_scales || !w13q || !w13s || !w2q || !w2s || !y)) return MOE_ERR_INVALID_ARG;
-    if (!aligned16(aq) || !aligned16(w13q) || !aligned16(w2q) || !aligned16(y) || !aligned16(ws))
-        return MOE_ERR_UNSUPPORTED;
-    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    MOE_TRY(clear_status(ws, s));
-    void* h = at<void>(ws, MOE_WS_HEADER_BYTES);
-    uint8_t* hq = at<uint8_t>(ws, MOE_WS_HEADER_BYTES + round_up((size_t)rows * I * 2, kAlign));
-    float* hs = at<float>(ws, MOE_WS_HEADER_BYTES + round_up((size_t)rows * I * 2, kAlign) +
-                                  round_up((size_t)rows * I, kAlign));
-    MOE_TRY(ffn_up_fp8(aq, a_scales, lda_scales, expert_offsets, E, rows, H, I, w13q, w13s, h, hq, hs, status_word(ws),
-                       s));
-    return ffn_down_fp8(hq, hs, expert_offsets, E, rows, H, I, w2q, w2s, y, status_word(ws), s);
+    return grouped_ffn_fp8(aq, a_scales, lda_scales, expert_offsets, E, rows, H, I, w13q, w13s, w2q, w2s, y, ws,
+                           ws_bytes, stream, false);
+}
+
+moe_status_t moe_grouped_ffn_fp8_pow2(const uint8_t* aq, const float* a_scales, int lda_scales,
+                                      const int32_t* expert_offsets, int E, int rows, int H, int I,
+                                      const uint8_t* w13q, const float* w13s, const uint8_t* w2q, const float* w2s,
+                                      void* y, void* ws, size_t ws_bytes, moe_stream_t stream) {
+    return grouped_ffn_fp8(aq, a_scales, lda_scales, expert_offsets, E, rows, H, I, w13q, w13s, w2q, w2s, y, ws,
+                           ws_bytes, stream, true);
 }
 
 size_t moe_init_routing_workspace_bytes(int T, int E, int k) {

@@ -88,10 +88,11 @@ const int32_t* ep_expert_offsets(const EpBuffers& b);       // [E + 1] rows of e
 moe_status_t ep_combine(const EpBuffers& b, const void* y_sorted, void* y_recv, void* y_expanded, cudaStream_t s);
 
 // quant.cu: FP8 (e4m3) block quantisation.
+// pow2: power-of-two block scales (the format the block-scaled tensor-core GEMM takes).
 moe_status_t launch_quantize_rows_fp8(const void* a, moe_dtype_t dt, int64_t rows, int cols, uint8_t* codes,
-                                      float* scales, int ld_scales, cudaStream_t s);
+                                      float* scales, int ld_scales, cudaStream_t s, bool pow2 = false);
 moe_status_t launch_quantize_tiles_fp8(const void* w, moe_dtype_t dt, int G, int rows, int cols, uint8_t* codes,
-                                       float* scales, cudaStream_t s);
+                                       float* scales, cudaStream_t s, bool pow2 = false);
 
 // finalize.cu
 moe_status_t launch_finalize(const void* y, int64_t y_rows, const void* skip, const float* w,
@@ -141,6 +142,11 @@ struct TcFp8GroupedGemm {
     uint8_t* q = nullptr;     // SwiGLU: also quantise h in 1x128 blocks into codes [M, N] (C may then be null)
     float* q_scales = nullptr;  // [M][ldq]
     int ldq = 0;
+    // Power-of-two scales: the tensor cores apply them (kind::mxf8f6f4 block
+    // scaling, one accumulator per tile, no promotion on CUDA cores) and the
+    // SwiGLU epilogue quantises h with power-of-two scales too.  Every scale of A
+    // and B must then be a power of two (its exponent is what is used).
+    bool pow2 = false;
 };
 moe_status_t launch_tc_fp8_grouped_gemm(const TcFp8GroupedGemm& g, cudaStream_t s);
 int tc_packed_block();        // rows of gate (and of up) per packed block: 128

@@ -3,17 +3,18 @@
 // "Lower latency and higher throughput with multi-node DeepSeek deployment"
 // (Perplexity blog), §Quantization: DeepSeek-V3/R1 quantises per block, with
 // scales per 128-element vector for activations (computed on the fly) and per
-// 128x128 tile for weights (static).  A block's scale is amax/448 in fp32 (1
-// for an all-zero block); each value becomes the e4m3 code of fl32(v / scale),
-// rounded to nearest even and saturated at +-448.
+// 128x128 tile for weights (static).  A block's scale is amax/448 in fp32, or
+// the smallest power of two bringing amax to 448 or below in the power-of-two
+// format (1 for an all-zero block); each value becomes the e4m3 code of
+// fl32(v / scale), rounded to nearest even and saturated at +-448.
 #include "fp8_codec.cuh"
 #include "moe_internal.cuh"
 
 namespace moe {
 namespace {
 
-using fp8::block_scale;
 using fp8::e4m3;
+using fp8::scale_for;
 
 __device__ __forceinline__ float to_f(__nv_bfloat16 v) { return __bfloat162float(v); }
 __device__ __forceinline__ float to_f(float v) { return v; }
@@ -39,7 +40,7 @@ __device__ __forceinline__ void load8(const float* p, float (&v)[8]) {
 template <typename T>
 __global__ void __launch_bounds__(256)
 quantize_rows_kernel(const T* __restrict__ a, int64_t rows, int cols, int kb, int ld_scales,
-                     uint8_t* __restrict__ codes, float* __restrict__ scales) {
+                     uint8_t* __restrict__ codes, float* __restrict__ scales, bool pow2) {
     const int lane = threadIdx.x & 31, hl = lane & 15;
     const int kb2 = (kb + 1) / 2;  // block pairs per row
     const bool vec = (cols & 7) == 0;
@@ -63,7 +64,7 @@ quantize_rows_kernel(const T* __restrict__ a, int64_t rows, int cols, int kb, in
 #pragma unroll
         for (int off = 8; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
         if (b >= kb) continue;  // the second half of the last pair of an odd block count
-        const float s = block_scale(amax);
+        const float s = scale_for(amax, pow2);
         uint8_t* crow = codes + r * cols;
         if (vec && c0 + 8 <= cols) {
             uint2 packed;
@@ -82,7 +83,7 @@ quantize_rows_kernel(const T* __restrict__ a, int64_t rows, int cols, int kb, in
 template <typename T>
 __global__ void __launch_bounds__(256)
 quantize_tiles_kernel(const T* __restrict__ w, int rows, int cols, int nb, int kb, uint8_t* __restrict__ codes,
-                      float* __restrict__ scales) {
+                      float* __restrict__ scales, bool pow2) {
     __shared__ float red[8];
     const int64_t tile = blockIdx.x;
     const int64_t g = tile / ((int64_t)nb * kb);
@@ -101,7 +102,7 @@ quantize_tiles_kernel(const T* __restrict__ w, int rows, int cols, int nb, int k
     __syncthreads();
     amax = red[0];
     for (int i = 1; i < (int)(blockDim.x >> 5); ++i) amax = fmaxf(amax, red[i]);
-    const float s = block_scale(amax);
+    const float s = scale_for(amax, pow2);
     uint8_t* cbase = codes + g * rows * (int64_t)cols;
     for (int i = threadIdx.x; i < 128 * 128; i += blockDim.x) {
         const int r = r0 + i / 128, c = c0 + i % 128;
@@ -113,32 +114,32 @@ quantize_tiles_kernel(const T* __restrict__ w, int rows, int cols, int nb, int k
 }  // namespace
 
 moe_status_t launch_quantize_rows_fp8(const void* a, moe_dtype_t dt, int64_t rows, int cols, uint8_t* codes,
-                                      float* scales, int ld_scales, cudaStream_t s) {
+                                      float* scales, int ld_scales, cudaStream_t s, bool pow2) {
     if (rows == 0) return MOE_OK;
     const int kb = (cols + 127) / 128;
     const int64_t items = rows * ((kb + 1) / 2);  // one warp per pair of blocks
     const int grid = (int)std::min<int64_t>(ceil_div(items, 8), (int64_t)sm_count() * 16);
     if (dt == MOE_BF16)
         quantize_rows_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(a), rows, cols, kb,
-                                                                 ld_scales, codes, scales);
+                                                                 ld_scales, codes, scales, pow2);
     else
         quantize_rows_kernel<float><<<grid, 256, 0, s>>>(static_cast<const float*>(a), rows, cols, kb, ld_scales,
-                                                         codes, scales);
+                                                         codes, scales, pow2);
     note_launch();
     return last_launch_status();
 }
 
 moe_status_t launch_quantize_tiles_fp8(const void* w, moe_dtype_t dt, int G, int rows, int cols, uint8_t* codes,
-                                       float* scales, cudaStream_t s) {
+                                       float* scales, cudaStream_t s, bool pow2) {
     const int nb = (rows + 127) / 128, kb = (cols + 127) / 128;
     const int64_t tiles = (int64_t)G * nb * kb;
     if (tiles == 0) return MOE_OK;
     if (dt == MOE_BF16)
         quantize_tiles_kernel<__nv_bfloat16><<<(unsigned)tiles, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(w),
-                                                                             rows, cols, nb, kb, codes, scales);
+                                                                             rows, cols, nb, kb, codes, scales, pow2);
     else
         quantize_tiles_kernel<float><<<(unsigned)tiles, 256, 0, s>>>(static_cast<const float*>(w), rows, cols, nb, kb,
-                                                                     codes, scales);
+                                                                     codes, scales, pow2);
     note_launch();
     return last_launch_status();
 }

@@ -95,6 +95,19 @@ __device__ __forceinline__ void mma_e4m3(uint32_t d, uint64_t adesc, uint64_t bd
         "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
+// kind::mxf8f6f4 with hardware block scaling (scale_vec::1X: one UE8M0 scale per
+// 32 K elements per row of A and per column of B), e4m3 A and B, fp32 accumulate.
+// The scale factors sit in TMEM at sfa / sfb (layout: see the caller); the
+// instruction descriptor's scale-factor ids pick the byte of each 32-bit column.
+__device__ __forceinline__ void mma_mx_e4m3(uint32_t d, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t sfa,
+                                            uint32_t sfb, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
+        : "memory");
+}
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
                  : "memory");
@@ -144,6 +157,25 @@ __device__ __forceinline__ void tmem_ld16x2(uint32_t taddr_a, uint32_t taddr_b, 
         : "r"(taddr_a), "r"(taddr_b)
         : "memory");
 }
+
+// Register -> TMEM stores: this warp's 32 lanes x 4 (or 32) consecutive columns.
+// Follow with tmem_wait_st() before the data is handed to another thread.
+__device__ __forceinline__ void tmem_st4(uint32_t taddr, const uint32_t (&v)[4]) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr), "r"(v[0]), "r"(v[1]),
+                 "r"(v[2]), "r"(v[3])
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+        "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
+        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
+        "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]), "r"(v[17]), "r"(v[18]),
+        "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]),
+        "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
+        : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 // ---- CTA pairs (a cluster of two CTAs sharing one tcgen05.mma.cta_group::2) ----
 __device__ __forceinline__ uint32_t cluster_ctarank() {
@@ -225,6 +257,13 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
 __host__ __device__ constexpr uint32_t idesc_e4m3(int M, int N) {
     return (1u << 4) | (0u << 7) | (0u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
+// Instruction descriptor, kind::mxf8f6f4 (block-scaled): A and B e4m3, both
+// K-major, M x N, UE8M0 scale factors (bit 23); the scale-factor ids (B: bits
+// 4-5, A: bits 29-30) are or-ed in per instruction.
+__host__ __device__ constexpr uint32_t idesc_mx_e4m3(int M, int N) {
+    return (0u << 7) | (0u << 10) | ((uint32_t)(N >> 3) << 17) | (1u << 23) | ((uint32_t)(M >> 4) << 24);
+}
+__host__ __device__ constexpr uint32_t idesc_sf_ids(uint32_t a_id, uint32_t b_id) { return (b_id << 4) | (a_id << 29); }
 
 // Bounded wait on an mbarrier phase.  Returns false when the wait ran out (and
 // then raises the abort flag) or when another role already aborted.

@@ -42,7 +42,7 @@ class LayerConfig:
     n_group: int = 1          # > 1: group-limited routing
     topk_group: int = 1
     group_rule: str = "max"   # "max" | "top2_sum"
-    weight_format: str = "native"  # "native" | "fp8" (e4m3 expert weights, 128x128 tile scales)
+    weight_format: str = "native"  # "native" | "fp8" (e4m3 expert weights, 128x128 tile scales) | "fp8_pow2"
 
     @property
     def R(self) -> int:
@@ -82,6 +82,13 @@ CONFIGS = {
                                    seed=3, weight_format="fp8"),
     "dsv3_prefill_slice_fp8": LayerConfig("dsv3_prefill_slice_fp8", T=512, H=7168, E=32, k=8, I=2048, S=1,
                                           dtype="bf16", seed=2, weight_format="fp8"),
+    # The same three with power-of-two block scales (products on block-scaled tensor-core MMAs).
+    "dsv3_prefill_fp8_pow2": LayerConfig("dsv3_prefill_fp8_pow2", T=4096, H=7168, E=256, k=8, I=2048, S=1,
+                                         dtype="bf16", seed=2, weight_format="fp8_pow2"),
+    "dsv3_decode_fp8_pow2": LayerConfig("dsv3_decode_fp8_pow2", T=128, H=7168, E=256, k=8, I=2048, S=1,
+                                        dtype="bf16", seed=3, weight_format="fp8_pow2"),
+    "dsv3_prefill_slice_fp8_pow2": LayerConfig("dsv3_prefill_slice_fp8_pow2", T=512, H=7168, E=32, k=8, I=2048,
+                                               S=1, dtype="bf16", seed=2, weight_format="fp8_pow2"),
     # Profiling slice: the DeepSeek-V3 prefill layer's per-expert shape (about 128 rows
     # per expert) on 32 experts, small enough for ncu captures (~5 GB on the device).
     "dsv3_prefill_slice": LayerConfig("dsv3_prefill_slice", T=512, H=7168, E=32, k=8, I=2048, S=1,

@@ -1,6 +1,8 @@
 """GPU parity of the FP8 (e4m3, block-scaled) path against the CPU oracle, through
 the C ABI: quantisers bit for bit, the FP8 grouped FFN and the FP8-weight layer
-within the bf16 tolerance of the oracle's FP8 definition."""
+within the bf16 tolerance of the oracle's FP8 definition -- with fp32 block
+scales (promotion on CUDA cores) and with power-of-two block scales (applied by
+the tensor cores' block-scaled MMA)."""
 import numpy as np
 import pytest
 import torch
@@ -22,14 +24,18 @@ def _lib():
     binding.lib()
 
 
+@pytest.mark.parametrize("pow2", [False, True], ids=["f32scale", "pow2scale"])
 @pytest.mark.parametrize("rows,cols,dtype", [(1, 128, torch.bfloat16), (37, 7168, torch.bfloat16),
                                              (100, 300, torch.float32), (5, 2048, torch.bfloat16),
                                              (64, 40, torch.float32)])
-def test_quantize_rows_fp8(oracle, rows, cols, dtype):
+def test_quantize_rows_fp8(oracle, rows, cols, dtype, pow2):
     a = inputs.random_rows(rows, cols, dtype, seed=rows + cols) * 3
     a[0, :5] = 0  # zeros and a partly zero block
-    codes, scales = binding.moe_quantize_rows_fp8(a.to(DEV))
-    rc, rs = oracle.quantize_rows_fp8(np_(a))
+    if rows > 2 and dtype == torch.float32:
+        a[1] *= 1e-30  # scales near the bottom of the exponent range
+        a[2] *= 1e20
+    codes, scales = binding.moe_quantize_rows_fp8(a.to(DEV), pow2=pow2)
+    rc, rs = oracle.quantize_rows_fp8(np_(a), pow2=pow2)
     assert np.array_equal(codes.cpu().numpy(), rc)
     assert np.array_equal(scales.cpu().numpy(), rs)
 
@@ -43,52 +49,58 @@ def test_quantize_rows_fp8_all_zero_block(oracle):
     assert np.array_equal(codes.cpu().numpy(), oracle.quantize_rows_fp8(np_(a))[0])
 
 
+@pytest.mark.parametrize("pow2", [False, True], ids=["f32scale", "pow2scale"])
 @pytest.mark.parametrize("G,n,k", [(2, 256, 512), (1, 200, 300), (3, 384, 7168)])
-def test_quantize_weights_fp8(oracle, G, n, k):
+def test_quantize_weights_fp8(oracle, G, n, k, pow2):
     w = inputs.random_rows(G * n, k, torch.bfloat16, seed=G * n + k).view(G, n, k)
-    codes, scales = binding.moe_quantize_weights_fp8(w.to(DEV))
+    codes, scales = binding.moe_quantize_weights_fp8(w.to(DEV), pow2=pow2)
     for g in range(G):
-        rc, rs = oracle.quantize_tiles_fp8(np_(w[g]))
+        rc, rs = oracle.quantize_tiles_fp8(np_(w[g]), pow2=pow2)
         assert np.array_equal(codes[g].cpu().numpy(), rc)
         assert np.array_equal(scales[g].cpu().numpy(), rs)
 
 
-def _oracle_fp8_weights(oracle, n: dict, shared: bool = True):
+def _oracle_fp8_weights(oracle, n: dict, shared: bool = True, pow2: bool = False):
     q = {}
     parts = [("", "w_gate", "w_up", "w2")] + ([("s", "s_gate", "s_up", "s2")] if shared else [])
     for pre, g, u, d in parts:
-        q[pre + "gq"], q[pre + "gs"] = oracle.quantize_experts_fp8(n[g])
-        q[pre + "uq"], q[pre + "us"] = oracle.quantize_experts_fp8(n[u])
-        q[pre + "dq"], q[pre + "ds"] = oracle.quantize_experts_fp8(n[d])
+        q[pre + "gq"], q[pre + "gs"] = oracle.quantize_experts_fp8(n[g], pow2)
+        q[pre + "uq"], q[pre + "us"] = oracle.quantize_experts_fp8(n[u], pow2)
+        q[pre + "dq"], q[pre + "ds"] = oracle.quantize_experts_fp8(n[d], pow2)
     return q
 
 
+@pytest.mark.parametrize("pow2", [False, True], ids=["f32scale", "pow2scale"])
 @pytest.mark.parametrize("T,k,E,H,I", [(300, 6, 16, 512, 256), (1000, 2, 8, 256, 384), (64, 8, 64, 256, 128),
-                                       (3, 1, 4, 256, 128), (120, 4, 8, 512, 208)])
-def test_grouped_ffn_fp8(oracle, T, k, E, H, I):
-    """I=208: a K tail of 80 in the down projection and padded gate/up packing."""
+                                       (3, 1, 4, 256, 128), (120, 4, 8, 512, 208), (200, 4, 8, 2304, 256)])
+def test_grouped_ffn_fp8(oracle, T, k, E, H, I, pow2):
+    """I=208: a K tail of 80 in the down projection and padded gate/up packing.  H=2304:
+    18 K blocks in the up projection, so with power-of-two scales a tile spans two
+    scale-factor groups (16 + 2 blocks)."""
     cfg = inputs.LayerConfig("f", T=T, H=H, E=E, k=k, I=I, S=0, dtype="bf16", seed=T + E)
     d = inputs.make_layer(cfg, "cpu")
     n = {key: np_(v) for key, v in d.items() if isinstance(v, torch.Tensor)}
     ids = inputs.random_ids(T, k, E, seed=T)
     ir = oracle.init_routing(ids.numpy(), n["x"], E)
-    xq, xs = oracle.quantize_rows_fp8(ir["expanded_x"])
-    q = _oracle_fp8_weights(oracle, n, shared=False)
+    xq, xs = oracle.quantize_rows_fp8(ir["expanded_x"], pow2=pow2)
+    q = _oracle_fp8_weights(oracle, n, shared=False, pow2=pow2)
     # the GPU quantises the packed gate/up weight; its codes are the oracle's, re-packed
     w13 = binding.moe_pack_w13(d["w_gate"].to(DEV), d["w_up"].to(DEV))
-    w13q, w13s = binding.moe_quantize_weights_fp8(w13)
-    w2q, w2s = binding.moe_quantize_weights_fp8(d["w2"].to(DEV))
+    w13q, w13s = binding.moe_quantize_weights_fp8(w13, pow2=pow2)
+    w2q, w2s = binding.moe_quantize_weights_fp8(d["w2"].to(DEV), pow2=pow2)
     if I % 128 == 0:
         e0 = w13q[0].cpu().numpy()
         assert np.array_equal(e0[0:128], q["gq"][0][0:128]) and np.array_equal(e0[128:256], q["uq"][0][0:128])
     y, ws = binding.moe_grouped_ffn_fp8(torch.from_numpy(xq).to(DEV), torch.from_numpy(xs).to(DEV),
-                                        torch.from_numpy(ir["expert_offsets"]).to(DEV), E, I, w13q, w13s, w2q, w2s)
+                                        torch.from_numpy(ir["expert_offsets"]).to(DEV), E, I, w13q, w13s, w2q, w2s,
+                                        pow2=pow2)
     assert binding.moe_check_device_status(ws) == 0
     expert_of_row = np.repeat(np.arange(E, dtype=np.int32), ir["tokens_per_expert"])
-    ref = oracle.expert_ffn_rows_fp8(xq, xs, expert_of_row, q)
+    ref = oracle.expert_ffn_rows_fp8(xq, xs, expert_of_row, q, pow2=pow2)
     assert rel_l2(y, ref) <= 1e-2
     rows_err = per_row_rel_l2(y, ref)
-    log_parity("ffn_fp8", rel_l2=rel_l2(y, ref), worst_token_rel_l2=float(rows_err.max()), compared=len(rows_err))
+    log_parity("ffn_fp8" + ("_pow2" if pow2 else ""), rel_l2=rel_l2(y, ref), worst_token_rel_l2=float(rows_err.max()),
+               compared=len(rows_err))
     assert rows_err.max() <= ROW_TOL["bf16"]
     # The up GEMM's epilogue quantises h itself; its codes and scales are those the
     # 1x128 quantiser gives for the bf16 h stored beside them.  Workspace of this
@@ -101,11 +113,11 @@ def test_grouped_ffn_fp8(oracle, T, k, E, H, I):
     hq = ws[o:o + rows * I].view(rows, I)
     o += up(rows * I)
     hs = ws[o:o + rows * ld * 4].view(torch.float32).view(rows, ld)
-    rq, rs = binding.moe_quantize_rows_fp8(h, ld_scales=ld)
+    rq, rs = binding.moe_quantize_rows_fp8(h, ld_scales=ld, pow2=pow2)
     nb = -(-I // 128)
     assert torch.equal(hq, rq) and torch.equal(hs[:, :nb], rs[:, :nb])
     # and both are the oracle's quantisation of that h
-    oq, os_ = oracle.quantize_rows_fp8(np_(h))
+    oq, os_ = oracle.quantize_rows_fp8(np_(h), pow2=pow2)
     assert np.array_equal(hq.cpu().numpy(), oq) and np.array_equal(hs[:, :nb].cpu().numpy(), os_)
 
 
@@ -116,6 +128,12 @@ FP8_LAYERS = [
                        topk_group=2, group_rule="top2_sum", weight_format="fp8"),
     inputs.LayerConfig("fp8_noshared", T=130, H=256, E=16, k=2, I=384, S=0, dtype="bf16", seed=53,
                        weight_format="fp8"),
+    inputs.LayerConfig("fp8_pow2_small", T=256, H=512, E=64, k=6, I=256, S=2, dtype="bf16", seed=54,
+                       weight_format="fp8_pow2"),
+    inputs.LayerConfig("fp8_pow2_grouped", T=200, H=2304, E=32, k=4, I=128, S=1, dtype="bf16", seed=55, n_group=4,
+                       topk_group=2, group_rule="top2_sum", weight_format="fp8_pow2"),
+    inputs.LayerConfig("fp8_pow2_noshared_zipf", T=300, H=256, E=16, k=2, I=384, S=0, dtype="bf16", seed=56,
+                       zipf_s=1.2, weight_format="fp8_pow2"),
 ]
 
 
@@ -125,11 +143,12 @@ def _check_fp8_layer(oracle, cfg, d, layer, out, tokens=None):
     n = host_arrays(d)
     check_routing(oracle, cfg, n, layer.field("logits").cpu().numpy(), layer.field("topk_ids").cpu().numpy(),
                   layer.field("topk_w").cpu().numpy())
-    q = _oracle_fp8_weights(oracle, n, shared=cfg.S > 0)
+    pow2 = cfg.weight_format == "fp8_pow2"
+    q = _oracle_fp8_weights(oracle, n, shared=cfg.S > 0, pow2=pow2)
     toks = np.arange(cfg.T, dtype=np.int32) if tokens is None else np.asarray(tokens, np.int32)
     ref = oracle.layer_fp8(n["x"], n["wg"], q, k=cfg.k, renorm=cfg.renormalize, bias=n.get("bias"),
                            tokens=None if tokens is None else toks, n_group=cfg.n_group, topk_group=cfg.topk_group,
-                           group_rule=cfg.group_rule)
+                           group_rule=cfg.group_rule, pow2=pow2)
     res = check_output(cfg, layer.field("topk_ids").cpu().numpy(), out, ref, toks)
     assert binding.moe_check_device_status(layer.ws) == 0
     return res
@@ -154,7 +173,8 @@ def test_layer_fp8_small(oracle, cfg):
     assert torch.equal(layer.forward(d["x"]), out)
 
 
-@pytest.mark.parametrize("name,n_sample", [("dsv3_prefill_fp8", 32), ("dsv3_decode_fp8", 16)])
+@pytest.mark.parametrize("name,n_sample", [("dsv3_prefill_fp8", 32), ("dsv3_decode_fp8", 16),
+                                           ("dsv3_prefill_fp8_pow2", 32), ("dsv3_decode_fp8_pow2", 16)])
 def test_layer_fp8_full_size_sampled(oracle, name, n_sample):
     cfg = inputs.CONFIGS[name]
     d, layer = _make(cfg)

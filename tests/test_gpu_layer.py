@@ -174,6 +174,8 @@ HOST = [
     inputs.LayerConfig("host_fp32_chunks", T=1500, H=128, E=16, k=2, I=64, S=1, dtype="f32", seed=26),
     inputs.LayerConfig("host_fp8_chunks", T=2048, H=512, E=32, k=4, I=256, S=1, dtype="bf16", seed=27,
                        weight_format="fp8"),
+    inputs.LayerConfig("host_fp8_pow2_chunks", T=2048, H=512, E=32, k=4, I=256, S=1, dtype="bf16", seed=28,
+                       weight_format="fp8_pow2"),
 ]
 
 
