@@ -196,6 +196,21 @@ moe_status_t moe_pack_w13(const void* w_gate, const void* w_up, moe_dtype_t dt, 
                           void* w13_packed, moe_stream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * Tiled weight layout.  [BLOG §Roofline / GroupGEMM]: at about 128 rows per
+ * expert the grouped GEMM streams its weights from HBM.  The tensor-core GEMM
+ * reads a weight as boxes of 256 rows x 128 bytes of K; in the row-major layout
+ * such a box is 256 pieces 2*K bytes apart, in this layout it is one contiguous
+ * 32 KB block, which HBM serves faster (fewer DRAM rows opened per byte):
+ *   tiled[g][t][b][r][0..128 B) = w[g][256*t + r][128*b .. 128*b + 128 B)
+ * for t < ceil(n_rows/256), b < ceil(row_bytes/128), zero past the matrix.
+ * w: [G][n_rows][row_bytes] (any element type; row_bytes % 16 == 0); tiled:
+ * moe_tiled_weight_bytes(G, n_rows, row_bytes) bytes.  For a layer, tile the
+ * moe_pack_w13 output ([E][2*Ip][H], row_bytes = 2*H for bf16), w2 ([E][H][I]),
+ * and the shared w13 ([1][2*Ips][H]) and w2 ([1][H][S*I]). */
+size_t moe_tiled_weight_bytes(int G, int n_rows, int row_bytes);
+moe_status_t moe_tile_weights(const void* w, int G, int n_rows, int row_bytes, void* tiled, moe_stream_t stream);
+
+/* ---------------------------------------------------------------------------
  * Grouped SwiGLU expert FFN.  [BLOG §Roofline / GroupGEMM]: g groups, group i
  * multiplies [m_i,k]x[k,n]; here group e is expert e's segment of rows
  * [expert_offsets[e], expert_offsets[e+1]) of `a`.  [BLOG §Expert Parallelism]
@@ -215,6 +230,11 @@ moe_status_t moe_pack_w13(const void* w_gate, const void* w_up, moe_dtype_t dt, 
  * average 256 rows or more; the environment variable MOE_GEMM_TILE=single or
  * MOE_GEMM_TILE=pair, read at every launch, forces one shape.  Both give the
  * same result up to fp32 summation order. */
+/* moe_grouped_ffn with both weights in the tiled layout (moe_tile_weights of the
+ * moe_pack_w13 output and of w2); bf16 only.  Same arguments and results. */
+moe_status_t moe_grouped_ffn_tiled(const void* a, moe_dtype_t dt, const int32_t* expert_offsets, int E, int rows,
+                                   int H, int I, const void* w13_tiled, const void* w2_tiled, void* y, void* ws,
+                                   size_t ws_bytes, moe_stream_t stream);
 size_t moe_grouped_ffn_workspace_bytes(moe_dtype_t dt, int rows, int I);
 moe_status_t moe_grouped_ffn(const void* a, moe_dtype_t dt, const int32_t* expert_offsets, int E,
                              int rows, int H, int I, const void* w13_packed, const void* w2, void* y,
@@ -343,7 +363,14 @@ typedef struct moe_layer_desc {
     const float* w2_scales;    /* FP8: tile scales of w2 [E][H/128][ceil(I/128)] */
     const float* w13_shared_scales; /* FP8: [1][2*Ips/128][ceil(H/128)], Ips = S*I rounded up to 128 */
     const float* w2_shared_scales;  /* FP8: [1][H/128][ceil(S*I/128)] */
+    int weight_layout;         /* MOE_LAYOUT_ROWS (0) or MOE_LAYOUT_TILED (bf16 native weights): the four
+                                  expert weights above (w13, w2 and the shared ones) passed through
+                                  moe_tile_weights; w_router stays row-major */
 } moe_layer_desc;
+
+/* Expert-weight layouts of moe_layer_desc (and of moe_grouped_ffn_tiled). */
+#define MOE_LAYOUT_ROWS 0
+#define MOE_LAYOUT_TILED 1
 
 /* Weight formats of moe_layer_desc.  With MOE_WEIGHTS_FP8 the w13/w2 pointers
  * (routed and shared) hold e4m3 codes in the same layouts (one byte per

@@ -27,6 +27,8 @@ WS_FIELDS = ["logits", "topk_ids", "topk_w", "tokens_per_expert", "expert_offset
 WS_FIELDS_EP = ["x_sorted", "gathered_ids_unsort", "recv_start", "expert_offsets"]
 MOE_WEIGHTS_NATIVE, MOE_WEIGHTS_FP8, MOE_WEIGHTS_FP8_POW2 = 0, 1, 2
 WEIGHT_FORMATS = {"native": MOE_WEIGHTS_NATIVE, "fp8": MOE_WEIGHTS_FP8, "fp8_pow2": MOE_WEIGHTS_FP8_POW2}
+MOE_LAYOUT_ROWS, MOE_LAYOUT_TILED = 0, 1
+WEIGHT_LAYOUTS = {"rows": MOE_LAYOUT_ROWS, "tiled": MOE_LAYOUT_TILED}
 
 # The exported entry points (name -> (restype, argtypes)).
 P, I32, I64, SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t
@@ -37,7 +39,7 @@ class LayerDesc(ctypes.Structure):
                 ("renormalize", I32), ("w_router", P), ("expert_bias", P), ("w13", P), ("w2", P),
                 ("w13_shared", P), ("w2_shared", P), ("n_group", I32), ("topk_group", I32), ("group_rule", I32),
                 ("weight_format", I32), ("w13_scales", P), ("w2_scales", P), ("w13_shared_scales", P),
-                ("w2_shared_scales", P)]
+                ("w2_shared_scales", P), ("weight_layout", I32)]
 
 
 _DP = ctypes.POINTER(LayerDesc)
@@ -57,6 +59,9 @@ SIGNATURES = {
     "moe_pack_w13": (I32, [P, P, I32, I32, I32, I32, P, P]),
     "moe_grouped_ffn_workspace_bytes": (SZ, [I32, I32, I32]),
     "moe_grouped_ffn": (I32, [P, I32, P, I32, I32, I32, I32, P, P, P, P, SZ, P]),
+    "moe_grouped_ffn_tiled": (I32, [P, I32, P, I32, I32, I32, I32, P, P, P, P, SZ, P]),
+    "moe_tiled_weight_bytes": (SZ, [I32, I32, I32]),
+    "moe_tile_weights": (I32, [P, I32, I32, I32, P, P]),
     "moe_finalize_routing": (I32, [P, I64, P, P, P, I32, I32, I32, I32, P, P, P]),
     "moe_re_routing_workspace_bytes": (SZ, [I32, I32]),
     "moe_re_routing": (I32, [P, I32, P, I32, I32, I32, I32, P, P, P, P, P, SZ, P]),
@@ -229,7 +234,8 @@ def moe_pack_w13(w_gate: torch.Tensor, w_up: torch.Tensor, stream=None) -> torch
 
 
 def moe_grouped_ffn(a: torch.Tensor, expert_offsets, E: int, I: int, w13_packed: torch.Tensor,
-                    w2: torch.Tensor, y: torch.Tensor | None = None, ws=None, stream=None):
+                    w2: torch.Tensor, y: torch.Tensor | None = None, ws=None, stream=None, tiled: bool = False):
+    """tiled: w13_packed and w2 are moe_tile_weights outputs (moe_grouped_ffn_tiled)."""
     rows, H = a.shape
     dt = _dt(a)
     need = lib().moe_grouped_ffn_workspace_bytes(dt, rows, I)
@@ -237,9 +243,25 @@ def moe_grouped_ffn(a: torch.Tensor, expert_offsets, E: int, I: int, w13_packed:
         ws = torch.empty(need, dtype=torch.uint8, device=a.device)
     if y is None:
         y = torch.zeros((rows, H), dtype=a.dtype, device=a.device)
-    _check(lib().moe_grouped_ffn(_ptr(a), dt, _ptr(expert_offsets), E, rows, H, I, _ptr(w13_packed), _ptr(w2),
-                                 _ptr(y), _ptr(ws), ws.numel(), _stream(stream)), "moe_grouped_ffn")
+    name = "moe_grouped_ffn_tiled" if tiled else "moe_grouped_ffn"
+    _check(getattr(lib(), name)(_ptr(a), dt, _ptr(expert_offsets), E, rows, H, I, _ptr(w13_packed), _ptr(w2),
+                                _ptr(y), _ptr(ws), ws.numel(), _stream(stream)), name)
     return y, ws
+
+
+def moe_tile_weights(w: torch.Tensor, stream=None) -> torch.Tensor:
+    """w [G, n_rows, K] (or [n_rows, K]) -> the tiled layout as a flat uint8 tensor."""
+    if w.dim() == 2:
+        w = w.unsqueeze(0)
+    w = w.contiguous()
+    G, n, k = w.shape
+    row_bytes = k * w.element_size()
+    nbytes = lib().moe_tiled_weight_bytes(G, n, row_bytes)
+    if nbytes == 0:
+        raise MoEError(MOE_ERR_INVALID_ARG, "moe_tiled_weight_bytes")
+    out = torch.empty(nbytes, dtype=torch.uint8, device=w.device)
+    _check(lib().moe_tile_weights(_ptr(w), G, n, row_bytes, _ptr(out), _stream(stream)), "moe_tile_weights")
+    return out
 
 
 def moe_finalize_routing(y: torch.Tensor, topk_w: torch.Tensor, expanded_row_idx: torch.Tensor,
@@ -332,7 +354,8 @@ class MoELayer:
 
     def __init__(self, *, T: int, k: int, w_router, w_gate, w_up, w2, s_gate=None, s_up=None, s2=None,
                  expert_bias=None, renormalize: bool = True, n_group: int = 1, topk_group: int = 1,
-                 group_rule: str = "max", weight_format: str = "native", stream=None):
+                 group_rule: str = "max", weight_format: str = "native", weight_layout: str | None = None,
+                 stream=None):
         E, I, H = w_gate.shape
         S = 0 if s_gate is None else s_gate.shape[0]
         self.T, self.H, self.E, self.k, self.I, self.S = T, H, E, k, I, S
@@ -362,13 +385,27 @@ class MoELayer:
                 self.w13_shared, ss13 = moe_quantize_weights_fp8(self.w13_shared, stream, pow2=p2)
                 self.w2_shared, ss2 = moe_quantize_weights_fp8(self.w2_shared, stream, pow2=p2)
                 scales[2], scales[3] = ss13, ss2
+        # bf16 expert weights go to the tiled layout (each 256-row x 128-byte weight box one contiguous
+        # block of HBM) unless asked otherwise; fp32 and FP8 layers keep rows
+        if weight_layout is None:
+            weight_layout = "tiled" if (self.dtype == torch.bfloat16 and weight_format == "native") else "rows"
+        if weight_layout not in WEIGHT_LAYOUTS:
+            raise ValueError(f"weight_layout must be one of {sorted(WEIGHT_LAYOUTS)}, got {weight_layout!r}")
+        self.weight_layout = weight_layout
+        if weight_layout == "tiled":
+            self.w13 = moe_tile_weights(self.w13, stream)
+            self.w2 = moe_tile_weights(self.w2, stream)
+            if S:
+                self.w13_shared = moe_tile_weights(self.w13_shared, stream)
+                self.w2_shared = moe_tile_weights(self.w2_shared, stream)
         self.scales = scales
         sp = [0 if t is None else t.data_ptr() for t in scales]
         self.desc = LayerDesc(T, H, E, k, I, S, _dt(w_gate), int(bool(renormalize)), self.w_router.data_ptr(),
                               0 if self.expert_bias is None else self.expert_bias.data_ptr(), self.w13.data_ptr(),
                               self.w2.data_ptr(), 0 if S == 0 else self.w13_shared.data_ptr(),
                               0 if S == 0 else self.w2_shared.data_ptr(), n_group, topk_group,
-                              GROUP_RULES[group_rule], WEIGHT_FORMATS[weight_format], *sp)
+                              GROUP_RULES[group_rule], WEIGHT_FORMATS[weight_format], *sp,
+                              WEIGHT_LAYOUTS[weight_layout])
         nbytes = lib().moe_layer_workspace_bytes(ctypes.byref(self.desc))
         if nbytes == 0:
             raise MoEError(MOE_ERR_INVALID_ARG, "moe_layer_workspace_bytes")

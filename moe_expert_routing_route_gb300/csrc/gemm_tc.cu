@@ -68,6 +68,7 @@ struct Cfg {
 struct Params {
     const int32_t* offsets;
     int G, M, K, Nb, N, NT;
+    int b_tiled, b_nt;        // B in the tiled layout, with b_nt 256-row tiles per group
     int ksplit;               // K split into this many slices (fp32 outputs only), each written at
     int64_t c_split_stride;   // C + slice * c_split_stride
     void* C;
@@ -232,6 +233,7 @@ tc_grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_co
                 decode_tile(tile, prefix, G, NT, p.ksplit, g, m, n, ks);
                 const int row0 = gstart[g] + m * BM;
                 const int brow = g * p.Nb + n * BN;
+                const int tbase = (g * p.b_nt + n) * KB;  // tiled B: this tile's first 256-row box
                 const int kb1 = min(KB, (ks + 1) * KBS);
                 for (int kb = ks * KBS; kb < kb1; ++kb) {
                     if (!wait_phase(empty_bar(s), ph ^ 1u, abort_flag, p.status)) {
@@ -240,7 +242,10 @@ tc_grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_co
                     }
                     mbar_arrive_expect_tx(full_bar(s), Cf::STAGE_BYTES);
                     tma_load_2d(smem_u32(sA + s * Cf::A_BYTES), &mapA, full_bar(s), kb * BK, row0);
-                    tma_load_2d(smem_u32(sB + s * Cf::B_BYTES), &mapB, full_bar(s), kb * BK, brow);
+                    if (p.b_tiled)  // one contiguous 32 KB box
+                        tma_load_2d(smem_u32(sB + s * Cf::B_BYTES), &mapB, full_bar(s), 0, (tbase + kb) * BN);
+                    else
+                        tma_load_2d(smem_u32(sB + s * Cf::B_BYTES), &mapB, full_bar(s), kb * BK, brow);
                     issued |= 1u << s;
                     issued_par = (issued_par & ~(1u << s)) | (ph << s);
                     if (++s == STAGES) {
@@ -495,6 +500,7 @@ tc_pair_gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_const
                 seg(g, ga, gb);
                 const int row0 = ga + m * BM2 + (int)rank * 128;
                 const int brow = g * p.Nb + n * BN2 + (int)rank * (BN2 / 2);
+                const int tbase = (g * p.b_nt + n) * KB;  // tiled B: this tile's first 256-row box
                 for (int kb = 0; kb < KB; ++kb) {
                     if (!wait_phase(empty_bar(s), ph ^ 1u, abort_flag, p.status)) {
                         ok = false;
@@ -503,7 +509,11 @@ tc_pair_gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_const
                     if (leader) mbar_arrive_expect_tx(full_bar(s), 2 * Cf::STAGE_BYTES);
                     const uint32_t fb = mapa_shared(full_bar(s), 0);  // the leader's full[s]
                     tma_load_2d_pair(smem_u32(sA + s * Cf::A_BYTES), &mapA, fb, kb * BK, row0);
-                    tma_load_2d_pair(smem_u32(sB + s * Cf::B_BYTES), &mapB, fb, kb * BK, brow);
+                    if (p.b_tiled)  // this CTA's half of a contiguous 256-row box
+                        tma_load_2d_pair(smem_u32(sB + s * Cf::B_BYTES), &mapB, fb, 0,
+                                         (tbase + kb) * BN2 + (int)rank * (BN2 / 2));
+                    else
+                        tma_load_2d_pair(smem_u32(sB + s * Cf::B_BYTES), &mapB, fb, kb * BK, brow);
                     issued |= 1u << s;
                     issued_par = (issued_par & ~(1u << s)) | (ph << s);
                     if (++s == STAGES) {
@@ -645,8 +655,15 @@ moe_status_t launch_impl(const TcGroupedGemm& g, cudaStream_t s) {
     MOE_CUDA_TRY(attr_err);
 
     CUtensorMap ma, mb;
+    const int b_nt = (int)ceil_div(g.Nb, 256), KBt = (int)ceil_div(g.K, BK);
     if (!make_map(&ma, g.A, (uint64_t)g.K, (uint64_t)g.M, BM)) return MOE_ERR_CUDA;
-    if (!make_map(&mb, g.B, (uint64_t)g.K, (uint64_t)g.G * g.Nb, BN)) return MOE_ERR_CUDA;
+    if (g.b_tiled) {
+        // box rows are addressed with int coordinates
+        if (BN != 256 || (int64_t)g.G * b_nt * KBt * 256 >= INT_MAX) return MOE_ERR_UNSUPPORTED;
+        if (!make_map(&mb, g.B, (uint64_t)BK, (uint64_t)g.G * b_nt * KBt * 256, BN)) return MOE_ERR_CUDA;
+    } else if (!make_map(&mb, g.B, (uint64_t)g.K, (uint64_t)g.G * g.Nb, BN)) {
+        return MOE_ERR_CUDA;
+    }
 
     Params p;
     p.offsets = g.offsets;
@@ -655,6 +672,8 @@ moe_status_t launch_impl(const TcGroupedGemm& g, cudaStream_t s) {
     p.K = g.K;
     p.Nb = g.Nb;
     p.N = g.N;
+    p.b_tiled = g.b_tiled ? 1 : 0;
+    p.b_nt = b_nt;
     p.NT = EPI == TC_EPI_SWIGLU ? g.Nb / BN : (int)ceil_div(g.N, BN);
     p.ksplit = EPI == TC_EPI_F32 ? effective_splits(g.K, g.ksplit) : 1;
     p.c_split_stride = g.c_split_stride;
@@ -706,8 +725,14 @@ moe_status_t launch_pair_impl(const TcGroupedGemm& g, cudaStream_t s) {
     if (pairs_max < 1) return MOE_ERR_UNSUPPORTED;
 
     CUtensorMap ma, mb;
+    const int b_nt = (int)ceil_div(g.Nb, 256), KBt = (int)ceil_div(g.K, BK);
     if (!make_map(&ma, g.A, (uint64_t)g.K, (uint64_t)g.M, 128)) return MOE_ERR_CUDA;
-    if (!make_map(&mb, g.B, (uint64_t)g.K, (uint64_t)g.G * g.Nb, BN2 / 2)) return MOE_ERR_CUDA;
+    if (g.b_tiled) {
+        if ((int64_t)g.G * b_nt * KBt * 256 >= INT_MAX) return MOE_ERR_UNSUPPORTED;
+        if (!make_map(&mb, g.B, (uint64_t)BK, (uint64_t)g.G * b_nt * KBt * 256, BN2 / 2)) return MOE_ERR_CUDA;
+    } else if (!make_map(&mb, g.B, (uint64_t)g.K, (uint64_t)g.G * g.Nb, BN2 / 2)) {
+        return MOE_ERR_CUDA;
+    }
 
     Params p;
     p.offsets = g.offsets;
@@ -716,6 +741,8 @@ moe_status_t launch_pair_impl(const TcGroupedGemm& g, cudaStream_t s) {
     p.K = g.K;
     p.Nb = g.Nb;
     p.N = g.N;
+    p.b_tiled = g.b_tiled ? 1 : 0;
+    p.b_nt = b_nt;
     p.NT = EPI == TC_EPI_SWIGLU ? g.Nb / BN2 : (int)ceil_div(g.N, BN2);
     p.ksplit = 1;
     p.c_split_stride = 0;
@@ -796,6 +823,7 @@ moe_status_t launch_tc_grouped_gemm(const TcGroupedGemm& g, cudaStream_t s) {
         case TC_EPI_BF16:
             return use_pair_tiles(g) ? launch_pair<TC_EPI_BF16>(g, s) : launch_impl<256, TC_EPI_BF16>(g, s);
         case TC_EPI_F32: {
+            if (g.b_tiled) return MOE_ERR_UNSUPPORTED;
             int bn, split;
             plan_f32(g.M, g.N, g.K, std::max(1, g.ksplit), bn, split);
             TcGroupedGemm gs = g;

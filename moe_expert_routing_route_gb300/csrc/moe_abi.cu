@@ -45,27 +45,34 @@ int packed_rows(int I) { return 2 * (int)round_up((size_t)I, (size_t)tc_packed_b
 // Grouped FFN halves: up (SwiGLU into h) and down (h into y); bf16 on tcgen05,
 // fp32 on the FFMA pipes.  offsets == nullptr means one dense group of `rows`.
 // headroom: leave shared memory on every SM for kernels running beside this one
+// tiled: the weight is in the tiled layout (bf16 only)
 moe_status_t ffn_up(const void* a, moe_dtype_t dt, const int32_t* offsets, int G, int rows, int H, int I,
-                    const void* w13p, void* h, uint32_t* status, cudaStream_t s, bool headroom = false) {
+                    const void* w13p, void* h, uint32_t* status, cudaStream_t s, bool headroom = false,
+                    bool tiled = false) {
     if (rows == 0) return MOE_OK;
     if (dt == MOE_BF16) {
         TcGroupedGemm up{a, rows, H, offsets, G, w13p, packed_rows(I), I, h, I, TC_EPI_SWIGLU, status};
         up.smem_headroom = headroom;
+        up.b_tiled = tiled;
         return launch_tc_grouped_gemm(up, s);
     }
+    if (tiled) return MOE_ERR_UNSUPPORTED;
     return launch_simt_grouped_ffn_up(static_cast<const float*>(a), rows, H, offsets, G,
                                       static_cast<const float*>(w13p), packed_rows(I) / 2, I, static_cast<float*>(h),
                                       status, s);
 }
 
 moe_status_t ffn_down(const void* h, moe_dtype_t dt, const int32_t* offsets, int G, int rows, int H, int I,
-                      const void* w2, void* y, uint32_t* status, cudaStream_t s, bool headroom = false) {
+                      const void* w2, void* y, uint32_t* status, cudaStream_t s, bool headroom = false,
+                      bool tiled = false) {
     if (rows == 0) return MOE_OK;
     if (dt == MOE_BF16) {
         TcGroupedGemm down{h, rows, I, offsets, G, w2, H, H, y, H, TC_EPI_BF16, status};
         down.smem_headroom = headroom;
+        down.b_tiled = tiled;
         return launch_tc_grouped_gemm(down, s);
     }
+    if (tiled) return MOE_ERR_UNSUPPORTED;
     return launch_simt_grouped_down(static_cast<const float*>(h), rows, I, offsets, G, static_cast<const float*>(w2),
                                     H, static_cast<float*>(y), status, s);
 }
@@ -203,6 +210,9 @@ moe_status_t check_desc(const moe_layer_desc* d) {
         if (!d->w13_scales || !d->w2_scales) return MOE_ERR_INVALID_ARG;
         if (d->S > 0 && (!d->w13_shared_scales || !d->w2_shared_scales)) return MOE_ERR_INVALID_ARG;
     }
+    if (d->weight_layout != MOE_LAYOUT_ROWS && d->weight_layout != MOE_LAYOUT_TILED) return MOE_ERR_INVALID_ARG;
+    if (d->weight_layout == MOE_LAYOUT_TILED && (d->dtype != MOE_BF16 || d->weight_format != MOE_WEIGHTS_NATIVE))
+        return MOE_ERR_UNSUPPORTED;
     if (!aligned16(d->w_router) || !aligned16(d->w13) || !aligned16(d->w2) || !aligned16(d->expert_bias) ||
         !aligned16(d->w13_shared) || !aligned16(d->w2_shared))
         return MOE_ERR_UNSUPPORTED;
@@ -331,6 +341,7 @@ moe_status_t layer_forward(const moe_layer_desc* d, const void* x, void* out, vo
 
     const bool fp8 = d->weight_format == MOE_WEIGHTS_FP8 || d->weight_format == MOE_WEIGHTS_FP8_POW2;
     const bool pow2 = d->weight_format == MOE_WEIGHTS_FP8_POW2;
+    const bool tiled = d->weight_layout == MOE_LAYOUT_TILED;
     uint8_t* xq = at<uint8_t>(ws, L.off[MOE_WS_XQ]);
     float* xs = at<float>(ws, L.off[MOE_WS_XQ_SCALES]);
     uint8_t* exq = at<uint8_t>(ws, L.off[MOE_WS_EXPANDED_XQ]);
@@ -375,8 +386,8 @@ moe_status_t layer_forward(const moe_layer_desc* d, const void* x, void* out, vo
                 const char* xc = static_cast<const char*>(x) + (size_t)c0 * row_bytes;
                 char* hsc = static_cast<char*>(hs) + (size_t)c0 * SI * dt_size(dt);
                 char* ysc = static_cast<char*>(ys) + (size_t)c0 * row_bytes;
-                MOE_TRY(ffn_up(xc, dt, nullptr, 1, c1 - c0, H, SI, d->w13_shared, hsc, status, ss));
-                MOE_TRY(ffn_down(hsc, dt, nullptr, 1, c1 - c0, H, SI, d->w2_shared, ysc, status, ss));
+                MOE_TRY(ffn_up(xc, dt, nullptr, 1, c1 - c0, H, SI, d->w13_shared, hsc, status, ss, false, tiled));
+                MOE_TRY(ffn_down(hsc, dt, nullptr, 1, c1 - c0, H, SI, d->w2_shared, ysc, status, ss, false, tiled));
             }
             MOE_TRY(mark(ev, ST_SHARED, 1, ss));
             MOE_CUDA_TRY(cudaEventRecord(side->join, ss));
@@ -406,8 +417,8 @@ moe_status_t layer_forward(const moe_layer_desc* d, const void* x, void* out, vo
                                  pow2));
         } else {
             // the routing kernels (histogram and scatter use shared memory) run beside them
-            MOE_TRY(ffn_up(x, dt, nullptr, 1, T, H, SI, d->w13_shared, hs, status, ss, true));
-            MOE_TRY(ffn_down(hs, dt, nullptr, 1, T, H, SI, d->w2_shared, ys, status, ss, true));
+            MOE_TRY(ffn_up(x, dt, nullptr, 1, T, H, SI, d->w13_shared, hs, status, ss, true, tiled));
+            MOE_TRY(ffn_down(hs, dt, nullptr, 1, T, H, SI, d->w2_shared, ys, status, ss, true, tiled));
         }
         MOE_TRY(mark(ev, ST_SHARED, 1, ss));
         MOE_CUDA_TRY(cudaEventRecord(side->join, ss));
@@ -435,11 +446,11 @@ moe_status_t layer_forward(const moe_layer_desc* d, const void* x, void* out, vo
     MOE_TRY(mark(ev, ST_UP, 0, s));
     if (fp8)
         MOE_TRY(ffn_up_fp8(exq, exs, ldx, offsets, E, R, H, I, d->w13, d->w13_scales, nullptr, hq, hqs, status, s, pow2));
-    else MOE_TRY(ffn_up(ex, dt, offsets, E, R, H, I, d->w13, h, status, s));
+    else MOE_TRY(ffn_up(ex, dt, offsets, E, R, H, I, d->w13, h, status, s, false, tiled));
     MOE_TRY(mark(ev, ST_UP, 1, s));
     MOE_TRY(mark(ev, ST_DOWN, 0, s));
     if (fp8) MOE_TRY(ffn_down_fp8(hq, hqs, offsets, E, R, H, I, d->w2, d->w2_scales, y, status, s, pow2));
-    else MOE_TRY(ffn_down(h, dt, offsets, E, R, H, I, d->w2, y, status, s));
+    else MOE_TRY(ffn_down(h, dt, offsets, E, R, H, I, d->w2, y, status, s, false, tiled));
     MOE_TRY(mark(ev, ST_DOWN, 1, s));
     MOE_TRY(mark(ev, ST_FINALIZE, 0, s));
     if (!io) {
@@ -506,6 +517,7 @@ moe_status_t layer_forward_ep(const moe_layer_desc* d, int W, const void* x, voi
     const int T = d->T, H = d->H, E = d->E, k = d->k, I = d->I, R = T * k, SI = d->S * d->I;
     const int El = E / W, Tp = T / W, Rp = Tp * k;
     const moe_dtype_t dt = d->dtype;
+    const bool tiled = d->weight_layout == MOE_LAYOUT_TILED;
     const size_t rb = (size_t)H * dt_size(dt), eb = dt_size(dt);
     uint32_t* status = status_word(ws);
     float* logits = at<float>(ws, L.off[MOE_WS_LOGITS]);
@@ -530,8 +542,8 @@ moe_status_t layer_forward_ep(const moe_layer_desc* d, int W, const void* x, voi
     MOE_TRY(layer_gate(*d, x, logits, &nsplit, s));
     if (side) {
         MOE_CUDA_TRY(cudaStreamWaitEvent(side->stream, side->fork, 0));
-        MOE_TRY(ffn_up(x, dt, nullptr, 1, T, H, SI, d->w13_shared, hs, status, side->stream));
-        MOE_TRY(ffn_down(hs, dt, nullptr, 1, T, H, SI, d->w2_shared, ys, status, side->stream));
+        MOE_TRY(ffn_up(x, dt, nullptr, 1, T, H, SI, d->w13_shared, hs, status, side->stream, false, tiled));
+        MOE_TRY(ffn_down(hs, dt, nullptr, 1, T, H, SI, d->w2_shared, ys, status, side->stream, false, tiled));
         MOE_CUDA_TRY(cudaEventRecord(side->join, side->stream));
     }
     MOE_TRY(launch_route_topk(logits, d->expert_bias, T, E, k, d->renormalize, ids, w, s, d->n_group, d->topk_group,
@@ -543,8 +555,8 @@ moe_status_t layer_forward_ep(const moe_layer_desc* d, int W, const void* x, voi
     // the ranks' local segments together segment the buffer by global expert: on
     // one GPU all ranks' expert GEMMs run as one persistent launch per projection
     // (the same tiles as W launches of El experts, without W tails).
-    MOE_TRY(ffn_up(b.sorted, dt, ep_expert_offsets(b), E, R, H, I, d->w13, h, status, s));
-    MOE_TRY(ffn_down(h, dt, ep_expert_offsets(b), E, R, H, I, d->w2, y, status, s));
+    MOE_TRY(ffn_up(b.sorted, dt, ep_expert_offsets(b), E, R, H, I, d->w13, h, status, s, false, tiled));
+    MOE_TRY(ffn_down(h, dt, ep_expert_offsets(b), E, R, H, I, d->w2, y, status, s, false, tiled));
     // steps 6-7: back to received order, back to the source ranks (into the free buffers)
     MOE_TRY(ep_combine(b, y, b.recv, b.expanded, s));
     // step 8: finalize on each source rank
@@ -595,6 +607,24 @@ moe_status_t quantize_weights(const void* w, moe_dtype_t dt, int G, int n_out, i
     return launch_quantize_tiles_fp8(w, dt, G, n_out, k_in, codes, scales, reinterpret_cast<cudaStream_t>(stream),
                                      pow2);
 }
+
+moe_status_t grouped_ffn(const void* a, moe_dtype_t dt, const int32_t* expert_offsets, int E, int rows, int H, int I,
+                         const void* w13_packed, const void* w2, void* y, void* ws, size_t ws_bytes,
+                         moe_stream_t stream, bool tiled) {
+    if (bad_dtype(dt) || rows < 0 || H <= 0 || I <= 0 || E <= 0 || E > 1024) return MOE_ERR_INVALID_ARG;
+    if (!expert_offsets && E != 1) return MOE_ERR_INVALID_ARG;
+    if (H % 8 != 0 || I % 8 != 0) return MOE_ERR_UNSUPPORTED;
+    if (!ws || ws_bytes < moe_grouped_ffn_workspace_bytes(dt, rows, I)) return MOE_ERR_INVALID_ARG;
+    if (rows > 0 && (!a || !w13_packed || !w2 || !y)) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(a) || !aligned16(w13_packed) || !aligned16(w2) || !aligned16(y) || !aligned16(ws))
+        return MOE_ERR_UNSUPPORTED;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    MOE_TRY(clear_status(ws, s));
+    void* h = at<void>(ws, MOE_WS_HEADER_BYTES);
+    MOE_TRY(ffn_up(a, dt, expert_offsets, E, rows, H, I, w13_packed, h, status_word(ws), s, false, tiled));
+    return ffn_down(h, dt, expert_offsets, E, rows, H, I, w2, y, status_word(ws), s, false, tiled);
+}
+
 moe_status_t grouped_ffn_fp8(const uint8_t* aq, const float* a_scales, int lda_scales, const int32_t* expert_offsets,
                              int E, int rows, int H, int I, const uint8_t* w13q, const float* w13s, const uint8_t* w2q,
                              const float* w2s, void* y, void* ws, size_t ws_bytes, moe_stream_t stream, bool pow2) {
@@ -803,19 +833,30 @@ size_t moe_grouped_ffn_workspace_bytes(moe_dtype_t dt, int rows, int I) {
 moe_status_t moe_grouped_ffn(const void* a, moe_dtype_t dt, const int32_t* expert_offsets, int E, int rows, int H,
                              int I, const void* w13_packed, const void* w2, void* y, void* ws, size_t ws_bytes,
                              moe_stream_t stream) {
-    if (bad_dtype(dt) || rows < 0 || H <= 0 || I <= 0 || E <= 0 || E > 1024) return MOE_ERR_INVALID_ARG;
-    if (!expert_offsets && E != 1) return MOE_ERR_INVALID_ARG;
-    if (H % 8 != 0 || I % 8 != 0) return MOE_ERR_UNSUPPORTED;
-    if (!ws || ws_bytes < moe_grouped_ffn_workspace_bytes(dt, rows, I)) return MOE_ERR_INVALID_ARG;
-    if (rows > 0 && (!a || !w13_packed || !w2 || !y)) return MOE_ERR_INVALID_ARG;
-    if (!aligned16(a) || !aligned16(w13_packed) || !aligned16(w2) || !aligned16(y) || !aligned16(ws))
-        return MOE_ERR_UNSUPPORTED;
-    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    MOE_TRY(clear_status(ws, s));
-    void* h = at<void>(ws, MOE_WS_HEADER_BYTES);
-    MOE_TRY(ffn_up(a, dt, expert_offsets, E, rows, H, I, w13_packed, h, status_word(ws), s));
-    return ffn_down(h, dt, expert_offsets, E, rows, H, I, w2, y, status_word(ws), s);
+    return grouped_ffn(a, dt, expert_offsets, E, rows, H, I, w13_packed, w2, y, ws, ws_bytes, stream, false);
 }
+
+moe_status_t moe_grouped_ffn_tiled(const void* a, moe_dtype_t dt, const int32_t* expert_offsets, int E, int rows,
+                                   int H, int I, const void* w13_tiled, const void* w2_tiled, void* y, void* ws,
+                                   size_t ws_bytes, moe_stream_t stream) {
+    if (dt != MOE_BF16) return MOE_ERR_UNSUPPORTED;
+    return grouped_ffn(a, dt, expert_offsets, E, rows, H, I, w13_tiled, w2_tiled, y, ws, ws_bytes, stream, true);
+}
+
+size_t moe_tiled_weight_bytes(int G, int n_rows, int row_bytes) {
+    if (G <= 0 || n_rows <= 0 || row_bytes <= 0 || row_bytes % 16 != 0) return 0;
+    return tiled_weight_bytes(G, n_rows, row_bytes);
+}
+
+moe_status_t moe_tile_weights(const void* w, int G, int n_rows, int row_bytes, void* tiled, moe_stream_t stream) {
+    if (G <= 0 || n_rows <= 0 || row_bytes <= 0) return MOE_ERR_INVALID_ARG;
+    if (row_bytes % 16 != 0) return MOE_ERR_UNSUPPORTED;
+    if (!w || !tiled) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(w) || !aligned16(tiled)) return MOE_ERR_UNSUPPORTED;
+    return launch_tile_weights(w, G, n_rows, row_bytes, tiled, reinterpret_cast<cudaStream_t>(stream));
+}
+
+
 
 moe_status_t moe_finalize_routing(const void* y, int64_t y_rows, const void* skip, const float* topk_w,
                                   const int32_t* expanded_row_idx, moe_dtype_t dt, int T, int H, int k, void* out,

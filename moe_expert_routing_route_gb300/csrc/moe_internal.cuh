@@ -55,6 +55,10 @@ moe_status_t launch_init_routing_index(const int32_t* ids, int R, int E, int32_t
                                        uint32_t* status, cudaStream_t s);
 moe_status_t launch_permute_rows(const void* x, size_t row_bytes, const int32_t* row_idx, int T, int k,
                                  void* expanded_x, cudaStream_t s);
+// The tiled weight layout of the tensor-core GEMMs' B operand: [G][ceil(n/256)][ceil(row_bytes/128)][256][128 B]
+// (each 256-row x 128-byte box one contiguous 32 KB block), zero-padded.
+size_t tiled_weight_bytes(int G, int n_rows, int row_bytes);
+moe_status_t launch_tile_weights(const void* w, int G, int n_rows, int row_bytes, void* tiled, cudaStream_t s);
 moe_status_t launch_pack_w13(const void* w_gate, const void* w_up, size_t esize, int E, int H, int I,
                              void* packed, cudaStream_t s);
 
@@ -118,6 +122,7 @@ struct TcGroupedGemm {
     int64_t c_split_stride = 0;   // C + s * c_split_stride (elements); the caller sums the slices
     bool smem_headroom = false;   // pair tiles: take the 6-stage ring, leaving ~24 KB of shared memory per SM
                                   // for kernels of other streams (the 7-stage ring leaves under 1 KB)
+    bool b_tiled = false;         // B in the tiled layout (tiled_weight_bytes(G, Nb, 2K)); bf16/SwiGLU epilogues only
 };
 moe_status_t launch_tc_grouped_gemm(const TcGroupedGemm& g, cudaStream_t s);
 int tc_gate_splits(int M, int N, int K, int max_split);  // K slices the fp32 launch will use

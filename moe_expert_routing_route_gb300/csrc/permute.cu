@@ -202,7 +202,45 @@ __global__ void pack_w13_kernel(const uint4* __restrict__ wg, const uint4* __res
     }
 }
 
+// Tiled weight layout: out[g][nt][kb][r][0..128 B) = w[g][256*nt + r][128*kb .. 128*kb + 128 B),
+// zero past the matrix.  One 16-byte chunk per thread and step, writes in output order.
+__global__ void tile_weights_kernel(const uint8_t* __restrict__ w, int G, int n_rows, int row_bytes, int NT, int KBt,
+                                    uint4* __restrict__ out) {
+    const int64_t total = (int64_t)G * NT * KBt * 256 * 8;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
+        const int c = (int)(i & 7);
+        int64_t t = i >> 3;
+        const int r = (int)(t & 255);
+        t >>= 8;
+        const int kb = (int)(t % KBt);
+        t /= KBt;
+        const int nt = (int)(t % NT);
+        const int64_t g = t / NT;
+        const int row = nt * 256 + r;
+        const int64_t byte = (int64_t)kb * 128 + c * 16;
+        uint4 v = make_uint4(0, 0, 0, 0);
+        if (row < n_rows && byte < row_bytes)
+            v = __ldg(reinterpret_cast<const uint4*>(w + (g * n_rows + row) * (int64_t)row_bytes + byte));
+        out[i] = v;
+    }
+}
+
 }  // namespace
+
+size_t tiled_weight_bytes(int G, int n_rows, int row_bytes) {
+    return (size_t)G * (size_t)ceil_div(n_rows, 256) * (size_t)ceil_div(row_bytes, 128) * 256 * 128;
+}
+
+moe_status_t launch_tile_weights(const void* w, int G, int n_rows, int row_bytes, void* tiled, cudaStream_t s) {
+    const int NT = (int)ceil_div(n_rows, 256), KBt = (int)ceil_div(row_bytes, 128);
+    const int64_t total = (int64_t)G * NT * KBt * 256 * 8;
+    if (total == 0) return MOE_OK;
+    const int grid = (int)std::min<int64_t>(ceil_div(total, 256), (int64_t)sm_count() * 16);
+    tile_weights_kernel<<<grid, 256, 0, s>>>(static_cast<const uint8_t*>(w), G, n_rows, row_bytes, NT, KBt,
+                                             static_cast<uint4*>(tiled));
+    note_launch();
+    return last_launch_status();
+}
 
 size_t init_routing_scratch_bytes(int T, int E, int k) {
     const int64_t R = (int64_t)T * k;

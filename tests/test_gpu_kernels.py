@@ -191,6 +191,24 @@ def test_pack_w13_layout(E, I, H):
                 assert torch.all(g_row == 0) and torch.all(u_row == 0)
 
 
+@pytest.mark.parametrize("G,n,K,dtype", [(2, 300, 200, torch.bfloat16), (1, 256, 64, torch.bfloat16),
+                                         (3, 512, 7168, torch.bfloat16), (2, 40, 160, torch.uint8)])
+def test_tile_weights_layout(G, n, K, dtype):
+    """tiled[g][t][b][r] = the 128 bytes of row 256*t + r at byte 128*b, zero past the matrix."""
+    if dtype == torch.uint8:
+        w = torch.randint(0, 256, (G, n, K), dtype=torch.uint8, generator=inputs.generator("cpu", 7, "misc"))
+    else:
+        w = inputs.random_rows(G * n, K, dtype, seed=G + n + K).view(G, n, K)
+    got = binding.moe_tile_weights(w.to(DEV)).cpu().numpy()
+    raw = w.view(torch.uint8).numpy().reshape(G, n, -1) if dtype != torch.uint8 else w.numpy()
+    rb = raw.shape[2]
+    NT, KB = -(-n // 256), -(-rb // 128)
+    pad = np.zeros((G, NT * 256, KB * 128), np.uint8)
+    pad[:, :n, :rb] = raw
+    want = pad.reshape(G, NT, 256, KB, 128).transpose(0, 1, 3, 2, 4).reshape(-1)
+    assert got.shape == want.shape and np.array_equal(got, want)
+
+
 # ---- gate GEMM -------------------------------------------------------------------------
 
 @pytest.mark.parametrize("T,H,E,dtype", [(1, 64, 8, torch.bfloat16), (300, 512, 64, torch.bfloat16),
@@ -222,7 +240,7 @@ def _close(y, ref, dtype_key: str):
     return err
 
 
-def _ffn_case(oracle, T, k, E, H, I, dtype, seed, ids=None):
+def _ffn_case(oracle, T, k, E, H, I, dtype, seed, ids=None, tiled=False):
     cfg = inputs.LayerConfig("f", T=T, H=H, E=E, k=k, I=I, S=0,
                              dtype="f32" if dtype == torch.float32 else "bf16", seed=seed)
     d = inputs.make_layer(cfg, "cpu")
@@ -233,7 +251,10 @@ def _ffn_case(oracle, T, k, E, H, I, dtype, seed, ids=None):
         else torch.from_numpy(ir["expanded_x"])
     offs = torch.from_numpy(ir["expert_offsets"])
     w13 = binding.moe_pack_w13(d["w_gate"].to(DEV), d["w_up"].to(DEV))
-    y, ws = binding.moe_grouped_ffn(ex.to(DEV), offs.to(DEV), E, I, w13, d["w2"].to(DEV))
+    w2 = d["w2"].to(DEV)
+    if tiled:
+        w13, w2 = binding.moe_tile_weights(w13), binding.moe_tile_weights(w2)
+    y, ws = binding.moe_grouped_ffn(ex.to(DEV), offs.to(DEV), E, I, w13, w2, tiled=tiled)
     assert binding.moe_check_device_status(ws) == 0
     expert_of_row = np.repeat(np.arange(E, dtype=np.int32), ir["tokens_per_expert"])
     ref = oracle.expert_ffn_rows(ir["expanded_x"], expert_of_row, np_(d["w_gate"]), np_(d["w_up"]), np_(d["w2"]))
@@ -285,11 +306,14 @@ TILE_CASES = [
 ]
 
 
+@pytest.mark.parametrize("layout", ["rows", "tiled"])
 @pytest.mark.parametrize("tile", ["single", "pair"])
 @pytest.mark.parametrize("T,k,E,H,I", TILE_CASES)
-def test_grouped_ffn_bf16_tile_shapes(oracle, monkeypatch, tile, T, k, E, H, I):
+def test_grouped_ffn_bf16_tile_shapes(oracle, monkeypatch, tile, T, k, E, H, I, layout):
+    """Both tile shapes, with the weights row-major and in the tiled layout (whose boxes
+    are padded with zero rows and columns past the matrix)."""
     monkeypatch.setenv("MOE_GEMM_TILE", tile)
-    y, ref, _ = _ffn_case(oracle, T, k, E, H, I, torch.bfloat16, seed=T + E + 1)
+    y, ref, _ = _ffn_case(oracle, T, k, E, H, I, torch.bfloat16, seed=T + E + 1, tiled=layout == "tiled")
     _close(y, ref, "bf16")
 
 

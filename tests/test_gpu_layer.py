@@ -60,6 +60,25 @@ def test_layer_small(oracle, cfg):
     check_layer(oracle, cfg, d, layer, out)
 
 
+ROWS = [c for c in SMALL if c.dtype == "bf16" and c.name in ("small_bf16", "ragged_bf16", "one_token_bf16")]
+
+
+@pytest.mark.parametrize("tile", ["single", "pair"])
+@pytest.mark.parametrize("cfg", ROWS, ids=[c.name for c in ROWS])
+def test_layer_small_row_major_weights(oracle, monkeypatch, cfg, tile):
+    """bf16 layers take tiled weights by default; the row-major layout stays supported."""
+    monkeypatch.setenv("MOE_GEMM_TILE", tile)
+    d = inputs.make_layer(cfg, DEV)
+    layer = binding.MoELayer(T=cfg.T, k=cfg.k, w_router=d["wg"], w_gate=d["w_gate"], w_up=d["w_up"], w2=d["w2"],
+                             s_gate=d["s_gate"] if cfg.S else None, s_up=d["s_up"] if cfg.S else None,
+                             s2=d["s2"] if cfg.S else None, expert_bias=d["bias"], renormalize=cfg.renormalize,
+                             weight_layout="rows")
+    out = layer.forward(d["x"])
+    check_layer(oracle, cfg, d, layer, out)
+    tiled = make(cfg)[1]
+    assert torch.equal(tiled.forward(d["x"]), out)  # the same products, whichever layout
+
+
 PAIR = [c for c in SMALL if c.dtype == "bf16" and c.name in ("small_bf16", "ragged_bf16", "zipf_bf16",
                                                                  "grouped_bf16", "dense_E1_bf16")]
 
