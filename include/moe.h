@@ -363,9 +363,9 @@ typedef struct moe_layer_desc {
     const float* w2_scales;    /* FP8: tile scales of w2 [E][H/128][ceil(I/128)] */
     const float* w13_shared_scales; /* FP8: [1][2*Ips/128][ceil(H/128)], Ips = S*I rounded up to 128 */
     const float* w2_shared_scales;  /* FP8: [1][H/128][ceil(S*I/128)] */
-    int weight_layout;         /* MOE_LAYOUT_ROWS (0) or MOE_LAYOUT_TILED (bf16 native weights): the four
-                                  expert weights above (w13, w2 and the shared ones) passed through
-                                  moe_tile_weights; w_router stays row-major */
+    int weight_layout;         /* MOE_LAYOUT_ROWS (0) or MOE_LAYOUT_TILED (bf16 layers): the four expert
+                                  weights above (w13, w2 and the shared ones; for FP8 their codes) passed
+                                  through moe_tile_weights; w_router and the FP8 scales stay as they are */
 } moe_layer_desc;
 
 /* Expert-weight layouts of moe_layer_desc (and of moe_grouped_ffn_tiled). */

@@ -92,6 +92,7 @@ struct Plan {
 struct Params {
     const int32_t* offsets;  // [G+1] or nullptr: one group of M rows
     int G, M, K, Nb, N, NT, KB;
+    int b_tiled, b_nt;       // B in the tiled layout, with b_nt 256-row tiles per group
     void* C;
     int64_t ldc;
     const float* a_scales;  // [M][lda_s]
@@ -286,6 +287,7 @@ tc_fp8_grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __gri
                 decode_tile(tile, prefix, G, NT, g, m, n);
                 const int row0 = gstart[g] + m * BM;
                 const int brow = g * p.Nb + n * BN;
+                const int tbase = (g * p.b_nt + n) * KB;  // tiled B: this tile's first 256-row box
                 for (int kb = 0; kb < KB; ++kb) {
                     if (!wait_phase_fast(empty_bar(s), ph ^ 1u, abort_flag, p.status)) {
                         ok = false;
@@ -293,7 +295,10 @@ tc_fp8_grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __gri
                     }
                     mbar_arrive_expect_tx(full_bar(s), STAGE_BYTES);
                     tma_load_2d(smem_u32(sA + s * A_BYTES), &mapA, full_bar(s), kb * BK, row0);
-                    tma_load_2d(smem_u32(sB + s * B_BYTES), &mapB, full_bar(s), kb * BK, brow);
+                    if (p.b_tiled)  // one contiguous 32 KB box
+                        tma_load_2d(smem_u32(sB + s * B_BYTES), &mapB, full_bar(s), 0, (tbase + kb) * BN);
+                    else
+                        tma_load_2d(smem_u32(sB + s * B_BYTES), &mapB, full_bar(s), kb * BK, brow);
                     issued |= 1u << s;
                     issued_par = (issued_par & ~(1u << s)) | (ph << s);
                     if (++s == STAGES) {
@@ -612,8 +617,15 @@ moe_status_t launch_impl(const TcFp8GroupedGemm& g, cudaStream_t s) {
     });
     MOE_CUDA_TRY(attr_err);
     CUtensorMap ma, mb, mc;
+    const int b_nt = (int)ceil_div(g.Nb, 256), KBt = (int)ceil_div(g.K, BK);
     if (!make_map(&ma, g.A, (uint64_t)g.K, (uint64_t)g.M, BM, 1)) return MOE_ERR_CUDA;
-    if (!make_map(&mb, g.B, (uint64_t)g.K, (uint64_t)g.G * g.Nb, BN, 1)) return MOE_ERR_CUDA;
+    if (g.b_tiled) {
+        // box rows are addressed with int coordinates
+        if ((int64_t)g.G * b_nt * KBt * 256 >= INT_MAX) return MOE_ERR_UNSUPPORTED;
+        if (!make_map(&mb, g.B, (uint64_t)BK, (uint64_t)g.G * b_nt * KBt * 256, BN, 1)) return MOE_ERR_CUDA;
+    } else if (!make_map(&mb, g.B, (uint64_t)g.K, (uint64_t)g.G * g.Nb, BN, 1)) {
+        return MOE_ERR_CUDA;
+    }
     // bf16 output through TMA stores when the map can describe it (else direct stores)
     const bool c_tma = EPI == TC_EPI_BF16 && g.C &&
                        make_store_map_bf16(&mc, g.C, (uint64_t)g.N, (uint64_t)g.M, (uint64_t)g.ldc, 32);
@@ -633,6 +645,8 @@ moe_status_t launch_impl(const TcFp8GroupedGemm& g, cudaStream_t s) {
     p.lda_s = g.lda_scales;
     p.b_scales = g.b_scales;
     p.c_tma = c_tma ? 1 : 0;
+    p.b_tiled = g.b_tiled ? 1 : 0;
+    p.b_nt = b_nt;
     p.q = g.q;
     p.q_scales = g.q_scales;
     p.ldq = g.ldq;

@@ -53,6 +53,8 @@ constexpr int kThreads = 192;
 constexpr int kMaxGroups = 1024;
 constexpr int kPackBlock = 128;  // gate rows (and up rows) per packed block
 
+constexpr int kOutBox = 32 * 128;  // bf16 epilogue: one warp's 32 rows x 64 columns, staged for a TMA store
+
 template <int BN>
 struct Cfg {
     static constexpr int A_BYTES = BM * BK * 2;
@@ -61,7 +63,8 @@ struct Cfg {
     static constexpr int STAGES = BN == 256 ? 4 : (BN == 128 ? 6 : 8);
     static constexpr int TMEM_COLS = 2 * BN;  // two fp32 accumulators
     static constexpr int NUM_BARS = 2 * STAGES + 5;
-    static constexpr size_t SMEM = 1024 + (size_t)STAGES * STAGE_BYTES + NUM_BARS * 8 + 16 +
+    static constexpr int OUT_BYTES = 4 * kOutBox;  // one staging box per epilogue warp
+    static constexpr size_t SMEM = 1024 + (size_t)STAGES * STAGE_BYTES + OUT_BYTES + NUM_BARS * 8 + 16 +
                                    (size_t)(3 * kMaxGroups + 1) * 4;
 };
 
@@ -69,6 +72,7 @@ struct Params {
     const int32_t* offsets;
     int G, M, K, Nb, N, NT;
     int b_tiled, b_nt;        // B in the tiled layout, with b_nt 256-row tiles per group
+    int c_tma;                // bf16 epilogue: C written through mapC (TMA stores of staged 32 x 64 boxes)
     int ksplit;               // K split into this many slices (fp32 outputs only), each written at
     int64_t c_split_stride;   // C + slice * c_split_stride
     void* C;
@@ -135,10 +139,24 @@ __device__ __forceinline__ void store_row32(void* C, int64_t ldc, int64_t row, i
     }
 }
 
+// 64 values of one row into a staging box laid out as the 128-byte swizzled TMA
+// box expects: 16-byte chunk c of row r at r*128 + ((c ^ (r % 8)) * 16).
+__device__ __forceinline__ void stage_row64_sw128(uint8_t* box, int r, const float* v) {
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+        uint4 u;
+        u.x = pack_bf16x2(v[8 * c + 0], v[8 * c + 1]);
+        u.y = pack_bf16x2(v[8 * c + 2], v[8 * c + 3]);
+        u.z = pack_bf16x2(v[8 * c + 4], v[8 * c + 5]);
+        u.w = pack_bf16x2(v[8 * c + 6], v[8 * c + 7]);
+        *reinterpret_cast<uint4*>(box + r * 128 + ((c ^ (r & 7)) << 4)) = u;
+    }
+}
+
 template <int BN, int EPI>
 __global__ void __launch_bounds__(kThreads, 1)
 tc_grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
-                       const __grid_constant__ Params p) {
+                       const __grid_constant__ CUtensorMap mapC, const __grid_constant__ Params p) {
     using Cf = Cfg<BN>;
     constexpr int STAGES = Cf::STAGES;
     constexpr uint32_t IDESC = idesc_bf16(BM, BN);
@@ -149,7 +167,8 @@ tc_grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_co
     uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
     uint8_t* sA = smem;
     uint8_t* sB = smem + STAGES * Cf::A_BYTES;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(sB + STAGES * Cf::B_BYTES);
+    uint8_t* sOut = sB + STAGES * Cf::B_BYTES;  // 1024-aligned: stage sizes are multiples of 1 KB
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sOut + Cf::OUT_BYTES);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + Cf::NUM_BARS);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     int* prefix = reinterpret_cast<int*>(tmem_slot + 4);  // [G+1]
@@ -329,6 +348,33 @@ tc_grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_co
                     }
                     if (valid) store_row32<EPI>(C, p.ldc, row, n * kPackBlock + c, p.N, h);
                 }
+            } else if (EPI == TC_EPI_BF16 && p.c_tma && __all_sync(0xffffffffu, valid)) {
+                // all 32 rows of this warp inside the expert's segment: 32 x 64 boxes through the
+                // warp's staging box, each leaving as one TMA store (full lines instead of 16-byte
+                // pieces of 32 rows per store instruction)
+                uint8_t* box = sOut + (warp - 2) * kOutBox;
+                const int row0 = gstart[g] + m * BM + eg * 32;
+#pragma unroll 1
+                for (int c = 0; c < BN; c += 64) {
+                    uint32_t v0[32], v1[32];
+                    tmem_ld32(taddr + c, v0);
+                    tmem_ld32(taddr + c + 32, v1);
+                    float v[64];
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        v[i] = __uint_as_float(v0[i]);
+                        v[32 + i] = __uint_as_float(v1[i]);
+                    }
+                    if (lane == 0) bulk_wait_read_all();  // the previous box has left
+                    __syncwarp();
+                    stage_row64_sw128(box, lane, v);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0 && n * BN + c < p.N) {
+                        tma_store_2d(&mapC, smem_u32(box), n * BN + c, row0);
+                        bulk_commit();
+                    }
+                }
             } else {
 #pragma unroll 1
                 for (int c = 0; c < BN; c += 32) {
@@ -348,6 +394,7 @@ tc_grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_co
                 aph ^= 1u;
             }
         }
+        if (EPI == TC_EPI_BF16 && lane == 0) bulk_wait_all();  // staged stores done before the CTA leaves
     }
 
     __syncwarp();
@@ -665,6 +712,12 @@ moe_status_t launch_impl(const TcGroupedGemm& g, cudaStream_t s) {
         return MOE_ERR_CUDA;
     }
 
+    // bf16 output through TMA stores when the map can describe it (else direct stores)
+    CUtensorMap mc;
+    const bool c_tma = EPI == TC_EPI_BF16 && g.C && g.ksplit <= 1 &&
+                       make_store_map_bf16(&mc, g.C, (uint64_t)g.N, (uint64_t)g.M, (uint64_t)g.ldc, 32);
+    if (!c_tma) mc = ma;  // never read
+
     Params p;
     p.offsets = g.offsets;
     p.G = g.G;
@@ -674,6 +727,7 @@ moe_status_t launch_impl(const TcGroupedGemm& g, cudaStream_t s) {
     p.N = g.N;
     p.b_tiled = g.b_tiled ? 1 : 0;
     p.b_nt = b_nt;
+    p.c_tma = c_tma ? 1 : 0;
     p.NT = EPI == TC_EPI_SWIGLU ? g.Nb / BN : (int)ceil_div(g.N, BN);
     p.ksplit = EPI == TC_EPI_F32 ? effective_splits(g.K, g.ksplit) : 1;
     p.c_split_stride = g.c_split_stride;
@@ -683,7 +737,7 @@ moe_status_t launch_impl(const TcGroupedGemm& g, cudaStream_t s) {
 
     const int64_t max_tiles = (int64_t)p.NT * p.ksplit * (ceil_div(g.M, BM) + (g.offsets ? g.G : 0));
     const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(sm_count(), max_tiles));
-    tc_grouped_gemm_kernel<BN, EPI><<<grid, kThreads, Cf::SMEM, s>>>(ma, mb, p);
+    tc_grouped_gemm_kernel<BN, EPI><<<grid, kThreads, Cf::SMEM, s>>>(ma, mb, mc, p);
     note_launch();
     return last_launch_status();
 }
@@ -743,6 +797,7 @@ moe_status_t launch_pair_impl(const TcGroupedGemm& g, cudaStream_t s) {
     p.N = g.N;
     p.b_tiled = g.b_tiled ? 1 : 0;
     p.b_nt = b_nt;
+    p.c_tma = 0;
     p.NT = EPI == TC_EPI_SWIGLU ? g.Nb / BN2 : (int)ceil_div(g.N, BN2);
     p.ksplit = 1;
     p.c_split_stride = 0;

@@ -85,20 +85,21 @@ int scale_ld(int cols) { return (int)round_up((size_t)ceil_div(cols, 128), 4); }
 // pow2: power-of-two scales throughout (block-scaled tensor-core MMAs).
 moe_status_t ffn_up_fp8(const uint8_t* aq, const float* as, int lda_s, const int32_t* offsets, int G, int rows, int H,
                         int I, const void* w13q, const float* w13s, void* h, uint8_t* hq, float* hs,
-                        uint32_t* status, cudaStream_t s, bool pow2) {
+                        uint32_t* status, cudaStream_t s, bool pow2, bool tiled = false) {
     if (rows == 0) return MOE_OK;
     // the SwiGLU epilogue writes the down projection's FP8 input directly; bf16 h
     // is stored too only when the caller gives a buffer for it (h may be null)
     TcFp8GroupedGemm up{aq, rows, H, offsets, G, w13q, packed_rows(I), I, h, I, TC_EPI_SWIGLU, as, lda_s,
-                        w13s, status, hq, hs, scale_ld(I), pow2};
+                        w13s, status, hq, hs, scale_ld(I), pow2, tiled};
     return launch_tc_fp8_grouped_gemm(up, s);
 }
 
 moe_status_t ffn_down_fp8(const uint8_t* hq, const float* hs, const int32_t* offsets, int G, int rows, int H, int I,
-                          const void* w2q, const float* w2s, void* y, uint32_t* status, cudaStream_t s, bool pow2) {
+                          const void* w2q, const float* w2s, void* y, uint32_t* status, cudaStream_t s, bool pow2,
+                          bool tiled = false) {
     if (rows == 0) return MOE_OK;
     TcFp8GroupedGemm down{hq, rows, I, offsets, G, w2q, H, H, y, H, TC_EPI_BF16, hs, scale_ld(I), w2s, status,
-                          nullptr, nullptr, 0, pow2};
+                          nullptr, nullptr, 0, pow2, tiled};
     return launch_tc_fp8_grouped_gemm(down, s);
 }
 
@@ -211,8 +212,7 @@ moe_status_t check_desc(const moe_layer_desc* d) {
         if (d->S > 0 && (!d->w13_shared_scales || !d->w2_shared_scales)) return MOE_ERR_INVALID_ARG;
     }
     if (d->weight_layout != MOE_LAYOUT_ROWS && d->weight_layout != MOE_LAYOUT_TILED) return MOE_ERR_INVALID_ARG;
-    if (d->weight_layout == MOE_LAYOUT_TILED && (d->dtype != MOE_BF16 || d->weight_format != MOE_WEIGHTS_NATIVE))
-        return MOE_ERR_UNSUPPORTED;
+    if (d->weight_layout == MOE_LAYOUT_TILED && d->dtype != MOE_BF16) return MOE_ERR_UNSUPPORTED;
     if (!aligned16(d->w_router) || !aligned16(d->w13) || !aligned16(d->w2) || !aligned16(d->expert_bias) ||
         !aligned16(d->w13_shared) || !aligned16(d->w2_shared))
         return MOE_ERR_UNSUPPORTED;
@@ -412,9 +412,9 @@ moe_status_t layer_forward(const moe_layer_desc* d, const void* x, void* out, vo
         MOE_TRY(mark(ev, ST_SHARED, 0, ss));
         if (fp8) {
             MOE_TRY(ffn_up_fp8(xq, xs, ldx, nullptr, 1, T, H, SI, d->w13_shared, d->w13_shared_scales, nullptr, hsq, hss,
-                               status, ss, pow2));
+                               status, ss, pow2, tiled));
             MOE_TRY(ffn_down_fp8(hsq, hss, nullptr, 1, T, H, SI, d->w2_shared, d->w2_shared_scales, ys, status, ss,
-                                 pow2));
+                                 pow2, tiled));
         } else {
             // the routing kernels (histogram and scatter use shared memory) run beside them
             MOE_TRY(ffn_up(x, dt, nullptr, 1, T, H, SI, d->w13_shared, hs, status, ss, true, tiled));
@@ -438,18 +438,21 @@ moe_status_t layer_forward(const moe_layer_desc* d, const void* x, void* out, vo
         MOE_TRY(launch_permute_rows(xq, (size_t)H, row_idx, T, k, exq, s));
         MOE_TRY(launch_permute_rows(xs, (size_t)ldx * 4, row_idx, T, k, exs, s));
     } else {
-        MOE_TRY(launch_permute_rows(x, (size_t)H * dt_size(dt), row_idx, T, k, ex, s));
+        // beside the shared experts' GEMM: two copy blocks per SM (measured on dsv3_prefill: the
+        // shared branch 329 -> 312 us; the copy itself unchanged at ~112 us, still off the critical path)
+        MOE_TRY(launch_permute_rows(x, (size_t)H * dt_size(dt), row_idx, T, k, ex, s, side ? 2 : 16));
     }
     MOE_TRY(mark(ev, ST_PERMUTE, 1, s));
     // join: the routed GEMMs need every SM, so they start after the shared experts
     if (side) MOE_CUDA_TRY(cudaStreamWaitEvent(s, side->join, 0));
     MOE_TRY(mark(ev, ST_UP, 0, s));
     if (fp8)
-        MOE_TRY(ffn_up_fp8(exq, exs, ldx, offsets, E, R, H, I, d->w13, d->w13_scales, nullptr, hq, hqs, status, s, pow2));
+        MOE_TRY(ffn_up_fp8(exq, exs, ldx, offsets, E, R, H, I, d->w13, d->w13_scales, nullptr, hq, hqs, status, s, pow2,
+                           tiled));
     else MOE_TRY(ffn_up(ex, dt, offsets, E, R, H, I, d->w13, h, status, s, false, tiled));
     MOE_TRY(mark(ev, ST_UP, 1, s));
     MOE_TRY(mark(ev, ST_DOWN, 0, s));
-    if (fp8) MOE_TRY(ffn_down_fp8(hq, hqs, offsets, E, R, H, I, d->w2, d->w2_scales, y, status, s, pow2));
+    if (fp8) MOE_TRY(ffn_down_fp8(hq, hqs, offsets, E, R, H, I, d->w2, d->w2_scales, y, status, s, pow2, tiled));
     else MOE_TRY(ffn_down(h, dt, offsets, E, R, H, I, d->w2, y, status, s, false, tiled));
     MOE_TRY(mark(ev, ST_DOWN, 1, s));
     MOE_TRY(mark(ev, ST_FINALIZE, 0, s));

@@ -53,8 +53,10 @@ size_t init_routing_scratch_bytes(int T, int E, int k);
 moe_status_t launch_init_routing_index(const int32_t* ids, int R, int E, int32_t* counts,
                                        int32_t* offsets, int32_t* row_idx, int32_t* scratch,
                                        uint32_t* status, cudaStream_t s);
+// blocks_per_sm: grid = SMs x this (16 saturates HBM alone; the layer takes 2 when the
+// shared experts' GEMM runs beside the copy, so fewer copy warps compete for its issue slots)
 moe_status_t launch_permute_rows(const void* x, size_t row_bytes, const int32_t* row_idx, int T, int k,
-                                 void* expanded_x, cudaStream_t s);
+                                 void* expanded_x, cudaStream_t s, int blocks_per_sm = 16);
 // The tiled weight layout of the tensor-core GEMMs' B operand: [G][ceil(n/256)][ceil(row_bytes/128)][256][128 B]
 // (each 256-row x 128-byte box one contiguous 32 KB block), zero-padded.
 size_t tiled_weight_bytes(int G, int n_rows, int row_bytes);
@@ -152,6 +154,7 @@ struct TcFp8GroupedGemm {
     // SwiGLU epilogue quantises h with power-of-two scales too.  Every scale of A
     // and B must then be a power of two (its exponent is what is used).
     bool pow2 = false;
+    bool b_tiled = false;     // B codes in the tiled layout (tiled_weight_bytes(G, Nb, K))
 };
 moe_status_t launch_tc_fp8_grouped_gemm(const TcFp8GroupedGemm& g, cudaStream_t s);
 int tc_packed_block();        // rows of gate (and of up) per packed block: 128

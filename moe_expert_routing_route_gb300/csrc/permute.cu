@@ -269,10 +269,10 @@ moe_status_t launch_init_routing_index(const int32_t* ids, int R, int E, int32_t
 }
 
 moe_status_t launch_permute_rows(const void* x, size_t row_bytes, const int32_t* row_idx, int T, int k,
-                                 void* expanded_x, cudaStream_t s) {
+                                 void* expanded_x, cudaStream_t s, int blocks_per_sm) {
     if (T == 0) return MOE_OK;
     const int nvec = (int)(row_bytes / 16);
-    const int grid = (int)std::min<int64_t>(T, (int64_t)sm_count() * 16);
+    const int grid = (int)std::min<int64_t>(T, (int64_t)sm_count() * std::max(1, blocks_per_sm));
     permute_rows_kernel<<<grid, kCopyThreads, 0, s>>>(static_cast<const uint4*>(x), nvec, row_idx, T, k,
                                                       T * k, static_cast<uint4*>(expanded_x));
     note_launch();

@@ -154,19 +154,21 @@ def _check_fp8_layer(oracle, cfg, d, layer, out, tokens=None):
     return res
 
 
-def _make(cfg):
+def _make(cfg, layout=None):
     d = inputs.make_layer(cfg, DEV)
     layer = binding.MoELayer(T=cfg.T, k=cfg.k, w_router=d["wg"], w_gate=d["w_gate"], w_up=d["w_up"], w2=d["w2"],
                              s_gate=d["s_gate"] if cfg.S else None, s_up=d["s_up"] if cfg.S else None,
                              s2=d["s2"] if cfg.S else None, expert_bias=d["bias"], renormalize=cfg.renormalize,
                              n_group=cfg.n_group, topk_group=cfg.topk_group, group_rule=cfg.group_rule,
-                             weight_format=cfg.weight_format)
+                             weight_format=cfg.weight_format, weight_layout=layout)
     return d, layer
 
 
+@pytest.mark.parametrize("layout", ["tiled", "rows"])
 @pytest.mark.parametrize("cfg", FP8_LAYERS, ids=[c.name for c in FP8_LAYERS])
-def test_layer_fp8_small(oracle, cfg):
-    d, layer = _make(cfg)
+def test_layer_fp8_small(oracle, cfg, layout):
+    """FP8 layers with the expert codes in the tiled layout (the default) and row-major."""
+    d, layer = _make(cfg, layout)
     out = layer.forward(d["x"])
     _check_fp8_layer(oracle, cfg, d, layer, out)
     # deterministic: a second forward gives the same bits
