@@ -438,6 +438,17 @@ moe_status_t moe_layer_forward(const moe_layer_desc* desc, const void* x, void* 
 moe_status_t moe_layer_forward_timed(const moe_layer_desc* desc, const void* x, void* out, void* ws,
                                      size_t ws_bytes, moe_stream_t stream, void* const* stage_events);
 
+/* SMs that moe_layer_forward gives the shared experts' GEMMs (persistent CTAs,
+ * in pairs) for the whole of the routed up projection, which takes the other
+ * SMs, so that the shared experts run beside it and only the routed down
+ * projection waits for them.  0 (the default) when the shared experts instead
+ * take every SM beside the routing steps and both routed GEMMs wait for them.
+ * The environment variable MOE_SHARED_SMS = n asks for the split (n rounded up
+ * to a pair; granted for bf16 layers with native weights and S > 0 when n is at
+ * most a quarter of the SMs).  The results are the same bits either way.
+ * Reads the current device's SM count; -1 for a NULL desc. */
+int moe_layer_shared_expert_sms(const moe_layer_desc* desc);
+
 /* The layer through expert-parallel Double-Routing with W virtual ranks on
  * one GPU ([CANN §MoE deployment], steps 1-8): rank p owns tokens
  * [p*T/W, (p+1)*T/W) and experts [p*E/W, (p+1)*E/W); init-routing runs per

@@ -81,6 +81,7 @@ SIGNATURES = {
     "moe_layer_workspace_field": (I32, [_DP, I32, ctypes.POINTER(SZ), ctypes.POINTER(SZ)]),
     "moe_layer_forward": (I32, [_DP, P, P, P, SZ, P]),
     "moe_layer_forward_timed": (I32, [_DP, P, P, P, SZ, P, ctypes.POINTER(P)]),
+    "moe_layer_shared_expert_sms": (I32, [_DP]),
     "moe_layer_forward_host": (I32, [_DP, P, P, P, SZ, P]),
 }
 
@@ -491,6 +492,10 @@ class MoELayer:
                       recv_start=((W + 1,), torch.int32), expert_offsets=((self.E + 1,), torch.int32))
         shape, dtype = shapes[name]
         return raw.view(dtype).view(shape)
+
+    def shared_expert_sms(self) -> int:
+        """SMs the shared experts' GEMMs take beside the routed up projection (0: no split)."""
+        return int(lib().moe_layer_shared_expert_sms(ctypes.byref(self.desc)))
 
     def device_status(self, stream=None) -> int:
         return moe_check_device_status(self.ws, stream)

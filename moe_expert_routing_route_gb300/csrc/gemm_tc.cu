@@ -736,7 +736,8 @@ moe_status_t launch_impl(const TcGroupedGemm& g, cudaStream_t s) {
     p.status = g.status;
 
     const int64_t max_tiles = (int64_t)p.NT * p.ksplit * (ceil_div(g.M, BM) + (g.offsets ? g.G : 0));
-    const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(sm_count(), max_tiles));
+    const int ctas = g.max_ctas > 0 ? std::min(g.max_ctas, sm_count()) : sm_count();
+    const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(ctas, max_tiles));
     tc_grouped_gemm_kernel<BN, EPI><<<grid, kThreads, Cf::SMEM, s>>>(ma, mb, mc, p);
     note_launch();
     return last_launch_status();
@@ -806,7 +807,8 @@ moe_status_t launch_pair_impl(const TcGroupedGemm& g, cudaStream_t s) {
     p.status = g.status;
 
     const int64_t max_tiles = (int64_t)p.NT * (ceil_div(g.M, BM2) + (g.offsets ? g.G : 0));
-    const int pairs = (int)std::max<int64_t>(1, std::min<int64_t>(pairs_max, max_tiles));
+    const int pair_cap = g.max_ctas > 0 ? std::min(pairs_max, std::max(1, g.max_ctas / 2)) : pairs_max;
+    const int pairs = (int)std::max<int64_t>(1, std::min<int64_t>(pair_cap, max_tiles));
     cfg.gridDim = dim3(2 * pairs);
     MOE_CUDA_TRY(cudaLaunchKernelEx(&cfg, tc_pair_gemm_kernel<EPI, STAGES, MAXG>, ma, mb, p));
     note_launch();

@@ -12,6 +12,7 @@
 
 #include <atomic>
 #include <climits>
+#include <cstdlib>
 #include <mutex>
 
 namespace moe {
@@ -46,14 +47,16 @@ int packed_rows(int I) { return 2 * (int)round_up((size_t)I, (size_t)tc_packed_b
 // fp32 on the FFMA pipes.  offsets == nullptr means one dense group of `rows`.
 // headroom: leave shared memory on every SM for kernels running beside this one
 // tiled: the weight is in the tiled layout (bf16 only)
+// max_ctas: persistent grid cap (bf16; 0 = every SM)
 moe_status_t ffn_up(const void* a, moe_dtype_t dt, const int32_t* offsets, int G, int rows, int H, int I,
                     const void* w13p, void* h, uint32_t* status, cudaStream_t s, bool headroom = false,
-                    bool tiled = false) {
+                    bool tiled = false, int max_ctas = 0) {
     if (rows == 0) return MOE_OK;
     if (dt == MOE_BF16) {
         TcGroupedGemm up{a, rows, H, offsets, G, w13p, packed_rows(I), I, h, I, TC_EPI_SWIGLU, status};
         up.smem_headroom = headroom;
         up.b_tiled = tiled;
+        up.max_ctas = max_ctas;
         return launch_tc_grouped_gemm(up, s);
     }
     if (tiled) return MOE_ERR_UNSUPPORTED;
@@ -64,12 +67,13 @@ moe_status_t ffn_up(const void* a, moe_dtype_t dt, const int32_t* offsets, int G
 
 moe_status_t ffn_down(const void* h, moe_dtype_t dt, const int32_t* offsets, int G, int rows, int H, int I,
                       const void* w2, void* y, uint32_t* status, cudaStream_t s, bool headroom = false,
-                      bool tiled = false) {
+                      bool tiled = false, int max_ctas = 0) {
     if (rows == 0) return MOE_OK;
     if (dt == MOE_BF16) {
         TcGroupedGemm down{h, rows, I, offsets, G, w2, H, H, y, H, TC_EPI_BF16, status};
         down.smem_headroom = headroom;
         down.b_tiled = tiled;
+        down.max_ctas = max_ctas;
         return launch_tc_grouped_gemm(down, s);
     }
     if (tiled) return MOE_ERR_UNSUPPORTED;
@@ -217,6 +221,21 @@ moe_status_t check_desc(const moe_layer_desc* d) {
         !aligned16(d->w13_shared) || !aligned16(d->w2_shared))
         return MOE_ERR_UNSUPPORTED;
     return MOE_OK;
+}
+
+// Shared experts on a fixed share of the SMs beside the routed up projection: with
+// MOE_SHARED_SMS = n (rounded up to whole CTA pairs, at most a quarter of the SMs) their GEMMs take n
+// persistent CTAs, the routed up projection the other SMs, and only the routed down projection waits
+// for them.  By default (0) they take every SM beside the routing steps and both routed GEMMs wait.
+// Measured on the DeepSeek-V3 prefill layer (4096 tokens, 128 rows per expert) the split loses: the
+// routed up projection slows in proportion to the SMs it gives up (2344 us on 148 SMs, 2635 on 132,
+// 2659 on 126; each SM's TMA pipeline, not HBM alone, sets its rate), more than the ~125 us the
+// shared experts add beside the routing steps.
+int shared_expert_ctas(const moe_layer_desc& d) {
+    if (d.S <= 0 || d.dtype != MOE_BF16 || d.weight_format != MOE_WEIGHTS_NATIVE || d.T <= 0) return 0;
+    const char* e = std::getenv("MOE_SHARED_SMS");
+    const int n = ((e ? std::atoi(e) : 0) + 1) & ~1;  // whole CTA pairs
+    return n > 0 && n <= sm_count() / 4 ? n : 0;
 }
 
 template <typename T>
@@ -399,6 +418,7 @@ moe_status_t layer_forward(const moe_layer_desc* d, const void* x, void* out, vo
     // fork: the shared experts need x alone (FP8: its codes), so they branch off
     // before the gate; the gate is enqueued first and starts first
     const bool fork = side && !chunked_shared;
+    const int shared_ctas = fork && !fp8 ? shared_expert_ctas(*d) : 0;  // > 0: beside the routed up projection
     if (fork) MOE_CUDA_TRY(cudaEventRecord(side->fork, s));
     int nsplit = 1;
     MOE_TRY(layer_gate(*d, x, logits, &nsplit, s));
@@ -417,8 +437,8 @@ moe_status_t layer_forward(const moe_layer_desc* d, const void* x, void* out, vo
                                  pow2, tiled));
         } else {
             // the routing kernels (histogram and scatter use shared memory) run beside them
-            MOE_TRY(ffn_up(x, dt, nullptr, 1, T, H, SI, d->w13_shared, hs, status, ss, true, tiled));
-            MOE_TRY(ffn_down(hs, dt, nullptr, 1, T, H, SI, d->w2_shared, ys, status, ss, true, tiled));
+            MOE_TRY(ffn_up(x, dt, nullptr, 1, T, H, SI, d->w13_shared, hs, status, ss, true, tiled, shared_ctas));
+            MOE_TRY(ffn_down(hs, dt, nullptr, 1, T, H, SI, d->w2_shared, ys, status, ss, true, tiled, shared_ctas));
         }
         MOE_TRY(mark(ev, ST_SHARED, 1, ss));
         MOE_CUDA_TRY(cudaEventRecord(side->join, ss));
@@ -438,19 +458,23 @@ moe_status_t layer_forward(const moe_layer_desc* d, const void* x, void* out, vo
         MOE_TRY(launch_permute_rows(xq, (size_t)H, row_idx, T, k, exq, s));
         MOE_TRY(launch_permute_rows(xs, (size_t)ldx * 4, row_idx, T, k, exs, s));
     } else {
-        // beside the shared experts' GEMM: two copy blocks per SM (measured on dsv3_prefill: the
-        // shared branch 329 -> 312 us; the copy itself unchanged at ~112 us, still off the critical path)
-        MOE_TRY(launch_permute_rows(x, (size_t)H * dt_size(dt), row_idx, T, k, ex, s, side ? 2 : 16));
+        // beside the shared experts' GEMM on every SM: two copy blocks per SM (measured on dsv3_prefill:
+        // the shared branch 329 -> 312 us; the copy itself unchanged at ~112 us, still off the critical
+        // path); beside it on a share of the SMs, eight
+        MOE_TRY(launch_permute_rows(x, (size_t)H * dt_size(dt), row_idx, T, k, ex, s,
+                                    !side ? 16 : (shared_ctas ? 8 : 2)));
     }
     MOE_TRY(mark(ev, ST_PERMUTE, 1, s));
-    // join: the routed GEMMs need every SM, so they start after the shared experts
-    if (side) MOE_CUDA_TRY(cudaStreamWaitEvent(s, side->join, 0));
+    // join: GEMMs on every SM start after the shared experts; with the SMs split, only the down projection
+    if (side && !shared_ctas) MOE_CUDA_TRY(cudaStreamWaitEvent(s, side->join, 0));
     MOE_TRY(mark(ev, ST_UP, 0, s));
     if (fp8)
         MOE_TRY(ffn_up_fp8(exq, exs, ldx, offsets, E, R, H, I, d->w13, d->w13_scales, nullptr, hq, hqs, status, s, pow2,
                            tiled));
-    else MOE_TRY(ffn_up(ex, dt, offsets, E, R, H, I, d->w13, h, status, s, false, tiled));
+    else MOE_TRY(ffn_up(ex, dt, offsets, E, R, H, I, d->w13, h, status, s, false, tiled,
+                        shared_ctas ? sm_count() - shared_ctas : 0));
     MOE_TRY(mark(ev, ST_UP, 1, s));
+    if (side && shared_ctas) MOE_CUDA_TRY(cudaStreamWaitEvent(s, side->join, 0));
     MOE_TRY(mark(ev, ST_DOWN, 0, s));
     if (fp8) MOE_TRY(ffn_down_fp8(hq, hqs, offsets, E, R, H, I, d->w2, d->w2_scales, y, status, s, pow2, tiled));
     else MOE_TRY(ffn_down(h, dt, offsets, E, R, H, I, d->w2, y, status, s, false, tiled));
@@ -879,6 +903,11 @@ const char* moe_stage_name(int stage) {
     static const char* names[MOE_NUM_STAGES] = {"gate",   "route", "init_routing", "permute_rows",
                                                 "shared", "up",    "down",         "finalize"};
     return (stage >= 0 && stage < MOE_NUM_STAGES) ? names[stage] : "";
+}
+
+int moe_layer_shared_expert_sms(const moe_layer_desc* desc) {
+    if (!desc) return -1;
+    return shared_expert_ctas(*desc);
 }
 
 size_t moe_layer_workspace_bytes(const moe_layer_desc* desc) {

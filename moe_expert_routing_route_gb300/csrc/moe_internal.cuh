@@ -125,6 +125,7 @@ struct TcGroupedGemm {
     bool smem_headroom = false;   // pair tiles: take the 6-stage ring, leaving ~24 KB of shared memory per SM
                                   // for kernels of other streams (the 7-stage ring leaves under 1 KB)
     bool b_tiled = false;         // B in the tiled layout (tiled_weight_bytes(G, Nb, 2K)); bf16/SwiGLU epilogues only
+    int max_ctas = 0;             // persistent grid cap (0: one CTA per SM), leaving SMs to other streams' kernels
 };
 moe_status_t launch_tc_grouped_gemm(const TcGroupedGemm& g, cudaStream_t s);
 int tc_gate_splits(int M, int N, int K, int max_split);  // K slices the fp32 launch will use

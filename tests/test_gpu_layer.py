@@ -158,6 +158,41 @@ def test_layer_prefill_slice_every_token(oracle, monkeypatch, prefill_slice, til
     assert res["compared"] >= cfg.T - max(1, cfg.T // 100)
 
 
+def test_layer_prefill_slice_shared_experts_beside_up(oracle, monkeypatch, prefill_slice):
+    """Full-K experts, 128 rows per expert: the shared experts on 22 SMs beside the routed
+    up projection give the bits of running them first on every SM (the default)."""
+    cfg, d, n, ref = prefill_slice
+    layer = binding.MoELayer(T=cfg.T, k=cfg.k, w_router=d["wg"], w_gate=d["w_gate"], w_up=d["w_up"], w2=d["w2"],
+                             s_gate=d["s_gate"], s_up=d["s_up"], s2=d["s2"], expert_bias=None,
+                             renormalize=cfg.renormalize)
+    assert layer.shared_expert_sms() == 0
+    whole = layer.forward(d["x"])
+    monkeypatch.setenv("MOE_SHARED_SMS", "22")
+    assert layer.shared_expert_sms() == 22
+    split = layer.forward(d["x"])
+    assert torch.equal(split, whole)
+    check_layer(oracle, cfg, d, layer, split, n=n, ref=ref)
+
+
+SPLIT = [c for c in SMALL if c.dtype == "bf16" and c.S > 0 and c.name in ("small_bf16", "ragged_bf16", "zipf_bf16",
+                                                                           "one_token_bf16", "grouped_bf16")]
+
+
+@pytest.mark.parametrize("cfg", SPLIT, ids=[c.name for c in SPLIT])
+def test_layer_shared_experts_on_a_share_of_the_sms(oracle, monkeypatch, cfg):
+    """Forcing the split (four SMs for the shared experts, the routed down projection
+    joining them) gives the bits of the unsplit layer, and the oracle's results."""
+    d, layer = make(cfg)
+    monkeypatch.setenv("MOE_SHARED_SMS", "0")
+    assert layer.shared_expert_sms() == 0
+    whole = layer.forward(d["x"])
+    monkeypatch.setenv("MOE_SHARED_SMS", "3")  # rounded up to two pairs
+    assert layer.shared_expert_sms() == 4
+    split = layer.forward(d["x"])
+    assert torch.equal(split, whole)
+    check_layer(oracle, cfg, d, layer, split)
+
+
 def test_layer_deterministic_and_graph_capturable(oracle):
     cfg = inputs.LayerConfig("graph_bf16", T=384, H=512, E=64, k=6, I=256, S=1, dtype="bf16", seed=21)
     d, layer = make(cfg)
@@ -178,6 +213,31 @@ def test_layer_deterministic_and_graph_capturable(oracle):
     graph.replay()
     torch.cuda.synchronize()
     assert torch.equal(static_out, out1)
+
+
+def test_layer_split_shared_experts_graph_capturable(oracle, monkeypatch):
+    """The split schedule (fork before the gate, join before the routed down projection)
+    captured into a CUDA graph replays the eager bits."""
+    monkeypatch.setenv("MOE_SHARED_SMS", "4")
+    cfg = inputs.LayerConfig("graph_split_bf16", T=384, H=512, E=64, k=6, I=256, S=1, dtype="bf16", seed=29)
+    d, layer = make(cfg)
+    assert layer.shared_expert_sms() == 4
+    x = d["x"]
+    eager = layer.forward(x)
+    static_out = torch.empty_like(x)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        layer.forward(x, out=static_out, stream=s)
+    torch.cuda.current_stream().wait_stream(s)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        layer.forward(x, out=static_out)
+    static_out.zero_()
+    graph.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(static_out, eager)
+    check_layer(oracle, cfg, d, layer, eager)
     # new input through the same graph
     x.copy_(inputs.random_rows(cfg.T, cfg.H, torch.bfloat16, seed=99, tag="x").to(DEV))
     graph.replay()
