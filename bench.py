@@ -158,6 +158,40 @@ def measured_traffic(stage: str, workload: str):
     return None
 
 
+def routing_ops_alone(layer, x, cfg, costs, peaks, steps, stream) -> dict:
+    """The routing ops each by itself on the GPU, on this batch's own routing (the layer's
+    workspace after its last forward): moe_init_routing (histogram, scan, stable scatter and
+    the expanded_x row gather) and moe_finalize_routing (weighted combine plus the shared
+    expert's rows).  CUDA events around `steps` calls on the launching stream after one
+    warm-up call; each call writes or reads more than L2 holds at the full sizes.  Bytes are
+    the algorithmic ones of roofline.stage_costs, against the measured HBM bandwidth."""
+    from moe_expert_routing_route_gb300 import binding
+    ids = layer.field("topk_ids").clone()
+    w = layer.field("topk_w").clone()
+    row_idx = layer.field("expanded_row_idx").clone()
+    y = layer.field("y_routed").clone()
+    ys = layer.field("y_shared").clone() if cfg.S else None
+    ws = torch.empty(binding.lib().moe_init_routing_workspace_bytes(cfg.T, cfg.E, cfg.k), dtype=torch.uint8,
+                     device=x.device)
+    calls = dict(init_routing=lambda: binding.moe_init_routing(x, ids, cfg.E, stream=stream, ws=ws),
+                 finalize=lambda: binding.moe_finalize_routing(y, w, row_idx, skip=ys, stream=stream))
+    nbytes = dict(init_routing=costs["init_routing"][1] + costs["permute_rows"][1], finalize=costs["finalize"][1])
+    res = {}
+    for name, call in calls.items():
+        call()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        a.record(stream)
+        for _ in range(steps):
+            call()
+        b.record(stream)
+        torch.cuda.synchronize()
+        us = a.elapsed_time(b) / steps * 1e3
+        gbs = nbytes[name] / (us / 1e6) / 1e9
+        res[name] = dict(us=round(us, 2), gbs=round(gbs, 1), frac=round(gbs / peaks["hbm_gbs"], 3))
+    return res
+
+
 # ---- the CPU oracle on a bounded sample ----
 
 def sample_tokens(cfg, n: int, offset: int = 0) -> np.ndarray:
@@ -354,6 +388,7 @@ def run_ours(args, world, rank, local):
     e2e_s = (time.perf_counter() - t0) / args.steps
     e2e_s = max_over_ranks(e2e_s, world)
     nbytes_io = x.numel() * x.element_size()
+    routing_ops = routing_ops_alone(layer, x, cfg, costs, peaks, args.steps, stream)
 
     cpu = None
     if world == 1 and rank == 0 and not args.no_cpu_baseline and not fp8:
@@ -377,7 +412,7 @@ def run_ours(args, world, rank, local):
                     roofline=rl, cpu_baseline=cpu,
                     e2e=dict(value=tokens / e2e_s, unit=UNIT, h2d_bytes_per_step=nbytes_io,
                              d2h_bytes_per_step=nbytes_io),
-                    gpu_launches=int(launches), clocks=clk, stages=stages,
+                    gpu_launches=int(launches), clocks=clk, stages=stages, routing_ops_alone=routing_ops,
                     grouped_gemm=dict(tflops=round(gemm_fl / (gemm_ms / 1e3) / 1e12, 1),
                                       frac_of_bf16_peak=round(gemm_fl / (gemm_ms / 1e3) / 1e12 /
                                                               peaks["bf16_tflops_sustained"], 3)),

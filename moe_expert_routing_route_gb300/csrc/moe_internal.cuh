@@ -7,6 +7,7 @@
 #include <cstdint>
 #include <cstddef>
 #include <algorithm>
+#include <utility>
 
 #include "moe.h"
 
@@ -28,6 +29,26 @@ int sm_count();                        // SMs of the current device (cached per 
         if ((expr) != cudaSuccess) return MOE_ERR_CUDA; \
     } while (0)
 
+// Programmatic dependent launch: the kernel may be scheduled while the previous kernel on the
+// stream is still running; it must call pdl_wait() before reading anything that work earlier on
+// the stream wrote (that wait covers the previous grid's completion and, through its own wait,
+// everything before it).  With no running predecessor kernel this is an ordinary launch.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                       Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 inline size_t round_up(size_t a, size_t b) { return (a + b - 1) / b * b; }
@@ -37,6 +58,11 @@ inline size_t dt_size(moe_dtype_t dt) { return dt == MOE_BF16 ? 2 : 4; }
 __device__ __forceinline__ void set_status(uint32_t* status, uint32_t bit) {
     if (status) atomicOr(status, bit);
 }
+// The dependent grid (launched with launch_pdl) may be scheduled once every CTA of this grid has
+// called this or exited; it still waits in pdl_wait() for this grid to complete.
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+// Waits until the preceding grid on the stream has completed and its writes are visible.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 // ---- launchers (stream-ordered, no host sync) ------------------------------------
 // route.cu

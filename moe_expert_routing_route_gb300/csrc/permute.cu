@@ -7,14 +7,18 @@
 // higher throughput with multi-node DeepSeek deployment" (Perplexity blog),
 // §MoE Router: dense dispatch needs the routing aggregated per expert.
 //
-// The sort is a stable counting sort in three small kernels plus one copy:
+// The sort is a stable counting sort in two small kernels plus one copy, chained
+// with programmatic dependent launch (each kernel's blocks are resident and
+// waiting when the previous kernel finishes):
 //   hist    one block per chunk of kChunk source rows -> per-chunk histogram
 //           hist[c][e] (chunk-major: coalesced writes)
-//   scan    one block: tokens_per_expert, expert_offsets and, for every
-//           (chunk, expert), the first destination row of that chunk's copies
-//   scatter one block per chunk; each warp ranks its 128 rows in source order
+//   scatter one block per chunk.  Each block first derives from the histograms
+//           what a scan would give it: every expert's total (block 0 writes
+//           tokens_per_expert and expert_offsets, the exclusive scan of the
+//           totals) and the first destination row of this chunk's copies per
+//           expert.  Then each warp ranks its 128 rows in source order
 //           (__match_any_sync groups the lanes with the same expert, the rank
-//           inside the group keeps source order), then the warps' per-expert
+//           inside the group keeps source order), and the warps' per-expert
 //           counts are prefix-summed in warp order: stable overall
 //   copy    x is read once (16-byte vectors) and each row is written to its
 //           k destinations (HBM-bound: T*H*b read + T*k*H*b written)
@@ -34,6 +38,8 @@ hist_kernel(const int32_t* __restrict__ ids, int R, int E, int NW, int32_t* __re
             uint32_t* status) {
     extern __shared__ int32_t sh[];  // [E]
     const int c = blockIdx.x;
+    pdl_trigger();
+    pdl_wait();  // ids come from the routing kernel
     for (int e = threadIdx.x; e < E; e += kChunkThreads) sh[e] = 0;
     __syncthreads();
     const int beg = c * kChunk, end = min(R, beg + kChunk);
@@ -48,69 +54,68 @@ hist_kernel(const int32_t* __restrict__ ids, int R, int E, int NW, int32_t* __re
     for (int e = threadIdx.x; e < E; e += kChunkThreads) hist[(size_t)c * E + e] = sh[e];
 }
 
-// 256 threads: small enough in registers and threads to run beside a resident
-// tensor-core GEMM CTA (the shared experts run concurrently on another stream).
-constexpr int kScanThreads = 256;
-
-__global__ void __launch_bounds__(kScanThreads)
-scan_kernel(int32_t* __restrict__ hist, int NW, int E, int32_t* __restrict__ counts,
-            int32_t* __restrict__ offsets) {
-    __shared__ int cnt[1024];
-    __shared__ int warp_tot[kScanThreads / 32];
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    // per-expert totals over the chunks (coalesced across experts)
-    for (int e = tid; e < E; e += kScanThreads) {
-        int sum = 0;
-        for (int c = 0; c < NW; ++c) sum += hist[(size_t)c * E + e];
-        cnt[e] = sum;
-        counts[e] = sum;
-    }
-    __syncthreads();
-    // exclusive scan over experts: 4 consecutive experts per thread, then across threads
-    const int e0 = tid * 4;
-    int loc[4], run = 0;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        loc[i] = run;
-        run += e0 + i < E ? cnt[e0 + i] : 0;
-    }
-    int incl = run;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-        const int n = __shfl_up_sync(0xffffffffu, incl, off);
-        if (lane >= off) incl += n;
-    }
-    if (lane == 31) warp_tot[warp] = incl;
-    __syncthreads();
-    int wbase = 0;
-    for (int w = 0; w < warp; ++w) wbase += warp_tot[w];
-    const int tbase = wbase + incl - run;
-    __syncthreads();
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-        if (e0 + i < E) cnt[e0 + i] = tbase + loc[i];
-    if (tid == kScanThreads - 1) offsets[E] = tbase + run;
-    __syncthreads();
-    // first destination row of every (chunk, expert), in chunk order inside an expert
-    for (int e = tid; e < E; e += kScanThreads) {
-        offsets[e] = cnt[e];
-        int r = cnt[e];
-        for (int c = 0; c < NW; ++c) {
-            const size_t i = (size_t)c * E + e;
-            const int v = hist[i];
-            hist[i] = r;
-            r += v;
-        }
-    }
-}
-
+// 256 threads, E <= 1024 (4 experts per thread in the scan); small enough to run beside a
+// resident tensor-core GEMM CTA (the shared experts run concurrently on another stream).
 __global__ void __launch_bounds__(kChunkThreads)
-scatter_kernel(const int32_t* __restrict__ ids, int R, int E, int NW, const int32_t* __restrict__ base,
-               int32_t* __restrict__ row_idx) {
-    extern __shared__ int32_t sh[];  // [kChunkWarps][E]: per-warp counts, then per-warp first rows
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+scatter_kernel(const int32_t* __restrict__ ids, int R, int E, int NW, const int32_t* __restrict__ hist,
+               int32_t* __restrict__ counts, int32_t* __restrict__ offsets, int32_t* __restrict__ row_idx) {
+    // [kChunkWarps][E]: per-warp counts, then per-warp first rows; [E] expert totals, then this
+    // chunk's first rows; [E] the counts of the chunks before this one
+    extern __shared__ int32_t sh[];
+    __shared__ int warp_tot[kChunkWarps];
+    int32_t* cfirst = sh + kChunkWarps * E;
+    int32_t* before = cfirst + E;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int c = blockIdx.x;
-    for (int i = threadIdx.x; i < kChunkWarps * E; i += kChunkThreads) sh[i] = 0;
+    pdl_trigger();
+    pdl_wait();  // the histograms (and, through the histogram kernel's own wait, the ids)
+    for (int i = tid; i < kChunkWarps * E; i += kChunkThreads) sh[i] = 0;
+    // every expert's total over the chunks, and its count in the chunks before this one
+    for (int e = tid; e < E; e += kChunkThreads) {
+        int tot = 0, pre = 0;
+        for (int q = 0; q < NW; ++q) {
+            const int v = hist[(size_t)q * E + e];
+            tot += v;
+            pre += q < c ? v : 0;
+        }
+        cfirst[e] = tot;
+        before[e] = pre;
+    }
+    __syncthreads();
+    // exclusive scan of the totals over experts: 4 consecutive experts per thread, then across threads
+    {
+        const int e0 = tid * 4;
+        int loc[4], run = 0;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            loc[i] = run;
+            run += e0 + i < E ? cfirst[e0 + i] : 0;
+        }
+        int incl = run;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int n = __shfl_up_sync(0xffffffffu, incl, off);
+            if (lane >= off) incl += n;
+        }
+        if (lane == 31) warp_tot[warp] = incl;
+        __syncthreads();
+        int wbase = 0;
+        for (int w = 0; w < warp; ++w) wbase += warp_tot[w];
+        const int tbase = wbase + incl - run;
+        if (c == 0) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                if (e0 + i < E) {
+                    counts[e0 + i] = cfirst[e0 + i];
+                    offsets[e0 + i] = tbase + loc[i];
+                }
+            if (tid == kChunkThreads - 1) offsets[E] = tbase + run;
+        }
+        __syncthreads();  // every total read before any is overwritten
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            if (e0 + i < E) cfirst[e0 + i] = tbase + loc[i] + before[e0 + i];
+    }
     const int beg = c * kChunk + warp * kRowsPerWarp, end = min(R, c * kChunk + kChunk);
     int id[kSteps], rank[kSteps];
 #pragma unroll
@@ -136,7 +141,7 @@ scatter_kernel(const int32_t* __restrict__ ids, int R, int E, int NW, const int3
     __syncthreads();
     // per expert: the chunk's first row plus the counts of the earlier warps
     for (int e = threadIdx.x; e < E; e += kChunkThreads) {
-        int run = base[(size_t)c * E + e];
+        int run = cfirst[e];
         for (int w = 0; w < kChunkWarps; ++w) {
             const int v = sh[w * E + e];
             sh[w * E + e] = run;
@@ -158,6 +163,8 @@ __global__ void __launch_bounds__(kCopyThreads)
 permute_rows_kernel(const uint4* __restrict__ x, int nvec, const int32_t* __restrict__ row_idx, int T,
                     int k, int R, uint4* __restrict__ out) {
     __shared__ int dst[32];
+    pdl_trigger();
+    pdl_wait();  // row_idx comes from the scatter kernel
     for (int t = blockIdx.x; t < T; t += gridDim.x) {
         if (threadIdx.x < k) {
             const int d = row_idx[(size_t)t * k + threadIdx.x];
@@ -251,20 +258,18 @@ size_t init_routing_scratch_bytes(int T, int E, int k) {
 moe_status_t launch_init_routing_index(const int32_t* ids, int R, int E, int32_t* counts, int32_t* offsets,
                                        int32_t* row_idx, int32_t* scratch, uint32_t* status, cudaStream_t s) {
     const int NW = (int)ceil_div(R, kChunk);
-    if (NW > 0) {
-        hist_kernel<<<NW, kChunkThreads, (size_t)E * sizeof(int32_t), s>>>(ids, R, E, NW, scratch, status);
-        note_launch();
-        MOE_TRY(last_launch_status());
+    if (NW == 0) {  // no rows: every expert empty
+        MOE_CUDA_TRY(cudaMemsetAsync(counts, 0, (size_t)E * sizeof(int32_t), s));
+        MOE_CUDA_TRY(cudaMemsetAsync(offsets, 0, (size_t)(E + 1) * sizeof(int32_t), s));
+        return MOE_OK;
     }
-    scan_kernel<<<1, kScanThreads, 0, s>>>(scratch, NW, E, counts, offsets);
+    MOE_CUDA_TRY(launch_pdl(hist_kernel, dim3(NW), dim3(kChunkThreads), (size_t)E * sizeof(int32_t), s, ids, R, E,
+                            NW, scratch, status));
     note_launch();
-    MOE_TRY(last_launch_status());
-    if (NW > 0) {
-        scatter_kernel<<<NW, kChunkThreads, (size_t)kChunkWarps * E * sizeof(int32_t), s>>>(ids, R, E, NW, scratch,
-                                                                                              row_idx);
-        note_launch();
-        MOE_TRY(last_launch_status());
-    }
+    MOE_CUDA_TRY(launch_pdl(scatter_kernel, dim3(NW), dim3(kChunkThreads),
+                            (size_t)(kChunkWarps + 2) * E * sizeof(int32_t), s, ids, R, E, NW,
+                            static_cast<const int32_t*>(scratch), counts, offsets, row_idx));
+    note_launch();
     return MOE_OK;
 }
 
@@ -273,10 +278,11 @@ moe_status_t launch_permute_rows(const void* x, size_t row_bytes, const int32_t*
     if (T == 0) return MOE_OK;
     const int nvec = (int)(row_bytes / 16);
     const int grid = (int)std::min<int64_t>(T, (int64_t)sm_count() * std::max(1, blocks_per_sm));
-    permute_rows_kernel<<<grid, kCopyThreads, 0, s>>>(static_cast<const uint4*>(x), nvec, row_idx, T, k,
-                                                      T * k, static_cast<uint4*>(expanded_x));
+    MOE_CUDA_TRY(launch_pdl(permute_rows_kernel, dim3(grid), dim3(kCopyThreads), 0, s,
+                            static_cast<const uint4*>(x), nvec, row_idx, T, k, T * k,
+                            static_cast<uint4*>(expanded_x)));
     note_launch();
-    return last_launch_status();
+    return MOE_OK;
 }
 
 moe_status_t launch_pack_w13(const void* w_gate, const void* w_up, size_t esize, int E, int H, int I,

@@ -61,6 +61,8 @@ route_topk_kernel(const float* logits, const float* __restrict__ bias, int T, in
     extern __shared__ float sh_scores[];  // [kWarps][E], grouped routing only
     const int lane = threadIdx.x & 31;
     const int t = blockIdx.x * kWarps + (threadIdx.x >> 5);
+    pdl_trigger();  // the init-routing histogram may be scheduled; it waits for these ids
+    pdl_wait();     // the logits come from the gate GEMM
     if (t >= T) return;  // whole warp leaves together
     const float* row = logits + (size_t)t * E;
 
@@ -187,8 +189,8 @@ cudaError_t launch(const float* logits, const float* bias, int T, int E, int k, 
                    int nsplit, int32_t* ids, float* w, cudaStream_t s) {
     const int blocks = (int)ceil_div(T, kWarps);
     const size_t smem = grp.n_group > 1 ? (size_t)kWarps * E * sizeof(float) : 0;
-    route_topk_kernel<VPL><<<blocks, kWarps * 32, smem, s>>>(logits, bias, T, E, k, grp, renorm, nsplit, ids, w);
-    return cudaGetLastError();
+    return launch_pdl(route_topk_kernel<VPL>, dim3(blocks), dim3(kWarps * 32), smem, s, logits, bias, T, E, k, grp,
+                      renorm, nsplit, ids, w);
 }
 
 }  // namespace
