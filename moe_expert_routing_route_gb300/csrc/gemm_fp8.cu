@@ -217,6 +217,8 @@ tc_fp8_grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __gri
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int G = p.G, NT = p.NT, KB = p.KB;
 
+    pdl_trigger();  // launched after another kernel: the next one may be scheduled
+    pdl_wait();     // before any read of what earlier work on the stream wrote
     for (int g = threadIdx.x; g < G; g += kThreads) {
         int a = 0, b = p.M;
         if (p.offsets) {
@@ -675,9 +677,15 @@ moe_status_t launch_impl(const TcFp8GroupedGemm& g, cudaStream_t s) {
     p.status = g.status;
     const int64_t max_tiles = (int64_t)p.NT * (ceil_div(g.M, BM) + (g.offsets ? g.G : 0));
     const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(sm_count(), max_tiles));
-    tc_fp8_grouped_gemm_kernel<EPI, MX><<<grid, kThreads, Plan<EPI>::SMEM, s>>>(ma, mb, mc, p);
+    if (g.pdl) {
+        MOE_CUDA_TRY(launch_pdl(tc_fp8_grouped_gemm_kernel<EPI, MX>, dim3(grid), dim3(kThreads), Plan<EPI>::SMEM, s,
+                                ma, mb, mc, p));
+    } else {
+        tc_fp8_grouped_gemm_kernel<EPI, MX><<<grid, kThreads, Plan<EPI>::SMEM, s>>>(ma, mb, mc, p);
+        MOE_CUDA_TRY(cudaGetLastError());
+    }
     note_launch();
-    return last_launch_status();
+    return MOE_OK;
 }
 
 }  // namespace

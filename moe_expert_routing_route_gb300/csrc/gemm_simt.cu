@@ -30,6 +30,8 @@ simt_grouped_kernel(const float* __restrict__ A, int M, int K, const int32_t* __
     __shared__ float Bs[BK][BN + 4];
     __shared__ float Us[SWIGLU ? BK : 1][BN + 4];
     __shared__ int sh_g, sh_r0, sh_r1;
+    pdl_trigger();  // launched after another kernel: the next one may be scheduled
+    pdl_wait();     // before any read of what earlier work on the stream wrote
 
     if (threadIdx.x == 0) {
         // slot blockIdx.y -> (group, row tile) from the device-side offsets
@@ -134,28 +136,40 @@ moe_status_t launch_simt_gate(const float* x, const float* wr, int T, int H, int
                               cudaStream_t s) {
     if (T == 0) return MOE_OK;
     dim3 grid((unsigned)ceil_div(E, BN), (unsigned)row_slots(T, 1, false));
-    simt_grouped_kernel<false><<<grid, 256, 0, s>>>(x, T, H, nullptr, 1, wr, E, E, logits, E, nullptr);
+    MOE_CUDA_TRY(launch_pdl(simt_grouped_kernel<false>, grid, dim3(256), 0, s, x, T, H, nullptr, 1, wr, E, E, logits,
+                            (int64_t)E, nullptr));
     note_launch();
-    return last_launch_status();
+    return MOE_OK;
 }
 
 moe_status_t launch_simt_grouped_ffn_up(const float* a, int M, int H, const int32_t* offsets, int G,
                                         const float* w13_packed, int Ip, int I, float* h, uint32_t* status,
-                                        cudaStream_t s) {
+                                        cudaStream_t s, bool pdl) {
     if (M == 0) return MOE_OK;
     dim3 grid((unsigned)ceil_div(I, BN), (unsigned)row_slots(M, G, offsets != nullptr));
-    simt_grouped_kernel<true><<<grid, 256, 0, s>>>(a, M, H, offsets, G, w13_packed, 2 * Ip, I, h, I, status);
+    if (pdl)
+        MOE_CUDA_TRY(launch_pdl(simt_grouped_kernel<true>, grid, dim3(256), 0, s, a, M, H, offsets, G, w13_packed,
+                                2 * Ip, I, h, (int64_t)I, status));
+    else
+        simt_grouped_kernel<true><<<grid, 256, 0, s>>>(a, M, H, offsets, G, w13_packed, 2 * Ip, I, h, I, status);
+    MOE_CUDA_TRY(cudaGetLastError());
     note_launch();
-    return last_launch_status();
+    return MOE_OK;
 }
 
 moe_status_t launch_simt_grouped_down(const float* h, int M, int I, const int32_t* offsets, int G,
-                                      const float* w2, int H, float* y, uint32_t* status, cudaStream_t s) {
+                                      const float* w2, int H, float* y, uint32_t* status, cudaStream_t s,
+                                      bool pdl) {
     if (M == 0) return MOE_OK;
     dim3 grid((unsigned)ceil_div(H, BN), (unsigned)row_slots(M, G, offsets != nullptr));
-    simt_grouped_kernel<false><<<grid, 256, 0, s>>>(h, M, I, offsets, G, w2, H, H, y, H, status);
+    if (pdl)
+        MOE_CUDA_TRY(launch_pdl(simt_grouped_kernel<false>, grid, dim3(256), 0, s, h, M, I, offsets, G, w2, H, H, y,
+                                (int64_t)H, status));
+    else
+        simt_grouped_kernel<false><<<grid, 256, 0, s>>>(h, M, I, offsets, G, w2, H, H, y, H, status);
+    MOE_CUDA_TRY(cudaGetLastError());
     note_launch();
-    return last_launch_status();
+    return MOE_OK;
 }
 
 }  // namespace moe

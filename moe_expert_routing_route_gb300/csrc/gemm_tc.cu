@@ -184,6 +184,11 @@ tc_grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_co
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int G = p.G, NT = p.NT;
 
+    // Launched after another kernel, the next one may be scheduled now, except after the gate: its
+    // follower (top-k) placed early would compete for SMs with the shared experts' GEMM on the other
+    // stream.
+    if constexpr (EPI != TC_EPI_F32) pdl_trigger();
+    pdl_wait();  // before any read of what earlier work on the stream wrote
     // ---- group table from the device-side offsets ----
     for (int g = threadIdx.x; g < G; g += kThreads) {
         int a = 0, b = p.M;
@@ -487,6 +492,8 @@ tc_pair_gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_const
         b = p.offsets ? __ldg(p.offsets + g + 1) : p.M;
     };
 
+    pdl_trigger();  // launched after another kernel: the next one may be scheduled
+    pdl_wait();     // before any read of what earlier work on the stream wrote
     if (threadIdx.x == 0) *abort_flag = 0;
     if (warp == 0) {
         int run = 0;
@@ -738,9 +745,15 @@ moe_status_t launch_impl(const TcGroupedGemm& g, cudaStream_t s) {
     const int64_t max_tiles = (int64_t)p.NT * p.ksplit * (ceil_div(g.M, BM) + (g.offsets ? g.G : 0));
     const int ctas = g.max_ctas > 0 ? std::min(g.max_ctas, sm_count()) : sm_count();
     const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(ctas, max_tiles));
-    tc_grouped_gemm_kernel<BN, EPI><<<grid, kThreads, Cf::SMEM, s>>>(ma, mb, mc, p);
+    if (g.pdl) {
+        MOE_CUDA_TRY(launch_pdl(tc_grouped_gemm_kernel<BN, EPI>, dim3(grid), dim3(kThreads), Cf::SMEM, s, ma, mb, mc,
+                                p));
+    } else {
+        tc_grouped_gemm_kernel<BN, EPI><<<grid, kThreads, Cf::SMEM, s>>>(ma, mb, mc, p);
+        MOE_CUDA_TRY(cudaGetLastError());
+    }
     note_launch();
-    return last_launch_status();
+    return MOE_OK;
 }
 
 template <int EPI, int STAGES, int MAXG>
@@ -753,11 +766,13 @@ moe_status_t launch_pair_impl(const TcGroupedGemm& g, cudaStream_t s) {
     cudaError_t attr_err = cudaSuccess;
 
     cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // as launch_pdl, when g.pdl
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = Cf::SMEM;
     cfg.stream = s;
@@ -810,6 +825,7 @@ moe_status_t launch_pair_impl(const TcGroupedGemm& g, cudaStream_t s) {
     const int pair_cap = g.max_ctas > 0 ? std::min(pairs_max, std::max(1, g.max_ctas / 2)) : pairs_max;
     const int pairs = (int)std::max<int64_t>(1, std::min<int64_t>(pair_cap, max_tiles));
     cfg.gridDim = dim3(2 * pairs);
+    cfg.numAttrs = g.pdl ? 2 : 1;  // the occupancy query above takes the cluster shape alone
     MOE_CUDA_TRY(cudaLaunchKernelEx(&cfg, tc_pair_gemm_kernel<EPI, STAGES, MAXG>, ma, mb, p));
     note_launch();
     return last_launch_status();

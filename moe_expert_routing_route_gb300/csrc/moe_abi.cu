@@ -48,37 +48,42 @@ int packed_rows(int I) { return 2 * (int)round_up((size_t)I, (size_t)tc_packed_b
 // headroom: leave shared memory on every SM for kernels running beside this one
 // tiled: the weight is in the tiled layout (bf16 only)
 // max_ctas: persistent grid cap (bf16; 0 = every SM)
+// pdl: programmatic dependent launch; false on the second stream, where a follower placed early
+// holds SMs that the first stream's routing kernels need (measured: mid_bf16 0.566 -> 0.542 ms,
+// dsv3_prefill 3.986 -> 3.965 ms without it there)
 moe_status_t ffn_up(const void* a, moe_dtype_t dt, const int32_t* offsets, int G, int rows, int H, int I,
                     const void* w13p, void* h, uint32_t* status, cudaStream_t s, bool headroom = false,
-                    bool tiled = false, int max_ctas = 0) {
+                    bool tiled = false, int max_ctas = 0, bool pdl = true) {
     if (rows == 0) return MOE_OK;
     if (dt == MOE_BF16) {
         TcGroupedGemm up{a, rows, H, offsets, G, w13p, packed_rows(I), I, h, I, TC_EPI_SWIGLU, status};
         up.smem_headroom = headroom;
         up.b_tiled = tiled;
         up.max_ctas = max_ctas;
+        up.pdl = pdl;
         return launch_tc_grouped_gemm(up, s);
     }
     if (tiled) return MOE_ERR_UNSUPPORTED;
     return launch_simt_grouped_ffn_up(static_cast<const float*>(a), rows, H, offsets, G,
                                       static_cast<const float*>(w13p), packed_rows(I) / 2, I, static_cast<float*>(h),
-                                      status, s);
+                                      status, s, pdl);
 }
 
 moe_status_t ffn_down(const void* h, moe_dtype_t dt, const int32_t* offsets, int G, int rows, int H, int I,
                       const void* w2, void* y, uint32_t* status, cudaStream_t s, bool headroom = false,
-                      bool tiled = false, int max_ctas = 0) {
+                      bool tiled = false, int max_ctas = 0, bool pdl = true) {
     if (rows == 0) return MOE_OK;
     if (dt == MOE_BF16) {
         TcGroupedGemm down{h, rows, I, offsets, G, w2, H, H, y, H, TC_EPI_BF16, status};
         down.smem_headroom = headroom;
         down.b_tiled = tiled;
         down.max_ctas = max_ctas;
+        down.pdl = pdl;
         return launch_tc_grouped_gemm(down, s);
     }
     if (tiled) return MOE_ERR_UNSUPPORTED;
     return launch_simt_grouped_down(static_cast<const float*>(h), rows, I, offsets, G, static_cast<const float*>(w2),
-                                    H, static_cast<float*>(y), status, s);
+                                    H, static_cast<float*>(y), status, s, pdl);
 }
 
 // FP8 halves: the up projection (SwiGLU into bf16 h) followed by the 1x128
@@ -89,21 +94,21 @@ int scale_ld(int cols) { return (int)round_up((size_t)ceil_div(cols, 128), 4); }
 // pow2: power-of-two scales throughout (block-scaled tensor-core MMAs).
 moe_status_t ffn_up_fp8(const uint8_t* aq, const float* as, int lda_s, const int32_t* offsets, int G, int rows, int H,
                         int I, const void* w13q, const float* w13s, void* h, uint8_t* hq, float* hs,
-                        uint32_t* status, cudaStream_t s, bool pow2, bool tiled = false) {
+                        uint32_t* status, cudaStream_t s, bool pow2, bool tiled = false, bool pdl = true) {
     if (rows == 0) return MOE_OK;
     // the SwiGLU epilogue writes the down projection's FP8 input directly; bf16 h
     // is stored too only when the caller gives a buffer for it (h may be null)
     TcFp8GroupedGemm up{aq, rows, H, offsets, G, w13q, packed_rows(I), I, h, I, TC_EPI_SWIGLU, as, lda_s,
-                        w13s, status, hq, hs, scale_ld(I), pow2, tiled};
+                        w13s, status, hq, hs, scale_ld(I), pow2, tiled, pdl};
     return launch_tc_fp8_grouped_gemm(up, s);
 }
 
 moe_status_t ffn_down_fp8(const uint8_t* hq, const float* hs, const int32_t* offsets, int G, int rows, int H, int I,
                           const void* w2q, const float* w2s, void* y, uint32_t* status, cudaStream_t s, bool pow2,
-                          bool tiled = false) {
+                          bool tiled = false, bool pdl = true) {
     if (rows == 0) return MOE_OK;
     TcFp8GroupedGemm down{hq, rows, I, offsets, G, w2q, H, H, y, H, TC_EPI_BF16, hs, scale_ld(I), w2s, status,
-                          nullptr, nullptr, 0, pow2, tiled};
+                          nullptr, nullptr, 0, pow2, tiled, pdl};
     return launch_tc_fp8_grouped_gemm(down, s);
 }
 
@@ -405,8 +410,10 @@ moe_status_t layer_forward(const moe_layer_desc* d, const void* x, void* out, vo
                 const char* xc = static_cast<const char*>(x) + (size_t)c0 * row_bytes;
                 char* hsc = static_cast<char*>(hs) + (size_t)c0 * SI * dt_size(dt);
                 char* ysc = static_cast<char*>(ys) + (size_t)c0 * row_bytes;
-                MOE_TRY(ffn_up(xc, dt, nullptr, 1, c1 - c0, H, SI, d->w13_shared, hsc, status, ss, false, tiled));
-                MOE_TRY(ffn_down(hsc, dt, nullptr, 1, c1 - c0, H, SI, d->w2_shared, ysc, status, ss, false, tiled));
+                MOE_TRY(ffn_up(xc, dt, nullptr, 1, c1 - c0, H, SI, d->w13_shared, hsc, status, ss, false, tiled, 0,
+                               false));
+                MOE_TRY(ffn_down(hsc, dt, nullptr, 1, c1 - c0, H, SI, d->w2_shared, ysc, status, ss, false, tiled, 0,
+                                 false));
             }
             MOE_TRY(mark(ev, ST_SHARED, 1, ss));
             MOE_CUDA_TRY(cudaEventRecord(side->join, ss));
@@ -432,13 +439,15 @@ moe_status_t layer_forward(const moe_layer_desc* d, const void* x, void* out, vo
         MOE_TRY(mark(ev, ST_SHARED, 0, ss));
         if (fp8) {
             MOE_TRY(ffn_up_fp8(xq, xs, ldx, nullptr, 1, T, H, SI, d->w13_shared, d->w13_shared_scales, nullptr, hsq, hss,
-                               status, ss, pow2, tiled));
+                               status, ss, pow2, tiled, false));
             MOE_TRY(ffn_down_fp8(hsq, hss, nullptr, 1, T, H, SI, d->w2_shared, d->w2_shared_scales, ys, status, ss,
-                                 pow2, tiled));
+                                 pow2, tiled, false));
         } else {
             // the routing kernels (histogram and scatter use shared memory) run beside them
-            MOE_TRY(ffn_up(x, dt, nullptr, 1, T, H, SI, d->w13_shared, hs, status, ss, true, tiled, shared_ctas));
-            MOE_TRY(ffn_down(hs, dt, nullptr, 1, T, H, SI, d->w2_shared, ys, status, ss, true, tiled, shared_ctas));
+            MOE_TRY(ffn_up(x, dt, nullptr, 1, T, H, SI, d->w13_shared, hs, status, ss, true, tiled, shared_ctas,
+                           false));
+            MOE_TRY(ffn_down(hs, dt, nullptr, 1, T, H, SI, d->w2_shared, ys, status, ss, true, tiled, shared_ctas,
+                             false));
         }
         MOE_TRY(mark(ev, ST_SHARED, 1, ss));
         MOE_CUDA_TRY(cudaEventRecord(side->join, ss));
@@ -569,8 +578,9 @@ moe_status_t layer_forward_ep(const moe_layer_desc* d, int W, const void* x, voi
     MOE_TRY(layer_gate(*d, x, logits, &nsplit, s));
     if (side) {
         MOE_CUDA_TRY(cudaStreamWaitEvent(side->stream, side->fork, 0));
-        MOE_TRY(ffn_up(x, dt, nullptr, 1, T, H, SI, d->w13_shared, hs, status, side->stream, false, tiled));
-        MOE_TRY(ffn_down(hs, dt, nullptr, 1, T, H, SI, d->w2_shared, ys, status, side->stream, false, tiled));
+        MOE_TRY(ffn_up(x, dt, nullptr, 1, T, H, SI, d->w13_shared, hs, status, side->stream, false, tiled, 0, false));
+        MOE_TRY(ffn_down(hs, dt, nullptr, 1, T, H, SI, d->w2_shared, ys, status, side->stream, false, tiled, 0,
+                         false));
         MOE_CUDA_TRY(cudaEventRecord(side->join, side->stream));
     }
     MOE_TRY(launch_route_topk(logits, d->expert_bias, T, E, k, d->renormalize, ids, w, s, d->n_group, d->topk_group,

@@ -152,6 +152,8 @@ struct TcGroupedGemm {
                                   // for kernels of other streams (the 7-stage ring leaves under 1 KB)
     bool b_tiled = false;         // B in the tiled layout (tiled_weight_bytes(G, Nb, 2K)); bf16/SwiGLU epilogues only
     int max_ctas = 0;             // persistent grid cap (0: one CTA per SM), leaving SMs to other streams' kernels
+    bool pdl = true;              // programmatic dependent launch (false for kernels on the second stream, whose
+                                  // followers placed early hold SMs the first stream's kernels need)
 };
 moe_status_t launch_tc_grouped_gemm(const TcGroupedGemm& g, cudaStream_t s);
 int tc_gate_splits(int M, int N, int K, int max_split);  // K slices the fp32 launch will use
@@ -182,6 +184,7 @@ struct TcFp8GroupedGemm {
     // and B must then be a power of two (its exponent is what is used).
     bool pow2 = false;
     bool b_tiled = false;     // B codes in the tiled layout (tiled_weight_bytes(G, Nb, K))
+    bool pdl = true;          // programmatic dependent launch (as TcGroupedGemm::pdl)
 };
 moe_status_t launch_tc_fp8_grouped_gemm(const TcFp8GroupedGemm& g, cudaStream_t s);
 int tc_packed_block();        // rows of gate (and of up) per packed block: 128
@@ -189,11 +192,12 @@ int tc_packed_block();        // rows of gate (and of up) per packed block: 128
 // gemm_simt.cu: fp32 (FFMA) GEMMs of the same shapes.
 moe_status_t launch_simt_gate(const float* x, const float* wr, int T, int H, int E, float* logits,
                               cudaStream_t s);
+// pdl: programmatic dependent launch (as TcGroupedGemm::pdl)
 moe_status_t launch_simt_grouped_ffn_up(const float* a, int M, int H, const int32_t* offsets, int G,
                                         const float* w13_packed, int Ip, int I, float* h,
-                                        uint32_t* status, cudaStream_t s);
+                                        uint32_t* status, cudaStream_t s, bool pdl = true);
 moe_status_t launch_simt_grouped_down(const float* h, int M, int I, const int32_t* offsets, int G,
                                       const float* w2, int H, float* y, uint32_t* status,
-                                      cudaStream_t s);
+                                      cudaStream_t s, bool pdl = true);
 
 }  // namespace moe

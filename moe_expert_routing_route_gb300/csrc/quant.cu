@@ -43,6 +43,9 @@ quantize_rows_kernel(const T* __restrict__ a, int64_t rows, int cols, int kb, in
                      uint8_t* __restrict__ codes, float* __restrict__ scales, bool pow2) {
     const int lane = threadIdx.x & 31, hl = lane & 15;
     const int kb2 = (kb + 1) / 2;  // block pairs per row
+    pdl_trigger();  // launched after another kernel: the next one may be scheduled
+    pdl_wait();     // before any read of what earlier work on the stream wrote
+
     const bool vec = (cols & 7) == 0;
     const int64_t nw = (int64_t)gridDim.x * (blockDim.x / 32);
     for (int64_t item = (int64_t)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5); item < rows * kb2;
@@ -120,13 +123,13 @@ moe_status_t launch_quantize_rows_fp8(const void* a, moe_dtype_t dt, int64_t row
     const int64_t items = rows * ((kb + 1) / 2);  // one warp per pair of blocks
     const int grid = (int)std::min<int64_t>(ceil_div(items, 8), (int64_t)sm_count() * 16);
     if (dt == MOE_BF16)
-        quantize_rows_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(a), rows, cols, kb,
-                                                                 ld_scales, codes, scales, pow2);
+        MOE_CUDA_TRY(launch_pdl(quantize_rows_kernel<__nv_bfloat16>, dim3(grid), dim3(256), 0, s,
+                                static_cast<const __nv_bfloat16*>(a), rows, cols, kb, ld_scales, codes, scales, pow2));
     else
-        quantize_rows_kernel<float><<<grid, 256, 0, s>>>(static_cast<const float*>(a), rows, cols, kb, ld_scales,
-                                                         codes, scales, pow2);
+        MOE_CUDA_TRY(launch_pdl(quantize_rows_kernel<float>, dim3(grid), dim3(256), 0, s, static_cast<const float*>(a),
+                                rows, cols, kb, ld_scales, codes, scales, pow2));
     note_launch();
-    return last_launch_status();
+    return MOE_OK;
 }
 
 moe_status_t launch_quantize_tiles_fp8(const void* w, moe_dtype_t dt, int G, int rows, int cols, uint8_t* codes,
