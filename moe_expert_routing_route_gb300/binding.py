@@ -447,11 +447,11 @@ class MoELayer:
                                          self.ws.numel(), _stream(stream))
         else:
             if len(events) != 2 * MOE_NUM_STAGES:
-                raise ValueError(f"{2 * MOE_NUM_STAGES} events expected (start, end per stage)")
+                raise ValueError(f"{2 * MOE_NUM_STAGES} events expected (start, end per stage; None skips one)")
             for e in events:  # torch creates the CUDA event on its first record
-                if e.cuda_event == 0:
+                if e is not None and e.cuda_event == 0:
                     e.record()
-            arr = (P * (2 * MOE_NUM_STAGES))(*[ctypes.c_void_p(e.cuda_event) for e in events])
+            arr = (P * (2 * MOE_NUM_STAGES))(*[ctypes.c_void_p(0 if e is None else e.cuda_event) for e in events])
             st = lib().moe_layer_forward_timed(ctypes.byref(self.desc), _ptr(x), _ptr(out), _ptr(self.ws),
                                                self.ws.numel(), _stream(stream), arr)
         _check(st, "moe_layer_forward")

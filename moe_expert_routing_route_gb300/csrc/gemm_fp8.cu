@@ -217,8 +217,10 @@ tc_fp8_grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __gri
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int G = p.G, NT = p.NT, KB = p.KB;
 
-    pdl_trigger();  // launched after another kernel: the next one may be scheduled
-    pdl_wait();     // before any read of what earlier work on the stream wrote
+    // launched after another kernel; only the up projection lets its follower be scheduled early
+    // (as in the bf16 kernels: the down projection's follower would wait beside it and slow it)
+    if constexpr (EPI == TC_EPI_SWIGLU) pdl_trigger();
+    pdl_wait();  // before any read of what earlier work on the stream wrote
     for (int g = threadIdx.x; g < G; g += kThreads) {
         int a = 0, b = p.M;
         if (p.offsets) {

@@ -184,10 +184,12 @@ tc_grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_co
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int G = p.G, NT = p.NT;
 
-    // Launched after another kernel, the next one may be scheduled now, except after the gate: its
-    // follower (top-k) placed early would compete for SMs with the shared experts' GEMM on the other
-    // stream.
-    if constexpr (EPI != TC_EPI_F32) pdl_trigger();
+    // Launched after another kernel.  Only the up projection lets its follower (the down projection,
+    // which cannot share an SM with it anyway) be scheduled early: the gate's follower (top-k) placed
+    // early competes for SMs with the shared experts' GEMM on the other stream, and the down
+    // projection's (finalize) waits beside it and slows it (DeepSeek-V3 prefill layer: 4.006 ->
+    // 3.978 ms with the down projection releasing nothing early; as a CUDA graph 4.061 -> 4.018).
+    if constexpr (EPI == TC_EPI_SWIGLU) pdl_trigger();
     pdl_wait();  // before any read of what earlier work on the stream wrote
     // ---- group table from the device-side offsets ----
     for (int g = threadIdx.x; g < G; g += kThreads) {
@@ -492,8 +494,8 @@ tc_pair_gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_const
         b = p.offsets ? __ldg(p.offsets + g + 1) : p.M;
     };
 
-    pdl_trigger();  // launched after another kernel: the next one may be scheduled
-    pdl_wait();     // before any read of what earlier work on the stream wrote
+    if constexpr (EPI == TC_EPI_SWIGLU) pdl_trigger();  // as in the single-CTA kernel
+    pdl_wait();  // before any read of what earlier work on the stream wrote
     if (threadIdx.x == 0) *abort_flag = 0;
     if (warp == 0) {
         int run = 0;

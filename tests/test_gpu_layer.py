@@ -292,3 +292,10 @@ def test_layer_stage_events():
     assert evs[2 * gate].elapsed_time(evs[2 * sh]) >= 0
     assert evs[2 * sh + 1].elapsed_time(evs[2 * up]) >= 0
     assert torch.equal(out, layer.forward(d["x"]))
+    # events for some stages only (the benchmark's timed region): the others are skipped
+    dn = names.index("down")
+    part = [e if i // 2 in (up, dn) else None for i, e in enumerate(evs)]
+    assert torch.equal(layer.forward(d["x"], events=part), out)
+    torch.cuda.synchronize()
+    assert part[2 * up].elapsed_time(part[2 * up + 1]) >= 0
+    assert part[2 * up + 1].elapsed_time(part[2 * dn]) >= 0
