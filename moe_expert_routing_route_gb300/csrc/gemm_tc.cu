@@ -78,6 +78,13 @@ struct Params {
     void* C;
     int64_t ldc;
     uint32_t* status;
+    // TC_EPI_FFN, phase 2 (the down projection of phase 1's output C): its tiles follow phase 1's
+    // total1; a tile of m-block m waits until sync[m] == sync_target (every phase-1 tile of the
+    // m-block counted once per epilogue warp of both CTAs)
+    int total1, NT2, KB2, Nb2, N2, b_nt2, sync_target;
+    void* C2;
+    int64_t ldc2;
+    int* sync;
 };
 
 // tile -> (group, m-tile, n-tile, K slice).  prefix[g] = first tile of group g,
@@ -460,11 +467,13 @@ static_assert(Cfg2<6, 1024>::SMEM <= 232448, "pair-tile stages exceed shared mem
 template <int EPI, int STAGES_, int MAXG_>
 __global__ void __launch_bounds__(kThreads, 1)
 tc_pair_gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
+                    const __grid_constant__ CUtensorMap mapA2, const __grid_constant__ CUtensorMap mapB2,
                     const __grid_constant__ Params p) {
     using Cf = Cfg2<STAGES_, MAXG_>;
     constexpr int STAGES = Cf::STAGES;
     constexpr uint32_t IDESC = idesc_bf16(BM2, BN2);
     static_assert(EPI != TC_EPI_F32, "fp32 outputs use the single-CTA kernel");
+    constexpr bool FFN = EPI == TC_EPI_FFN;  // phase 1 SwiGLU into C, phase 2 bf16 into C2 (mapA2, mapB2)
 
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_u32(smem_raw);
@@ -492,6 +501,21 @@ tc_pair_gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_const
     auto seg = [&](int g, int& a, int& b) {
         a = p.offsets ? __ldg(p.offsets + g) : 0;
         b = p.offsets ? __ldg(p.offsets + g + 1) : p.M;
+    };
+    // tile -> (phase, group, m-tile, n-tile).  Two-phase launches (one group) order each phase
+    // m-tile by m-tile, n fastest, so that the rows of an m-tile are finished early in phase 1
+    auto decode = [&](int tile, int& phs, int& g, int& m, int& n) {
+        if constexpr (FFN) {
+            g = 0;
+            phs = tile >= p.total1 ? 1 : 0;
+            const int t = phs ? tile - p.total1 : tile, nt = phs ? p.NT2 : p.NT;
+            m = t / nt;
+            n = t - m * nt;
+        } else {
+            int ks;
+            phs = 0;
+            decode_tile(tile, prefix, G, NT, 1, g, m, n, ks);
+        }
     };
 
     if constexpr (EPI == TC_EPI_SWIGLU) pdl_trigger();  // as in the single-CTA kernel
@@ -540,7 +564,7 @@ tc_pair_gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_const
     cluster_sync_all();  // the peer's barriers exist before anything signals them
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
-    const int total = prefix[G];
+    const int total = FFN ? p.total1 + p.total1 / NT * p.NT2 : prefix[G];
     const int KB = (p.K + BK - 1) / BK;
 
     if (warp == 0) {
@@ -550,26 +574,48 @@ tc_pair_gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_const
             uint32_t ph = 0, issued = 0, issued_par = 0;
             bool ok = true;
             for (int tile = pair; ok && tile < total; tile += npairs) {
-                int g, m, n, ks;
-                decode_tile(tile, prefix, G, NT, 1, g, m, n, ks);
+                int phs, g, m, n;
+                decode(tile, phs, g, m, n);
                 int ga, gb;
                 seg(g, ga, gb);
+                const CUtensorMap* mA = phs ? &mapA2 : &mapA;
+                const CUtensorMap* mB = phs ? &mapB2 : &mapB;
+                const int kbn = phs ? p.KB2 : KB;
                 const int row0 = ga + m * BM2 + (int)rank * 128;
-                const int brow = g * p.Nb + n * BN2 + (int)rank * (BN2 / 2);
-                const int tbase = (g * p.b_nt + n) * KB;  // tiled B: this tile's first 256-row box
-                for (int kb = 0; kb < KB; ++kb) {
+                const int brow = g * (phs ? p.Nb2 : p.Nb) + n * BN2 + (int)rank * (BN2 / 2);
+                const int tbase = (g * (phs ? p.b_nt2 : p.b_nt) + n) * kbn;  // tiled B: the tile's first box
+                if (FFN && phs) {
+                    // phase 2 reads the rows phase 1 wrote: wait until every phase-1 tile of this
+                    // m-tile is stored (bounded), then order that view before the TMA reads
+                    const uint64_t t0 = globaltimer();
+                    while (ld_acquire_gpu(p.sync + m) < p.sync_target) {
+                        if (*abort_flag) {
+                            ok = false;
+                            break;
+                        }
+                        if (globaltimer() - t0 > kWaitLimitNs) {
+                            *abort_flag = 1;
+                            set_status(p.status, MOE_DEVERR_TIMEOUT);
+                            ok = false;
+                            break;
+                        }
+                    }
+                    if (!ok) break;
+                    fence_proxy_async_global();
+                }
+                for (int kb = 0; kb < kbn; ++kb) {
                     if (!wait_phase(empty_bar(s), ph ^ 1u, abort_flag, p.status)) {
                         ok = false;
                         break;
                     }
                     if (leader) mbar_arrive_expect_tx(full_bar(s), 2 * Cf::STAGE_BYTES);
                     const uint32_t fb = mapa_shared(full_bar(s), 0);  // the leader's full[s]
-                    tma_load_2d_pair(smem_u32(sA + s * Cf::A_BYTES), &mapA, fb, kb * BK, row0);
+                    tma_load_2d_pair(smem_u32(sA + s * Cf::A_BYTES), mA, fb, kb * BK, row0);
                     if (p.b_tiled)  // this CTA's half of a contiguous 256-row box
-                        tma_load_2d_pair(smem_u32(sB + s * Cf::B_BYTES), &mapB, fb, 0,
+                        tma_load_2d_pair(smem_u32(sB + s * Cf::B_BYTES), mB, fb, 0,
                                          (tbase + kb) * BN2 + (int)rank * (BN2 / 2));
                     else
-                        tma_load_2d_pair(smem_u32(sB + s * Cf::B_BYTES), &mapB, fb, kb * BK, brow);
+                        tma_load_2d_pair(smem_u32(sB + s * Cf::B_BYTES), mB, fb, kb * BK, brow);
                     issued |= 1u << s;
                     issued_par = (issued_par & ~(1u << s)) | (ph << s);
                     if (++s == STAGES) {
@@ -596,10 +642,11 @@ tc_pair_gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_const
             uint32_t ph = 0, aph = 0;
             bool ok = true;
             for (int tile = pair; ok && tile < total; tile += npairs) {
+                const int kbn = FFN && tile >= p.total1 ? p.KB2 : KB;
                 if (!wait_phase(tempty_bar(acc), aph ^ 1u, abort_flag, p.status)) break;
                 tc_fence_after();
                 const uint32_t d = tmem_base + (uint32_t)(acc * BN2);
-                for (int kb = 0; kb < KB; ++kb) {
+                for (int kb = 0; kb < kbn; ++kb) {
                     if (!wait_phase(full_bar(s), ph, abort_flag, p.status)) {
                         ok = false;
                         break;
@@ -633,8 +680,8 @@ tc_pair_gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_const
         int acc = 0;
         uint32_t aph = 0;
         for (int tile = pair; tile < total; tile += npairs) {
-            int g, m, n, ks;
-            decode_tile(tile, prefix, G, NT, 1, g, m, n, ks);
+            int phs, g, m, n;
+            decode(tile, phs, g, m, n);
             int ga, gb;
             seg(g, ga, gb);
             const int64_t row = (int64_t)ga + (int64_t)m * BM2 + (int64_t)rank * 128 + r;
@@ -642,7 +689,7 @@ tc_pair_gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_const
             if (!__all_sync(0xffffffffu, wait_phase(tfull_bar(acc), aph, abort_flag, p.status))) break;
             tc_fence_after();
             const uint32_t taddr = tmem_base + ((uint32_t)(eg * 32) << 16) + (uint32_t)(acc * BN2);
-            if (EPI == TC_EPI_SWIGLU) {
+            if (EPI == TC_EPI_SWIGLU || (FFN && !phs)) {
 #pragma unroll 1
                 for (int c = 0; c < kPackBlock; c += 32) {
                     uint32_t gr[32], ur[32];
@@ -654,9 +701,19 @@ tc_pair_gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_const
                         const float gv = __uint_as_float(gr[i]);
                         h[i] = gv / (1.0f + __expf(-gv)) * __uint_as_float(ur[i]);
                     }
-                    if (valid) store_row32<EPI>(p.C, p.ldc, row, n * kPackBlock + c, p.N, h);
+                    if (valid) store_row32<TC_EPI_SWIGLU>(p.C, p.ldc, row, n * kPackBlock + c, p.N, h);
+                }
+                if (FFN) {
+                    // count this warp's rows of the m-tile as stored (every lane's stores are
+                    // visible GPU-wide before the count; phase 2 acquires it)
+                    __threadfence();
+                    __syncwarp();
+                    if (lane == 0) atomicAdd(p.sync + m, 1);
                 }
             } else {
+                void* C = FFN ? p.C2 : p.C;
+                const int64_t ldc = FFN ? p.ldc2 : p.ldc;
+                const int N = FFN ? p.N2 : p.N;
 #pragma unroll 1
                 for (int c = 0; c < BN2; c += 32) {
                     uint32_t vr[32];
@@ -664,7 +721,7 @@ tc_pair_gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_const
                     float v[32];
 #pragma unroll
                     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(vr[i]);
-                    if (valid) store_row32<EPI>(p.C, p.ldc, row, n * BN2 + c, p.N, v);
+                    if (valid) store_row32<TC_EPI_BF16>(C, ldc, row, n * BN2 + c, N, v);
                 }
             }
             tc_fence_before();
@@ -727,7 +784,7 @@ moe_status_t launch_impl(const TcGroupedGemm& g, cudaStream_t s) {
                        make_store_map_bf16(&mc, g.C, (uint64_t)g.N, (uint64_t)g.M, (uint64_t)g.ldc, 32);
     if (!c_tma) mc = ma;  // never read
 
-    Params p;
+    Params p{};
     p.offsets = g.offsets;
     p.G = g.G;
     p.M = g.M;
@@ -758,9 +815,15 @@ moe_status_t launch_impl(const TcGroupedGemm& g, cudaStream_t s) {
     return MOE_OK;
 }
 
+// g2, sync: TC_EPI_FFN only (g the up projection, g2 the down projection of its output)
 template <int EPI, int STAGES, int MAXG>
-moe_status_t launch_pair_impl(const TcGroupedGemm& g, cudaStream_t s) {
+moe_status_t launch_pair_impl(const TcGroupedGemm& g, cudaStream_t s, const TcGroupedGemm* g2 = nullptr,
+                              int* sync = nullptr) {
     using Cf = Cfg2<STAGES, MAXG>;
+    constexpr bool FFN = EPI == TC_EPI_FFN;
+    if (FFN != (g2 != nullptr) || (FFN && (!sync || g.G != 1 || g.offsets || g2->G != 1 || g2->offsets ||
+                                           g2->b_tiled != g.b_tiled || g2->M != g.M)))
+        return MOE_ERR_INVALID_ARG;
     static std::once_flag attr_once[64];
     static int max_clusters[64];
     int dev = 0;
@@ -796,17 +859,29 @@ moe_status_t launch_pair_impl(const TcGroupedGemm& g, cudaStream_t s) {
     const int pairs_max = max_clusters[dev & 63];
     if (pairs_max < 1) return MOE_ERR_UNSUPPORTED;
 
-    CUtensorMap ma, mb;
-    const int b_nt = (int)ceil_div(g.Nb, 256), KBt = (int)ceil_div(g.K, BK);
-    if (!make_map(&ma, g.A, (uint64_t)g.K, (uint64_t)g.M, 128)) return MOE_ERR_CUDA;
-    if (g.b_tiled) {
-        if ((int64_t)g.G * b_nt * KBt * 256 >= INT_MAX) return MOE_ERR_UNSUPPORTED;
-        if (!make_map(&mb, g.B, (uint64_t)BK, (uint64_t)g.G * b_nt * KBt * 256, BN2 / 2)) return MOE_ERR_CUDA;
-    } else if (!make_map(&mb, g.B, (uint64_t)g.K, (uint64_t)g.G * g.Nb, BN2 / 2)) {
-        return MOE_ERR_CUDA;
+    // A: 128-row boxes of [M, K]; B: this CTA's 128 rows of a 256-row block (row-major or tiled)
+    auto maps = [](const TcGroupedGemm& q, CUtensorMap& ma, CUtensorMap& mb) -> moe_status_t {
+        const int b_nt = (int)ceil_div(q.Nb, 256), KBt = (int)ceil_div(q.K, BK);
+        if (!make_map(&ma, q.A, (uint64_t)q.K, (uint64_t)q.M, 128)) return MOE_ERR_CUDA;
+        if (q.b_tiled) {
+            if ((int64_t)q.G * b_nt * KBt * 256 >= INT_MAX) return MOE_ERR_UNSUPPORTED;
+            if (!make_map(&mb, q.B, (uint64_t)BK, (uint64_t)q.G * b_nt * KBt * 256, BN2 / 2)) return MOE_ERR_CUDA;
+        } else if (!make_map(&mb, q.B, (uint64_t)q.K, (uint64_t)q.G * q.Nb, BN2 / 2)) {
+            return MOE_ERR_CUDA;
+        }
+        return MOE_OK;
+    };
+    CUtensorMap ma, mb, ma2, mb2;
+    const int b_nt = (int)ceil_div(g.Nb, 256);
+    MOE_TRY(maps(g, ma, mb));
+    if (FFN) {
+        MOE_TRY(maps(*g2, ma2, mb2));
+    } else {
+        ma2 = ma;  // never read
+        mb2 = mb;
     }
 
-    Params p;
+    Params p{};
     p.offsets = g.offsets;
     p.G = g.G;
     p.M = g.M;
@@ -816,19 +891,33 @@ moe_status_t launch_pair_impl(const TcGroupedGemm& g, cudaStream_t s) {
     p.b_tiled = g.b_tiled ? 1 : 0;
     p.b_nt = b_nt;
     p.c_tma = 0;
-    p.NT = EPI == TC_EPI_SWIGLU ? g.Nb / BN2 : (int)ceil_div(g.N, BN2);
+    p.NT = EPI != TC_EPI_BF16 ? g.Nb / BN2 : (int)ceil_div(g.N, BN2);
     p.ksplit = 1;
     p.c_split_stride = 0;
     p.C = g.C;
     p.ldc = g.ldc;
     p.status = g.status;
 
-    const int64_t max_tiles = (int64_t)p.NT * (ceil_div(g.M, BM2) + (g.offsets ? g.G : 0));
+    int64_t max_tiles = (int64_t)p.NT * (ceil_div(g.M, BM2) + (g.offsets ? g.G : 0));
+    if (FFN) {
+        const int mt = (int)ceil_div(g.M, BM2);
+        p.total1 = p.NT * mt;
+        p.NT2 = (int)ceil_div(g2->N, BN2);
+        p.KB2 = (int)ceil_div(g2->K, BK);
+        p.Nb2 = g2->Nb;
+        p.N2 = g2->N;
+        p.b_nt2 = (int)ceil_div(g2->Nb, 256);
+        p.C2 = g2->C;
+        p.ldc2 = g2->ldc;
+        p.sync = sync;
+        p.sync_target = 8 * p.NT;  // every phase-1 tile of an m-tile, once per epilogue warp of both CTAs
+        max_tiles = p.total1 + (int64_t)mt * p.NT2;
+    }
     const int pair_cap = g.max_ctas > 0 ? std::min(pairs_max, std::max(1, g.max_ctas / 2)) : pairs_max;
     const int pairs = (int)std::max<int64_t>(1, std::min<int64_t>(pair_cap, max_tiles));
     cfg.gridDim = dim3(2 * pairs);
     cfg.numAttrs = g.pdl ? 2 : 1;  // the occupancy query above takes the cluster shape alone
-    MOE_CUDA_TRY(cudaLaunchKernelEx(&cfg, tc_pair_gemm_kernel<EPI, STAGES, MAXG>, ma, mb, p));
+    MOE_CUDA_TRY(cudaLaunchKernelEx(&cfg, tc_pair_gemm_kernel<EPI, STAGES, MAXG>, ma, mb, ma2, mb2, p));
     note_launch();
     return last_launch_status();
 }
@@ -886,6 +975,15 @@ int tc_gate_splits(int M, int N, int K, int max_split) {
     int bn, split;
     plan_f32(M, N, K, std::max(1, max_split), bn, split);
     return effective_splits(K, split);
+}
+
+moe_status_t launch_tc_pair_ffn(const TcGroupedGemm& up, const TcGroupedGemm& down, int* sync, cudaStream_t s) {
+    if (up.M == 0) return MOE_OK;
+    if (up.epi != TC_EPI_SWIGLU || down.epi != TC_EPI_BF16 || down.A != up.C || up.Nb % (2 * kPackBlock) != 0)
+        return MOE_ERR_INVALID_ARG;
+    if (!use_pair_tiles(up) || !use_pair_tiles(down)) return MOE_ERR_UNSUPPORTED;
+    return up.smem_headroom ? launch_pair_impl<TC_EPI_FFN, 6, 1024>(up, s, &down, sync)
+                            : launch_pair_impl<TC_EPI_FFN, 7, 256>(up, s, &down, sync);
 }
 
 moe_status_t launch_tc_grouped_gemm(const TcGroupedGemm& g, cudaStream_t s) {

@@ -86,6 +86,24 @@ moe_status_t ffn_down(const void* h, moe_dtype_t dt, const int32_t* offsets, int
                                     H, static_cast<float*>(y), status, s, pdl);
 }
 
+// The shared experts (one dense FFN over all T rows, bf16) in one pair-tile launch when both of
+// its GEMMs take pair tiles: the down projection's tiles of 256 rows start as soon as the up
+// projection has stored those rows, instead of after the up projection's last tile (measured on
+// the DeepSeek-V3 prefill layer: see the design notes).  MOE_SHARED_FUSED=0 keeps two launches.
+// Returns MOE_ERR_UNSUPPORTED when the shapes take the two-launch path.
+moe_status_t shared_ffn_fused(const void* x, int T, int H, int SI, const void* w13s, const void* w2s, void* hs,
+                              void* ys, int* sync, uint32_t* status, cudaStream_t s, bool headroom, bool tiled) {
+    if (const char* e = std::getenv("MOE_SHARED_FUSED"))
+        if (e[0] == '0') return MOE_ERR_UNSUPPORTED;
+    TcGroupedGemm up{x, T, H, nullptr, 1, w13s, packed_rows(SI), SI, hs, SI, TC_EPI_SWIGLU, status};
+    TcGroupedGemm down{hs, T, SI, nullptr, 1, w2s, H, H, ys, H, TC_EPI_BF16, status};
+    up.smem_headroom = down.smem_headroom = headroom;
+    up.b_tiled = down.b_tiled = tiled;
+    up.pdl = down.pdl = false;
+    MOE_CUDA_TRY(cudaMemsetAsync(sync, 0, (size_t)ceil_div(T, 256) * sizeof(int), s));
+    return launch_tc_pair_ffn(up, down, sync, s);
+}
+
 // FP8 halves: the up projection (SwiGLU into bf16 h) followed by the 1x128
 // quantisation of h, and the down projection.  Scale rows are padded to a
 // multiple of 4 floats so they can be permuted as 16-byte vectors.
@@ -149,7 +167,7 @@ moe_status_t layer_gate(const moe_layer_desc& d, const void* x, float* logits, i
 struct Layout {
     size_t off[MOE_WS_NUM_FIELDS];
     size_t bytes[MOE_WS_NUM_FIELDS];
-    size_t scratch_off, scratch_bytes, total;
+    size_t scratch_off, scratch_bytes, sync_off, total;
 };
 
 Layout layout(const moe_layer_desc& d) {
@@ -189,7 +207,10 @@ Layout layout(const moe_layer_desc& d) {
     }
     L.scratch_off = cur;
     L.scratch_bytes = init_routing_scratch_bytes(d.T, d.E, d.k);
-    L.total = cur + round_up(L.scratch_bytes, kAlign);
+    cur += round_up(L.scratch_bytes, kAlign);
+    L.sync_off = cur;  // the fused shared-expert FFN's counter per 256 rows
+    cur += round_up((size_t)ceil_div(std::max(d.T, 1), 256) * 4, kAlign);
+    L.total = cur;
     return L;
 }
 
@@ -444,10 +465,18 @@ moe_status_t layer_forward(const moe_layer_desc* d, const void* x, void* out, vo
                                  pow2, tiled, false));
         } else {
             // the routing kernels (histogram and scatter use shared memory) run beside them
-            MOE_TRY(ffn_up(x, dt, nullptr, 1, T, H, SI, d->w13_shared, hs, status, ss, true, tiled, shared_ctas,
-                           false));
-            MOE_TRY(ffn_down(hs, dt, nullptr, 1, T, H, SI, d->w2_shared, ys, status, ss, true, tiled, shared_ctas,
-                             false));
+            moe_status_t st = MOE_ERR_UNSUPPORTED;
+            if (dt == MOE_BF16 && shared_ctas == 0)
+                st = shared_ffn_fused(x, T, H, SI, d->w13_shared, d->w2_shared, hs, ys, at<int>(ws, L.sync_off), status,
+                                      ss, true, tiled);
+            if (st == MOE_ERR_UNSUPPORTED) {
+                MOE_TRY(ffn_up(x, dt, nullptr, 1, T, H, SI, d->w13_shared, hs, status, ss, true, tiled, shared_ctas,
+                               false));
+                MOE_TRY(ffn_down(hs, dt, nullptr, 1, T, H, SI, d->w2_shared, ys, status, ss, true, tiled,
+                                 shared_ctas, false));
+            } else {
+                MOE_TRY(st);
+            }
         }
         MOE_TRY(mark(ev, ST_SHARED, 1, ss));
         MOE_CUDA_TRY(cudaEventRecord(side->join, ss));

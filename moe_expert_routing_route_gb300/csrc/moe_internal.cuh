@@ -132,7 +132,9 @@ moe_status_t launch_finalize(const void* y, int64_t y_rows, const void* skip, co
                              uint32_t* status, cudaStream_t s);
 
 // gemm_tc.cu: bf16 tcgen05 grouped GEMM, C = A B^T per group.
-enum TcEpilogue { TC_EPI_SWIGLU = 0, TC_EPI_BF16 = 1, TC_EPI_F32 = 2 };
+// TC_EPI_FFN: one pair-tile launch runs an up projection (SwiGLU) and then the down projection of
+// its output (launch_tc_pair_ffn)
+enum TcEpilogue { TC_EPI_SWIGLU = 0, TC_EPI_BF16 = 1, TC_EPI_F32 = 2, TC_EPI_FFN = 3 };
 struct TcGroupedGemm {
     const void* A;            // [M, K] bf16, row stride K
     int M;                    // rows of A
@@ -156,6 +158,11 @@ struct TcGroupedGemm {
                                   // followers placed early hold SMs the first stream's kernels need)
 };
 moe_status_t launch_tc_grouped_gemm(const TcGroupedGemm& g, cudaStream_t s);
+// One dense FFN (one group, no offsets: the shared experts) in one persistent pair-tile launch:
+// the up projection's tiles (SwiGLU epilogue into up.C), then the down projection's (down.A ==
+// up.C), whose tiles of 256 rows start as soon as every up tile of those rows is stored.  sync:
+// ceil(M / 256) zeroed ints of device memory.  UNSUPPORTED unless both would take pair tiles.
+moe_status_t launch_tc_pair_ffn(const TcGroupedGemm& up, const TcGroupedGemm& down, int* sync, cudaStream_t s);
 int tc_gate_splits(int M, int N, int K, int max_split);  // K slices the fp32 launch will use
 
 // gemm_fp8.cu: e4m3 block-scaled grouped GEMM (bf16 out), C = A B^T per group.

@@ -174,6 +174,36 @@ def test_layer_prefill_slice_shared_experts_beside_up(oracle, monkeypatch, prefi
     check_layer(oracle, cfg, d, layer, split, n=n, ref=ref)
 
 
+FUSED = [c for c in SMALL if c.dtype == "bf16" and c.S > 0 and c.T >= 256]
+
+
+@pytest.mark.parametrize("cfg", FUSED, ids=[c.name for c in FUSED])
+def test_layer_shared_experts_one_launch(oracle, monkeypatch, cfg):
+    """The shared experts' up and down projections in one pair-tile launch (the down
+    projection's tiles waiting on per-256-row counters) give the bits of two launches."""
+    d, layer = make(cfg)
+    fused = layer.forward(d["x"])
+    assert layer.device_status() == 0
+    monkeypatch.setenv("MOE_SHARED_FUSED", "0")
+    assert torch.equal(layer.forward(d["x"]), fused)
+    check_layer(oracle, cfg, d, layer, fused)
+
+
+def test_layer_prefill_slice_shared_experts_one_launch(oracle, monkeypatch, prefill_slice):
+    """Full-K shared experts (H=7168, I=2048, 512 rows: two m-tiles) in one launch: the
+    same bits as two launches, in the same repeated forward."""
+    cfg, d, n, ref = prefill_slice
+    layer = binding.MoELayer(T=cfg.T, k=cfg.k, w_router=d["wg"], w_gate=d["w_gate"], w_up=d["w_up"], w2=d["w2"],
+                             s_gate=d["s_gate"], s_up=d["s_up"], s2=d["s2"], expert_bias=None,
+                             renormalize=cfg.renormalize)
+    fused = [layer.forward(d["x"]) for _ in range(3)]
+    assert layer.device_status() == 0
+    assert all(torch.equal(f, fused[0]) for f in fused)
+    monkeypatch.setenv("MOE_SHARED_FUSED", "0")
+    assert torch.equal(layer.forward(d["x"]), fused[0])
+    check_layer(oracle, cfg, d, layer, fused[0], n=n, ref=ref)
+
+
 SPLIT = [c for c in SMALL if c.dtype == "bf16" and c.S > 0 and c.name in ("small_bf16", "ragged_bf16", "zipf_bf16",
                                                                            "one_token_bf16", "grouped_bf16")]
 
