@@ -795,7 +795,7 @@ moe_status_t launch_impl(const TcGroupedGemm& g, cudaStream_t s) {
     p.b_nt = b_nt;
     p.c_tma = c_tma ? 1 : 0;
     p.NT = EPI == TC_EPI_SWIGLU ? g.Nb / BN : (int)ceil_div(g.N, BN);
-    p.ksplit = EPI == TC_EPI_F32 ? effective_splits(g.K, g.ksplit) : 1;
+    p.ksplit = EPI == TC_EPI_F32 ? (g.exact_split ? g.ksplit : effective_splits(g.K, g.ksplit)) : 1;
     p.c_split_stride = g.c_split_stride;
     p.C = g.C;
     p.ldc = g.ldc;
@@ -1000,7 +1000,11 @@ moe_status_t launch_tc_grouped_gemm(const TcGroupedGemm& g, cudaStream_t s) {
             int bn, split;
             plan_f32(g.M, g.N, g.K, std::max(1, g.ksplit), bn, split);
             TcGroupedGemm gs = g;
-            gs.ksplit = split;
+            if (g.exact_split) {
+                if (g.ksplit < 1 || effective_splits(g.K, g.ksplit) != g.ksplit) return MOE_ERR_INVALID_ARG;
+            } else {
+                gs.ksplit = split;
+            }
             switch (bn) {
                 case 64: return launch_impl<64, TC_EPI_F32>(gs, s);
                 case 128: return launch_impl<128, TC_EPI_F32>(gs, s);

@@ -163,6 +163,21 @@ moe_status_t layer_gate(const moe_layer_desc& d, const void* x, float* logits, i
     return gate(x, d.w_router, d.dtype, d.T, d.H, d.E, logits, s);
 }
 
+// The gate for rows [r0, r1) only, with the K slices of the whole batch's gate (nsplit from
+// gate_splits), writing rows r0.. of every slice: the same logits, bit for bit, as layer_gate.
+moe_status_t layer_gate_rows(const moe_layer_desc& d, const void* x, float* logits, int r0, int r1, int nsplit,
+                             cudaStream_t s) {
+    const void* xr = static_cast<const char*>(x) + (size_t)r0 * d.H * dt_size(d.dtype);
+    float* lr = logits + (size_t)r0 * d.E;
+    if (d.dtype == MOE_BF16) {
+        TcGroupedGemm g{xr, r1 - r0, d.H, nullptr, 1, d.w_router, d.E, d.E, lr, d.E, TC_EPI_F32, nullptr,
+                        nsplit, (int64_t)d.T * d.E};
+        g.exact_split = true;
+        return launch_tc_grouped_gemm(g, s);
+    }
+    return gate(xr, d.w_router, d.dtype, r1 - r0, d.H, d.E, lr, s);
+}
+
 // ---- layer workspace layout ----
 struct Layout {
     size_t off[MOE_WS_NUM_FIELDS];
@@ -407,6 +422,8 @@ moe_status_t layer_forward(const moe_layer_desc* d, const void* x, void* out, vo
     // host path: chunks of T/1024 rows (at most kMaxIoChunks), one when T is small
     const int io_chunks = io ? std::max(1, std::min(kMaxIoChunks, (T + 1023) / 1024)) : 0;
     const bool chunked_shared = io && side && !fp8;  // FP8 shared experts read x quantised on the main stream
+    // gate and top-k chunk by chunk as x arrives too (per-token work; the sort needs the whole batch)
+    const bool chunked_gate = io && !fp8 && io_chunks > 1;
     if (io) {
         HostPipe* hp = io->pipe;
         MOE_CUDA_TRY(cudaEventRecord(hp->entry, s));  // after the status reset and all earlier work on s
@@ -439,7 +456,7 @@ moe_status_t layer_forward(const moe_layer_desc* d, const void* x, void* out, vo
             MOE_TRY(mark(ev, ST_SHARED, 1, ss));
             MOE_CUDA_TRY(cudaEventRecord(side->join, ss));
         }
-        MOE_CUDA_TRY(cudaStreamWaitEvent(s, hp->in[io_chunks - 1], 0));  // the gate reads all of x
+        if (!chunked_gate) MOE_CUDA_TRY(cudaStreamWaitEvent(s, hp->in[io_chunks - 1], 0));  // the gate reads all of x
     }
     MOE_TRY(mark(ev, ST_GATE, 0, s));
     if (fp8) MOE_TRY(launch_quantize_rows_fp8(x, dt, T, H, xq, xs, ldx, s, pow2));  // activations, 1x128 blocks
@@ -449,7 +466,21 @@ moe_status_t layer_forward(const moe_layer_desc* d, const void* x, void* out, vo
     const int shared_ctas = fork && !fp8 ? shared_expert_ctas(*d) : 0;  // > 0: beside the routed up projection
     if (fork) MOE_CUDA_TRY(cudaEventRecord(side->fork, s));
     int nsplit = 1;
-    MOE_TRY(layer_gate(*d, x, logits, &nsplit, s));
+    if (chunked_gate) {
+        // each chunk's logits and top-k as soon as its rows of x have arrived
+        nsplit = gate_splits(*d);
+        for (int c = 0; c < io_chunks; ++c) {
+            int c0, c1;
+            chunk_rows(T, io_chunks, c, c0, c1);
+            MOE_CUDA_TRY(cudaStreamWaitEvent(s, io->pipe->in[c], 0));
+            MOE_TRY(layer_gate_rows(*d, x, logits, c0, c1, nsplit, s));
+            MOE_TRY(launch_route_topk(logits + (size_t)c0 * E, d->expert_bias, c1 - c0, E, k, d->renormalize,
+                                      ids + (size_t)c0 * k, w + (size_t)c0 * k, s, d->n_group, d->topk_group,
+                                      d->group_rule, nsplit, (int64_t)T * E));
+        }
+    } else {
+        MOE_TRY(layer_gate(*d, x, logits, &nsplit, s));
+    }
     MOE_TRY(mark(ev, ST_GATE, 1, s));
     if (chunked_shared) {
         // launched above
@@ -485,8 +516,9 @@ moe_status_t layer_forward(const moe_layer_desc* d, const void* x, void* out, vo
         MOE_TRY(mark(ev, ST_SHARED, 1, s));
     }
     MOE_TRY(mark(ev, ST_ROUTE, 0, s));
-    MOE_TRY(launch_route_topk(logits, d->expert_bias, T, E, k, d->renormalize, ids, w, s, d->n_group,
-                              d->topk_group, d->group_rule, nsplit));
+    if (!chunked_gate)
+        MOE_TRY(launch_route_topk(logits, d->expert_bias, T, E, k, d->renormalize, ids, w, s, d->n_group,
+                                  d->topk_group, d->group_rule, nsplit));
     MOE_TRY(mark(ev, ST_ROUTE, 1, s));
     MOE_TRY(mark(ev, ST_INIT, 0, s));
     MOE_TRY(launch_init_routing_index(ids, R, E, counts, offsets, row_idx, scratch, status, s));

@@ -68,11 +68,11 @@ __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;"
 // route.cu
 // n_group <= 1: flat top-k; otherwise group-limited (topk_group groups kept,
 // rule 0 = group max, rule 1 = sum of the group's two largest scores).
-// nsplit > 1: the logits arrive as nsplit partial sums, slice i at logits + i*T*E;
-// they are added in slice order and the sums written back to slice 0.
+// nsplit > 1: the logits arrive as nsplit partial sums, slice i at logits + i*slice_stride
+// (0: T*E); they are added in slice order and the sums written back to slice 0.
 moe_status_t launch_route_topk(const float* logits, const float* bias, int T, int E, int k, int renorm,
                                int32_t* ids, float* w, cudaStream_t s, int n_group = 1, int topk_group = 1,
-                               int rule = 0, int nsplit = 1);
+                               int rule = 0, int nsplit = 1, int64_t slice_stride = 0);
 
 // permute.cu
 size_t init_routing_scratch_bytes(int T, int E, int k);
@@ -156,6 +156,8 @@ struct TcGroupedGemm {
     int max_ctas = 0;             // persistent grid cap (0: one CTA per SM), leaving SMs to other streams' kernels
     bool pdl = true;              // programmatic dependent launch (false for kernels on the second stream, whose
                                   // followers placed early hold SMs the first stream's kernels need)
+    bool exact_split = false;     // fp32 output: exactly ksplit K slices (the slices of another launch over more
+                                  // rows, so that the partial sums agree bit for bit)
 };
 moe_status_t launch_tc_grouped_gemm(const TcGroupedGemm& g, cudaStream_t s);
 // One dense FFN (one group, no offsets: the shared experts) in one persistent pair-tile launch:

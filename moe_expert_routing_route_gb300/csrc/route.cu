@@ -57,7 +57,7 @@ __device__ __forceinline__ void warp_argmax(float& bv, int& bi) {
 template <int VPL>
 __global__ void __launch_bounds__(kWarps * 32)
 route_topk_kernel(const float* logits, const float* __restrict__ bias, int T, int E, int k, Grouping grp,
-                  int renorm, int nsplit, int32_t* __restrict__ ids, float* __restrict__ w) {
+                  int renorm, int nsplit, int64_t slice_stride, int32_t* __restrict__ ids, float* __restrict__ w) {
     extern __shared__ float sh_scores[];  // [kWarps][E], grouped routing only
     const int lane = threadIdx.x & 31;
     const int t = blockIdx.x * kWarps + (threadIdx.x >> 5);
@@ -73,7 +73,7 @@ route_topk_kernel(const float* logits, const float* __restrict__ bias, int T, in
         // K slices of the gate GEMM, added in slice order; each round issues all
         // of a lane's loads before any add, and the sums go back to slice 0 last
         for (int q = 1; q < nsplit; ++q) {
-            const float* sl = row + (size_t)q * T * E;
+            const float* sl = row + (size_t)q * slice_stride;
             float p[VPL];
 #pragma unroll
             for (int i = 0; i < VPL; ++i) p[i] = i * 32 + lane < E ? sl[i * 32 + lane] : 0.0f;
@@ -186,28 +186,29 @@ route_topk_kernel(const float* logits, const float* __restrict__ bias, int T, in
 
 template <int VPL>
 cudaError_t launch(const float* logits, const float* bias, int T, int E, int k, Grouping grp, int renorm,
-                   int nsplit, int32_t* ids, float* w, cudaStream_t s) {
+                   int nsplit, int64_t slice_stride, int32_t* ids, float* w, cudaStream_t s) {
     const int blocks = (int)ceil_div(T, kWarps);
     const size_t smem = grp.n_group > 1 ? (size_t)kWarps * E * sizeof(float) : 0;
     return launch_pdl(route_topk_kernel<VPL>, dim3(blocks), dim3(kWarps * 32), smem, s, logits, bias, T, E, k, grp,
-                      renorm, nsplit, ids, w);
+                      renorm, nsplit, slice_stride, ids, w);
 }
 
 }  // namespace
 
 moe_status_t launch_route_topk(const float* logits, const float* bias, int T, int E, int k, int renorm,
                                int32_t* ids, float* w, cudaStream_t s, int n_group, int topk_group, int rule,
-                               int nsplit) {
+                               int nsplit, int64_t slice_stride) {
     if (T == 0) return MOE_OK;
     const Grouping grp{n_group > 1 ? n_group : 1, topk_group, rule};
     const int ns = nsplit > 1 ? nsplit : 1;
+    const int64_t ss = slice_stride > 0 ? slice_stride : (int64_t)T * E;
     cudaError_t err;
-    if (E <= 32) err = launch<1>(logits, bias, T, E, k, grp, renorm, ns, ids, w, s);
-    else if (E <= 64) err = launch<2>(logits, bias, T, E, k, grp, renorm, ns, ids, w, s);
-    else if (E <= 128) err = launch<4>(logits, bias, T, E, k, grp, renorm, ns, ids, w, s);
-    else if (E <= 256) err = launch<8>(logits, bias, T, E, k, grp, renorm, ns, ids, w, s);
-    else if (E <= 512) err = launch<16>(logits, bias, T, E, k, grp, renorm, ns, ids, w, s);
-    else err = launch<32>(logits, bias, T, E, k, grp, renorm, ns, ids, w, s);
+    if (E <= 32) err = launch<1>(logits, bias, T, E, k, grp, renorm, ns, ss, ids, w, s);
+    else if (E <= 64) err = launch<2>(logits, bias, T, E, k, grp, renorm, ns, ss, ids, w, s);
+    else if (E <= 128) err = launch<4>(logits, bias, T, E, k, grp, renorm, ns, ss, ids, w, s);
+    else if (E <= 256) err = launch<8>(logits, bias, T, E, k, grp, renorm, ns, ss, ids, w, s);
+    else if (E <= 512) err = launch<16>(logits, bias, T, E, k, grp, renorm, ns, ss, ids, w, s);
+    else err = launch<32>(logits, bias, T, E, k, grp, renorm, ns, ss, ids, w, s);
     note_launch();
     return err == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
