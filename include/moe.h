@@ -72,7 +72,8 @@ typedef enum moe_dtype { MOE_F32 = 0, MOE_BF16 = 1 } moe_dtype_t;
 /* Every workspace starts with this many bytes of header (the status word). */
 #define MOE_WS_HEADER_BYTES 256
 
-/* Version of this ABI; bumped on any incompatible change. */
+/* Version of this ABI; bumped on any incompatible change.  2: moe_layer_desc
+ * ends with a weight_layout field; weight_format takes MOE_WEIGHTS_FP8_POW2. */
 int moe_abi_version(void);
 
 /* Human-readable name of a status code (static storage). */

@@ -751,7 +751,7 @@ using namespace moe;
 
 extern "C" {
 
-int moe_abi_version(void) { return 1; }
+int moe_abi_version(void) { return 2; }
 
 const char* moe_status_string(moe_status_t st) {
     switch (st) {
