@@ -31,7 +31,7 @@ def _config(i: int) -> tuple[inputs.LayerConfig, str]:
     return cfg, tile
 
 
-CASES = [_config(i) for i in range(16)]
+CASES = [_config(i) for i in range(32)]
 
 
 @pytest.mark.parametrize("cfg,tile", CASES, ids=[f"{c.name}-{t}" for c, t in CASES])
@@ -45,3 +45,34 @@ def test_random_layer(oracle, monkeypatch, cfg, tile):
     d, layer = make(cfg)
     out = layer.forward(d["x"])
     check_layer(oracle, cfg, d, layer, out)
+
+
+def _host_config(i: int) -> inputs.LayerConfig:
+    """Batches of 1025-3600 tokens: the host-buffer forward copies x in 2-4 chunks and runs the
+    gate and top-k chunk by chunk as they arrive."""
+    rng = np.random.default_rng(5000 + i)
+    dtype = "f32" if i % 4 == 3 else "bf16"
+    E = int(rng.choice([8, 32, 64]))
+    k = int(rng.integers(1, min(E, 8) + 1))
+    return inputs.LayerConfig(f"host{i}", T=int(rng.integers(1025, 3600)), H=int(rng.choice([128, 256, 512])),
+                              E=E, k=k, I=int(rng.choice([64, 128, 256])), S=int(rng.integers(0, 3)),
+                              dtype=dtype, seed=6000 + i)
+
+
+HOST_CASES = [_host_config(i) for i in range(10)]
+
+
+@pytest.mark.parametrize("cfg", HOST_CASES, ids=[c.name for c in HOST_CASES])
+def test_random_host_path_matches_device(cfg):
+    """The host-buffer forward (chunked copies, chunked gate and top-k) gives the device-buffer
+    forward's output bit for bit."""
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    d, layer = make(cfg)
+    dev = layer.forward(d["x"])
+    x_host = d["x"].cpu().pin_memory()
+    out_host = torch.empty_like(x_host).pin_memory()
+    layer.forward_host(x_host, out_host)
+    torch.cuda.synchronize()
+    assert layer.device_status() == 0
+    assert torch.equal(out_host, dev.cpu())
