@@ -428,7 +428,9 @@ moe_status_t moe_layer_workspace_field(const moe_layer_desc* desc, moe_ws_field 
  * With S > 0 the first call on a device creates the library's second stream
  * and two events for that device (no device memory is allocated); make that
  * first call outside stream capture.  The call's work forks onto that stream
- * and joins back into `stream`. */
+ * and joins back into `stream`.  bf16 layers with T >= 256 run the shared
+ * experts' two projections as one launch; the environment variable
+ * MOE_SHARED_FUSED=0 keeps two launches (the same bits). */
 moe_status_t moe_layer_forward(const moe_layer_desc* desc, const void* x, void* out, void* ws,
                                size_t ws_bytes, moe_stream_t stream);
 
