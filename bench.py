@@ -396,6 +396,9 @@ def run_ours(args, world, rank, local):
         f_, b_ = costs[name]
         stages[name] = dict(us=round(t * 1e3, 2), tflops=round(f_ / (t / 1e3) / 1e12, 2) if t > 0 else None,
                             gbs=round(b_ / (t / 1e3) / 1e9, 1) if t > 0 else None)
+        if name in timed_ms:  # the same stage inside the timed region (events around it alone)
+            tt = timed_ms[name]
+            stages[name].update(timed_us=round(tt * 1e3, 2), timed_gbs=round(b_ / (tt / 1e3) / 1e9, 1) if tt > 0 else None)
     layer_fl = sum(f for f, _ in costs.values())
     gemm_fl = sum(costs[s][0] for s in ("up", "down", "shared"))
     gemm_ms = sum(stage_ms[s] for s in ("up", "down", "shared"))

@@ -558,10 +558,13 @@ tc_fp8_grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __gri
                 // h in bf16 (the precision it is stored and quantised in)
                 float h[kCols];
                 float am = 0.0f;
+                // silu(g) = g / (1 + e^-g) with the fast reciprocal (2 ulp; h is then rounded to bf16):
+                // the IEEE division's 64 per thread sat on the tile's tail, which the next tile's
+                // MMAs wait behind
 #pragma unroll
                 for (int i = 0; i < kCols; ++i) {
                     h[i] = __bfloat162float(
-                        __float2bfloat16_rn(acc[i] / (1.0f + __expf(-acc[i])) * acc[kCols + i]));
+                        __float2bfloat16_rn(__fdividef(acc[i], 1.0f + __expf(-acc[i])) * acc[kCols + i]));
                     am = fmaxf(am, fabsf(h[i]));
                 }
                 const int col0 = n * 128 + part * kCols;
@@ -578,6 +581,18 @@ tc_fp8_grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __gri
                     for (int o = 0; o < kSplit; ++o) am = fmaxf(am, slot[o * BM + r]);
                     const float sc = fp8::scale_for(am, MX);
                     if (valid) {
+                        // fl32(h / sc) with one division per block, as the row quantiser takes it
+                        const float rsc = 1.0f / sc;
+                        if (MX) {
+#pragma unroll
+                            for (int i = 0; i < kCols; ++i) h[i] = __fmul_rn(h[i], rsc);
+                        } else if (fp8::quotient_ok(sc)) {
+#pragma unroll
+                            for (int i = 0; i < kCols; ++i) h[i] = fp8::quotient(h[i], sc, rsc);
+                        } else {
+#pragma unroll
+                            for (int i = 0; i < kCols; ++i) h[i] = h[i] / sc;
+                        }
                         uint8_t* qrow = p.q + row * (int64_t)p.N + col0;
 #pragma unroll
                         for (int c = 0; c < kCols / 16; ++c) {  // 16 codes per store; N % 16 == 0
@@ -585,10 +600,8 @@ tc_fp8_grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __gri
                                 uint32_t w4[4];
 #pragma unroll
                                 for (int t = 0; t < 4; ++t)
-                                    w4[t] = fp8::e4m3(h[16 * c + 4 * t] / sc) |
-                                            (fp8::e4m3(h[16 * c + 4 * t + 1] / sc) << 8) |
-                                            (fp8::e4m3(h[16 * c + 4 * t + 2] / sc) << 16) |
-                                            (fp8::e4m3(h[16 * c + 4 * t + 3] / sc) << 24);
+                                    w4[t] = fp8::e4m3x4(h[16 * c + 4 * t], h[16 * c + 4 * t + 1],
+                                                        h[16 * c + 4 * t + 2], h[16 * c + 4 * t + 3]);
                                 reinterpret_cast<uint4*>(qrow)[c] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
                             }
                         }

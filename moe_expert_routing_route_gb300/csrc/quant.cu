@@ -68,15 +68,27 @@ quantize_rows_kernel(const T* __restrict__ a, int64_t rows, int cols, int kb, in
         for (int off = 8; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
         if (b >= kb) continue;  // the second half of the last pair of an odd block count
         const float s = scale_for(amax, pow2);
+        // fl32(v / s) for each value: one division per block (fp8_codec.cuh)
+        const float rs = 1.0f / s;
+        if (pow2) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) v[i] = __fmul_rn(v[i], rs);
+        } else if (fp8::quotient_ok(s)) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) v[i] = fp8::quotient(v[i], s, rs);
+        } else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) v[i] = v[i] / s;
+        }
         uint8_t* crow = codes + r * cols;
         if (vec && c0 + 8 <= cols) {
             uint2 packed;
-            packed.x = e4m3(v[0] / s) | (e4m3(v[1] / s) << 8) | (e4m3(v[2] / s) << 16) | (e4m3(v[3] / s) << 24);
-            packed.y = e4m3(v[4] / s) | (e4m3(v[5] / s) << 8) | (e4m3(v[6] / s) << 16) | (e4m3(v[7] / s) << 24);
+            packed.x = fp8::e4m3x4(v[0], v[1], v[2], v[3]);
+            packed.y = fp8::e4m3x4(v[4], v[5], v[6], v[7]);
             *reinterpret_cast<uint2*>(crow + c0) = packed;
         } else {
             for (int i = 0; i < 8; ++i)
-                if (c0 + i < cols) crow[c0 + i] = (uint8_t)e4m3(v[i] / s);
+                if (c0 + i < cols) crow[c0 + i] = (uint8_t)e4m3(v[i]);
         }
         if (hl == 0) scales[r * ld_scales + b] = s;
     }

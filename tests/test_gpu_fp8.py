@@ -40,6 +40,43 @@ def test_quantize_rows_fp8(oracle, rows, cols, dtype, pow2):
     assert np.array_equal(scales.cpu().numpy(), rs)
 
 
+def _boundary_rows(oracle, pow2: bool, rows: int, cols: int, seed: int) -> np.ndarray:
+    """fp32 rows whose values, divided by their block's scale, land on or within four fp32 ulps of
+    the e4m3 rounding midpoints (between adjacent codes, subnormal ones and the one next to zero
+    included).  Each 128-value block starts with its amax A, drawn over 48 decades (the smallest
+    below the range where the kernels divide each value); the other values are fl32(M * s) moved
+    by -4..4 ulps for random midpoints M, where s is A / 448 in fp32 (or the power of two above
+    it), and kept at or below A so that A stays the block's amax."""
+    rng = np.random.default_rng(seed)
+    vals = np.unique(np.abs(oracle.e4m3_table()[np.isfinite(oracle.e4m3_table())]))  # 0 .. 448
+    mids = ((vals[:-1] + vals[1:]) / 2).astype(np.float32)
+    a = np.empty((rows, cols), np.float32)
+    for r in range(rows):
+        for b0 in range(0, cols, 128):
+            A = np.float32(10.0 ** rng.uniform(-28, 20))
+            s = np.float32(2.0 ** np.ceil(np.log2(float(A) / 448.0))) if pow2 else A / np.float32(448)
+            n = min(128, cols - b0)
+            m = rng.choice(mids, size=n - 1)
+            v = (m * s).astype(np.float32)
+            bits = v.view(np.int32) + rng.integers(-4, 5, size=n - 1).astype(np.int32)
+            v = np.minimum(bits.view(np.float32), A)
+            a[r, b0] = A
+            a[r, b0 + 1:b0 + n] = np.where(rng.random(n - 1) < 0.5, -v, v)
+    return a
+
+
+@pytest.mark.parametrize("pow2", [False, True], ids=["f32scale", "pow2scale"])
+def test_quantize_rows_fp8_rounding_midpoints(oracle, pow2):
+    """The kernels take fl32(v / s) with one division per block (a reciprocal and two fma
+    correction steps); on values whose quotients sit at the e4m3 rounding midpoints every code
+    must still equal the oracle's, which divides each value."""
+    a = _boundary_rows(oracle, pow2, rows=96, cols=1000, seed=11 + pow2)
+    codes, scales = binding.moe_quantize_rows_fp8(torch.from_numpy(a).to(DEV), pow2=pow2)
+    rc, rs = oracle.quantize_rows_fp8(a, pow2=pow2)
+    assert np.array_equal(scales.cpu().numpy(), rs)
+    assert np.array_equal(codes.cpu().numpy(), rc)
+
+
 def test_quantize_rows_fp8_all_zero_block(oracle):
     a = torch.zeros((2, 256), dtype=torch.bfloat16)
     a[1, 200] = 1.5
