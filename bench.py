@@ -153,7 +153,10 @@ def measured_traffic(stage: str, workload: str):
     for line in open(TRAFFIC_FILE):
         parts = line.split()
         if len(parts) >= 4 and not line.startswith("#") and parts[0] == stage and parts[1] == workload:
-            if parts[3] == source_hash(KERNEL_SOURCES[stage]):
+            src = KERNEL_SOURCES[stage]
+            if "fp8" in workload and stage in ("up", "down", "shared"):
+                src = "gemm_fp8.cu"  # FP8 layers run their expert GEMMs on the e4m3 kernel
+            if parts[3] == source_hash(src):
                 return float(parts[2])
     return None
 
