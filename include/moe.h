@@ -230,7 +230,10 @@ moe_status_t moe_tile_weights(const void* w, int G, int n_rows, int row_bytes, v
  * or 256 rows on a two-CTA cluster (tcgen05.mma.cta_group::2) once the groups
  * average 256 rows or more; the environment variable MOE_GEMM_TILE=single or
  * MOE_GEMM_TILE=pair, read at every launch, forces one shape.  Both give the
- * same result up to fp32 summation order. */
+ * same result up to fp32 summation order.  With pair tiles over 128 groups or
+ * more that average 512 rows or more, each group's tail of at most 128 rows goes
+ * to a second, single-CTA launch instead of a half-empty pair tile (the same
+ * bits); MOE_GEMM_MIXED=1 or 0 forces that split on or off. */
 /* moe_grouped_ffn with both weights in the tiled layout (moe_tile_weights of the
  * moe_pack_w13 output and of w2); bf16 only.  Same arguments and results. */
 moe_status_t moe_grouped_ffn_tiled(const void* a, moe_dtype_t dt, const int32_t* expert_offsets, int E, int rows,

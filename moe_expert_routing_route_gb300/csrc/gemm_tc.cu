@@ -75,6 +75,7 @@ struct Params {
     int c_tma;                // bf16 epilogue: C written through mapC (TMA stores of staged 32 x 64 boxes)
     int ksplit;               // K split into this many slices (fp32 outputs only), each written at
     int64_t c_split_stride;   // C + slice * c_split_stride
+    int part;                 // rows of each group this launch covers (split_rows)
     void* C;
     int64_t ldc;
     uint32_t* status;
@@ -104,6 +105,19 @@ __device__ __forceinline__ void decode_tile(int tile, const int* prefix, int G, 
     const int rem = local - n * mts;
     m = rem / S;
     ks = rem - m * S;
+}
+
+// Rows [a, b) of a group that a launch covers.  part 0: all of them.  Mixed tile shapes split a
+// group between two launches: part 1, the pair-tile launch, takes its 256-row blocks, and the tail
+// too when more than 128 rows are left (one more, partly filled pair tile); part 2, a single-CTA
+// launch, takes a tail of at most 128 rows (one m-tile) -- instead of a pair tile that would be
+// half or more the next group's rows.  Left alone when the offsets are bad (the caller flags them).
+__device__ __forceinline__ void split_rows(int part, int& a, int& b) {
+    if (part == 0 || b < a) return;
+    const int blocks = (b - a) >> 8, tail = (b - a) & 255;
+    const int cut = a + (blocks << 8) + (tail > 128 ? tail : 0);
+    if (part == 1) b = cut;
+    else a = cut;
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
@@ -209,6 +223,7 @@ tc_grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_co
             set_status(p.status, MOE_DEVERR_BAD_OFFSETS);
             a = b = 0;
         }
+        split_rows(p.part, a, b);
         gstart[g] = a;
         gend[g] = b;
     }
@@ -501,6 +516,7 @@ tc_pair_gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_const
     auto seg = [&](int g, int& a, int& b) {
         a = p.offsets ? __ldg(p.offsets + g) : 0;
         b = p.offsets ? __ldg(p.offsets + g + 1) : p.M;
+        if (a >= 0 && b <= p.M) split_rows(p.part, a, b);
     };
     // tile -> (phase, group, m-tile, n-tile).  Two-phase launches (one group) order each phase
     // m-tile by m-tile, n fastest, so that the rows of an m-tile are finished early in phase 1
@@ -800,6 +816,7 @@ moe_status_t launch_impl(const TcGroupedGemm& g, cudaStream_t s) {
     p.C = g.C;
     p.ldc = g.ldc;
     p.status = g.status;
+    p.part = g.part;
 
     const int64_t max_tiles = (int64_t)p.NT * p.ksplit * (ceil_div(g.M, BM) + (g.offsets ? g.G : 0));
     const int ctas = g.max_ctas > 0 ? std::min(g.max_ctas, sm_count()) : sm_count();
@@ -897,6 +914,7 @@ moe_status_t launch_pair_impl(const TcGroupedGemm& g, cudaStream_t s, const TcGr
     p.C = g.C;
     p.ldc = g.ldc;
     p.status = g.status;
+    p.part = g.part;
 
     int64_t max_tiles = (int64_t)p.NT * (ceil_div(g.M, BM2) + (g.offsets ? g.G : 0));
     if (FFN) {
@@ -925,6 +943,33 @@ moe_status_t launch_pair_impl(const TcGroupedGemm& g, cudaStream_t s, const TcGr
 template <int EPI>
 moe_status_t launch_pair(const TcGroupedGemm& g, cudaStream_t s) {
     return g.G <= 256 && !g.smem_headroom ? launch_pair_impl<EPI, 7, 256>(g, s) : launch_pair_impl<EPI, 6, 1024>(g, s);
+}
+
+// Pair tiles for each group's 256-row blocks and a single-CTA launch for the tails of at most 128
+// rows (split_rows), for grouped launches that take pair tiles.  A tail on a single-CTA tile costs
+// one SM where a pair tile costs two, but the second launch waits for the first and ends in a
+// partial wave of its own, a cost that only many groups' tails outweigh.  Measured: the Zipf-skewed
+// DeepSeek-V3 prefill batch (256 experts, 512 rows each on average) 10.79-10.92 -> 10.29-10.33 ms;
+// its 32-expert slice (512 rows each) 1.276 -> 1.334 ms; mid_bf16 (64 experts, 384 rows each)
+// 0.526-0.530 -> 0.582-0.584 ms.  So: 128 groups or more, averaging two 256-row blocks or more.
+// MOE_GEMM_MIXED=1 or 0 forces the choice; a forced MOE_GEMM_TILE=pair keeps pair tiles throughout.
+bool mixed_tiles(const TcGroupedGemm& g) {
+    if (!g.offsets || g.G < 2) return false;
+    if (const char* e = std::getenv("MOE_GEMM_TILE"))
+        if (std::strcmp(e, "pair") == 0) return false;
+    if (const char* e = std::getenv("MOE_GEMM_MIXED")) return e[0] == '1';
+    return g.G >= 128 && (int64_t)g.M >= (int64_t)2 * BM2 * g.G;
+}
+
+template <int EPI>
+moe_status_t launch_mixed(const TcGroupedGemm& g, cudaStream_t s) {
+    TcGroupedGemm pairs = g, tails = g;
+    pairs.part = 1;
+    tails.part = 2;
+    MOE_TRY(launch_pair<EPI>(pairs, s));
+    // programmatic: its blocks wait (griddepcontrol.wait) for the pair launch, which waited for
+    // everything before it
+    return launch_impl<256, EPI>(tails, s);
 }
 
 // Tile shape for the bf16 / SwiGLU outputs.  MOE_GEMM_TILE = "single" or "pair"
@@ -992,9 +1037,13 @@ moe_status_t launch_tc_grouped_gemm(const TcGroupedGemm& g, cudaStream_t s) {
     switch (g.epi) {
         case TC_EPI_SWIGLU:
             if (g.Nb % (2 * kPackBlock) != 0) return MOE_ERR_INVALID_ARG;
-            return use_pair_tiles(g) ? launch_pair<TC_EPI_SWIGLU>(g, s) : launch_impl<256, TC_EPI_SWIGLU>(g, s);
+            if (!use_pair_tiles(g)) return launch_impl<256, TC_EPI_SWIGLU>(g, s);
+            if (!mixed_tiles(g)) return launch_pair<TC_EPI_SWIGLU>(g, s);
+            return launch_mixed<TC_EPI_SWIGLU>(g, s);
         case TC_EPI_BF16:
-            return use_pair_tiles(g) ? launch_pair<TC_EPI_BF16>(g, s) : launch_impl<256, TC_EPI_BF16>(g, s);
+            if (!use_pair_tiles(g)) return launch_impl<256, TC_EPI_BF16>(g, s);
+            if (!mixed_tiles(g)) return launch_pair<TC_EPI_BF16>(g, s);
+            return launch_mixed<TC_EPI_BF16>(g, s);
         case TC_EPI_F32: {
             if (g.b_tiled) return MOE_ERR_UNSUPPORTED;
             int bn, split;

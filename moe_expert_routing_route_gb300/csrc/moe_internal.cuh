@@ -158,6 +158,7 @@ struct TcGroupedGemm {
                                   // followers placed early hold SMs the first stream's kernels need)
     bool exact_split = false;     // fp32 output: exactly ksplit K slices (the slices of another launch over more
                                   // rows, so that the partial sums agree bit for bit)
+    int part = 0;                 // rows of each group to cover: all (0), the pair-tile part (1) or the tail (2)
 };
 moe_status_t launch_tc_grouped_gemm(const TcGroupedGemm& g, cudaStream_t s);
 // One dense FFN (one group, no offsets: the shared experts) in one persistent pair-tile launch:

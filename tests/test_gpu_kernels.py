@@ -317,6 +317,40 @@ def test_grouped_ffn_bf16_tile_shapes(oracle, monkeypatch, tile, T, k, E, H, I, 
     _close(y, ref, "bf16")
 
 
+# Launches that take pair tiles (rows >= 256 per group on average) cover each group's 256-row
+# blocks with pair tiles and a tail of at most 128 rows with a single-CTA launch.
+MIXED_CASES = [
+    (1600, 4, 16, 512, 256),   # ~400 rows per expert: one 256-row block, tails around 128
+    (3000, 2, 16, 264, 200),   # ~375 rows: tails mostly at most 128; K tails, down N tail
+    (2100, 4, 8, 256, 128),    # ~1050 rows: four blocks and short tails
+]
+
+
+def _mixed_ids(T, k, E, seed):
+    w = torch.tensor([12.0, 6.0, 3.0] + [1.0] * (E - 3))  # some groups many blocks, some below 128 rows
+    return inputs.random_ids(T, k, E, seed=seed, weights=w)
+
+
+@pytest.mark.parametrize("layout", ["rows", "tiled"])
+@pytest.mark.parametrize("skewed", [False, True], ids=["uniform", "skewed"])
+@pytest.mark.parametrize("T,k,E,H,I", MIXED_CASES)
+def test_grouped_ffn_bf16_mixed_tiles(oracle, monkeypatch, T, k, E, H, I, skewed, layout):
+    """Pair tiles for the 256-row blocks plus single-CTA tiles for tails of at most 128 rows
+    (MOE_GEMM_MIXED=1; the default for 128 groups or more averaging 512 rows) match the oracle and give
+    the bits of pair tiles throughout (MOE_GEMM_MIXED=0)."""
+    monkeypatch.delenv("MOE_GEMM_TILE", raising=False)
+    monkeypatch.setenv("MOE_GEMM_MIXED", "1")
+    ids = _mixed_ids(T, k, E, seed=T + 7) if skewed else None
+    y, ref, ir = _ffn_case(oracle, T, k, E, H, I, torch.bfloat16, seed=T + E + 4, ids=ids, tiled=layout == "tiled")
+    cnt = ir["tokens_per_expert"]
+    assert cnt.sum() >= 256 * E  # the launch takes pair tiles
+    assert (((cnt % 256) > 0) & ((cnt % 256) <= 128)).any()  # and some tails go to single tiles
+    _close(y, ref, "bf16")
+    monkeypatch.setenv("MOE_GEMM_MIXED", "0")
+    y0, _, _ = _ffn_case(oracle, T, k, E, H, I, torch.bfloat16, seed=T + E + 4, ids=ids, tiled=layout == "tiled")
+    assert torch.equal(y, y0)
+
+
 @pytest.mark.parametrize("tile", ["single", "pair"])
 def test_grouped_ffn_bf16_tile_shapes_skewed_and_dense(oracle, monkeypatch, tile):
     monkeypatch.setenv("MOE_GEMM_TILE", tile)

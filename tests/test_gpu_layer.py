@@ -174,6 +174,23 @@ def test_layer_prefill_slice_shared_experts_beside_up(oracle, monkeypatch, prefi
     check_layer(oracle, cfg, d, layer, split, n=n, ref=ref)
 
 
+def test_layer_mixed_tiles_zipf(oracle, monkeypatch):
+    """A Zipf-skewed layer (1024 rows per expert on average) with pair tiles for each expert's
+    256-row blocks and single-CTA tiles for tails of at most 128 rows (MOE_GEMM_MIXED=1, hot and
+    cold experts alike): the bits of pair tiles throughout, and the oracle's output."""
+    cfg = inputs.LayerConfig("zipf_mixed_bf16", T=2048, H=256, E=16, k=8, I=128, S=1, dtype="bf16", seed=17,
+                             zipf_s=1.2)
+    monkeypatch.delenv("MOE_GEMM_TILE", raising=False)
+    monkeypatch.setenv("MOE_GEMM_MIXED", "1")
+    d, layer = make(cfg)
+    mixed = layer.forward(d["x"]).clone()
+    cnt = layer.field("tokens_per_expert").cpu().numpy()
+    assert (((cnt % 256) > 0) & ((cnt % 256) <= 128)).any()
+    monkeypatch.setenv("MOE_GEMM_MIXED", "0")
+    assert torch.equal(layer.forward(d["x"]), mixed)
+    check_layer(oracle, cfg, d, layer, mixed)
+
+
 FUSED = [c for c in SMALL if c.dtype == "bf16" and c.S > 0 and c.T >= 256]
 
 
