@@ -301,7 +301,7 @@ moe_status_t mark(void* const* ev, int stage, int end, cudaStream_t s) {
 // together when several host threads use one device.
 struct SideStream {
     cudaStream_t stream = nullptr;
-    cudaEvent_t fork = nullptr, join = nullptr;
+    cudaEvent_t fork = nullptr, join = nullptr, xq = nullptr;  // xq: FP8 layers' x codes are ready
     std::mutex mu;
 };
 SideStream g_side[64];
@@ -319,6 +319,7 @@ moe_status_t side_stream(SideStream** out) {
         MOE_CUDA_TRY(cudaStreamCreateWithPriority(&ss.stream, cudaStreamNonBlocking, lo));
         MOE_CUDA_TRY(cudaEventCreateWithFlags(&ss.fork, cudaEventDisableTiming));
         MOE_CUDA_TRY(cudaEventCreateWithFlags(&ss.join, cudaEventDisableTiming));
+        MOE_CUDA_TRY(cudaEventCreateWithFlags(&ss.xq, cudaEventDisableTiming));
     }
     *out = &ss;
     return MOE_OK;
@@ -459,10 +460,14 @@ moe_status_t layer_forward(const moe_layer_desc* d, const void* x, void* out, vo
         if (!chunked_gate) MOE_CUDA_TRY(cudaStreamWaitEvent(s, hp->in[io_chunks - 1], 0));  // the gate reads all of x
     }
     MOE_TRY(mark(ev, ST_GATE, 0, s));
-    if (fp8) MOE_TRY(launch_quantize_rows_fp8(x, dt, T, H, xq, xs, ldx, s, pow2));  // activations, 1x128 blocks
     // fork: the shared experts need x alone (FP8: its codes), so they branch off
     // before the gate; the gate is enqueued first and starts first
     const bool fork = side && !chunked_shared;
+    // FP8: x is quantised (1x128 blocks) on the second stream ahead of the shared experts that read
+    // its codes, and the main stream waits for the codes only at the permute (the gate reads x);
+    // without a second stream, here
+    const bool xq_side = fp8 && fork;
+    if (fp8 && !xq_side) MOE_TRY(launch_quantize_rows_fp8(x, dt, T, H, xq, xs, ldx, s, pow2));
     const int shared_ctas = fork && !fp8 ? shared_expert_ctas(*d) : 0;  // > 0: beside the routed up projection
     if (fork) MOE_CUDA_TRY(cudaEventRecord(side->fork, s));
     int nsplit = 1;
@@ -490,6 +495,8 @@ moe_status_t layer_forward(const moe_layer_desc* d, const void* x, void* out, vo
         cudaStream_t ss = side->stream;
         MOE_TRY(mark(ev, ST_SHARED, 0, ss));
         if (fp8) {
+            MOE_TRY(launch_quantize_rows_fp8(x, dt, T, H, xq, xs, ldx, ss, pow2, false));
+            MOE_CUDA_TRY(cudaEventRecord(side->xq, ss));
             MOE_TRY(ffn_up_fp8(xq, xs, ldx, nullptr, 1, T, H, SI, d->w13_shared, d->w13_shared_scales, nullptr, hsq, hss,
                                status, ss, pow2, tiled, false));
             MOE_TRY(ffn_down_fp8(hsq, hss, nullptr, 1, T, H, SI, d->w2_shared, d->w2_shared_scales, ys, status, ss,
@@ -525,6 +532,7 @@ moe_status_t layer_forward(const moe_layer_desc* d, const void* x, void* out, vo
     MOE_TRY(mark(ev, ST_INIT, 1, s));
     MOE_TRY(mark(ev, ST_PERMUTE, 0, s));
     if (fp8) {
+        if (xq_side) MOE_CUDA_TRY(cudaStreamWaitEvent(s, side->xq, 0));
         MOE_TRY(launch_permute_rows(xq, (size_t)H, row_idx, T, k, exq, s));
         MOE_TRY(launch_permute_rows(xs, (size_t)ldx * 4, row_idx, T, k, exs, s));
     } else {

@@ -121,8 +121,10 @@ moe_status_t ep_combine(const EpBuffers& b, const void* y_sorted, void* y_recv, 
 
 // quant.cu: FP8 (e4m3) block quantisation.
 // pow2: power-of-two block scales (the format the block-scaled tensor-core GEMM takes).
+// pdl: programmatic dependent launch (false on the second stream, as the other launchers)
 moe_status_t launch_quantize_rows_fp8(const void* a, moe_dtype_t dt, int64_t rows, int cols, uint8_t* codes,
-                                      float* scales, int ld_scales, cudaStream_t s, bool pow2 = false);
+                                      float* scales, int ld_scales, cudaStream_t s, bool pow2 = false,
+                                      bool pdl = true);
 moe_status_t launch_quantize_tiles_fp8(const void* w, moe_dtype_t dt, int G, int rows, int cols, uint8_t* codes,
                                        float* scales, cudaStream_t s, bool pow2 = false);
 

@@ -129,17 +129,27 @@ quantize_tiles_kernel(const T* __restrict__ w, int rows, int cols, int nb, int k
 }  // namespace
 
 moe_status_t launch_quantize_rows_fp8(const void* a, moe_dtype_t dt, int64_t rows, int cols, uint8_t* codes,
-                                      float* scales, int ld_scales, cudaStream_t s, bool pow2) {
+                                      float* scales, int ld_scales, cudaStream_t s, bool pow2, bool pdl) {
     if (rows == 0) return MOE_OK;
     const int kb = (cols + 127) / 128;
     const int64_t items = rows * ((kb + 1) / 2);  // one warp per pair of blocks
     const int grid = (int)std::min<int64_t>(ceil_div(items, 8), (int64_t)sm_count() * 16);
-    if (dt == MOE_BF16)
-        MOE_CUDA_TRY(launch_pdl(quantize_rows_kernel<__nv_bfloat16>, dim3(grid), dim3(256), 0, s,
-                                static_cast<const __nv_bfloat16*>(a), rows, cols, kb, ld_scales, codes, scales, pow2));
-    else
-        MOE_CUDA_TRY(launch_pdl(quantize_rows_kernel<float>, dim3(grid), dim3(256), 0, s, static_cast<const float*>(a),
-                                rows, cols, kb, ld_scales, codes, scales, pow2));
+    if (dt == MOE_BF16) {
+        const __nv_bfloat16* ab = static_cast<const __nv_bfloat16*>(a);
+        if (pdl)
+            MOE_CUDA_TRY(launch_pdl(quantize_rows_kernel<__nv_bfloat16>, dim3(grid), dim3(256), 0, s, ab, rows, cols,
+                                    kb, ld_scales, codes, scales, pow2));
+        else
+            quantize_rows_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(ab, rows, cols, kb, ld_scales, codes, scales, pow2);
+    } else {
+        const float* af = static_cast<const float*>(a);
+        if (pdl)
+            MOE_CUDA_TRY(launch_pdl(quantize_rows_kernel<float>, dim3(grid), dim3(256), 0, s, af, rows, cols, kb,
+                                    ld_scales, codes, scales, pow2));
+        else
+            quantize_rows_kernel<float><<<grid, 256, 0, s>>>(af, rows, cols, kb, ld_scales, codes, scales, pow2);
+    }
+    MOE_CUDA_TRY(cudaGetLastError());
     note_launch();
     return MOE_OK;
 }
