@@ -391,7 +391,9 @@ typedef struct moe_layer_desc {
 /* Layer steps timed by moe_layer_forward_timed.  "shared" (both projections of
  * the shared experts) runs on a second stream of the library's, forked when
  * the gate starts and joined before "up", concurrently with gate, route,
- * init_routing and permute_rows; "up" and "down" are the routed experts. */
+ * init_routing and permute_rows; "up" and "down" are the routed experts.  In
+ * FP8 layers with shared experts, "shared" also holds the quantisation of x
+ * (its codes are waited for before permute_rows); without them, "gate" does. */
 #define MOE_NUM_STAGES 8
 const char* moe_stage_name(int stage); /* "gate", "route", "init_routing", "permute_rows",
                                           "shared", "up", "down", "finalize" */
@@ -429,7 +431,7 @@ moe_status_t moe_layer_workspace_field(const moe_layer_desc* desc, moe_ws_field 
 /* x [T,H] dt, out [T,H] dt, ws of moe_layer_workspace_bytes(desc) bytes.
  * T == 0 is a no-op that returns MOE_OK (x, out and ws may then be NULL).
  * With S > 0 the first call on a device creates the library's second stream
- * and two events for that device (no device memory is allocated); make that
+ * and three events for that device (no device memory is allocated); make that
  * first call outside stream capture.  The call's work forks onto that stream
  * and joins back into `stream`.  bf16 layers with T >= 256 run the shared
  * experts' two projections as one launch; the environment variable
