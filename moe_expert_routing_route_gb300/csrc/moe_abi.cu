@@ -538,9 +538,11 @@ moe_status_t layer_forward(const moe_layer_desc* d, const void* x, void* out, vo
     } else {
         // beside the shared experts' GEMM on every SM: two copy blocks per SM (measured on dsv3_prefill:
         // the shared branch 329 -> 312 us; the copy itself unchanged at ~112 us, still off the critical
-        // path); beside it on a share of the SMs, eight
-        MOE_TRY(launch_permute_rows(x, (size_t)H * dt_size(dt), row_idx, T, k, ex, s,
-                                    !side ? 16 : (shared_ctas ? 8 : 2)));
+        // path); beside it on a share of the SMs, eight.  In the host path the shared experts ran chunk
+        // by chunk while x arrived and only the last chunk's remain, so the copy is the longer branch
+        // and takes sixteen (dsv3_prefill from host buffers: 4.55-4.57 -> 4.51-4.52 ms)
+        const int copy_blocks = !side || chunked_shared ? 16 : (shared_ctas ? 8 : 2);
+        MOE_TRY(launch_permute_rows(x, (size_t)H * dt_size(dt), row_idx, T, k, ex, s, copy_blocks));
     }
     MOE_TRY(mark(ev, ST_PERMUTE, 1, s));
     // join: GEMMs on every SM start after the shared experts; with the SMs split, only the down projection
