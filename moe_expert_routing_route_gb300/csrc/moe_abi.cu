@@ -449,10 +449,20 @@ moe_status_t layer_forward(const moe_layer_desc* d, const void* x, void* out, vo
                 const char* xc = static_cast<const char*>(x) + (size_t)c0 * row_bytes;
                 char* hsc = static_cast<char*>(hs) + (size_t)c0 * SI * dt_size(dt);
                 char* ysc = static_cast<char*>(ys) + (size_t)c0 * row_bytes;
-                MOE_TRY(ffn_up(xc, dt, nullptr, 1, c1 - c0, H, SI, d->w13_shared, hsc, status, ss, false, tiled, 0,
-                               false));
-                MOE_TRY(ffn_down(hsc, dt, nullptr, 1, c1 - c0, H, SI, d->w2_shared, ysc, status, ss, false, tiled, 0,
-                                 false));
+                // both projections in one launch, leaving shared memory for the gate and routing kernels
+                // that run beside it chunk by chunk (the device-buffer forward's choice too)
+                moe_status_t st = MOE_ERR_UNSUPPORTED;
+                if (dt == MOE_BF16)
+                    st = shared_ffn_fused(xc, c1 - c0, H, SI, d->w13_shared, d->w2_shared, hsc, ysc,
+                                          at<int>(ws, L.sync_off), status, ss, true, tiled);
+                if (st == MOE_ERR_UNSUPPORTED) {
+                    MOE_TRY(ffn_up(xc, dt, nullptr, 1, c1 - c0, H, SI, d->w13_shared, hsc, status, ss, false, tiled, 0,
+                                   false));
+                    MOE_TRY(ffn_down(hsc, dt, nullptr, 1, c1 - c0, H, SI, d->w2_shared, ysc, status, ss, false, tiled,
+                                     0, false));
+                } else {
+                    MOE_TRY(st);
+                }
             }
             MOE_TRY(mark(ev, ST_SHARED, 1, ss));
             MOE_CUDA_TRY(cudaEventRecord(side->join, ss));

@@ -127,6 +127,13 @@ def test_layer_full_size_sampled(oracle, name, n_sample):
         counts = layer.field("tokens_per_expert").cpu().numpy()
         assert counts.max() > 8 * counts.mean()  # the skew is really there
     check_layer(oracle, cfg, d, layer, out, tokens=toks)
+    # the host-buffer entry point at full size (x and out in 1024-row chunks or more, the shared
+    # experts chunk by chunk as x arrives) gives the device-buffer output bit for bit
+    x_host = d["x"].cpu().pin_memory()
+    out_host = torch.empty_like(x_host).pin_memory()
+    layer.forward_host(x_host, out_host)
+    assert layer.device_status() == 0
+    assert torch.equal(out_host, out.cpu())
     del layer, d
     torch.cuda.empty_cache()
 
