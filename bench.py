@@ -233,6 +233,15 @@ def cpu_baseline(cfg, host: dict, budget_s: float = 15.0) -> dict:
 
 # ---- arms ----
 
+def workload_config(cfg, world: int) -> dict:
+    """The bench line's `config`: the workload alone, identical in both arms (the reference arm
+    times a sample of the same batch, which its cpu_baseline names)."""
+    return dict(workload=cfg.name, T=cfg.T, H=cfg.H, E=cfg.E, k=cfg.k, I=cfg.I, S=cfg.S, global_batch=cfg.T * world,
+                parallelism=f"replicas{world}",
+                l2="inputs larger than L2: 22.6 GB of expert weights streamed every step"
+                if cfg.H == 7168 else "small workload")
+
+
 def run_reference(args, world, rank):
     cfg = inputs.CONFIGS[args.workload]
     if rank != 0:
@@ -253,8 +262,7 @@ def run_reference(args, world, rank):
     line = dict(metric=METRIC, value=value, unit=UNIT, n_gpus=args.gpus, steps=args.steps, warmup=args.warmup,
                 ms_per_step=per_step * 1e3, higher_is_better=True, scaling="weak", vs_baseline=None,
                 dtype="f64", data="synthetic", impl="reference",
-                config=dict(workload=cfg.name, T=cfg.T, H=cfg.H, E=cfg.E, k=cfg.k, I=cfg.I, S=cfg.S,
-                            tokens_per_step=args.ref_tokens),
+                config=workload_config(cfg, world), tokens_per_step=args.ref_tokens,
                 cpu_baseline=dict(value=value, unit=UNIT, cores=cores, kind="oracle",
                                   sample=f"{args.ref_tokens} of {cfg.T} tokens of {cfg.name} per step"),
                 e2e=dict(value=value, unit=UNIT, h2d_bytes_per_step=0, d2h_bytes_per_step=0))
@@ -433,11 +441,9 @@ def run_ours(args, world, rank, local):
                     # FP8 layers multiply e4m3 codes in the expert GEMMs; gate, routing and outputs stay bf16
                     dtype="e4m3+bf16" if fp8 else cfg.dtype, data="synthetic (seeded N(0,1) x, N(0,1/sqrt(fan_in)) "
                     "weights, random-init DeepSeek-V3-shaped MoE layer)",
-                    config=dict(workload=cfg.name, T=cfg.T, H=cfg.H, E=cfg.E, k=cfg.k, I=cfg.I, S=cfg.S,
-                                global_batch=tokens, parallelism=f"replicas{world}", expert_load=load,
-                                shared_expert_sms=layer.shared_expert_sms(),
-                                l2="inputs larger than L2: 22.6 GB of expert weights streamed every step"
-                                if cfg.H == 7168 else "small workload"),
+                    config=workload_config(cfg, world),
+                    # what this batch realised: the expert histogram and the SMs given to the shared experts
+                    workload_stats=dict(expert_load=load, shared_expert_sms=layer.shared_expert_sms()),
                     roofline=rl, cpu_baseline=cpu,
                     e2e=dict(value=tokens / e2e_s, unit=UNIT, h2d_bytes_per_step=nbytes_io,
                              d2h_bytes_per_step=nbytes_io),

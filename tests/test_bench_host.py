@@ -74,5 +74,11 @@ def test_reference_arm_json_line_on_cpu():
         assert key in d, key
     assert d["impl"] == "reference" and d["steps"] == 2 and d["warmup"] == 1 and d["value"] > 0
     assert d["config"]["workload"] == "tiny_fp32"
+    # the same config object as the GPU arm's line, so that the two lines compare as one workload
+    sys.path.insert(0, root)
+    import bench
+    from moe_expert_routing_route_gb300 import inputs
+    assert d["config"] == bench.workload_config(inputs.CONFIGS["tiny_fp32"], 1)
+    assert d["tokens_per_step"] == 8
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] == d["value"]
     assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}

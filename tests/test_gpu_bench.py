@@ -27,6 +27,11 @@ def test_bench_json_line_keys():
         assert key in d, key
     assert d["n_gpus"] == 1 and d["steps"] == 5 and d["warmup"] == 3 and d["value"] > 0
     assert d["config"]["workload"] == "tiny_fp32" and "model" not in d["config"]
+    sys.path.insert(0, root)
+    import bench
+    from moe_expert_routing_route_gb300 import inputs
+    assert d["config"] == bench.workload_config(inputs.CONFIGS["tiny_fp32"], 1)  # the reference arm's too
+    assert {"expert_load", "shared_expert_sms"} <= set(d["workload_stats"])
     rl = d["roofline"]
     assert rl["bound"] in ("hbm", "tensor") and rl["unit"] in ("GB/s", "TFLOP/s")
     assert rl["achieved"] > 0 and rl["peak"] > 0 and abs(rl["frac"] - rl["achieved"] / rl["peak"]) < 1e-9
