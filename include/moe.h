@@ -172,9 +172,10 @@ moe_status_t moe_init_routing(const void* x, moe_dtype_t dt, const int32_t* topk
  * device current) and keeps it; make that first call before any stream
  * capture.  The address is tied to the device's context: the first call after
  * a cudaDeviceReset of that device (a new context) looks it up again, so make
- * that call outside stream capture too.  All calls share the array and it keeps the last call's contents
- * (every entry a call reads is rewritten by that call, so nothing needs
- * clearing), but calls whose kernels overlap on the GPU race on it.  There is
+ * that call outside stream capture too.  All calls share the array and it
+ * keeps the last call's contents (every entry a call reads is rewritten by
+ * that call, so nothing needs clearing), but calls whose kernels overlap on
+ * the GPU race on it.  There is
  * no status word: an id outside [0,E) shows as expanded_row_idx = -1 and is not
  * counted in tokens_per_expert. */
 moe_status_t moe_init_routing_noalloc(const void* x, moe_dtype_t dt, const int32_t* topk_ids, int T, int H,
