@@ -116,3 +116,77 @@ def test_e4m3_encode_is_nearest_and_monotone(oracle, values):
         assert np.all(np.abs(table[finite] - vc) >= abs(d - vc) - 1e-12)
     enc = [table[oracle.e4m3_encode(v)] for v in sorted(values)]
     assert all(a <= b for a, b in zip(enc, enc[1:]))
+
+
+@st.composite
+def re_routing_case(draw):
+    W = draw(st.integers(1, 6))
+    El = draw(st.integers(1, 9))
+    seed = draw(st.integers(0, 2 ** 31 - 1))
+    rng = np.random.default_rng(seed)
+    counts = rng.integers(0, draw(st.sampled_from([1, 3, 6])), size=(W, El)).astype(np.int32)
+    return counts
+
+
+@SETTINGS
+@given(re_routing_case())
+def test_re_routing_is_the_stable_sort_by_local_expert(oracle, counts):
+    """Rows arrive source after source, each source's rows in local-expert order; the
+    second routing sorts them by local expert, stably (arrival order inside an expert),
+    and the un-sort puts every row back where it arrived."""
+    W, El = counts.shape
+    N, H = int(counts.sum()), 3
+    x = np.arange(N * H, dtype=np.float32).reshape(N, H)  # every row distinct
+    r = oracle.re_routing(x, counts)
+    keys = np.concatenate([np.repeat(np.arange(El), counts[p]) for p in range(W)]) if N else np.zeros(0, int)
+    order = np.argsort(keys, kind="stable")
+    assert np.array_equal(r["gathered_ids_unsort"], order)
+    assert np.array_equal(r["x_sorted"], x[order])
+    assert np.array_equal(r["tokens_per_local_expert"], counts.sum(0))
+    assert r["local_offsets"][0] == 0 and np.array_equal(np.diff(r["local_offsets"]), counts.sum(0))
+    assert np.array_equal(oracle.unsort_rows(r["x_sorted"], r["gathered_ids_unsort"]), x)
+
+
+@st.composite
+def fp8_rows_case(draw):
+    rows = draw(st.integers(1, 4))
+    cols = draw(st.integers(1, 400))
+    seed = draw(st.integers(0, 2 ** 31 - 1))
+    rng = np.random.default_rng(seed)
+    mag = 10.0 ** rng.uniform(-6, 6, size=(rows, 1))  # a magnitude per row, 12 decades apart at most
+    a = (rng.standard_normal((rows, cols)) * mag).astype(np.float32)
+    nb = (cols + 127) // 128
+    for r in range(rows):  # some all-zero blocks
+        for b in range(nb):
+            if rng.random() < 0.15:
+                a[r, b * 128:(b + 1) * 128] = 0.0
+    return a
+
+
+@SETTINGS
+@given(fp8_rows_case(), st.booleans())
+def test_fp8_row_blocks_scales_and_codes(oracle, a, pow2):
+    """1x128 blocks: fp32 scales put the block's largest magnitude at 448, power-of-two
+    scales are the smallest 2^e that keep it at or below 448; an all-zero block gets
+    scale 1 and zero codes; every element decodes within half an e4m3 step."""
+    rows, cols = a.shape
+    codes, scales = oracle.quantize_rows_fp8(a, pow2=pow2)
+    nb = (cols + 127) // 128
+    assert codes.shape == (rows, cols) and scales.shape == (rows, nb)
+    table = oracle.e4m3_table()
+    for r in range(rows):
+        for b in range(nb):
+            blk = a[r, b * 128:(b + 1) * 128].astype(np.float64)
+            s = float(scales[r, b])
+            amax = np.abs(blk).max()
+            deq = table[codes[r, b * 128:(b + 1) * 128]]
+            if amax == 0:
+                assert s == 1.0 and np.all(deq == 0)
+                continue
+            if pow2:
+                assert s == 2.0 ** np.round(np.log2(s))
+                assert amax / s <= 448.0 < amax / (s / 2)
+            else:
+                assert np.isclose(amax / s, 448.0, rtol=1e-6)
+            sub = 2.0 ** -10 if pow2 else 2.0 ** -9
+            assert np.all(np.abs(deq * s - blk) <= np.abs(blk) * 2.0 ** -4 + s * sub)
